@@ -1,0 +1,228 @@
+"""fp64 CPU oracle for length-aware GQA decode attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the benchmark's CPU-baseline leg may import this package.  The product path
+(``decode_attention_preallocated_gb300``) never imports it, and it never
+imports the product path: the two share no code.  Inputs reach both sides
+from ``decode_attention_preallocated_gb300.workloads`` (seeded generators
+only, no attention arithmetic).
+
+``dense`` and ``gather`` call the plain C loops in ``fd_oracle.c``
+(definition in that file's header); ``bruteforce`` is a second, pure-Python
+path used to pin the C code on tiny inputs.
+
+Parity pins (each checked by ``tests/test_oracle_pins.py``):
+  * closed forms: one visible key returns its value row; identical keys
+    return the mean of the visible value rows; constant values are returned
+    unchanged; q = 0 gives the uniform mean; a dominant key returns its row;
+  * library special case: ``torch.nn.functional.scaled_dot_product_attention``
+    in float64 with an explicit boolean mask and repeated KV heads;
+  * brute force: ``oracle.bruteforce`` (math.fsum over Python floats);
+  * invariants: gather over 0..L-1 equals the dense prefix, gather over a
+    selection equals the masked dense path, permutation invariance of the
+    gather list, independence from capacity beyond the length and from the
+    tail contents, causal row i ignores drafts after i, length rollback;
+  * hand-derived closed-form fixtures under ``tests/golden``.
+The pages print no attention values for a worked example, so no pin comes
+from printed numbers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fd_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``fd_oracle.c`` into ``liboracle.so`` (gcc, OpenMP, -O2)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c99",
+           "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(path):
+    lib = ctypes.CDLL(path)
+    p = ctypes.c_void_p
+    i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    lib.fdo_dense.argtypes = [p, p, p, p, p, p, i32, p, p, p, p,
+                              i32, i32, i32, i32, i32, i64, i32, f64, p]
+    lib.fdo_dense.restype = i32
+    lib.fdo_gather.argtypes = [p, p, p, p, p, p, i32, p, p, p, p, i64,
+                               i32, i32, i32, i32, i32, i64, f64, p]
+    lib.fdo_gather.restype = i32
+    lib.fdo_set_threads.argtypes = [i32]
+    lib.fdo_set_threads.restype = None
+    lib.fdo_max_threads.argtypes = []
+    lib.fdo_max_threads.restype = i32
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(_LIB_PATH)
+    return _lib
+
+
+def load_variant(path: str):
+    """Bind another build of ``fd_oracle.c`` (used by the mutation tests that
+    plant mistakes in copies of the oracle).  Returns an object with the same
+    ``dense`` / ``gather`` functions as this module."""
+    lib = _bind(path)
+
+    class _Variant:
+        @staticmethod
+        def dense(*a, **kw):
+            return dense(*a, _lib_override=lib, **kw)
+
+        @staticmethod
+        def gather(*a, **kw):
+            return gather(*a, _lib_override=lib, **kw)
+
+    return _Variant
+
+
+def set_threads(n: int) -> None:
+    _load().fdo_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(_load().fdo_max_threads())
+
+
+def _as_np(t):
+    """torch CPU tensor or numpy array -> (numpy array, element strides).
+
+    bf16 tensors are reinterpreted as their uint16 bit patterns; the oracle
+    widens them exactly.  Strides are kept, so strided views work.
+    """
+    try:
+        import torch
+    except ImportError:  # pragma: no cover
+        torch = None
+    if torch is not None and isinstance(t, torch.Tensor):
+        t = t.detach()
+        if t.device.type != "cpu":
+            t = t.cpu()
+        if t.dtype == torch.bfloat16:
+            base = t.view(torch.int16)
+            arr = base.numpy().view(np.uint16)
+        else:
+            arr = t.numpy()
+        return arr
+    return np.asarray(t)
+
+
+def _strides(arr):
+    return np.asarray([s // arr.itemsize for s in arr.strides], dtype=np.int64)
+
+
+def _ptr(arr):
+    return arr.ctypes.data_as(ctypes.c_void_p)
+
+
+def _kv_args(k, v, k_scale, v_scale):
+    ka, va = _as_np(k), _as_np(v)
+    if ka.dtype == np.int8:
+        if k_scale is None or v_scale is None:
+            raise ValueError("int8 caches need k_scale and v_scale")
+        ks_a = np.asarray(_as_np(k_scale), dtype=np.float32)
+        vs_a = np.asarray(_as_np(v_scale), dtype=np.float32)
+        if _strides(ks_a).tolist() != _strides(vs_a).tolist():
+            vs_a = np.ascontiguousarray(vs_a)
+            ks_a = np.ascontiguousarray(ks_a)
+        int8 = 1
+    elif ka.dtype == np.uint16:
+        ks_a = vs_a = None
+        int8 = 0
+    else:
+        raise TypeError("k/v must be bf16 or int8, got %s" % ka.dtype)
+    if va.dtype != ka.dtype:
+        raise TypeError("k and v must have the same dtype")
+    return ka, va, ks_a, vs_a, int8
+
+
+def dense(q, k, v, kv_lengths, n_q, causal, scale, k_scale=None,
+          v_scale=None, _lib_override=None):
+    """fp64 attention over the filled prefix (optionally bottom-right causal).
+
+    q [B, n_q, Hq, d] bf16; k, v [B, Hkv, cap, d] bf16 or int8 (any strides);
+    kv_lengths [B] int32 host values; int8 caches take fp32 scales
+    [B, Hkv, cap].  Returns float64 [B, n_q, Hq, d].
+    """
+    lib = _lib_override or _load()
+    qa = _as_np(q)
+    if qa.dtype != np.uint16:
+        raise TypeError("q must be bf16")
+    ka, va, ksa, vsa, int8 = _kv_args(k, v, k_scale, v_scale)
+    B, nq_, Hq, d = qa.shape
+    if nq_ != n_q:
+        raise ValueError("q.shape[1] != n_q")
+    _, Hkv, cap, d2 = ka.shape
+    if d2 != d or va.shape != ka.shape:
+        raise ValueError("shape mismatch")
+    lens = np.ascontiguousarray(np.asarray(_as_np(kv_lengths), dtype=np.int32))
+    if lens.shape != (B,):
+        raise ValueError("kv_lengths must be [B]")
+    out = np.zeros((B, n_q, Hq, d), dtype=np.float64)
+    qs, ks, vs = _strides(qa), _strides(ka), _strides(va)
+    ss = _strides(ksa) if int8 else np.zeros(3, dtype=np.int64)
+    rc = lib.fdo_dense(_ptr(qa), _ptr(qs), _ptr(ka), _ptr(ks), _ptr(va),
+                       _ptr(vs), int8,
+                       _ptr(ksa) if int8 else None,
+                       _ptr(vsa) if int8 else None, _ptr(ss), _ptr(lens),
+                       B, n_q, Hq, Hkv, d, cap, 1 if causal else 0,
+                       float(scale), _ptr(out))
+    if rc != 0:
+        raise RuntimeError("fdo_dense failed: %d" % rc)
+    return out
+
+
+def gather(q, k, v, idx, scale, k_scale=None, v_scale=None,
+           _lib_override=None):
+    """fp64 attention over the cache rows named by ``idx`` [B, n_q, K].
+
+    One list per (sequence, query row), shared by every head of that row;
+    entries < 0 or >= cap are skipped.  Returns float64 [B, n_q, Hq, d].
+    """
+    lib = _lib_override or _load()
+    qa = _as_np(q)
+    if qa.dtype != np.uint16:
+        raise TypeError("q must be bf16")
+    ka, va, ksa, vsa, int8 = _kv_args(k, v, k_scale, v_scale)
+    B, n_q, Hq, d = qa.shape
+    _, Hkv, cap, d2 = ka.shape
+    if d2 != d or va.shape != ka.shape:
+        raise ValueError("shape mismatch")
+    ia = np.ascontiguousarray(np.asarray(_as_np(idx), dtype=np.int32))
+    if ia.ndim != 3 or ia.shape[:2] != (B, n_q):
+        raise ValueError("idx must be [B, n_q, K]")
+    K = ia.shape[2]
+    out = np.zeros((B, n_q, Hq, d), dtype=np.float64)
+    qs, ks, vs = _strides(qa), _strides(ka), _strides(va)
+    ss = _strides(ksa) if int8 else np.zeros(3, dtype=np.int64)
+    rc = lib.fdo_gather(_ptr(qa), _ptr(qs), _ptr(ka), _ptr(ks), _ptr(va),
+                        _ptr(vs), int8,
+                        _ptr(ksa) if int8 else None,
+                        _ptr(vsa) if int8 else None, _ptr(ss), _ptr(ia), K,
+                        B, n_q, Hq, Hkv, d, cap, float(scale), _ptr(out))
+    if rc != 0:
+        raise RuntimeError("fdo_gather failed: %d" % rc)
+    return out
