@@ -1,0 +1,504 @@
+#!/usr/bin/env python
+"""Benchmark: length-aware GQA decode attention on GB300.
+
+One step = one fd_decode call over the batched ragged workload (8 sequences,
+lengths uniform in [1024, 32768] from the seed, capacity 32768, 6-row causal
+window, 16 q / 4 kv heads, head_dim 128 x 2 = 256, bf16 cache).  The metric is
+KV-read HBM bandwidth: the K and V bytes of the filled prefixes
+(sum_b L_b * Hkv * d * 2 bytes * 2 tensors) divided by the step time.  The
+filled prefixes (~0.5 GB) are larger than L2, so no flush is needed between
+steps.
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle on the
+host cores on a bounded sample of the same workload instead.
+
+Multi-GPU (torchrun, one process per GPU): every rank runs its own replica on
+its own batch (no collective on the data path); ``value`` sums the bytes of
+all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "KV-read HBM GB/s per decode-attention call"
+UNIT = "GB/s"
+WORKLOAD = "ragged"
+WORKLOAD_DESC = ("batched ragged decode: B=8, kv_len uniform[1024,32768] (seed), "
+                 "cap=32768, n_q=6 causal, Hq=16, Hkv=4, head_dim=256, bf16 K/V")
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------- helpers
+def rank_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kv_bytes(lengths, Hkv, d, esize):
+    return sum(int(L) for L in lengths) * Hkv * d * esize * 2
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_attention_preallocated_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic_%s.txt" % workload)
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_sources") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- workloads
+def make_inputs(name, seed, device):
+    from decode_attention_preallocated_gb300 import workloads as W
+    return W.workload(name, seed=seed, device=device)
+
+
+def call_fn(inp, out, ws, kernel, num_ctas=0):
+    from decode_attention_preallocated_gb300 import fd
+    if inp.idx is not None:
+        return lambda: fd.decode_gather(inp.q, inp.k, inp.v, inp.idx, scale=inp.scale, out=out,
+                                        workspace=ws, kernel=kernel, num_ctas=num_ctas)
+    if inp.k.dtype == torch.int8:
+        return lambda: fd.decode_int8(inp.q, inp.k, inp.v, inp.k_scale, inp.v_scale,
+                                      inp.kv_lengths, n_q=inp.n_q, causal=inp.causal,
+                                      scale=inp.scale, out=out, workspace=ws, kernel=kernel,
+                                      num_ctas=num_ctas)
+    return lambda: fd.decode(inp.q, inp.k, inp.v, inp.kv_lengths, n_q=inp.n_q,
+                             causal=inp.causal, scale=inp.scale, out=out, workspace=ws,
+                             kernel=kernel, num_ctas=num_ctas)
+
+
+def algorithmic_bytes(inp):
+    B, n_q, Hq, d = inp.q.shape
+    Hkv = inp.k.shape[1]
+    if inp.idx is not None:
+        valid = int(((inp.idx >= 0) & (inp.idx < inp.k.shape[2])).sum())
+        return valid * Hkv * d * 2 * 2
+    es = 1 if inp.k.dtype == torch.int8 else 2
+    b = kv_bytes(inp.lengths_host, Hkv, d, es)
+    if es == 1:
+        b += sum(inp.lengths_host) * Hkv * 4 * 2   # fp32 per-token scales
+    return b
+
+
+def time_calls(fn, n, stream):
+    """Average ms per call of n back-to-back calls (CUDA events on `stream`)."""
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def workspace_for(inp, device):
+    from decode_attention_preallocated_gb300 import fd
+    B, n_q, Hq, d = inp.q.shape
+    Hkv = inp.k.shape[1]
+    g = Hq // Hkv
+    if inp.idx is not None:
+        return fd.Workspace(B * n_q * Hkv, g, 256, 4096, device=device)
+    return fd.Workspace(B * Hkv, g * n_q, 256, 4096, device=device)
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample(inp_cpu, budget_s=10.0, max_calls=50):
+    """Time the fp64 oracle on the host cores on whole sequences of the
+    workload until ~budget_s of CPU work; returns (GB/s, threads, sample text)."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    B = inp_cpu.q.shape[0]
+    bytes_done, t_used, seqs = 0, 0.0, 0
+    b = 0
+    while t_used < budget_s and seqs < max_calls:
+        sl = slice(b, b + 1)
+        L = [inp_cpu.lengths_host[b]]
+        t0 = time.perf_counter()
+        if inp_cpu.idx is not None:
+            oracle.gather(inp_cpu.q[sl], inp_cpu.k[sl], inp_cpu.v[sl], inp_cpu.idx[sl],
+                          inp_cpu.scale)
+        else:
+            oracle.dense(inp_cpu.q[sl], inp_cpu.k[sl], inp_cpu.v[sl], L, inp_cpu.n_q,
+                         inp_cpu.causal, inp_cpu.scale,
+                         None if inp_cpu.k_scale is None else inp_cpu.k_scale[sl],
+                         None if inp_cpu.v_scale is None else inp_cpu.v_scale[sl])
+        t_used += time.perf_counter() - t0
+        sub = type(inp_cpu)(q=inp_cpu.q[sl], k=inp_cpu.k[sl], v=inp_cpu.v[sl],
+                            kv_lengths=inp_cpu.kv_lengths[sl], n_q=inp_cpu.n_q,
+                            causal=inp_cpu.causal, scale=inp_cpu.scale,
+                            k_scale=None if inp_cpu.k_scale is None else inp_cpu.k_scale[sl],
+                            idx=None if inp_cpu.idx is None else inp_cpu.idx[sl],
+                            lengths_host=L)
+        bytes_done += algorithmic_bytes(sub)
+        seqs += 1
+        b = (b + 1) % B
+    gbs = bytes_done / t_used / 1e9
+    sample = "%d whole sequence(s) of the workload (%.1f MB of KV), %.1f s" % (
+        seqs, bytes_done / 1e6, t_used)
+    return gbs, cores, sample
+
+
+def cpu_view(inp):
+    from decode_attention_preallocated_gb300 import workloads as W
+    return W.DecodeInputs(
+        q=inp.q.cpu(), k=inp.k.cpu(), v=inp.v.cpu(), kv_lengths=inp.kv_lengths.cpu(),
+        n_q=inp.n_q, causal=inp.causal, scale=inp.scale,
+        k_scale=None if inp.k_scale is None else inp.k_scale.cpu(),
+        v_scale=None if inp.v_scale is None else inp.v_scale.cpu(),
+        idx=None if inp.idx is None else inp.idx.cpu(),
+        lengths_host=list(inp.lengths_host), name=inp.name)
+
+
+# --------------------------------------------------------------- the arms
+def run_reference(args):
+    rank, world, local = rank_info()
+    if world > 1 and rank != 0:
+        return 0
+    from decode_attention_preallocated_gb300 import workloads as W
+    inp = W.workload(WORKLOAD, seed=1, device="cpu")
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    # one step = the oracle on one whole sequence of the batch (bounded sample)
+    per_step = []
+    steps = max(1, args.steps)
+    warm = max(0, min(args.warmup, 1))
+    B = inp.q.shape[0]
+    total_bytes, total_t = 0, 0.0
+    for s in range(warm + steps):
+        b = s % B
+        sl = slice(b, b + 1)
+        t0 = time.perf_counter()
+        oracle.dense(inp.q[sl], inp.k[sl], inp.v[sl], [inp.lengths_host[b]], inp.n_q,
+                     inp.causal, inp.scale)
+        dt = time.perf_counter() - t0
+        if s >= warm:
+            nb = kv_bytes([inp.lengths_host[b]], inp.k.shape[1], inp.q.shape[3], 2)
+            total_bytes += nb
+            total_t += dt
+            per_step.append(dt)
+    value = total_bytes / total_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total_t / steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "step": "fp64 oracle over one whole sequence "
+                   "of the batch (all 16 heads x 6 rows)", "l2": "host run"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                         "kind": "oracle",
+                         "sample": "%d whole sequence(s), round-robin over the batch" % steps},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def extras(args, device, stream, peak, kernel):
+    """Per-mode timings beside the headline: the other workloads, the
+    capacity-independence check and the depth sweep (µs/call and GB/s)."""
+    from decode_attention_preallocated_gb300 import workloads as W
+    res = {}
+
+    def measure(tag, inp, n=200):
+        ws = workspace_for(inp, device)
+        out = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=device)
+        fn = call_fn(inp, out, ws, kernel)
+        for _ in range(5):
+            fn()
+        ms = time_calls(fn, n, stream)
+        nbytes = algorithmic_bytes(inp)
+        res[tag] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
+                    "frac": round(nbytes / ms / 1e6 / peak, 4), "bytes": nbytes}
+        ws.close()
+
+    for name in ("dense_1k", "mtp_verify", "gather", "int8"):
+        inp = W.workload(name, seed=1, device=device)
+        measure(name, inp, 50 if name == "int8" else 200)
+        del inp
+        torch.cuda.empty_cache()
+    for cap in (3000, 131072):
+        inp = W.dense_inputs(1, 4, 16, 4, 256, cap, [3000], 1, True, device=device)
+        measure("mtp_verify_cap%d" % cap, inp)
+        del inp
+    inp = W.dense_inputs(1, 1, 32, 4, 128, 131072, [131072], 1, False, device=device)
+    measure("dense_scan_131k_32q4kv", inp, 50)
+    del inp
+    for L in (32768, 65536, 131072):
+        for (Hq, Hkv, d, n_q, B) in ((16, 4, 256, 6, 8), (16, 4, 256, 1, 4), (8, 2, 128, 1, 8)):
+            inp = W.dense_inputs(B, n_q, Hq, Hkv, d, L + 1000, [L] * B, 100, n_q > 1,
+                                 device=device)
+            measure("sweep_L%d_B%d_%dq%dkv_d%d_nq%d" % (L, B, Hq, Hkv, d, n_q), inp, 30)
+            del inp
+            torch.cuda.empty_cache()
+    return res
+
+
+def run_fd(args):
+    from decode_attention_preallocated_gb300 import build as fdbuild
+    from decode_attention_preallocated_gb300 import fd
+
+    rank, world, local = rank_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    fdbuild.build()
+    fd.lib()
+    kernel = {"auto": fd.FD_KERNEL_AUTO, "simt": fd.FD_KERNEL_SIMT,
+              "tc": fd.FD_KERNEL_TC}[args.kernel]
+    peak, peak_kind = peaks()
+
+    inp = make_inputs(WORKLOAD, seed=1 + rank, device=device)
+    nbytes = algorithmic_bytes(inp)
+    ws = workspace_for(inp, device)
+    out = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.Stream(device)
+    fn = call_fn(inp, out, ws, kernel)
+
+    warm = max(3, args.warmup)
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            fn()
+    torch.cuda.synchronize()
+    steps = args.steps
+    if steps <= 0:   # auto: about 3 s of timed work so the clock samples mean something
+        ms = time_calls(fn, 5, stream)
+        steps = int(max(20, min(20000, 3000.0 / max(ms, 1e-3))))
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local])
+    barrier()
+    sampler.start()
+    time.sleep(0.25)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(steps):
+            fn()
+        ev1.record(stream)
+    ev1.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ms_step = ev0.elapsed_time(ev1) / steps
+    t = torch.tensor([ms_step], device=device, dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    all_bytes = nbytes * world
+    value = all_bytes / (ms_max * 1e-3) / 1e9
+
+    # end to end through the public call with host buffers: every step copies
+    # q, both caches and kv_lengths from pinned host memory, decodes, and reads
+    # the output back
+    host = {} if args.no_e2e else {
+        n: getattr(inp, n).cpu().pin_memory() for n in ("q", "k", "v", "kv_lengths")}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        inp.q.copy_(host["q"], non_blocking=True)
+        inp.k.copy_(host["k"], non_blocking=True)
+        inp.v.copy_(host["v"], non_blocking=True)
+        inp.kv_lengths.copy_(host["kv_lengths"], non_blocking=True)
+        fn()
+        out_host.copy_(out, non_blocking=True)
+
+    e2e_value = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(20, steps))
+        with torch.cuda.stream(stream):
+            e2e_step()
+        barrier()
+        e_ms = time_calls(e2e_step, e2e_steps, stream)
+        et = torch.tensor([e_ms], device=device, dtype=torch.float64)
+        if world > 1:
+            import torch.distributed as dist
+            dist.all_reduce(et, op=dist.ReduceOp.MAX)
+        e2e_value = round(all_bytes / (float(et.item()) * 1e-3) / 1e9, 3)
+
+    result = None
+    if rank == 0:
+        achieved = nbytes / (ms_step * 1e-3) / 1e9
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cpu_inp = cpu_view(inp)
+            gbs, cores, sample = oracle_sample(cpu_inp, budget_s=args.cpu_budget)
+            cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                   "sample": sample}
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": steps, "warmup": warm, "ms_per_step": round(ms_max, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "seed": 1,
+                       "kv_lengths": inp.lengths_host,
+                       "kv_bytes_per_step": nbytes, "us_per_call": round(ms_step * 1e3, 2),
+                       "l2": "inputs larger than L2 (no flush)",
+                       "parallelism": "replicas (one batch per GPU, no collective)",
+                       "kernel": args.kernel},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": recorded_traffic(WORKLOAD),
+                         "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
+                         if peak_kind == "measured" else "fallback 6.8 TB/s"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "clocks": clocks,
+            "gpu_launches": steps,
+        }
+        if not args.no_extras and world == 1:
+            result["modes"] = extras(args, device, stream, peak, kernel)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    ws.close()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="0 = auto (~3 s timed)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
+    ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_fd(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,356 @@
+// fd_api.cu -- the C ABI of libfd.so (declared in include/fd.h): host-side
+// validation, workspace management, the thread-block count and the launch.
+// Every check runs before the first CUDA call; nothing here allocates,
+// frees, synchronises or reads device data during a decode call.
+#include <cuda_runtime.h>
+
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+#include <new>
+
+#include "fd.h"
+#include "fd_internal.h"
+#include "fd_launch.h"
+
+struct fd_workspace {
+    void *base;
+    size_t bytes;
+    int64_t max_segments;
+    int32_t max_rows, head_dim, max_ctas;
+    int32_t *counters;
+    int32_t *status;
+    float *partials;
+    size_t partial_floats;
+    int device;
+};
+
+namespace {
+
+constexpr int kVersion = 1;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t counters_off, status_off, partials_off, total;
+    size_t partial_floats;
+};
+
+WsLayout ws_layout(int64_t max_segments, int32_t max_rows, int32_t head_dim,
+                   int32_t max_ctas) {
+    WsLayout L;
+    L.counters_off = 0;
+    L.status_off = align_up((size_t)max_segments * 4, 256);
+    L.partials_off = L.status_off + 256;
+    L.partial_floats = (size_t)(max_segments + max_ctas) *
+                       (size_t)fd::slot_floats(max_rows, head_dim);
+    L.total = L.partials_off + align_up(L.partial_floats * 4, 256);
+    return L;
+}
+
+int sm_count_current() {
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+int esize(int32_t dt) {
+    switch (dt) {
+        case FD_BF16: return 2;
+        case FD_F32: return 4;
+        case FD_I8: return 1;
+        case FD_I32: return 4;
+        default: return 0;
+    }
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Basic structural check of a tensor descriptor.
+int check_tensor(const fd_tensor *t, int ndim) {
+    if (!t || !t->data || t->ndim != ndim || esize(t->dtype) == 0) return FD_ERR_ARG;
+    for (int i = 0; i < ndim; ++i)
+        if (t->shape[i] < 0 || t->stride[i] < 0) return FD_ERR_ARG;
+    return FD_OK;
+}
+
+int kernel_tile(int32_t kernel) {
+    (void)kernel;
+    return fd::simt_tile_tokens();
+}
+
+int32_t auto_ctas(int32_t kernel, int64_t max_tiles) {
+    const int sms = sm_count_current();
+    if (sms <= 0) return 0;
+    (void)kernel;
+    int64_t g = (int64_t)sms * 2;
+    if (max_tiles > 0 && g > max_tiles) g = max_tiles;
+    return (int32_t)(g < 1 ? 1 : g);
+}
+
+// Shared validation and launch for the three entry points.
+struct Call {
+    const fd_tensor *q, *k, *v, *ks, *vs, *out;
+    const int32_t *kv_lengths;
+    const int32_t *idx;
+    int32_t idx_len;
+    int32_t n_q, causal;
+    float scale;
+    int mode;         // fd::Mode
+    int kv_int8;
+    const fd_opts *opts;
+};
+
+int run(const Call &c) {
+    int rc;
+    if (!c.opts) return FD_ERR_ARG;
+    const fd_opts &o = *c.opts;
+    if (o.reserved[0] || o.reserved[1] || o.reserved[2]) return FD_ERR_ARG;
+    if (o.kernel != FD_KERNEL_AUTO && o.kernel != FD_KERNEL_SIMT && o.kernel != FD_KERNEL_TC)
+        return FD_ERR_ARG;
+    if (o.num_ctas < 0) return FD_ERR_ARG;
+    if ((rc = check_tensor(c.q, 4)) || (rc = check_tensor(c.k, 4)) ||
+        (rc = check_tensor(c.v, 4)) || (rc = check_tensor(c.out, 4)))
+        return rc;
+    const int kvdt = c.kv_int8 ? FD_I8 : FD_BF16;
+    if (c.q->dtype != FD_BF16 || c.k->dtype != kvdt || c.v->dtype != kvdt) return FD_ERR_ARG;
+    if (c.out->dtype != FD_BF16 && c.out->dtype != FD_F32) return FD_ERR_ARG;
+
+    const int64_t B = c.q->shape[0], n_q = c.q->shape[1], Hq = c.q->shape[2], d = c.q->shape[3];
+    const int64_t Hkv = c.k->shape[1], cap = c.k->shape[2];
+    if (n_q != c.n_q) return FD_ERR_ARG;
+    for (int i = 0; i < 4; ++i) {
+        if (c.k->shape[i] != c.v->shape[i]) return FD_ERR_ARG;
+        if (c.out->shape[i] != c.q->shape[i]) return FD_ERR_ARG;
+    }
+    if (c.k->shape[0] != B || c.k->shape[3] != d) return FD_ERR_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || B > (1 << 24) || Hq > 4096 || cap > ((int64_t)1 << 40))
+        return FD_ERR_ARG;
+    if (Hq % Hkv != 0) return FD_ERR_ARG;
+    if (d != 128 && d != 256) return FD_ERR_UNSUPPORTED;
+    if (n_q < 1 || n_q > 6) return FD_ERR_UNSUPPORTED;
+    const int64_t g = Hq / Hkv;
+    const int64_t rows = c.mode == fd::kGather ? g : g * n_q;
+    if (rows > FD_MAX_ROWS) return FD_ERR_UNSUPPORTED;
+    if (c.q->stride[3] != 1 || c.k->stride[3] != 1 || c.v->stride[3] != 1 ||
+        c.out->stride[3] != 1)
+        return FD_ERR_ARG;
+    // 16-byte aligned cache rows: base pointer and every stride.
+    const int es = esize(kvdt);
+    if (!aligned16(c.k->data) || !aligned16(c.v->data)) return FD_ERR_ALIGN;
+    for (int i = 0; i < 3; ++i)
+        if ((c.k->stride[i] * es) % 16 || (c.v->stride[i] * es) % 16) return FD_ERR_ALIGN;
+    if (!isfinite(c.scale)) return FD_ERR_ARG;
+    if (c.kv_int8) {
+        if ((rc = check_tensor(c.ks, 3)) || (rc = check_tensor(c.vs, 3))) return rc;
+        if (c.ks->dtype != FD_F32 || c.vs->dtype != FD_F32) return FD_ERR_ARG;
+        const int64_t want[3] = {B, Hkv, cap};
+        for (int i = 0; i < 3; ++i)
+            if (c.ks->shape[i] != want[i] || c.vs->shape[i] != want[i]) return FD_ERR_ARG;
+    }
+    if (c.mode == fd::kDense && !c.kv_lengths) return FD_ERR_ARG;
+    if (c.mode == fd::kGather && (c.idx_len < 0 || (!c.idx && c.idx_len > 0))) return FD_ERR_ARG;
+    if (c.causal != 0 && c.causal != 1) return FD_ERR_ARG;
+
+    fd_workspace *ws = o.ws;
+    if (!ws) return FD_ERR_WORKSPACE;
+    const int64_t nseg = c.mode == fd::kGather ? B * n_q * Hkv : B * Hkv;
+    const int tile = kernel_tile(o.kernel);
+    const int64_t max_tiles =
+        c.mode == fd::kGather ? nseg * fd::ceil_div(c.idx_len, tile) : nseg * fd::ceil_div(cap, tile);
+    int32_t G = o.num_ctas;
+    if (G == 0) {
+        G = auto_ctas(o.kernel, max_tiles);
+        if (G <= 0) return FD_ERR_CUDA;
+    }
+    if (nseg > ws->max_segments || rows > ws->max_rows || d > ws->head_dim || G > ws->max_ctas)
+        return FD_ERR_WORKSPACE;
+    if ((size_t)(nseg + G) * (size_t)fd::slot_floats(rows, d) > ws->partial_floats)
+        return FD_ERR_WORKSPACE;
+
+    fd::Params p;
+    memset(&p, 0, sizeof p);
+    p.B = (int32_t)B; p.n_q = (int32_t)n_q; p.Hq = (int32_t)Hq; p.Hkv = (int32_t)Hkv;
+    p.g = (int32_t)g; p.d = (int32_t)d; p.cap = cap; p.rows = (int32_t)rows;
+    p.mode = c.mode; p.causal = c.mode == fd::kDense ? c.causal : 0;
+    p.kv_int8 = c.kv_int8; p.out_f32 = c.out->dtype == FD_F32; p.tile = tile;
+    p.scale_log2 = c.scale * 1.4426950408889634f;
+    p.idx_len = c.idx_len; p.nseg = nseg;
+    p.q = static_cast<const uint16_t *>(c.q->data);
+    p.k = c.k->data; p.v = c.v->data;
+    for (int i = 0; i < 4; ++i) {
+        p.qs[i] = c.q->stride[i]; p.ks[i] = c.k->stride[i];
+        p.vs[i] = c.v->stride[i]; p.os[i] = c.out->stride[i];
+    }
+    if (c.kv_int8) {
+        p.k_scale = static_cast<const float *>(c.ks->data);
+        p.v_scale = static_cast<const float *>(c.vs->data);
+        for (int i = 0; i < 3; ++i) { p.kss[i] = c.ks->stride[i]; p.vss[i] = c.vs->stride[i]; }
+    }
+    p.kv_lengths = c.kv_lengths;
+    p.idx = c.idx;
+    p.out = c.out->data;
+    p.counters = ws->counters;
+    p.status = ws->status;
+    p.partials = ws->partials;
+
+    cudaStream_t st = static_cast<cudaStream_t>(o.stream);
+    rc = fd::launch_simt(p, G, st);
+    return rc == 0 ? FD_OK : (rc == -2 ? FD_ERR_UNSUPPORTED : FD_ERR_CUDA);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fd_decode(const fd_tensor *q, const fd_tensor *k_cache, const fd_tensor *v_cache,
+              const int32_t *kv_lengths, int32_t n_q, int32_t causal, float scale,
+              const fd_tensor *out, const fd_opts *opts) {
+    Call c{q, k_cache, v_cache, nullptr, nullptr, out, kv_lengths, nullptr, 0,
+           n_q, causal, scale, fd::kDense, 0, opts};
+    return run(c);
+}
+
+int fd_decode_int8(const fd_tensor *q, const fd_tensor *k_cache, const fd_tensor *v_cache,
+                   const fd_tensor *k_scale, const fd_tensor *v_scale,
+                   const int32_t *kv_lengths, int32_t n_q, int32_t causal, float scale,
+                   const fd_tensor *out, const fd_opts *opts) {
+    Call c{q, k_cache, v_cache, k_scale, v_scale, out, kv_lengths, nullptr, 0,
+           n_q, causal, scale, fd::kDense, 1, opts};
+    return run(c);
+}
+
+int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache, const fd_tensor *v_cache,
+                     const int32_t *idx, int32_t idx_len, const fd_tensor *out,
+                     const fd_opts *opts) {
+    if (!q || !opts) return FD_ERR_ARG;
+    float scale = opts->scale;
+    if (scale == 0.f && q->ndim == 4 && q->shape[3] > 0) scale = 1.f / sqrtf((float)q->shape[3]);
+    Call c{q, k_cache, v_cache, nullptr, nullptr, out, nullptr, idx, idx_len,
+           q->ndim == 4 ? (int32_t)q->shape[1] : 0, 0, scale, fd::kGather, 0, opts};
+    return run(c);
+}
+
+size_t fd_workspace_bytes(int64_t max_segments, int32_t max_rows, int32_t head_dim,
+                          int32_t max_ctas) {
+    if (max_segments < 1 || max_rows < 1 || head_dim < 1 || max_ctas < 1) return 0;
+    return ws_layout(max_segments, max_rows, head_dim, max_ctas).total;
+}
+
+int fd_workspace_create(int64_t max_segments, int32_t max_rows, int32_t head_dim,
+                        int32_t max_ctas, void *stream, fd_workspace **out) {
+    if (!out || max_segments < 1 || max_rows < 1 || max_rows > FD_MAX_ROWS ||
+        head_dim < 1 || head_dim > 256 || max_ctas < 1)
+        return FD_ERR_ARG;
+    *out = nullptr;
+    const WsLayout L = ws_layout(max_segments, max_rows, head_dim, max_ctas);
+    fd_workspace *ws = new (std::nothrow) fd_workspace;
+    if (!ws) return FD_ERR_ARG;
+    void *base = nullptr;
+    if (cudaMalloc(&base, L.total) != cudaSuccess) {
+        delete ws;
+        return FD_ERR_CUDA;
+    }
+    ws->base = base;
+    ws->bytes = L.total;
+    ws->max_segments = max_segments;
+    ws->max_rows = max_rows;
+    ws->head_dim = head_dim;
+    ws->max_ctas = max_ctas;
+    ws->counters = reinterpret_cast<int32_t *>(static_cast<char *>(base) + L.counters_off);
+    ws->status = reinterpret_cast<int32_t *>(static_cast<char *>(base) + L.status_off);
+    ws->partials = reinterpret_cast<float *>(static_cast<char *>(base) + L.partials_off);
+    ws->partial_floats = L.partial_floats;
+    cudaGetDevice(&ws->device);
+    if (cudaMemsetAsync(base, 0, L.partials_off, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaFree(base);
+        delete ws;
+        return FD_ERR_CUDA;
+    }
+    *out = ws;
+    return FD_OK;
+}
+
+int fd_workspace_reset(fd_workspace *ws, void *stream) {
+    if (!ws) return FD_ERR_ARG;
+    const size_t n = reinterpret_cast<char *>(ws->partials) - static_cast<char *>(ws->base);
+    return cudaMemsetAsync(ws->base, 0, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? FD_OK : FD_ERR_CUDA;
+}
+
+int fd_workspace_destroy(fd_workspace *ws) {
+    if (!ws) return FD_ERR_ARG;
+    const cudaError_t e = cudaFree(ws->base);
+    delete ws;
+    return e == cudaSuccess ? FD_OK : FD_ERR_CUDA;
+}
+
+int fd_get_device_status(fd_workspace *ws, int32_t *status) {
+    if (!ws || !status) return FD_ERR_ARG;
+    return cudaMemcpy(status, ws->status, sizeof(int32_t), cudaMemcpyDeviceToHost) == cudaSuccess
+               ? FD_OK : FD_ERR_CUDA;
+}
+
+int32_t fd_auto_num_ctas(int32_t kernel, int32_t head_dim, int32_t kv_dtype, int32_t rows,
+                         int64_t max_tiles) {
+    (void)head_dim; (void)kv_dtype; (void)rows;
+    return auto_ctas(kernel, max_tiles);
+}
+
+int32_t fd_tile_tokens(int32_t kernel, int32_t head_dim, int32_t kv_dtype) {
+    (void)head_dim; (void)kv_dtype;
+    return kernel_tile(kernel);
+}
+
+int64_t fd_plan(const int64_t *seg_len, int64_t nseg, int32_t tile_tokens, int32_t num_ctas,
+                int32_t *first_cta, int32_t *n_pieces) {
+    if (!seg_len || nseg < 0 || tile_tokens < 1 || num_ctas < 1 || !first_cta || !n_pieces)
+        return FD_ERR_ARG;
+    int64_t total = 0;
+    for (int64_t s = 0; s < nseg; ++s) {
+        if (seg_len[s] < 0) return FD_ERR_ARG;
+        total += fd::ceil_div(seg_len[s], tile_tokens);
+    }
+    const fd::Split sp{total, fd::working_blocks(total, num_ctas)};
+    int64_t first = 0;
+    for (int64_t s = 0; s < nseg; ++s) {
+        const int64_t n = fd::ceil_div(seg_len[s], tile_tokens);
+        if (n == 0) {
+            first_cta[s] = (int32_t)(s % num_ctas);   // block that zeroes it
+            n_pieces[s] = 0;
+        } else {
+            const int32_t a = sp.owner(first), b = sp.owner(first + n - 1);
+            first_cta[s] = a;
+            n_pieces[s] = b - a + 1;
+        }
+        first += n;
+    }
+    return total;
+}
+
+const char *fd_status_string(int status) {
+    switch (status) {
+        case FD_OK: return "ok";
+        case FD_ERR_ARG: return "invalid argument";
+        case FD_ERR_UNSUPPORTED: return "unsupported head_dim, query rows or group size";
+        case FD_ERR_ALIGN: return "cache pointer or stride not 16-byte aligned";
+        case FD_ERR_WORKSPACE: return "missing or too small workspace";
+        case FD_ERR_CUDA: return "CUDA runtime error";
+        default: return "unknown status";
+    }
+}
+
+int32_t fd_version(void) { return kVersion; }
+
+}  // extern "C"

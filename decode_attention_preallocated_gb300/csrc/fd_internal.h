@@ -1,0 +1,81 @@
+// fd_internal.h -- launch parameters and the split-KV partitioner, shared by
+// the host launcher and the kernels (plain C++, usable from host and device).
+#pragma once
+
+#include <stdint.h>
+
+#ifdef __CUDACC__
+#define FD_HD __host__ __device__ __forceinline__
+#else
+#define FD_HD inline
+#endif
+
+namespace fd {
+
+enum Mode : int32_t { kDense = 0, kGather = 1 };
+
+// Everything a kernel needs, passed by value as one __grid_constant__ block.
+struct Params {
+    // problem
+    int32_t B, n_q, Hq, Hkv, g, d;
+    int64_t cap;
+    int32_t rows;          // query rows per segment: g*n_q (dense) or g (gather)
+    int32_t mode;          // Mode
+    int32_t causal;
+    int32_t kv_int8;
+    int32_t out_f32;
+    int32_t tile;          // cache positions per tile
+    float scale_log2;      // scale * log2(e): scores are kept in the log2 domain
+    int32_t idx_len;
+    int64_t nseg;          // segments: B*Hkv (dense) or B*n_q*Hkv (gather)
+    // tensors (strides in elements)
+    const uint16_t *q;     int64_t qs[4];
+    const void *k;         int64_t ks[4];
+    const void *v;         int64_t vs[4];
+    const float *k_scale;  int64_t kss[3];
+    const float *v_scale;  int64_t vss[3];
+    const int32_t *kv_lengths;
+    const int32_t *idx;
+    void *out;             int64_t os[4];
+    // workspace
+    int32_t *counters;     // [nseg], zero between launches
+    int32_t *status;       // sticky FD_DEV_* bits
+    float *partials;       // [(nseg + num_ctas - 1) * slot_floats(rows, d)]
+};
+
+// Balanced split of `total` tiles over G thread blocks: block c takes tiles
+// [start(c), start(c+1)).  A (sequence, kv head) segment whose tiles straddle
+// block boundaries is shared by several blocks ("pieces"); piece (s, c) uses
+// workspace slot s + c, which is unique because block ranges are ordered the
+// same way as segments.
+struct Split {
+    int64_t total;
+    int32_t G;
+    FD_HD int64_t start(int32_t c) const { return (int64_t)c * total / G; }
+    // The block whose range holds tile t (0 <= t < total).
+    FD_HD int32_t owner(int64_t t) const {
+        return (int32_t)(((t + 1) * (int64_t)G + total - 1) / total - 1);
+    }
+};
+
+FD_HD int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Floats in one workspace slot: O[rows][d], then m[rows] and l[rows], padded
+// so that every slot starts on a 16-byte boundary.
+FD_HD int64_t slot_floats(int64_t rows, int64_t d) {
+    return rows * d + ((2 * rows + 3) / 4) * 4;
+}
+
+// Blocks that get work: never more than there are tiles, so every working
+// block owns at least one tile and the blocks sharing a segment are
+// consecutive.
+FD_HD int32_t working_blocks(int64_t total, int32_t grid) {
+    return total < (int64_t)grid ? (int32_t)total : grid;
+}
+
+// Length of sequence b after clamping to [0, cap].
+FD_HD int64_t clamp_len(int64_t L, int64_t cap) {
+    return L < 0 ? 0 : (L > cap ? cap : L);
+}
+
+}  // namespace fd

@@ -1,0 +1,14 @@
+// fd_launch.h -- kernel launchers called by the C ABI layer (fd_api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "fd_internal.h"
+
+namespace fd {
+
+// CUDA-core kernel (fd_simt.cu): every mode, head_dim 128 / 256.
+int simt_tile_tokens();
+int launch_simt(const Params &p, int num_ctas, cudaStream_t stream);
+
+}  // namespace fd

@@ -1,0 +1,385 @@
+// fd_simt.cu -- CUDA-core decode kernel: every mode (dense prefix, causal
+// window, index gather, int8 cache), head_dim 128 and 256.
+//
+// One thread block walks a contiguous range of 32-position tiles chosen by
+// the balanced split partitioner (fd_internal.h).  Per tile it stages K and
+// V in shared memory, computes the scores of every packed query row of the
+// segment (GQA heads x window rows) against the tile, runs one step of the
+// online softmax, and accumulates P.V in registers.  A segment that spans
+// several blocks is finished by the last block to arrive (comfy-kitchen
+// #239, "GQA decode": splits combined inside the same launch).
+#include <cuda_runtime.h>
+
+#include "fd_device.cuh"
+#include "fd_launch.h"
+
+namespace fd {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int T = 32;          // cache positions per tile
+
+template <int D>
+struct Layout {
+    static constexpr int KST = D + 8;                 // padded K/V row (bf16)
+    static constexpr int PV_CG = D / 8;               // threads across one row
+    static constexpr int PV_RG = kThreads / PV_CG;    // row groups
+    static constexpr int PV_RMAX = (64 + PV_RG - 1) / PV_RG;
+    static constexpr int QK_RMAX = 64 / kWarps;
+    static size_t smem_bytes(int rows) {
+        return (size_t)rows * D * 4          // Q (fp32)
+               + 2 * (size_t)T * KST * 2     // K, V tiles (bf16)
+               + (size_t)T * 8               // positions (int64, 8-byte aligned here)
+               + (size_t)rows * (T + 1) * 4  // P
+               + 3 * (size_t)T * 4           // k scale, v scale, valid
+               + 3 * (size_t)rows * 4;       // m, l, alpha
+    }
+};
+
+__device__ __forceinline__ void unpack8(const uint4 &w, float *f) {
+    f[0] = bf16lo(w.x); f[1] = bf16hi(w.x);
+    f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
+    f[4] = bf16lo(w.z); f[5] = bf16hi(w.z);
+    f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
+}
+
+// int8 code -> bf16 bits (exact: |code| <= 128 needs 8 significant bits).
+__device__ __forceinline__ uint32_t i8pair_to_bf16x2(int lo, int hi) {
+    return pack_bf16x2((float)lo, (float)hi);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+simt_kernel(const __grid_constant__ Params p) {
+    using Ly = Layout<D>;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int rows = p.rows;
+    // Q, K and V sizes are multiples of 16 bytes, so the int64 positions
+    // that follow them are aligned whatever the row count.
+    float *Qs = reinterpret_cast<float *>(smem);
+    uint16_t *Ks = reinterpret_cast<uint16_t *>(Qs + rows * D);
+    uint16_t *Vs = Ks + T * Ly::KST;
+    int64_t *tpos = reinterpret_cast<int64_t *>(Vs + T * Ly::KST);
+    float *Ps = reinterpret_cast<float *>(tpos + T);
+    float *ksc = Ps + rows * (T + 1);
+    float *vsc = ksc + T;
+    int *tval = reinterpret_cast<int *>(vsc + T);
+    float *m_s = reinterpret_cast<float *>(tval + T);
+    float *l_s = m_s + rows;
+    float *a_s = l_s + rows;
+
+    __shared__ int64_t sh_total, sh_seg, sh_first, sh_n;
+    __shared__ int sh_last;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x, c = blockIdx.x;
+
+    if (warp == 0) {
+        int64_t tot = total_tiles_warp(p);
+        if (lane == 0) sh_total = tot;
+    }
+    __syncthreads();
+    const int64_t total = sh_total;
+
+    // Segments with nothing to attend still need their output rows zeroed.
+    for (int64_t s = c; s < p.nseg; s += G)
+        if (seg_tiles(p, s) == 0) zero_segment(p, s);
+    if (total == 0) return;
+
+    const int32_t Gw = working_blocks(total, G);
+    if (c >= Gw) return;
+    const Split sp{total, Gw};
+    const int64_t t_begin = sp.start(c), t_end = sp.start(c + 1);
+
+    // PV ownership: thread -> 8 dims of up to PV_RMAX rows.
+    const int cg = tid % Ly::PV_CG, rg = tid / Ly::PV_CG;
+
+    int64_t t = t_begin;
+    while (t < t_end) {
+        __syncthreads();
+        if (warp == 0) {
+            SegPos pos;
+            int64_t s = seg_of_tile_warp(p, t, &pos);
+            if (lane == 0) { sh_seg = s; sh_first = pos.first; sh_n = pos.ntiles; }
+        }
+        __syncthreads();
+        const int64_t s = sh_seg, first = sh_first, nt = sh_n;
+        if (s < 0 || nt <= 0) break;   // cannot happen for t < total
+        const int64_t piece_end = min(t_end, first + nt);
+        const int c_first = sp.owner(first), c_last = sp.owner(first + nt - 1);
+        const int npieces = c_last - c_first + 1;
+
+        // Segment geometry.
+        const RowMap m0 = row_of(p, s, 0);
+        const int b = m0.b;
+        const int hk = (int)(s % p.Hkv);
+        const int64_t len = p.mode == kGather ? (int64_t)p.idx_len : seq_len(p, b);
+        const int32_t *list = p.mode == kGather
+                                  ? p.idx + ((int64_t)b * p.n_q + m0.i) * p.idx_len
+                                  : nullptr;
+
+        // Q rows of the segment (fp32) and fresh softmax state.
+        for (int e = tid; e < rows * D; e += kThreads) {
+            const int r = e / D, dd = e % D;
+            const RowMap m = row_of(p, s, r);
+            const uint16_t bits = p.q[(int64_t)m.b * p.qs[0] + (int64_t)m.i * p.qs[1] +
+                                      (int64_t)m.h * p.qs[2] + dd];
+            Qs[e] = __uint_as_float((uint32_t)bits << 16);
+        }
+        if (tid < rows) { m_s[tid] = neg_inf(); l_s[tid] = 0.f; a_s[tid] = 1.f; }
+
+        float O[Ly::PV_RMAX][8];
+#pragma unroll
+        for (int k = 0; k < Ly::PV_RMAX; ++k)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) O[k][e] = 0.f;
+
+        const char *kbase = reinterpret_cast<const char *>(p.k);
+        const char *vbase = reinterpret_cast<const char *>(p.v);
+        const int esz = p.kv_int8 ? 1 : 2;
+        const int64_t kb_off = (int64_t)b * p.ks[0] + (int64_t)hk * p.ks[1];
+        const int64_t vb_off = (int64_t)b * p.vs[0] + (int64_t)hk * p.vs[1];
+
+        for (int64_t tt = t - first; tt < piece_end - first; ++tt) {
+            const int64_t j0 = tt * T;
+            const int ntok = (int)min((int64_t)T, len - j0);
+            __syncthreads();   // previous tile fully consumed
+            if (tid < T) {
+                int64_t pos = j0 + tid;
+                int ok = tid < ntok;
+                if (ok && list) {
+                    const int64_t cell = list[pos];
+                    if (cell >= p.cap) atomicOr(p.status, kDevBadIndex);
+                    ok = cell >= 0 && cell < p.cap;
+                    pos = cell;
+                }
+                tpos[tid] = ok ? pos : 0;
+                tval[tid] = ok;
+                float kscale = 1.f, vscale = 1.f;
+                if (ok && p.kv_int8) {
+                    kscale = p.k_scale[(int64_t)b * p.kss[0] + (int64_t)hk * p.kss[1] + pos * p.kss[2]];
+                    vscale = p.v_scale[(int64_t)b * p.vss[0] + (int64_t)hk * p.vss[1] + pos * p.vss[2]];
+                }
+                ksc[tid] = kscale;
+                vsc[tid] = vscale;
+            }
+            __syncthreads();
+            // Stage the K and V rows (zeros for positions that are not visible).
+            if (!p.kv_int8) {
+                constexpr int CPR = D / 8;   // 16-byte chunks per row
+                for (int e = tid; e < 2 * T * CPR; e += kThreads) {
+                    const int which = e / (T * CPR);
+                    const int jj = (e / CPR) % T, cc = e % CPR;
+                    uint4 w = make_uint4(0, 0, 0, 0);
+                    if (tval[jj]) {
+                        const char *src = which
+                            ? vbase + (vb_off + tpos[jj] * p.vs[2] + cc * 8) * 2
+                            : kbase + (kb_off + tpos[jj] * p.ks[2] + cc * 8) * 2;
+                        w = ldg_stream(src);
+                    }
+                    uint16_t *dst = (which ? Vs : Ks) + jj * Ly::KST + cc * 8;
+                    *reinterpret_cast<uint4 *>(dst) = w;
+                }
+            } else {
+                constexpr int CPR = D / 16;
+                for (int e = tid; e < 2 * T * CPR; e += kThreads) {
+                    const int which = e / (T * CPR);
+                    const int jj = (e / CPR) % T, cc = e % CPR;
+                    uint4 w = make_uint4(0, 0, 0, 0);
+                    if (tval[jj]) {
+                        const char *src = which
+                            ? vbase + (vb_off + tpos[jj] * p.vs[2] + cc * 16)
+                            : kbase + (kb_off + tpos[jj] * p.ks[2] + cc * 16);
+                        w = ldg_stream(src);
+                    }
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                    uint32_t o[8];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int8_t *by = reinterpret_cast<const int8_t *>(&ws[q4]);
+                        o[2 * q4] = i8pair_to_bf16x2(by[0], by[1]);
+                        o[2 * q4 + 1] = i8pair_to_bf16x2(by[2], by[3]);
+                    }
+                    uint16_t *dst = (which ? Vs : Ks) + jj * Ly::KST + cc * 16;
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            }
+            (void)esz;
+            __syncthreads();
+
+            // Scores: warp w owns rows w, w+8, ...; lane = position in tile.
+            float acc[Ly::QK_RMAX];
+#pragma unroll
+            for (int k = 0; k < Ly::QK_RMAX; ++k) acc[k] = 0.f;
+#pragma unroll 4
+            for (int cc = 0; cc < D / 8; ++cc) {
+                float kf[8];
+                unpack8(*reinterpret_cast<const uint4 *>(Ks + lane * Ly::KST + cc * 8), kf);
+#pragma unroll
+                for (int k = 0; k < Ly::QK_RMAX; ++k) {
+                    const int r = warp + kWarps * k;
+                    if (r < rows) {
+                        const float4 qa = *reinterpret_cast<const float4 *>(Qs + r * D + cc * 8);
+                        const float4 qb = *reinterpret_cast<const float4 *>(Qs + r * D + cc * 8 + 4);
+                        acc[k] += qa.x * kf[0] + qa.y * kf[1] + qa.z * kf[2] + qa.w * kf[3] +
+                                  qb.x * kf[4] + qb.y * kf[5] + qb.z * kf[6] + qb.w * kf[7];
+                    }
+                }
+            }
+            // Mask and one online-softmax step per row (same warp owns the row).
+#pragma unroll
+            for (int k = 0; k < Ly::QK_RMAX; ++k) {
+                const int r = warp + kWarps * k;
+                if (r < rows) {
+                    bool vis = tval[lane] != 0;
+                    if (p.causal && p.mode == kDense) {
+                        const int i = r % p.n_q;
+                        vis = vis && tpos[lane] <= len - p.n_q + i;
+                    }
+                    const float sc = vis ? acc[k] * ksc[lane] * p.scale_log2 : neg_inf();
+                    float tmax = sc;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+                    const float m_old = m_s[r];
+                    const float m_new = fmaxf(m_old, tmax);
+                    const float m_use = m_new == neg_inf() ? 0.f : m_new;
+                    const float alpha = fast_exp2(m_old - m_use);
+                    const float pr = vis ? fast_exp2(sc - m_use) : 0.f;
+                    float psum = pr;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1)
+                        psum += __shfl_xor_sync(0xffffffffu, psum, o);
+                    Ps[r * (T + 1) + lane] = pr * vsc[lane];
+                    __syncwarp();
+                    if (lane == 0) {
+                        m_s[r] = m_new;
+                        l_s[r] = l_s[r] * alpha + psum;
+                        a_s[r] = alpha;
+                    }
+                }
+            }
+            __syncthreads();
+
+            // O = alpha * O + P . V
+#pragma unroll
+            for (int k = 0; k < Ly::PV_RMAX; ++k) {
+                const int r = rg + Ly::PV_RG * k;
+                if (r < rows) {
+                    const float a = a_s[r];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) O[k][e] *= a;
+                }
+            }
+            for (int jj = 0; jj < ntok; ++jj) {
+                float vf[8];
+                unpack8(*reinterpret_cast<const uint4 *>(Vs + jj * Ly::KST + cg * 8), vf);
+#pragma unroll
+                for (int k = 0; k < Ly::PV_RMAX; ++k) {
+                    const int r = rg + Ly::PV_RG * k;
+                    if (r < rows) {
+                        const float pw = Ps[r * (T + 1) + jj];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) O[k][e] += pw * vf[e];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- finish the piece
+        if (npieces == 1) {
+#pragma unroll
+            for (int k = 0; k < Ly::PV_RMAX; ++k) {
+                const int r = rg + Ly::PV_RG * k;
+                if (r < rows) {
+                    const float l = l_s[r];
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    float o[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = O[k][e] * inv;
+                    store_out8(p, row_of(p, s, r), cg * 8, o);
+                }
+            }
+        } else {
+            float *slot = slot_ptr(p, s, c);
+#pragma unroll
+            for (int k = 0; k < Ly::PV_RMAX; ++k) {
+                const int r = rg + Ly::PV_RG * k;
+                if (r < rows) {
+                    float4 *dst = reinterpret_cast<float4 *>(slot + r * D + cg * 8);
+                    dst[0] = make_float4(O[k][0], O[k][1], O[k][2], O[k][3]);
+                    dst[1] = make_float4(O[k][4], O[k][5], O[k][6], O[k][7]);
+                }
+            }
+            if (tid < rows) {
+                slot[rows * D + tid] = m_s[tid];
+                slot[rows * D + rows + tid] = l_s[tid];
+            }
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) {
+                const int old = atomicAdd(p.counters + s, 1);
+                sh_last = old == npieces - 1;
+            }
+            __syncthreads();
+            if (sh_last) {
+                __threadfence();
+#pragma unroll
+                for (int k = 0; k < Ly::PV_RMAX; ++k) {
+                    const int r = rg + Ly::PV_RG * k;
+                    if (r < rows) {
+                        float M = neg_inf();
+                        for (int c2 = c_first; c2 <= c_last; ++c2)
+                            M = fmaxf(M, __ldcg(slot_ptr(p, s, c2) + rows * D + r));
+                        float o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                        if (M != neg_inf()) {
+                            float lsum = 0.f;
+                            for (int c2 = c_first; c2 <= c_last; ++c2) {
+                                const float *sl = slot_ptr(p, s, c2);
+                                const float w = fast_exp2(__ldcg(sl + rows * D + r) - M);
+                                lsum += w * __ldcg(sl + rows * D + rows + r);
+                                const float4 a = __ldcg(reinterpret_cast<const float4 *>(sl + r * D + cg * 8));
+                                const float4 bq = __ldcg(reinterpret_cast<const float4 *>(sl + r * D + cg * 8 + 4));
+                                o[0] += w * a.x; o[1] += w * a.y; o[2] += w * a.z; o[3] += w * a.w;
+                                o[4] += w * bq.x; o[5] += w * bq.y; o[6] += w * bq.z; o[7] += w * bq.w;
+                            }
+                            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) o[e] *= inv;
+                        }
+                        store_out8(p, row_of(p, s, r), cg * 8, o);
+                    }
+                }
+                if (tid == 0) p.counters[s] = 0;
+            }
+        }
+        t = piece_end;
+    }
+}
+
+template <int D>
+int launch_d(const Params &p, int G, cudaStream_t st) {
+    const size_t smem = Layout<D>::smem_bytes(p.rows);
+    cudaError_t e = cudaFuncSetAttribute(simt_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return -5;
+    simt_kernel<D><<<G, kThreads, smem, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+}
+
+}  // namespace
+
+int simt_tile_tokens() { return T; }
+
+int launch_simt(const Params &p, int G, cudaStream_t st) {
+    if (p.d == 128) return launch_d<128>(p, G, st);
+    if (p.d == 256) return launch_d<256>(p, G, st);
+    return -2;
+}
+
+}  // namespace fd

@@ -1,0 +1,331 @@
+"""ctypes binding of libfd.so (the C ABI in include/fd.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels inside libfd.so.  PyTorch supplies device memory and the current
+stream.  There is no fallback: if libfd.so is missing or cannot be loaded,
+every call raises.
+
+Low-level names mirror the C ABI (``fd_decode``, ``fd_decode_int8``,
+``fd_decode_gather``, ``fd_workspace_create`` ...) and take ``FdTensor`` /
+``FdOpts`` structures; ``decode``, ``decode_int8`` and ``decode_gather`` take
+torch tensors, allocate ``out`` with torch when it is not given, and keep one
+workspace per (device, stream).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfd.so")
+
+# constants from include/fd.h
+FD_OK, FD_ERR_ARG, FD_ERR_UNSUPPORTED, FD_ERR_ALIGN, FD_ERR_WORKSPACE, FD_ERR_CUDA = 0, -1, -2, -3, -4, -5
+FD_BF16, FD_F32, FD_I8, FD_I32 = 0, 1, 2, 3
+FD_DEV_BAD_LENGTH, FD_DEV_BAD_INDEX = 1, 2
+FD_KERNEL_AUTO, FD_KERNEL_SIMT, FD_KERNEL_TC = 0, 1, 2
+FD_MAX_ROWS = 64
+
+_DTYPES = {torch.bfloat16: FD_BF16, torch.float32: FD_F32, torch.int8: FD_I8,
+           torch.int32: FD_I32}
+
+
+class FdTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32),
+                ("ndim", ctypes.c_int32), ("shape", ctypes.c_int64 * 4),
+                ("stride", ctypes.c_int64 * 4)]
+
+
+class FdOpts(ctypes.Structure):
+    _fields_ = [("stream", ctypes.c_void_p), ("ws", ctypes.c_void_p),
+                ("num_ctas", ctypes.c_int32), ("kernel", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("reserved", ctypes.c_int32 * 3)]
+
+
+class FdError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (what, status_string(code), code))
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+# (name, restype, argtypes) for every symbol declared in include/fd.h
+_P = ctypes.POINTER
+_SIGNATURES = [
+    ("fd_decode", ctypes.c_int,
+     [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_int32,
+      ctypes.c_int32, ctypes.c_float, _P(FdTensor), _P(FdOpts)]),
+    ("fd_decode_int8", ctypes.c_int,
+     [_P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor),
+      ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+      _P(FdTensor), _P(FdOpts)]),
+    ("fd_decode_gather", ctypes.c_int,
+     [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_int32,
+      _P(FdTensor), _P(FdOpts)]),
+    ("fd_workspace_bytes", ctypes.c_size_t,
+     [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    ("fd_workspace_create", ctypes.c_int,
+     [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+      ctypes.c_void_p, _P(ctypes.c_void_p)]),
+    ("fd_workspace_reset", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    ("fd_workspace_destroy", ctypes.c_int, [ctypes.c_void_p]),
+    ("fd_get_device_status", ctypes.c_int, [ctypes.c_void_p, _P(ctypes.c_int32)]),
+    ("fd_auto_num_ctas", ctypes.c_int32,
+     [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64]),
+    ("fd_tile_tokens", ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    ("fd_plan", ctypes.c_int64,
+     [_P(ctypes.c_int64), ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+      _P(ctypes.c_int32), _P(ctypes.c_int32)]),
+    ("fd_status_string", ctypes.c_char_p, [ctypes.c_int]),
+    ("fd_version", ctypes.c_int32, []),
+]
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfd.so (raises if it has not been built)."""
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    "libfd.so is not built (%s); run "
+                    "decode_attention_preallocated_gb300.build.build()" % LIB_PATH)
+            h = ctypes.CDLL(LIB_PATH)
+            for name, res, args in _SIGNATURES:
+                fn = getattr(h, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = h
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().fd_status_string(int(code)).decode()
+
+
+# ------------------------------------------------------------- marshalling
+def as_fd_tensor(t: torch.Tensor) -> FdTensor:
+    if t.dtype not in _DTYPES:
+        raise TypeError("unsupported dtype %s" % t.dtype)
+    if t.dim() > 4:
+        raise ValueError("at most 4 dimensions")
+    ft = FdTensor()
+    ft.data = t.data_ptr()
+    ft.dtype = _DTYPES[t.dtype]
+    ft.ndim = t.dim()
+    for i in range(t.dim()):
+        ft.shape[i] = t.shape[i]
+        ft.stride[i] = t.stride(i)
+    return ft
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+def _check(code: int, what: str):
+    if code != FD_OK:
+        raise FdError(code, what)
+
+
+# -------------------------------------------------------------- workspace
+class Workspace:
+    """Owns one fd_workspace (device memory allocated by libfd.so).
+
+    Size it for the largest call it will serve; a call that needs more fails
+    with FD_ERR_WORKSPACE.  Create it before capturing a CUDA graph.
+    """
+
+    def __init__(self, max_segments: int, max_rows: int, head_dim: int,
+                 max_ctas: int, stream: Optional[torch.cuda.Stream] = None,
+                 device=None):
+        self.max_segments, self.max_rows = int(max_segments), int(max_rows)
+        self.head_dim, self.max_ctas = int(head_dim), int(max_ctas)
+        self.device = torch.device("cuda", torch.cuda.current_device()) \
+            if device is None else torch.device(device)
+        h = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            _check(lib().fd_workspace_create(self.max_segments, self.max_rows,
+                                             self.head_dim, self.max_ctas,
+                                             _stream_handle(stream, self.device),
+                                             ctypes.byref(h)),
+                   "fd_workspace_create")
+        self.handle = h
+
+    def fits(self, segments, rows, head_dim, ctas) -> bool:
+        return (segments <= self.max_segments and rows <= self.max_rows
+                and head_dim <= self.head_dim and ctas <= self.max_ctas)
+
+    def reset(self, stream=None):
+        _check(lib().fd_workspace_reset(self.handle, _stream_handle(stream, self.device)),
+               "fd_workspace_reset")
+
+    def device_status(self) -> int:
+        st = ctypes.c_int32(0)
+        with torch.cuda.device(self.device):
+            _check(lib().fd_get_device_status(self.handle, ctypes.byref(st)),
+                   "fd_get_device_status")
+        return int(st.value)
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            with torch.cuda.device(self.device):
+                torch.cuda.synchronize(self.device)
+                lib().fd_workspace_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):  # pragma: no cover - best effort at interpreter exit
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+_ws_cache = {}
+_ws_lock = threading.Lock()
+
+
+def workspace_for(device, stream_handle, segments, rows, head_dim, ctas) -> Workspace:
+    """Workspace shared by calls on one (device, stream); grown when needed
+    (growth synchronises the device, so size it up front for graph capture)."""
+    key = (torch.device(device).index, int(stream_handle))
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None or not ws.fits(segments, rows, head_dim, ctas):
+            want = dict(max_segments=max(segments, 64), max_rows=max(rows, 16),
+                        head_dim=max(head_dim, 256), max_ctas=max(ctas, 1024))
+            if ws is not None:
+                want = dict(max_segments=max(want["max_segments"], ws.max_segments),
+                            max_rows=max(want["max_rows"], ws.max_rows),
+                            head_dim=max(want["head_dim"], ws.head_dim),
+                            max_ctas=max(want["max_ctas"], ws.max_ctas))
+                ws.close()
+            ws = Workspace(device=device, **want)
+            _ws_cache[key] = ws
+        return ws
+
+
+def auto_num_ctas(kernel=FD_KERNEL_AUTO, head_dim=128, kv_dtype=FD_BF16, rows=1,
+                  max_tiles=0) -> int:
+    return int(lib().fd_auto_num_ctas(kernel, head_dim, kv_dtype, rows, max_tiles))
+
+
+def tile_tokens(kernel=FD_KERNEL_AUTO, head_dim=128, kv_dtype=FD_BF16) -> int:
+    return int(lib().fd_tile_tokens(kernel, head_dim, kv_dtype))
+
+
+def plan(seg_len, tile, num_ctas):
+    """Host mirror of the device partitioner: (total tiles, first block of
+    each segment, number of blocks sharing each segment)."""
+    n = len(seg_len)
+    arr = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in seg_len])
+    first = (ctypes.c_int32 * max(n, 1))()
+    pieces = (ctypes.c_int32 * max(n, 1))()
+    total = lib().fd_plan(arr, n, int(tile), int(num_ctas), first, pieces)
+    if total < 0:
+        raise FdError(int(total), "fd_plan")
+    return int(total), list(first)[:n], list(pieces)[:n]
+
+
+# ---------------------------------------------------------- torch wrappers
+def _opts(stream_handle, ws, num_ctas, kernel, scale=0.0) -> FdOpts:
+    o = FdOpts()
+    o.stream = stream_handle
+    o.ws = ws.handle
+    o.num_ctas = int(num_ctas)
+    o.kernel = int(kernel)
+    o.scale = float(scale)
+    return o
+
+
+def _prepare(q, k, out, out_dtype, segments, rows, num_ctas, kernel, stream, ws):
+    if not q.is_cuda:
+        raise ValueError("q must be a CUDA tensor")
+    device = q.device
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=device)
+    sh = _stream_handle(stream, device)
+    ctas = num_ctas
+    if ctas == 0:
+        with torch.cuda.device(device):
+            ctas = auto_num_ctas(kernel, q.shape[-1], _DTYPES.get(k.dtype, FD_BF16), rows, 0)
+    if ws is None:
+        ws = workspace_for(device, sh, segments, rows, q.shape[-1], max(ctas, 1))
+    return out, sh, ws
+
+
+def decode(q, k_cache, v_cache, kv_lengths, n_q=None, causal=False, scale=None,
+           out=None, out_dtype=torch.bfloat16, num_ctas=0, kernel=FD_KERNEL_AUTO,
+           stream=None, workspace: Optional[Workspace] = None):
+    """Attention of q [B, n_q, Hq, d] over the first kv_lengths[b] positions of
+    k_cache / v_cache [B, Hkv, cap, d] (bf16).  kv_lengths: int32 [B] on the
+    device.  Returns out [B, n_q, Hq, d]."""
+    B, nq, Hq, d = q.shape
+    n_q = nq if n_q is None else n_q
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    Hkv = k_cache.shape[1]
+    rows = (Hq // max(Hkv, 1)) * nq
+    out, sh, ws = _prepare(q, k_cache, out, out_dtype, B * Hkv, rows, num_ctas,
+                           kernel, stream, workspace)
+    tq, tk, tv, to = map(as_fd_tensor, (q, k_cache, v_cache, out))
+    o = _opts(sh, ws, num_ctas, kernel)
+    with torch.cuda.device(q.device):
+        rc = lib().fd_decode(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                             kv_lengths.data_ptr(), int(n_q), int(bool(causal)),
+                             float(scale), ctypes.byref(to), ctypes.byref(o))
+    _check(rc, "fd_decode")
+    return out
+
+
+def decode_int8(q, k_cache, v_cache, k_scale, v_scale, kv_lengths, n_q=None,
+                causal=False, scale=None, out=None, out_dtype=torch.bfloat16,
+                num_ctas=0, kernel=FD_KERNEL_AUTO, stream=None,
+                workspace: Optional[Workspace] = None):
+    """As ``decode`` for an int8 cache with fp32 scales [B, Hkv, cap]."""
+    B, nq, Hq, d = q.shape
+    n_q = nq if n_q is None else n_q
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    Hkv = k_cache.shape[1]
+    rows = (Hq // max(Hkv, 1)) * nq
+    out, sh, ws = _prepare(q, k_cache, out, out_dtype, B * Hkv, rows, num_ctas,
+                           kernel, stream, workspace)
+    tq, tk, tv, tks, tvs, to = map(as_fd_tensor, (q, k_cache, v_cache, k_scale, v_scale, out))
+    o = _opts(sh, ws, num_ctas, kernel)
+    with torch.cuda.device(q.device):
+        rc = lib().fd_decode_int8(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                  ctypes.byref(tks), ctypes.byref(tvs),
+                                  kv_lengths.data_ptr(), int(n_q), int(bool(causal)),
+                                  float(scale), ctypes.byref(to), ctypes.byref(o))
+    _check(rc, "fd_decode_int8")
+    return out
+
+
+def decode_gather(q, k_cache, v_cache, idx, scale=None, out=None,
+                  out_dtype=torch.bfloat16, num_ctas=0, kernel=FD_KERNEL_AUTO,
+                  stream=None, workspace: Optional[Workspace] = None):
+    """Attention of q [B, n_q, Hq, d] over the cache cells listed in
+    idx [B, n_q, K] (int32, contiguous, on the device; < 0 = padding)."""
+    B, nq, Hq, d = q.shape
+    Hkv = k_cache.shape[1]
+    if not idx.is_contiguous() or idx.dtype != torch.int32 or idx.dim() != 3:
+        raise ValueError("idx must be a contiguous int32 [B, n_q, K] tensor")
+    rows = Hq // max(Hkv, 1)
+    out, sh, ws = _prepare(q, k_cache, out, out_dtype, B * nq * Hkv, rows, num_ctas,
+                           kernel, stream, workspace)
+    tq, tk, tv, to = map(as_fd_tensor, (q, k_cache, v_cache, out))
+    o = _opts(sh, ws, num_ctas, kernel, 0.0 if scale is None else scale)
+    with torch.cuda.device(q.device):
+        rc = lib().fd_decode_gather(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                    idx.data_ptr(), int(idx.shape[2]), ctypes.byref(to),
+                                    ctypes.byref(o))
+    _check(rc, "fd_decode_gather")
+    return out

@@ -1,0 +1,200 @@
+/*
+ * fd.h -- C ABI of libfd.so: length-aware GQA decode attention over a
+ * preallocated KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * What the calls compute.  For sequence b, query row i, query head h and
+ * kv head hk = h / (Hq / Hkv):
+ *
+ *     out[b,i,h,:] = sum_{j in V} softmax_j(scale * q[b,i,h,:] . k[b,hk,j,:]) v[b,hk,j,:]
+ *
+ * over the visible cache positions V, and 0 where V is empty.
+ *   - fd_decode / fd_decode_int8: V = the filled prefix 0 .. L-1 with
+ *     L = kv_lengths[b] read on the device, so the call never touches the
+ *     unused tail of the cache ("Qwen3.5 text generation attends over the
+ *     full KV capacity", ComfyUI #16509: problem statement and the
+ *     length-aware FixedKV path).  With causal != 0 the n_q query rows are
+ *     the newest n_q positions of the cache (the decode token plus MTP
+ *     drafts already written at L-n_q .. L-1) and row i sees 0 .. L-n_q+i
+ *     (same issue, list item 2 and "Existing Solutions": a bottom-right
+ *     aligned causal window, up to 6 rows).
+ *   - fd_decode_gather: V = the cells listed for that (b, i) in idx
+ *     ("attend the selected cells instead of masking the window",
+ *     llama.cpp #28244, Conversation; "gather-based sparse attention for
+ *     QSA decode", llama.cpp #28213: per-token lists for multi-row verify).
+ * The prefix is split across thread blocks and the last block to finish a
+ * (sequence, kv head) combines the splits inside the same launch
+ * (comfy-kitchen #239, "GQA decode"); the query heads of one GQA group share
+ * each K/V tile.
+ *
+ * Conventions shared by every call.
+ *   - Tensors are described by fd_tensor: a data pointer, a dtype, 4 sizes
+ *     and 4 strides counted in ELEMENTS.  The innermost (head_dim) stride
+ *     must be 1.  Device pointers unless stated otherwise.
+ *   - q      : [B, n_q, Hq, d] bf16.
+ *   - caches : [B, Hkv, cap, d] bf16 (fd_decode, fd_decode_gather) or int8
+ *              (fd_decode_int8); any strides that are multiples of 16 bytes,
+ *              so the canonical [B, Hkv, cap, d] and the token-major
+ *              [B, cap, Hkv, d] (seen through a transpose) both work; the
+ *              data pointer must be 16-byte aligned.
+ *   - out    : [B, n_q, Hq, d] bf16 or fp32 (round to nearest even for bf16).
+ *   - d (head_dim) is 128 or 256; 1 <= n_q <= 6; Hq % Hkv == 0;
+ *     (Hq / Hkv) * n_q <= 64 query rows share one kv head per launch unit.
+ *   - The caller owns every tensor, kv_lengths and idx.  The library owns
+ *     only the workspace (fd_workspace_create) and never allocates, frees or
+ *     synchronises inside a decode call, and never reads device data on the
+ *     host, so the calls can be captured in a CUDA graph and replayed with
+ *     new lengths or index lists written on the device.
+ *   - Work is queued on opts->stream (a cudaStream_t; NULL = the legacy
+ *     default stream).  One workspace serves one stream at a time.
+ *   - Return value: FD_OK, or a negative FD_ERR_* code.  Every argument is
+ *     checked on the host before any CUDA call; on error nothing is
+ *     launched.  FD_ERR_CUDA reports a launch failure (cudaGetLastError).
+ *   - Bad device-side data (a length outside [0, cap], an index >= cap) never
+ *     faults: the value is clamped or the cell skipped, and a sticky bit is
+ *     set in the workspace status word (fd_get_device_status).
+ */
+#ifndef FD_H
+#define FD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define FD_OK 0
+#define FD_ERR_ARG (-1)          /* null pointer, bad shape/dtype/stride   */
+#define FD_ERR_UNSUPPORTED (-2)  /* head_dim, n_q or group size not served */
+#define FD_ERR_ALIGN (-3)        /* pointer or stride not 16-byte aligned  */
+#define FD_ERR_WORKSPACE (-4)    /* missing or too small workspace         */
+#define FD_ERR_CUDA (-5)         /* CUDA runtime error                     */
+
+/* dtypes */
+#define FD_BF16 0
+#define FD_F32 1
+#define FD_I8 2
+#define FD_I32 3
+
+/* sticky device status bits (fd_get_device_status) */
+#define FD_DEV_BAD_LENGTH 1      /* some kv_lengths[b] outside [0, cap]    */
+#define FD_DEV_BAD_INDEX 2       /* some idx entry >= cap (skipped)        */
+
+/* kernel selection (fd_opts.kernel) */
+#define FD_KERNEL_AUTO 0
+#define FD_KERNEL_SIMT 1         /* CUDA-core kernel, every mode           */
+#define FD_KERNEL_TC 2           /* tensor-core (tcgen05) kernel           */
+
+#define FD_MAX_ROWS 64           /* query rows per kv head per launch unit */
+
+typedef struct fd_tensor {
+    void *data;
+    int32_t dtype;               /* FD_BF16, FD_F32, FD_I8, FD_I32          */
+    int32_t ndim;                /* 1 .. 4                                  */
+    int64_t shape[4];
+    int64_t stride[4];           /* in elements                             */
+} fd_tensor;
+
+/* Opaque device workspace: per-split partial results, one completion counter
+ * per (sequence, kv head) and the sticky status word. */
+typedef struct fd_workspace fd_workspace;
+
+typedef struct fd_opts {
+    void *stream;                /* cudaStream_t, NULL = legacy default      */
+    fd_workspace *ws;            /* required                                 */
+    int32_t num_ctas;            /* 0 = auto (from the SM count); > 0 forces
+                                    the number of thread blocks, which sets
+                                    the split count                          */
+    int32_t kernel;              /* FD_KERNEL_*                              */
+    float scale;                 /* fd_decode_gather only: 0 = 1/sqrt(d)     */
+    int32_t reserved[3];         /* must be zero                             */
+} fd_opts;
+
+/*
+ * Dense prefix decode (bf16 cache).
+ *   q [B, n_q, Hq, d] bf16; k_cache, v_cache [B, Hkv, cap, d] bf16;
+ *   kv_lengths: device int32[B], L_b = number of filled positions;
+ *   n_q: query rows (must equal q->shape[1]); causal: 0 or 1;
+ *   scale: multiplies q.k (usually 1/sqrt(d));
+ *   out [B, n_q, Hq, d] bf16 or fp32.
+ */
+int fd_decode(const fd_tensor *q, const fd_tensor *k_cache,
+              const fd_tensor *v_cache, const int32_t *kv_lengths,
+              int32_t n_q, int32_t causal, float scale, const fd_tensor *out,
+              const fd_opts *opts);
+
+/*
+ * Dense prefix decode over an int8 cache with one fp32 scale per
+ * (sequence, kv head, position): k = k_code * k_scale[b, hk, j], likewise v
+ * (comfy-kitchen #239, commit list: bounded paged INT8 decode cache; the
+ * cache here is not paged).  k_scale, v_scale: fp32 [B, Hkv, cap] with any
+ * strides.  Other arguments as fd_decode.
+ */
+int fd_decode_int8(const fd_tensor *q, const fd_tensor *k_cache,
+                   const fd_tensor *v_cache, const fd_tensor *k_scale,
+                   const fd_tensor *v_scale, const int32_t *kv_lengths,
+                   int32_t n_q, int32_t causal, float scale,
+                   const fd_tensor *out, const fd_opts *opts);
+
+/*
+ * Index-gather decode (bf16 cache).
+ *   idx: device int32 [B, n_q, idx_len], contiguous (may be NULL when idx_len
+ *   is 0: every output row is then 0); one list per (sequence,
+ *   query row), shared by all heads of that row.  Entries < 0 are padding;
+ *   entries >= cap are skipped and flag FD_DEV_BAD_INDEX.  Lists are read as
+ *   given: a cell listed twice counts twice (distinct cells reproduce the
+ *   masked path exactly).  No length and no causal mask apply: the list is
+ *   the visible set.  Scale: opts->scale, or 1/sqrt(d) when 0.
+ */
+int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache,
+                     const fd_tensor *v_cache, const int32_t *idx,
+                     int32_t idx_len, const fd_tensor *out,
+                     const fd_opts *opts);
+
+/*
+ * Workspace.  A launch unit ("segment") is one (sequence, kv head) in the
+ * dense modes and one (sequence, query row, kv head) in gather mode; rows is
+ * the number of query rows sharing it ((Hq/Hkv) * n_q dense, Hq/Hkv gather).
+ * Size for the largest segment count, row count, head_dim and num_ctas any
+ * call will use.  fd_workspace_create allocates device memory (cudaMalloc)
+ * and zeroes the counters on `stream`; it is the only allocating call.
+ */
+size_t fd_workspace_bytes(int64_t max_segments, int32_t max_rows,
+                          int32_t head_dim, int32_t max_ctas);
+int fd_workspace_create(int64_t max_segments, int32_t max_rows,
+                        int32_t head_dim, int32_t max_ctas, void *stream,
+                        fd_workspace **ws);
+/* Clears the completion counters and the status word on `stream` (needed
+ * only after a launch was aborted part-way; every completed launch leaves the
+ * counters at zero). */
+int fd_workspace_reset(fd_workspace *ws, void *stream);
+int fd_workspace_destroy(fd_workspace *ws);
+/* Synchronously reads the sticky status word (FD_DEV_* bits). */
+int fd_get_device_status(fd_workspace *ws, int32_t *status);
+
+/* Number of thread blocks an auto launch would use on the current device
+ * (host query; 0 on error). */
+int32_t fd_auto_num_ctas(int32_t kernel, int32_t head_dim, int32_t kv_dtype,
+                         int32_t rows, int64_t max_tiles);
+/* Cache positions per K/V tile for a kernel / head_dim / cache dtype. */
+int32_t fd_tile_tokens(int32_t kernel, int32_t head_dim, int32_t kv_dtype);
+
+/*
+ * Host mirror of the device split partitioner, for inspection and tests.
+ * For segment lengths seg_len[0..nseg) (positions), tile size and num_ctas,
+ * writes for every segment the first thread block that works on it and the
+ * number of blocks that share it (0 for an empty segment).  Returns the total
+ * tile count, or a negative FD_ERR_* code.
+ */
+int64_t fd_plan(const int64_t *seg_len, int64_t nseg, int32_t tile_tokens,
+                int32_t num_ctas, int32_t *first_cta, int32_t *n_pieces);
+
+const char *fd_status_string(int status);
+int32_t fd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FD_H */

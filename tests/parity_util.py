@@ -1,0 +1,85 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI and
+the fp64 oracle on the same seeded inputs, and compare with the tolerances
+the decode-attention contract states (bf16 output: max |err| <= 1e-2 and
+mean |err| <= 1e-3; fp32 output: max |err| <= 2e-3)."""
+from __future__ import annotations
+
+import torch
+
+import oracle
+from decode_attention_preallocated_gb300 import fd
+
+TOL = {torch.bfloat16: (1e-2, 1e-3), torch.float32: (2e-3, 2e-3)}
+
+
+def to_dev(inp, device="cuda"):
+    """Copy a DecodeInputs to the GPU (keeping strided cache layouts)."""
+    import copy
+    out = copy.copy(inp)
+    for name in ("q", "kv_lengths", "k_scale", "v_scale", "idx"):
+        t = getattr(inp, name)
+        if t is not None:
+            setattr(out, name, t.to(device))
+    for name in ("k", "v"):
+        t = getattr(inp, name)
+        if t.is_contiguous():
+            setattr(out, name, t.to(device))
+        else:
+            # token-major view [B, cap, Hkv, d] seen as [B, Hkv, cap, d]
+            base = t.transpose(1, 2).contiguous().to(device)
+            setattr(out, name, base.transpose(1, 2))
+    return out
+
+
+def run_gpu(inp, out_dtype=torch.bfloat16, num_ctas=0, kernel=fd.FD_KERNEL_AUTO,
+            workspace=None):
+    if inp.idx is not None:
+        return fd.decode_gather(inp.q, inp.k, inp.v, inp.idx, scale=inp.scale,
+                                out_dtype=out_dtype, num_ctas=num_ctas, kernel=kernel,
+                                workspace=workspace)
+    if inp.k.dtype == torch.int8:
+        return fd.decode_int8(inp.q, inp.k, inp.v, inp.k_scale, inp.v_scale,
+                              inp.kv_lengths, n_q=inp.n_q, causal=inp.causal,
+                              scale=inp.scale, out_dtype=out_dtype, num_ctas=num_ctas,
+                              kernel=kernel, workspace=workspace)
+    return fd.decode(inp.q, inp.k, inp.v, inp.kv_lengths, n_q=inp.n_q,
+                     causal=inp.causal, scale=inp.scale, out_dtype=out_dtype,
+                     num_ctas=num_ctas, kernel=kernel, workspace=workspace)
+
+
+def run_oracle(inp):
+    if inp.idx is not None:
+        return torch.from_numpy(oracle.gather(inp.q, inp.k, inp.v, inp.idx, inp.scale))
+    lens = inp.kv_lengths.cpu()
+    return torch.from_numpy(oracle.dense(inp.q, inp.k, inp.v, lens, inp.n_q, inp.causal,
+                                         inp.scale, inp.k_scale, inp.v_scale))
+
+
+def bf16_half_ulp(x: torch.Tensor) -> torch.Tensor:
+    """Half a bf16 ulp at |x| (the largest error of a correctly rounded store)."""
+    _, e = torch.frexp(x.abs())
+    half = torch.ldexp(torch.ones_like(x), (e - 9).to(torch.int32))
+    return torch.where(x == 0, torch.zeros_like(x), half)
+
+
+def compare(got, ref, out_dtype, what=""):
+    """Element-by-element check; returns (max abs, mean abs, normalised).
+
+    For bf16 outputs the bound applies on top of the output's own rounding:
+    |got - ref| <= 1e-2 + half a bf16 ulp of ref (an exactly computed value
+    rounded to bf16 is already 0.0156 away from the fp64 answer when
+    |ref| >= 4)."""
+    g = got.detach().double().cpu()
+    r = ref.double().cpu()
+    assert g.shape == r.shape, (g.shape, r.shape)
+    assert torch.isfinite(g).all(), "%s: non-finite output" % what
+    err = (g - r).abs()
+    mx, mean = float(err.max()), float(err.mean())
+    norm = mx / max(float(r.abs().max()), 1e-30)
+    tmax, tmean = TOL[out_dtype]
+    slack = bf16_half_ulp(r) if out_dtype == torch.bfloat16 else torch.zeros_like(r)
+    excess = float((err - slack).max())
+    assert excess <= tmax, "%s: max abs err %.3e (beyond output rounding %.3e) > %.1e (mean %.3e)" % (
+        what, mx, excess, tmax, mean)
+    assert mean <= tmean, "%s: mean abs err %.3e > %.1e" % (what, mean, tmean)
+    return mx, mean, norm

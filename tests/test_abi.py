@@ -1,0 +1,181 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+symbol include/fd.h declares, rejects bad arguments on the host before any
+CUDA call, and its host partitioner mirror covers every tile exactly once."""
+import ctypes
+import os
+import random
+import re
+
+import pytest
+
+from decode_attention_preallocated_gb300 import build as fdbuild
+from decode_attention_preallocated_gb300 import fd
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "fd.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    fdbuild.build()
+    return fd.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fd_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported_and_bound(L):
+    names = declared_functions()
+    assert "fd_decode" in names and "fd_decode_gather" in names
+    bound = {n for n, _, _ in fd._SIGNATURES}
+    for n in names:
+        assert hasattr(L, n), "libfd.so does not export " + n
+        assert n in bound, "binding does not declare " + n
+
+
+def test_version_and_status_strings(L):
+    assert L.fd_version() >= 1
+    for code in (0, -1, -2, -3, -4, -5):
+        assert fd.status_string(code) not in ("", "unknown status")
+    assert fd.status_string(-99) == "unknown status"
+
+
+def fake(shape, dtype=fd.FD_BF16, strides=None, ptr=0x100000):
+    t = fd.FdTensor()
+    t.data = ptr
+    t.dtype = dtype
+    t.ndim = len(shape)
+    if strides is None:
+        strides, acc = [], 1
+        for s in reversed(shape):
+            strides.insert(0, acc)
+            acc *= s
+    for i, (s, st) in enumerate(zip(shape, strides)):
+        t.shape[i], t.stride[i] = s, st
+    return t
+
+
+def call_dense(q, k, v, out, n_q=1, causal=0, ws=None, lens=0x200000, opts=True, **kw):
+    o = fd.FdOpts()
+    o.ws = ws
+    for key, val in kw.items():
+        setattr(o, key, val)
+    return fd.lib().fd_decode(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), lens,
+                              n_q, causal, 0.1, ctypes.byref(out),
+                              ctypes.byref(o) if opts else None)
+
+
+def good(B=1, n_q=1, Hq=8, Hkv=2, d=128, cap=64):
+    return (fake([B, n_q, Hq, d]), fake([B, Hkv, cap, d]), fake([B, Hkv, cap, d]),
+            fake([B, n_q, Hq, d]))
+
+
+def test_host_validation_codes(L):
+    q, k, v, o = good()
+    # all arguments valid but no workspace: rejected before any CUDA call
+    assert call_dense(q, k, v, o) == fd.FD_ERR_WORKSPACE
+    assert call_dense(q, k, v, o, opts=False) == fd.FD_ERR_ARG
+    assert call_dense(q, k, v, o, lens=None) == fd.FD_ERR_ARG
+    assert call_dense(q, k, v, o, n_q=2) == fd.FD_ERR_ARG          # n_q != q.shape[1]
+    assert call_dense(q, k, v, o, causal=3) == fd.FD_ERR_ARG
+    assert call_dense(q, k, v, o, kernel=7) == fd.FD_ERR_ARG
+    assert call_dense(q, k, v, o, num_ctas=-1) == fd.FD_ERR_ARG
+    qq, kk, vv, oo = good(d=64)
+    assert call_dense(qq, kk, vv, oo) == fd.FD_ERR_UNSUPPORTED
+    qq, kk, vv, oo = good(n_q=7)
+    assert call_dense(qq, kk, vv, oo, n_q=7) == fd.FD_ERR_UNSUPPORTED
+    qq, kk, vv, oo = good(Hq=6, Hkv=4)
+    assert call_dense(qq, kk, vv, oo) == fd.FD_ERR_ARG              # Hq % Hkv
+    qq, kk, vv, oo = good(Hq=72, Hkv=1)
+    assert call_dense(qq, kk, vv, oo) == fd.FD_ERR_UNSUPPORTED      # 72 rows > 64
+    # misaligned cache pointer / stride
+    q, k, v, o = good()
+    k.data = 0x100008
+    assert call_dense(q, k, v, o) == fd.FD_ERR_ALIGN
+    q, k, v, o = good()
+    k2 = fake([1, 2, 64, 128], strides=[2 * 64 * 132, 64 * 132, 132, 1])
+    assert call_dense(q, k2, k2, o) == fd.FD_ERR_ALIGN
+    # wrong dtypes / shapes / inner stride
+    q, k, v, o = good()
+    assert call_dense(q, fake([1, 2, 64, 128], fd.FD_F32), v, o) == fd.FD_ERR_ARG
+    assert call_dense(q, k, v, fake([1, 1, 8, 128], fd.FD_I8)) == fd.FD_ERR_ARG
+    assert call_dense(q, k, fake([1, 2, 32, 128]), o) == fd.FD_ERR_ARG
+    assert call_dense(q, k, v, fake([1, 1, 8, 128], strides=[1024, 1024, 128, 2])) == fd.FD_ERR_ARG
+    q, k, v, o = good()
+    q.data = None
+    assert call_dense(q, k, v, o) == fd.FD_ERR_ARG
+
+
+def test_int8_and_gather_validation(L):
+    q, _, _, o = good()
+    k8 = fake([1, 2, 64, 128], fd.FD_I8)
+    ks = fake([1, 2, 64], fd.FD_F32)
+    op = fd.FdOpts()
+    rc = L.fd_decode_int8(ctypes.byref(q), ctypes.byref(k8), ctypes.byref(k8),
+                          ctypes.byref(ks), ctypes.byref(ks), 0x200000, 1, 0, 0.1,
+                          ctypes.byref(o), ctypes.byref(op))
+    assert rc == fd.FD_ERR_WORKSPACE
+    bad = fake([1, 2, 63], fd.FD_F32)
+    rc = L.fd_decode_int8(ctypes.byref(q), ctypes.byref(k8), ctypes.byref(k8),
+                          ctypes.byref(bad), ctypes.byref(ks), 0x200000, 1, 0, 0.1,
+                          ctypes.byref(o), ctypes.byref(op))
+    assert rc == fd.FD_ERR_ARG
+    _, k, v, _ = good()
+    rc = L.fd_decode_gather(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), 0x300000,
+                            16, ctypes.byref(o), ctypes.byref(op))
+    assert rc == fd.FD_ERR_WORKSPACE
+    rc = L.fd_decode_gather(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), None,
+                            16, ctypes.byref(o), ctypes.byref(op))
+    assert rc == fd.FD_ERR_ARG
+
+
+def test_workspace_size_formula(L):
+    n = L.fd_workspace_bytes(10, 24, 256, 300)
+    floats = (10 + 300) * 24 * 258
+    assert n >= floats * 4 + 10 * 4 + 4
+    assert n % 256 == 0
+    assert L.fd_workspace_bytes(0, 1, 1, 1) == 0
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_partition_covers_each_tile_once(L, seed):
+    rnd = random.Random(seed)
+    nseg = rnd.randint(1, 40)
+    tile = rnd.choice([16, 32, 64, 128])
+    maxlen = 5000 if seed % 2 else 300           # odd seeds: more blocks than tiles
+    lens = [rnd.choice([0, rnd.randint(1, maxlen)]) for _ in range(nseg)]
+    grid = rnd.randint(1, 400)
+    total, first, pieces = fd.plan(lens, tile, grid)
+    ntiles = [-(-x // tile) for x in lens]
+    assert total == sum(ntiles)
+    if total == 0:
+        assert all(p == 0 for p in pieces)
+        return
+    G = min(grid, total)          # blocks beyond the tile count get no work
+    starts = [c * total // G for c in range(G + 1)]
+    assert all(starts[c + 1] > starts[c] for c in range(G))
+    # balanced: block ranges differ by at most one tile
+    sizes = [starts[c + 1] - starts[c] for c in range(G)]
+    assert max(sizes) - min(sizes) <= 1
+    seen = [0] * total
+    slots = set()
+    t = 0
+    for s in range(nseg):
+        if ntiles[s] == 0:
+            assert pieces[s] == 0
+            continue
+        blocks = [c for c in range(G)
+                  if starts[c] < t + ntiles[s] and starts[c + 1] > t]
+        assert blocks == list(range(first[s], first[s] + pieces[s]))
+        for c in blocks:
+            lo, hi = max(starts[c], t), min(starts[c + 1], t + ntiles[s])
+            for x in range(lo, hi):
+                seen[x] += 1
+            assert s + c not in slots          # workspace slot is unique
+            slots.add(s + c)
+            assert s + c < nseg + G - 1
+        t += ntiles[s]
+    assert all(x == 1 for x in seen)

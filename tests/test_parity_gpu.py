@@ -1,0 +1,306 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs, element by element, for every mode and the edge
+cases.  Sizes span several tiles and a ragged tail; the named workloads also
+run at full size."""
+import math
+
+import pytest
+import torch
+
+from decode_attention_preallocated_gb300 import build as fdbuild
+from decode_attention_preallocated_gb300 import fd
+from decode_attention_preallocated_gb300 import workloads as W
+from golden_cases import fixture_names, load as load_fixture
+from parity_util import TOL, compare, run_gpu, run_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = [fd.FD_KERNEL_SIMT]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    fdbuild.build()
+    fd.lib()
+
+
+def check(inp_cpu, out_dtype=torch.bfloat16, num_ctas=0, kernel=fd.FD_KERNEL_AUTO,
+          ref=None, what=""):
+    if ref is None:
+        ref = run_oracle(inp_cpu)
+    dev = to_dev(inp_cpu)
+    got = run_gpu(dev, out_dtype, num_ctas, kernel)
+    torch.cuda.synchronize()
+    return compare(got, ref, out_dtype, what or inp_cpu.name), got
+
+
+# --------------------------------------------------------------- fixtures
+@pytest.mark.parametrize("name", fixture_names())
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_golden_fixture_on_gpu(name, d, kernel):
+    fx = load_fixture(name, pad_d=d)
+    dev = lambda t: None if t is None else t.cuda()
+    for out_dtype in (torch.float32, torch.bfloat16):
+        if fx["mode"] == "gather":
+            got = fd.decode_gather(dev(fx["q"]), dev(fx["k"]), dev(fx["v"]), dev(fx["idx"]),
+                                   scale=fx["scale"], out_dtype=out_dtype, kernel=kernel)
+        elif fx.get("int8"):
+            got = fd.decode_int8(dev(fx["q"]), dev(fx["k"]), dev(fx["v"]),
+                                 dev(fx["k_scale"]), dev(fx["v_scale"]),
+                                 dev(fx["kv_lengths"]), n_q=fx["n_q"], causal=fx["causal"],
+                                 scale=fx["scale"], out_dtype=out_dtype, kernel=kernel)
+        else:
+            got = fd.decode(dev(fx["q"]), dev(fx["k"]), dev(fx["v"]), dev(fx["kv_lengths"]),
+                            n_q=fx["n_q"], causal=fx["causal"], scale=fx["scale"],
+                            out_dtype=out_dtype, kernel=kernel)
+        compare(got, fx["expected"], out_dtype, name)
+
+
+# ---------------------------------------------------- reduced-size workloads
+SMALL = {
+    # name: (B, n_q, Hq, Hkv, d, cap, lengths, causal)
+    "dense_d128": (1, 1, 8, 2, 128, 600, [517], False),
+    "mtp_d256": (1, 4, 16, 4, 256, 1201, [999], True),
+    "ragged_d256": (4, 6, 16, 4, 256, 700, [1, 65, 333, 700], True),
+    "ragged_d128": (3, 3, 12, 3, 128, 450, [450, 7, 129], True),
+    "mqa_rows64": (2, 2, 32, 1, 128, 300, [300, 77], True),
+    "mha_g1": (2, 5, 3, 3, 256, 260, [2, 259], True),
+}
+
+
+@pytest.mark.parametrize("case", sorted(SMALL))
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_dense_small(case, out_dtype, kernel):
+    B, n_q, Hq, Hkv, d, cap, lens, causal = SMALL[case]
+    inp = W.dense_inputs(B, n_q, Hq, Hkv, d, cap, lens, 11, causal, name=case)
+    check(inp, out_dtype, kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("num_ctas", [1, 2, 3, 7, 19, 64, 300, 1000])
+def test_split_count_does_not_change_result(kernel, num_ctas):
+    inp = W.dense_inputs(3, 4, 16, 4, 256, 900, [900, 31, 450], 12, True)
+    ref = run_oracle(inp)
+    check(inp, torch.float32, num_ctas=num_ctas, kernel=kernel, ref=ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_capacity_beyond_length_is_never_read(kernel):
+    # NaN in every cache row past the length, capacities from L to 4L
+    L = 700
+    base = W.dense_inputs(2, 4, 16, 4, 256, L, [L, L], 13, True)
+    ref = run_oracle(base)
+    for cap in (L, L + 1, 2 * L + 3, 4 * L):
+        inp = W.dense_inputs(2, 4, 16, 4, 256, cap, [L, L], 13, True, tail="nan")
+        inp.q.copy_(base.q)
+        inp.k[:, :, :L] = base.k
+        inp.v[:, :, :L] = base.v
+        (mx, _, _), got = check(inp, torch.float32, kernel=kernel, ref=ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_token_major_cache_layout(kernel):
+    inp = W.dense_inputs(2, 3, 8, 2, 128, 333, [333, 100], 14, True, layout="bthd")
+    assert inp.k.stride(2) == 2 * 128
+    check(inp, torch.float32, kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_empty_windows_give_zero(kernel):
+    # L = 0, and causal rows whose window would start before position 0
+    inp = W.dense_inputs(3, 6, 8, 2, 128, 64, [0, 3, 64], 15, True)
+    (_, _, _), got = check(inp, torch.float32, kernel=kernel)
+    g = got.cpu()
+    assert torch.count_nonzero(g[0]) == 0
+    assert torch.count_nonzero(g[1, :3]) == 0
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_bad_lengths_are_clamped_and_flagged(kernel):
+    inp = W.dense_inputs(2, 1, 8, 2, 128, 100, [100, 100], 16, False)
+    dev = to_dev(inp)
+    dev.kv_lengths = torch.tensor([-5, 1000], dtype=torch.int32, device="cuda")
+    ws = fd.Workspace(8, 16, 256, 1024)
+    got = run_gpu(dev, torch.float32, kernel=kernel, workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.device_status() & fd.FD_DEV_BAD_LENGTH
+    inp.kv_lengths = torch.tensor([0, 100], dtype=torch.int32)
+    compare(got, run_oracle(inp), torch.float32, "clamped lengths")
+    ws.reset()
+    assert ws.device_status() == 0
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_peaky_scores(kernel):
+    # q scaled x8: outputs are O(1), so absolute tolerances bite
+    inp = W.dense_inputs(2, 2, 8, 2, 256, 400, [400, 250], 17, True, q_mult=8.0)
+    ref = run_oracle(inp)
+    assert float(ref.abs().max()) > 1.0
+    check(inp, torch.float32, kernel=kernel, ref=ref)
+    check(inp, torch.bfloat16, kernel=kernel, ref=ref)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_rollback_by_length(kernel):
+    inp = W.dense_inputs(1, 4, 16, 4, 256, 800, [703], 18, True)
+    dev = to_dev(inp)
+    a = run_gpu(dev, torch.float32, kernel=kernel)
+    dev.kv_lengths.fill_(700)               # reject three drafts
+    b = run_gpu(dev, torch.float32, kernel=kernel)
+    fresh = W.dense_inputs(1, 4, 16, 4, 256, 800, [700], 18, True)
+    compare(b, run_oracle(fresh), torch.float32, "rolled back")
+    compare(a, run_oracle(inp), torch.float32, "before rollback")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_causal_row_ignores_later_drafts(kernel):
+    n_q, L = 6, 500
+    a = W.dense_inputs(1, n_q, 16, 4, 256, 512, [L], 19, True)
+    b = W.dense_inputs(1, n_q, 16, 4, 256, 512, [L], 19, True)
+    b.k[:, :, L - 3:L] = 5.0
+    b.v[:, :, L - 3:L] = -9.0
+    ga = run_gpu(to_dev(a), torch.float32, kernel=kernel).cpu()
+    gb = run_gpu(to_dev(b), torch.float32, kernel=kernel).cpu()
+    # rows 0..2 see positions <= L-4 only
+    assert torch.equal(ga[0, :3], gb[0, :3])
+    assert not torch.equal(ga[0, 3:], gb[0, 3:])
+
+
+# ------------------------------------------------------------------ gather
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("n_q", [1, 3])
+def test_gather_small(kernel, n_q):
+    inp = W.gather_inputs(2, n_q, 32, 4, 128, 3000, 200, 16, 20)
+    inp.idx[0, 0, 5] = -1
+    inp.idx[1, n_q - 1, 7] = -3
+    check(inp, torch.float32, kernel=kernel)
+    check(inp, torch.bfloat16, kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_gather_prefix_equals_dense(kernel):
+    L = 333
+    inp = W.dense_inputs(1, 1, 8, 2, 128, 400, [L], 21, False)
+    dev = to_dev(inp)
+    dense = run_gpu(dev, torch.float32, kernel=kernel)
+    idx = torch.arange(L, dtype=torch.int32, device="cuda").view(1, 1, L)
+    g = fd.decode_gather(dev.q, dev.k, dev.v, idx, scale=inp.scale,
+                         out_dtype=torch.float32, kernel=kernel)
+    torch.testing.assert_close(g, dense, rtol=0, atol=2e-6)
+    perm = idx[:, :, torch.randperm(L, device="cuda")].contiguous()
+    g2 = fd.decode_gather(dev.q, dev.k, dev.v, perm, scale=inp.scale,
+                          out_dtype=torch.float32, kernel=kernel)
+    torch.testing.assert_close(g2, dense, rtol=0, atol=2e-6)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_gather_out_of_range_index_is_skipped_and_flagged(kernel):
+    inp = W.gather_inputs(1, 1, 8, 2, 128, 500, 64, 4, 22)
+    dev = to_dev(inp)
+    dev.idx[0, 0, 3] = 500
+    dev.idx[0, 0, 9] = 1 << 30
+    ws = fd.Workspace(8, 16, 256, 1024)
+    got = fd.decode_gather(dev.q, dev.k, dev.v, dev.idx, scale=inp.scale,
+                           out_dtype=torch.float32, kernel=kernel, workspace=ws)
+    torch.cuda.synchronize()
+    assert ws.device_status() & fd.FD_DEV_BAD_INDEX
+    inp.idx = dev.idx.cpu()
+    compare(got, run_oracle(inp), torch.float32, "gather skip")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_gather_empty_list(kernel):
+    inp = W.gather_inputs(1, 2, 8, 2, 128, 100, 8, 2, 23)
+    dev = to_dev(inp)
+    idx = torch.full((1, 2, 8), -1, dtype=torch.int32, device="cuda")
+    got = fd.decode_gather(dev.q, dev.k, dev.v, idx, out_dtype=torch.float32, kernel=kernel)
+    assert torch.count_nonzero(got) == 0
+    idx0 = torch.empty((1, 2, 0), dtype=torch.int32, device="cuda")
+    got = fd.decode_gather(dev.q, dev.k, dev.v, idx0, out_dtype=torch.float32, kernel=kernel)
+    assert torch.count_nonzero(got) == 0
+
+
+# -------------------------------------------------------------------- int8
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("causal,n_q", [(False, 1), (True, 4)])
+def test_int8_small(kernel, causal, n_q):
+    inp = W.dense_inputs(3, n_q, 32, 8, 128, 640, [640, 200, 1], 24, causal, int8=True)
+    check(inp, torch.bfloat16, kernel=kernel)
+    check(inp, torch.float32, kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_int8_poisoned_tail_scales(kernel):
+    inp = W.dense_inputs(2, 1, 16, 4, 256, 300, [150, 299], 25, False, int8=True, tail="nan")
+    check(inp, torch.float32, kernel=kernel)
+
+
+# ------------------------------------------------------------- CUDA graphs
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_graph_capture_and_replay_with_new_lengths(kernel):
+    inp = W.dense_inputs(2, 4, 16, 4, 256, 1000, [1000, 1000], 26, True)
+    dev = to_dev(inp)
+    ws = fd.Workspace(16, 64, 256, 1024)
+    out = torch.empty(dev.q.shape, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fd.decode(dev.q, dev.k, dev.v, dev.kv_lengths, n_q=4, causal=True, scale=inp.scale,
+                  out=out, kernel=kernel, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        fd.decode(dev.q, dev.k, dev.v, dev.kv_lengths, n_q=4, causal=True, scale=inp.scale,
+                  out=out, kernel=kernel, workspace=ws)
+    for lens in ([1000, 1000], [17, 999], [513, 4], [0, 640]):
+        dev.kv_lengths.copy_(torch.tensor(lens, dtype=torch.int32))
+        graph.replay()
+        torch.cuda.synchronize()
+        inp.kv_lengths = torch.tensor(lens, dtype=torch.int32)
+        compare(out, run_oracle(inp), torch.float32, "graph replay %s" % lens)
+
+
+# ------------------------------------------------------- full-size workloads
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("name", ["dense_1k", "mtp_verify", "gather", "ragged"])
+def test_named_workload_full_size(kernel, name):
+    inp = W.workload(name, seed=1)
+    check(inp, torch.bfloat16, kernel=kernel)
+    if name == "dense_1k":
+        check(inp, torch.float32, kernel=kernel)
+        poisoned = W.workload(name, seed=1, tail="nan")
+        check(poisoned, torch.bfloat16, kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_mtp_verify_capacity_independent_output(kernel):
+    # the MTP-verify shape at capacities 3000, 24007 and 131072 with the same
+    # 3000 filled positions gives the same result
+    base = W.workload("mtp_verify", seed=2)
+    ref = run_oracle(base)
+    outs = []
+    for cap in (3000, 24007, 131072):
+        inp = W.dense_inputs(1, 4, 16, 4, 256, cap, [3000], 2, True)
+        inp.q.copy_(base.q)
+        inp.k[:, :, :3000] = base.k[:, :, :3000]
+        inp.v[:, :, :3000] = base.v[:, :, :3000]
+        (_, _, _), got = check(inp, torch.float32, kernel=kernel, ref=ref)
+        outs.append(got.cpu())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_int8_workload_full_size_sampled(kernel):
+    # full int8 workload (4 x 131072 tokens, 32/8 heads): generated on the GPU,
+    # every output row checked against the oracle on the same bits
+    inp = W.workload("int8", seed=1, device="cuda")
+    got = run_gpu(inp, torch.bfloat16, kernel=kernel)
+    torch.cuda.synchronize()
+    cpu = W.DecodeInputs(q=inp.q.cpu(), k=inp.k.cpu(), v=inp.v.cpu(),
+                         kv_lengths=inp.kv_lengths.cpu(), n_q=1, causal=False,
+                         scale=inp.scale, k_scale=inp.k_scale.cpu(),
+                         v_scale=inp.v_scale.cpu())
+    compare(got, run_oracle(cpu), torch.bfloat16, "int8 full")
