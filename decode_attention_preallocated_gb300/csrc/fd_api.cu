@@ -347,6 +347,7 @@ const char *fd_status_string(int status) {
         case FD_ERR_ALIGN: return "cache pointer or stride not 16-byte aligned";
         case FD_ERR_WORKSPACE: return "missing or too small workspace";
         case FD_ERR_CUDA: return "CUDA runtime error";
+        case FD_ERR_SCRATCH: return "problem exceeds the fixed scratch of fd_decode_noalloc";
         default: return "unknown status";
     }
 }

@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libfd.so")
 
 # constants from include/fd.h
 FD_OK, FD_ERR_ARG, FD_ERR_UNSUPPORTED, FD_ERR_ALIGN, FD_ERR_WORKSPACE, FD_ERR_CUDA = 0, -1, -2, -3, -4, -5
+FD_ERR_SCRATCH = -6
 FD_BF16, FD_F32, FD_I8, FD_I32 = 0, 1, 2, 3
 FD_DEV_BAD_LENGTH, FD_DEV_BAD_INDEX = 1, 2
 FD_KERNEL_AUTO, FD_KERNEL_SIMT, FD_KERNEL_TC = 0, 1, 2
@@ -69,6 +70,9 @@ _SIGNATURES = [
     ("fd_decode_gather", ctypes.c_int,
      [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_int32,
       _P(FdTensor), _P(FdOpts)]),
+    ("fd_decode_noalloc", ctypes.c_int,
+     [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_int32,
+      ctypes.c_int32, ctypes.c_float, _P(FdTensor), ctypes.c_void_p, ctypes.c_int32]),
     ("fd_workspace_bytes", ctypes.c_size_t,
      [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     ("fd_workspace_create", ctypes.c_int,

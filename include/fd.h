@@ -70,6 +70,7 @@ extern "C" {
 #define FD_ERR_ALIGN (-3)        /* pointer or stride not 16-byte aligned  */
 #define FD_ERR_WORKSPACE (-4)    /* missing or too small workspace         */
 #define FD_ERR_CUDA (-5)         /* CUDA runtime error                     */
+#define FD_ERR_SCRATCH (-6)      /* problem exceeds fd_decode_noalloc's fixed scratch */
 
 /* dtypes */
 #define FD_BF16 0
@@ -151,6 +152,34 @@ int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache,
                      const fd_tensor *v_cache, const int32_t *idx,
                      int32_t idx_len, const fd_tensor *out,
                      const fd_opts *opts);
+
+/*
+ * Dense prefix decode that allocates nothing (no counterpart in the paper).
+ *
+ * For callers that cannot call cudaMalloc: an application whose own allocator
+ * owns all device memory, a process under a hard device-memory cap, or a
+ * plugin inside an engine that forbids allocation after start-up.  Computes
+ * exactly what fd_decode computes (bf16 cache, optional causal window) on
+ * `stream`, with the same arguments minus the workspace; num_ctas = 0 picks
+ * the block count automatically.
+ *
+ * Its scratch (split partials, per-(sequence, kv head) completion counters,
+ * status word) is a fixed 8 MiB array in device memory that every GPU which
+ * loads libfd.so holds until the process exits.  Limits: at most 4096
+ * (sequence, kv head) pairs, and the split partials must fit: the block count
+ * is lowered to fit, and a problem that cannot fit even with one block per
+ * (sequence, kv head), or an explicit num_ctas that does not fit, returns
+ * FD_ERR_SCRATCH before anything is launched.  Each call clears the counters
+ * and status word on `stream` first (cudaMemsetAsync, which allocates
+ * nothing).  All calls share the one array: calls that overlap on the GPU
+ * race and must not be issued.  The first call on a device (with that device
+ * current) looks up the array's device address; make it before any stream
+ * capture.  Returns FD_OK or a negative FD_ERR_* code.
+ */
+int fd_decode_noalloc(const fd_tensor *q, const fd_tensor *k_cache,
+                      const fd_tensor *v_cache, const int32_t *kv_lengths,
+                      int32_t n_q, int32_t causal, float scale,
+                      const fd_tensor *out, void *stream, int32_t num_ctas);
 
 /*
  * Workspace.  A launch unit ("segment") is one (sequence, kv head) in the
