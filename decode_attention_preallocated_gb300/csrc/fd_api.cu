@@ -86,17 +86,24 @@ int check_tensor(const fd_tensor *t, int ndim) {
 }
 
 int kernel_tile(int32_t kernel) {
-    (void)kernel;
-    return fd::simt_tile_tokens();
+    return kernel == FD_KERNEL_TC ? fd::tc_tile_tokens() : fd::simt_tile_tokens();
 }
 
+// Blocks for an auto launch: one per SM for the tensor-core kernel (its
+// shared-memory ring fills an SM), two per SM for the CUDA-core kernel;
+// never more than the largest possible tile count.
 int32_t auto_ctas(int32_t kernel, int64_t max_tiles) {
     const int sms = sm_count_current();
     if (sms <= 0) return 0;
-    (void)kernel;
-    int64_t g = (int64_t)sms * 2;
+    int64_t g = (int64_t)sms * (kernel == FD_KERNEL_TC ? 1 : 2);
     if (max_tiles > 0 && g > max_tiles) g = max_tiles;
     return (int32_t)(g < 1 ? 1 : g);
+}
+
+// The kernel an auto request runs for a dense call with this cache dtype.
+int32_t resolve(int32_t kernel, int32_t kv_dtype) {
+    if (kernel != FD_KERNEL_AUTO) return kernel;
+    return kv_dtype == FD_BF16 ? FD_KERNEL_TC : FD_KERNEL_SIMT;
 }
 
 // Shared validation and launch for the three entry points.
@@ -166,12 +173,17 @@ int run(const Call &c) {
     fd_workspace *ws = o.ws;
     if (!ws) return FD_ERR_WORKSPACE;
     const int64_t nseg = c.mode == fd::kGather ? B * n_q * Hkv : B * Hkv;
-    const int tile = kernel_tile(o.kernel);
+    // Kernel choice: the tensor-core kernel serves the dense bf16 modes; the
+    // CUDA-core kernel serves every mode.
+    const bool tc_ok = c.mode == fd::kDense && !c.kv_int8 && cap < ((int64_t)1 << 31);
+    int32_t kernel = o.kernel == FD_KERNEL_AUTO ? (tc_ok ? FD_KERNEL_TC : FD_KERNEL_SIMT) : o.kernel;
+    if (kernel == FD_KERNEL_TC && !tc_ok) return FD_ERR_UNSUPPORTED;
+    const int tile = kernel_tile(kernel);
     const int64_t max_tiles =
         c.mode == fd::kGather ? nseg * fd::ceil_div(c.idx_len, tile) : nseg * fd::ceil_div(cap, tile);
     int32_t G = o.num_ctas;
     if (G == 0) {
-        G = auto_ctas(o.kernel, max_tiles);
+        G = auto_ctas(kernel, max_tiles);
         if (G <= 0) return FD_ERR_CUDA;
     }
     if (nseg > ws->max_segments || rows > ws->max_rows || d > ws->head_dim || G > ws->max_ctas)
@@ -206,7 +218,7 @@ int run(const Call &c) {
     p.partials = ws->partials;
 
     cudaStream_t st = static_cast<cudaStream_t>(o.stream);
-    rc = fd::launch_simt(p, G, st);
+    rc = kernel == FD_KERNEL_TC ? fd::launch_tc(p, G, st) : fd::launch_simt(p, G, st);
     return rc == 0 ? FD_OK : (rc == -2 ? FD_ERR_UNSUPPORTED : FD_ERR_CUDA);
 }
 
@@ -305,12 +317,12 @@ int fd_get_device_status(fd_workspace *ws, int32_t *status) {
 int32_t fd_auto_num_ctas(int32_t kernel, int32_t head_dim, int32_t kv_dtype, int32_t rows,
                          int64_t max_tiles) {
     (void)head_dim; (void)kv_dtype; (void)rows;
-    return auto_ctas(kernel, max_tiles);
+    return auto_ctas(resolve(kernel, kv_dtype), max_tiles);
 }
 
 int32_t fd_tile_tokens(int32_t kernel, int32_t head_dim, int32_t kv_dtype) {
-    (void)head_dim; (void)kv_dtype;
-    return kernel_tile(kernel);
+    (void)head_dim;
+    return kernel_tile(resolve(kernel, kv_dtype));
 }
 
 int64_t fd_plan(const int64_t *seg_len, int64_t nseg, int32_t tile_tokens, int32_t num_ctas,

@@ -11,4 +11,10 @@ namespace fd {
 int simt_tile_tokens();
 int launch_simt(const Params &p, int num_ctas, cudaStream_t stream);
 
+// Tensor-core kernel (fd_tc.cu): dense bf16 prefix (optionally causal),
+// head_dim 128 / 256, up to 64 packed rows; one block per SM.
+int tc_tile_tokens();
+bool tc_supports(const Params &p);
+int launch_tc(const Params &p, int num_ctas, cudaStream_t stream);
+
 }  // namespace fd

@@ -1,0 +1,670 @@
+// fd_tc.cu -- tensor-core (tcgen05) decode kernel for the dense bf16 prefix
+// mode (optionally causal), head_dim 128 / 256, up to 64 packed query rows.
+//
+// Work split: the same balanced tile partition as the CUDA-core kernel
+// (fd_internal.h), with 128-position tiles and one block per SM.  Roles
+// inside a block (192 threads):
+//   warp 4      TMA producer: streams K and V tiles of the block's range into
+//               a ring of shared-memory slots (4-D tensor maps, 128-byte
+//               swizzle, out-of-capacity rows zero-filled).
+//   warp 5      MMA issuer (one thread): S^T = K . Q^T   (M = 128 positions,
+//               N = padded query rows, K = head_dim) into TMEM, then
+//               O^T += V^T . P^T (M = 128 dims per chunk, N = rows,
+//               K = 128 positions) into TMEM; completion via tcgen05.commit.
+//   warps 0-3   softmax and epilogue: thread i owns TMEM lane i = cache
+//               position i of the tile (scores) and dim i of each 128-dim
+//               chunk (output).  Per tile: mask (length, causal window),
+//               column max over the 128 positions (warp shuffles + shared
+//               memory), online-softmax rescale of O in TMEM when a row's
+//               maximum grows, P = 2^(s - m) written to shared memory in the
+//               MMA operand layout.  At the end of a segment it normalises
+//               and stores, or hands a split partial to the in-launch
+//               combine (last block to arrive merges; comfy-kitchen #239,
+//               "GQA decode").
+// Rows of V at or past the length are zeroed in shared memory before the PV
+// product, so garbage in the unused tail of the cache never reaches the
+// arithmetic.  Every wait is bounded (2 s); a timeout sets FD_DEV_INTERNAL
+// in the status word and the block drains its copies and MMAs and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fd_device.cuh"
+#include "fd_launch.h"
+#include "fd_ptx.cuh"
+
+namespace fd {
+
+namespace {
+
+constexpr int TT = 128;                 // cache positions per tile (MMA M)
+constexpr int kThreadsTC = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kDevTimeout = 4;          // mirrors FD_DEV_INTERNAL
+
+struct TcArgs {   // CUtensorMap members carry their own alignment
+    CUtensorMap tk;
+    CUtensorMap tv;
+    Params p;
+};
+
+template <int D, int N>
+struct Cfg {
+    static constexpr int KB = D / 64;            // 128-byte boxes per cache row
+    static constexpr int DC = D / 128;           // 128-dim chunks of O
+    static constexpr uint32_t BOX = TT * 128;    // bytes of one box of a slot
+    static constexpr uint32_t SLOT = KB * BOX;   // one K or V tile
+    static constexpr uint32_t QB = N * 128;      // one 64-column box of Q or P
+    static constexpr uint32_t QBYTES = KB * QB;
+    static constexpr uint32_t PPLANE = 2 * QB;   // one bf16 plane of P (128 positions)
+    static constexpr uint32_t PSTAGE = 2 * PPLANE;   // P = hi plane + lo plane
+    // Barriers and the reduction scratch come first, then 1024-byte aligned
+    // operand buffers.
+    static constexpr uint32_t RED = 2 * 4 * N * 4;
+    static constexpr uint32_t MISC = ((512 + RED) + 1023) / 1024 * 1024;
+    static constexpr uint32_t BUDGET = 232448;   // max dynamic shared memory per block
+    // Two P stages when that still leaves three K/V slots, else one.
+    static constexpr int NS2 = (int)((BUDGET - MISC - QBYTES - 2 * PSTAGE) / SLOT);
+    static constexpr int PST = NS2 >= 3 ? 2 : 1;
+    static constexpr int NS_RAW = (int)((BUDGET - MISC - QBYTES - PST * PSTAGE) / SLOT);
+    static constexpr int NS = NS_RAW > 8 ? 8 : NS_RAW;
+    static_assert(NS >= 2, "need two K/V slots");
+    static constexpr uint32_t OFF_SLOTS = MISC;
+    static constexpr uint32_t OFF_Q = OFF_SLOTS + NS * SLOT;
+    static constexpr uint32_t OFF_P = OFF_Q + QBYTES;
+    static constexpr uint32_t SMEM = OFF_P + PST * PSTAGE;
+    static_assert(SMEM <= BUDGET, "shared memory budget");
+    static constexpr uint32_t COLS = 2 * N + DC * N;
+    static constexpr uint32_t TMEM_COLS = COLS <= 32 ? 32 : COLS <= 64 ? 64 : COLS <= 128 ? 128 : 256;
+    static constexpr uint32_t IDESC_QK = ptx::idesc_bf16(128, N, 0, 0);
+    static constexpr uint32_t IDESC_PV = ptx::idesc_bf16(128, N, 1, 0);
+};
+
+struct Bars {
+    uint64_t slot_full[8], slot_empty[8];
+    uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+    uint64_t q_full, q_free, o_done, o_free, exit_mma, wg_bar;
+    uint32_t tmem_base;
+    int abort_flag;
+    int last_flag;
+    int pad;
+    int64_t total;
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+__device__ __forceinline__ void set_abort(Bars *bs, const Params &p) {
+    bs->abort_flag = 1;
+    atomicOr(p.status, kDevTimeout);
+}
+
+template <int D, int N>
+__global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant__ TcArgs a) {
+    using C = Cfg<D, N>;
+    const Params &p = a.p;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const uint32_t smem_base = ptx::smem_u32(smem);
+    Bars *bs = reinterpret_cast<Bars *>(smem);
+    float *red = reinterpret_cast<float *>(smem + 512);   // [2][4][N]
+    volatile int *abort_flag = &bs->abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x, c = blockIdx.x;
+    // The swizzled operand layouts need 1024-byte aligned buffers; the
+    // dynamic shared window starts aligned, and a block that finds otherwise
+    // reports it instead of computing.
+    if (smem_base & 1023u) {
+        if (tid == 0) atomicOr(p.status, kDevTimeout);
+        return;
+    }
+
+    // Segments with nothing to attend still need their output rows zeroed.
+    for (int64_t s = c; s < p.nseg; s += G)
+        if (seg_tiles(p, s) == 0) zero_segment(p, s);
+    if (warp == 0) {
+        const int64_t tot = total_tiles_warp(p);
+        if (lane == 0) bs->total = tot;
+    }
+    __syncthreads();
+    const int64_t total = bs->total;
+    if (total == 0) return;
+    const int32_t Gw = working_blocks(total, G);
+    if (c >= Gw) return;
+    const Split sp{total, Gw};
+    const int64_t t_begin = sp.start(c), t_end = sp.start(c + 1);
+
+    if (tid == 0) {
+        for (int i = 0; i < C::NS; ++i) {
+            ptx::mbar_init(&bs->slot_full[i], 1);
+            ptx::mbar_init(&bs->slot_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&bs->s_full[i], 1);
+            ptx::mbar_init(&bs->s_free[i], 128);
+            ptx::mbar_init(&bs->p_full[i], 128);
+            ptx::mbar_init(&bs->p_free[i], 1);
+        }
+        ptx::mbar_init(&bs->q_full, 128);
+        ptx::mbar_init(&bs->q_free, 1);
+        ptx::mbar_init(&bs->o_done, 1);
+        ptx::mbar_init(&bs->o_free, 128);
+        ptx::mbar_init(&bs->exit_mma, 1);
+        ptx::mbar_init(&bs->wg_bar, 128);
+        bs->abort_flag = 0;
+        ptx::mbar_fence_init();
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(&bs->tmem_base, C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        ptx::prefetch_tmap(&a.tk);
+        ptx::prefetch_tmap(&a.tv);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bs->tmem_base;
+    const uint32_t q_addr = smem_base + C::OFF_Q;
+    const uint32_t p_addr = smem_base + C::OFF_P;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------ TMA producer
+        uint32_t issued = 0;
+        bool ok = true;
+        int64_t t = t_begin;
+        while (t < t_end && ok) {
+            SegPos pos;
+            const int64_t s = seg_of_tile_warp(p, t, &pos);
+            if (s < 0) break;
+            const int64_t piece_end = min(t_end, pos.first + pos.ntiles);
+            const int b = (int)(s / p.Hkv), hk = (int)(s % p.Hkv);
+            for (int64_t tt = t - pos.first; tt < piece_end - pos.first && ok; ++tt) {
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
+                    if (lane == 0) {
+                        ok = ptx::mbar_wait(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+                        if (ok) {
+                            ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
+                            unsigned char *dst = smem + C::OFF_SLOTS + slot * C::SLOT;
+#pragma unroll
+                            for (int cb = 0; cb < C::KB; ++cb)
+                                ptx::tma_load_4d(dst + cb * C::BOX, kv ? (const void *)&a.tv
+                                                                       : (const void *)&a.tk,
+                                                 &bs->slot_full[slot], cb * 64, (int)(tt * TT),
+                                                 hk, b);
+                        } else {
+                            set_abort(bs, p);
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (ok) ++issued;
+                }
+            }
+            t = piece_end;
+        }
+        // Drain: every issued copy must land before the block exits.
+        if (lane == 0) {
+            const uint32_t n = issued < (uint32_t)C::NS ? issued : (uint32_t)C::NS;
+            for (uint32_t k = 0; k < n; ++k) {
+                const uint32_t idx = issued - 1 - k;
+                ptx::mbar_wait(&bs->slot_full[idx % C::NS], (idx / C::NS) & 1, abort_flag,
+                               kWaitNs);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // -------------------------------------------------------- MMA issuer
+        uint32_t tile_ctr = 0;
+        int piece = 0;
+        bool ok = true;
+        bool issued_any = false;
+        int64_t t = t_begin;
+        while (t < t_end && ok) {
+            SegPos pos;
+            const int64_t s = seg_of_tile_warp(p, t, &pos);
+            if (s < 0) break;
+            const int64_t piece_end = min(t_end, pos.first + pos.ntiles);
+            const int64_t n_in = piece_end - t;
+            if (lane == 0) {
+                ok = ptx::mbar_wait(&bs->q_full, piece & 1, abort_flag, kWaitNs);
+                if (ok && piece > 0)
+                    ok = ptx::mbar_wait(&bs->o_free, (piece - 1) & 1, abort_flag, kWaitNs);
+                ptx::tc_fence_after();
+                for (int64_t j = 0; j < n_in && ok; ++j) {
+                    const uint32_t sb = tile_ctr & 1, u = tile_ctr >> 1;
+                    const uint32_t ki = 2 * tile_ctr, vi = 2 * tile_ctr + 1;
+                    const uint32_t ks = ki % C::NS, vs = vi % C::NS;
+                    ok = ptx::mbar_wait(&bs->slot_full[ks], (ki / C::NS) & 1, abort_flag, kWaitNs) &&
+                         ptx::mbar_wait(&bs->s_free[sb], (u & 1) ^ 1, abort_flag, kWaitNs);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    // S^T[pos, row] = sum_d K[pos, d] Q[row, d]
+                    const uint32_t k_addr = smem_base + C::OFF_SLOTS + ks * C::SLOT;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t da = ptx::smem_desc(k_addr + (kk >> 2) * C::BOX + (kk & 3) * 32,
+                                                           16, 1024, ptx::kLayoutSwizzle128);
+                        const uint64_t db = ptx::smem_desc(q_addr + (kk >> 2) * C::QB + (kk & 3) * 32,
+                                                           16, 1024, ptx::kLayoutSwizzle128);
+                        ptx::mma_f16_ss(tmem + sb * N, da, db, C::IDESC_QK, kk > 0);
+                    }
+                    ptx::mma_commit(&bs->slot_empty[ks]);
+                    ptx::mma_commit(&bs->s_full[sb]);
+                    if (j == n_in - 1) ptx::mma_commit(&bs->q_free);
+                    issued_any = true;
+                    const uint32_t ps = tile_ctr % C::PST, pu = tile_ctr / C::PST;
+                    ok = ptx::mbar_wait(&bs->slot_full[vs], (vi / C::NS) & 1, abort_flag, kWaitNs) &&
+                         ptx::mbar_wait(&bs->p_full[ps], pu & 1, abort_flag, kWaitNs);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    // O^T[dim, row] += sum_pos V[pos, dim] (P_hi + P_lo)[row, pos]
+                    const uint32_t v_addr = smem_base + C::OFF_SLOTS + vs * C::SLOT;
+                    const uint32_t pb = p_addr + ps * C::PSTAGE;
+#pragma unroll
+                    for (int dc = 0; dc < C::DC; ++dc) {
+#pragma unroll
+                        for (int kt = 0; kt < TT / 16; ++kt) {
+                            const uint64_t da = ptx::smem_desc(v_addr + (2 * dc) * C::BOX + kt * 2048,
+                                                               C::BOX, 1024, ptx::kLayoutSwizzle128);
+#pragma unroll
+                            for (int plane = 0; plane < 2; ++plane) {
+                                const uint64_t db = ptx::smem_desc(
+                                    pb + plane * C::PPLANE + (kt >> 2) * C::QB + (kt & 3) * 32, 16,
+                                    1024, ptx::kLayoutSwizzle128);
+                                ptx::mma_f16_ss(tmem + 2 * N + dc * N, da, db, C::IDESC_PV,
+                                                (j > 0 || kt > 0 || plane > 0) ? 1u : 0u);
+                            }
+                        }
+                    }
+                    ptx::mma_commit(&bs->slot_empty[vs]);
+                    ptx::mma_commit(&bs->p_free[ps]);
+                    ptx::mma_commit(&bs->o_done);
+                    ++tile_ctr;
+                }
+                if (!ok) set_abort(bs, p);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            tile_ctr = __shfl_sync(0xffffffffu, tile_ctr, 0);
+            t = piece_end;
+            ++piece;
+        }
+        // Drain: all MMAs issued by this thread complete before TMEM is freed.
+        if (lane == 0 && issued_any) {
+            ptx::mma_commit(&bs->exit_mma);
+            ptx::mbar_wait(&bs->exit_mma, 0, abort_flag, kWaitNs);
+        }
+    } else {
+        // ------------------------------------------- softmax and epilogue
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        uint32_t tile_ctr = 0;
+        uint32_t o_seen = 0;      // o_done phases observed, consumed strictly in order
+        uint32_t wg_ctr = 0;      // uses of the group barrier
+        int piece = 0;
+        bool ok = true;
+        // Completion of PV number k (k = 0, 1, ...): wait phase by phase, so a
+        // parity test never aliases with a phase two steps ahead or behind.
+        auto wait_pv = [&](uint32_t k) -> bool {
+            for (; o_seen <= k; ++o_seen)
+                if (!ptx::mbar_wait(&bs->o_done, o_seen & 1, abort_flag, kWaitNs)) return false;
+            return true;
+        };
+        // Barrier over the 128 softmax threads with a bounded wait.
+        auto wg_sync = [&]() -> bool {
+            ptx::mbar_arrive(&bs->wg_bar);
+            return ptx::mbar_wait(&bs->wg_bar, (wg_ctr++) & 1, abort_flag, kWaitNs);
+        };
+        int64_t t = t_begin;
+        while (t < t_end && ok) {
+            SegPos pos;
+            const int64_t s = seg_of_tile_warp(p, t, &pos);
+            if (s < 0) break;
+            const int64_t piece_end = min(t_end, pos.first + pos.ntiles);
+            const int64_t n_in = piece_end - t;
+            const int64_t tt0 = t - pos.first;
+            const int b = (int)(s / p.Hkv);
+            const int64_t L = seq_len(p, b);
+            const int rows = p.rows;
+
+            // Q rows of this segment -> shared memory (K-major, 128-byte swizzle).
+            if (piece > 0) ok = ptx::mbar_wait(&bs->q_free, (piece - 1) & 1, abort_flag, kWaitNs);
+            if (!ok) { set_abort(bs, p); break; }
+            for (int e = tid; e < N * (D / 8); e += 128) {
+                const int r = e / (D / 8), cc = e % (D / 8);
+                uint32_t w[4] = {0, 0, 0, 0};
+                if (r < rows) {
+                    const RowMap m = row_of(p, s, r);
+                    const uint16_t *src = p.q + (int64_t)m.b * p.qs[0] + (int64_t)m.i * p.qs[1] +
+                                          (int64_t)m.h * p.qs[2] + cc * 8;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        w[k] = (uint32_t)src[2 * k] | ((uint32_t)src[2 * k + 1] << 16);
+                }
+                unsigned char *dst = smem + C::OFF_Q + (cc >> 3) * C::QB + r * 128 +
+                                     (((cc & 7) ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(&bs->q_full);
+
+            float mrun[N], lpart[N];
+#pragma unroll
+            for (int r = 0; r < N; ++r) { mrun[r] = neg_inf(); lpart[r] = 0.f; }
+
+            for (int64_t j = 0; j < n_in && ok; ++j) {
+                const int64_t y0 = (tt0 + j) * TT;
+                const int64_t token = y0 + tid;
+                const uint32_t sb = tile_ctr & 1, u = tile_ctr >> 1;
+                ok = ptx::mbar_wait(&bs->s_full[sb], u & 1, abort_flag, kWaitNs);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                float sv[N];
+#pragma unroll
+                for (int cb = 0; cb < N / 16; ++cb)
+                    ptx::tmem_ld16(tmem + lane_base + sb * N + cb * 16, sv + cb * 16);
+                ptx::tmem_wait_ld();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&bs->s_free[sb]);
+
+                // Visibility: inside the filled prefix and, for causal windows,
+                // at or before L - n_q + i for the row's query index i.
+                const bool in_len = token < L;
+#pragma unroll
+                for (int r = 0; r < N; ++r) {
+                    bool vis = in_len && r < rows;
+                    if (p.causal) vis = vis && token <= L - p.n_q + (r % p.n_q);
+                    sv[r] = vis ? sv[r] * p.scale_log2 : neg_inf();
+                }
+                // Column maxima over the 128 positions of the tile.
+                float *rb = red + (tile_ctr & 1) * (4 * N);
+#pragma unroll
+                for (int r = 0; r < N; ++r) {
+                    const float mx = warp_max(sv[r]);
+                    if (lane == 0) rb[warp * N + r] = mx;
+                }
+                ok = wg_sync();
+                if (!ok) break;
+                float alpha[N];
+                bool grow = false;
+#pragma unroll
+                for (int r = 0; r < N; ++r) {
+                    const float tmax = fmaxf(fmaxf(rb[r], rb[N + r]), fmaxf(rb[2 * N + r], rb[3 * N + r]));
+                    const float mnew = fmaxf(mrun[r], tmax);
+                    const float muse = mnew == neg_inf() ? 0.f : mnew;
+                    alpha[r] = fast_exp2(mrun[r] - muse);
+                    grow = grow || (alpha[r] < 1.f);
+                    mrun[r] = mnew;
+                    const float pr = fast_exp2(sv[r] - muse);
+                    lpart[r] = lpart[r] * alpha[r] + pr;
+                    sv[r] = pr;
+                }
+                // Rescale the running O in TMEM (after the previous PV landed).
+                if (grow && j > 0) {
+                    ok = wait_pv(tile_ctr - 1);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int dc = 0; dc < C::DC; ++dc) {
+#pragma unroll
+                        for (int cb = 0; cb < N / 16; ++cb) {
+                            float o[16];
+                            const uint32_t ta = tmem + lane_base + 2 * N + dc * N + cb * 16;
+                            ptx::tmem_ld16(ta, o);
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) o[k] *= alpha[cb * 16 + k];
+                            ptx::tmem_st16(ta, o);
+                        }
+                    }
+                    ptx::tmem_wait_st();
+                }
+                // Zero the V rows at or past the length in the segment's last tile.
+                if (y0 + TT > L) {
+                    const uint32_t vi = 2 * tile_ctr + 1;
+                    ok = ptx::mbar_wait(&bs->slot_full[vi % C::NS], (vi / C::NS) & 1, abort_flag,
+                                        kWaitNs);
+                    if (!ok) break;
+                    if (!in_len) {
+                        unsigned char *row = smem + C::OFF_SLOTS + (vi % C::NS) * C::SLOT + tid * 128;
+#pragma unroll
+                        for (int cb = 0; cb < C::KB; ++cb)
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                *reinterpret_cast<uint4 *>(row + cb * C::BOX + k * 16) =
+                                    make_uint4(0, 0, 0, 0);
+                    }
+                }
+                // P^T (rows x positions, K-major) for the PV product.
+                const uint32_t ps = tile_ctr % C::PST, pu = tile_ctr / C::PST;
+                ok = ptx::mbar_wait(&bs->p_free[ps], (pu & 1) ^ 1, abort_flag, kWaitNs);
+                if (!ok) break;
+                {
+                    // P = hi + lo, both bf16: hi = rn(p), lo = rn(p - hi), so the
+                    // PV product sees p to about 2^-17 relative.
+                    unsigned char *pbuf = smem + C::OFF_P + ps * C::PSTAGE + (tid >> 6) * C::QB;
+                    const int ch = (tid & 63) >> 3, el = tid & 7;
+#pragma unroll
+                    for (int r = 0; r < N; ++r) {
+                        const uint16_t hi = bf16_bits(sv[r]);
+                        const float hf = __uint_as_float((uint32_t)hi << 16);
+                        const uint16_t lo = bf16_bits(sv[r] - hf);
+                        const uint32_t off = r * 128 + ((ch ^ (r & 7)) << 4) + el * 2;
+                        *reinterpret_cast<uint16_t *>(pbuf + off) = hi;
+                        *reinterpret_cast<uint16_t *>(pbuf + C::PPLANE + off) = lo;
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&bs->p_full[ps]);
+                ++tile_ctr;
+            }
+            if (!ok) { set_abort(bs, p); break; }
+
+            // ------------------------------------------ segment epilogue
+            ok = wait_pv(tile_ctr - 1);
+            if (!ok) { set_abort(bs, p); break; }
+            ptx::tc_fence_after();
+            float o[C::DC][N];
+#pragma unroll
+            for (int dc = 0; dc < C::DC; ++dc)
+#pragma unroll
+                for (int cb = 0; cb < N / 16; ++cb)
+                    ptx::tmem_ld16(tmem + lane_base + 2 * N + dc * N + cb * 16, &o[dc][cb * 16]);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bs->o_free);
+
+            // Row sums of P over the segment piece.
+            float *lb = red + (tile_ctr & 1) * (4 * N);
+#pragma unroll
+            for (int r = 0; r < N; ++r) {
+                const float v = warp_sum(lpart[r]);
+                if (lane == 0) lb[warp * N + r] = v;
+            }
+            ok = wg_sync();
+            float lsum[N];
+#pragma unroll
+            for (int r = 0; r < N; ++r) lsum[r] = lb[r] + lb[N + r] + lb[2 * N + r] + lb[3 * N + r];
+            ok = ok && wg_sync();
+            if (!ok) { set_abort(bs, p); break; }
+
+            const int c_first = sp.owner(pos.first), c_last = sp.owner(pos.first + pos.ntiles - 1);
+            if (c_first == c_last) {
+#pragma unroll
+                for (int r = 0; r < N; ++r) {
+                    if (r < rows) {
+                        const RowMap m = row_of(p, s, r);
+                        const float inv = lsum[r] > 0.f ? 1.f / lsum[r] : 0.f;
+                        const int64_t off = (int64_t)m.b * p.os[0] + (int64_t)m.i * p.os[1] +
+                                            (int64_t)m.h * p.os[2];
+#pragma unroll
+                        for (int dc = 0; dc < C::DC; ++dc) {
+                            const float val = o[dc][r] * inv;
+                            if (p.out_f32)
+                                reinterpret_cast<float *>(p.out)[off + dc * 128 + tid] = val;
+                            else
+                                reinterpret_cast<uint16_t *>(p.out)[off + dc * 128 + tid] = bf16_bits(val);
+                        }
+                    }
+                }
+            } else {
+                float *slot = slot_ptr(p, s, c);
+#pragma unroll
+                for (int r = 0; r < N; ++r) {
+                    if (r < rows) {
+#pragma unroll
+                        for (int dc = 0; dc < C::DC; ++dc) slot[r * D + dc * 128 + tid] = o[dc][r];
+                    }
+                }
+                if (tid < rows) {
+                    // lane tid of every thread holds the same mrun/lsum values
+#pragma unroll
+                    for (int r = 0; r < N; ++r) {
+                        if (r == tid) {
+                            slot[rows * D + r] = mrun[r];
+                            slot[rows * D + rows + r] = lsum[r];
+                        }
+                    }
+                }
+                __threadfence();
+                ok = wg_sync();
+                if (tid == 0 && ok) bs->last_flag = atomicAdd(p.counters + s, 1) == c_last - c_first;
+                ok = ok && wg_sync();
+                if (!ok) { set_abort(bs, p); break; }
+                if (bs->last_flag) {
+                    __threadfence();
+                    for (int r = 0; r < rows; ++r) {
+                        float M = neg_inf();
+                        for (int c2 = c_first; c2 <= c_last; ++c2)
+                            M = fmaxf(M, __ldcg(slot_ptr(p, s, c2) + rows * D + r));
+                        float acc[C::DC];
+#pragma unroll
+                        for (int dc = 0; dc < C::DC; ++dc) acc[dc] = 0.f;
+                        float ls = 0.f;
+                        if (M != neg_inf()) {
+                            for (int c2 = c_first; c2 <= c_last; ++c2) {
+                                const float *sl = slot_ptr(p, s, c2);
+                                const float w = fast_exp2(__ldcg(sl + rows * D + r) - M);
+                                ls += w * __ldcg(sl + rows * D + rows + r);
+#pragma unroll
+                                for (int dc = 0; dc < C::DC; ++dc)
+                                    acc[dc] += w * __ldcg(sl + r * D + dc * 128 + tid);
+                            }
+                        }
+                        const float inv = ls > 0.f ? 1.f / ls : 0.f;
+                        const RowMap m = row_of(p, s, r);
+                        const int64_t off = (int64_t)m.b * p.os[0] + (int64_t)m.i * p.os[1] +
+                                            (int64_t)m.h * p.os[2];
+#pragma unroll
+                        for (int dc = 0; dc < C::DC; ++dc) {
+                            const float val = acc[dc] * inv;
+                            if (p.out_f32)
+                                reinterpret_cast<float *>(p.out)[off + dc * 128 + tid] = val;
+                            else
+                                reinterpret_cast<uint16_t *>(p.out)[off + dc * 128 + tid] = bf16_bits(val);
+                        }
+                    }
+                    if (tid == 0) p.counters[s] = 0;
+                }
+            }
+            t = piece_end;
+            ++piece;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// [B, Hkv, cap, d] cache -> 4-D map (d, cap, Hkv, B), box (64, 128, 1, 1),
+// 128-byte swizzle, rows past the capacity read as zeros.
+bool make_map(CUtensorMap *m, const void *base, const int64_t *st, const Params &p) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)p.cap, (cuuint64_t)p.Hkv, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)TT, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int N>
+int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
+    using C = Cfg<D, N>;
+    if (cudaFuncSetAttribute(tc_kernel<D, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM) != cudaSuccess)
+        return -5;
+    tc_kernel<D, N><<<G, kThreadsTC, C::SMEM, st>>>(args);
+    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+}
+
+template <int D>
+int launch_d(const TcArgs &args, int G, cudaStream_t st) {
+    const int rows = args.p.rows;
+    if (rows <= 16) return launch_dn<D, 16>(args, G, st);
+    if (rows <= 32) return launch_dn<D, 32>(args, G, st);
+    if (rows <= 48) return launch_dn<D, 48>(args, G, st);
+    if (rows <= 64) return launch_dn<D, 64>(args, G, st);
+    return -2;
+}
+
+}  // namespace
+
+int tc_tile_tokens() { return TT; }
+
+bool tc_supports(const Params &p) {
+    return p.mode == kDense && !p.kv_int8 && (p.d == 128 || p.d == 256) && p.rows >= 1 &&
+           p.rows <= 64 && p.cap < (int64_t)1 << 31 && p.B < (1 << 30) && p.Hkv < (1 << 30);
+}
+
+int launch_tc(const Params &p, int G, cudaStream_t st) {
+    if (!tc_supports(p)) return -2;
+    TcArgs args;
+    memset(&args, 0, sizeof args);
+    args.p = p;
+    if (!make_map(&args.tk, p.k, p.ks, p) || !make_map(&args.tv, p.v, p.vs, p)) return -5;
+    if (p.d == 128) return launch_d<128>(args, G, st);
+    return launch_d<256>(args, G, st);
+}
+
+}  // namespace fd

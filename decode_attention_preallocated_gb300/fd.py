@@ -28,7 +28,7 @@ LIB_PATH = os.path.join(_HERE, "libfd.so")
 FD_OK, FD_ERR_ARG, FD_ERR_UNSUPPORTED, FD_ERR_ALIGN, FD_ERR_WORKSPACE, FD_ERR_CUDA = 0, -1, -2, -3, -4, -5
 FD_ERR_SCRATCH = -6
 FD_BF16, FD_F32, FD_I8, FD_I32 = 0, 1, 2, 3
-FD_DEV_BAD_LENGTH, FD_DEV_BAD_INDEX = 1, 2
+FD_DEV_BAD_LENGTH, FD_DEV_BAD_INDEX, FD_DEV_INTERNAL = 1, 2, 4
 FD_KERNEL_AUTO, FD_KERNEL_SIMT, FD_KERNEL_TC = 0, 1, 2
 FD_MAX_ROWS = 64
 
@@ -260,8 +260,10 @@ def _prepare(q, k, out, out_dtype, segments, rows, num_ctas, kernel, stream, ws)
     sh = _stream_handle(stream, device)
     ctas = num_ctas
     if ctas == 0:
+        # an upper bound on what either kernel picks for an auto launch
         with torch.cuda.device(device):
-            ctas = auto_num_ctas(kernel, q.shape[-1], _DTYPES.get(k.dtype, FD_BF16), rows, 0)
+            ctas = max(auto_num_ctas(FD_KERNEL_SIMT, q.shape[-1], FD_BF16, rows, 0),
+                       auto_num_ctas(FD_KERNEL_TC, q.shape[-1], FD_BF16, rows, 0))
     if ws is None:
         ws = workspace_for(device, sh, segments, rows, q.shape[-1], max(ctas, 1))
     return out, sh, ws

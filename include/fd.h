@@ -81,11 +81,15 @@ extern "C" {
 /* sticky device status bits (fd_get_device_status) */
 #define FD_DEV_BAD_LENGTH 1      /* some kv_lengths[b] outside [0, cap]    */
 #define FD_DEV_BAD_INDEX 2       /* some idx entry >= cap (skipped)        */
+#define FD_DEV_INTERNAL 4        /* a bounded internal wait gave up; the
+                                    call's output is not valid              */
 
-/* kernel selection (fd_opts.kernel) */
+/* kernel selection (fd_opts.kernel); AUTO takes the tensor-core kernel for
+ * the dense bf16 modes and the CUDA-core kernel otherwise */
 #define FD_KERNEL_AUTO 0
 #define FD_KERNEL_SIMT 1         /* CUDA-core kernel, every mode           */
-#define FD_KERNEL_TC 2           /* tensor-core (tcgen05) kernel           */
+#define FD_KERNEL_TC 2           /* tensor-core (tcgen05) kernel, dense
+                                    bf16 modes only (else FD_ERR_UNSUPPORTED) */
 
 #define FD_MAX_ROWS 64           /* query rows per kv head per launch unit */
 
@@ -202,8 +206,8 @@ int fd_workspace_destroy(fd_workspace *ws);
 /* Synchronously reads the sticky status word (FD_DEV_* bits). */
 int fd_get_device_status(fd_workspace *ws, int32_t *status);
 
-/* Number of thread blocks an auto launch would use on the current device
- * (host query; 0 on error). */
+/* Number of thread blocks an auto launch of a dense call with this cache
+ * dtype would use on the current device (host query; 0 on error). */
 int32_t fd_auto_num_ctas(int32_t kernel, int32_t head_dim, int32_t kv_dtype,
                          int32_t rows, int64_t max_tiles);
 /* Cache positions per K/V tile for a kernel / head_dim / cache dtype. */
