@@ -314,6 +314,12 @@ int fd_get_device_status(fd_workspace *ws, int32_t *status) {
                ? FD_OK : FD_ERR_CUDA;
 }
 
+int fd_get_device_diagnostics(fd_workspace *ws, int32_t *words) {
+    if (!ws || !words) return FD_ERR_ARG;
+    return cudaMemcpy(words, ws->status, 13 * sizeof(int32_t), cudaMemcpyDeviceToHost) == cudaSuccess
+               ? FD_OK : FD_ERR_CUDA;
+}
+
 int32_t fd_auto_num_ctas(int32_t kernel, int32_t head_dim, int32_t kv_dtype, int32_t rows,
                          int64_t max_tiles) {
     (void)head_dim; (void)kv_dtype; (void)rows;

@@ -177,6 +177,7 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
 // Shared-memory matrix descriptor (sm_100 family): start address, leading and
 // stride byte offsets (all >> 4), descriptor version 1, layout type.
 constexpr uint64_t kLayoutSwizzle128 = 2;
+constexpr uint64_t kLayoutSwizzle32 = 6;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
                                               uint64_t layout) {

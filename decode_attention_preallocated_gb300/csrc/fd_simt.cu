@@ -328,30 +328,63 @@ simt_kernel(const __grid_constant__ Params p) {
             __syncthreads();
             if (sh_last) {
                 __threadfence();
+                // Merge the pieces' partials with independent loads: per-row
+                // maxima and merged sums first (one thread per row, kept in
+                // m_s / l_s), then piece by piece for every row of the thread.
+                if (tid < rows) {
+                    float M = neg_inf();
+#pragma unroll 8
+                    for (int c2 = c_first; c2 <= c_last; ++c2)
+                        M = fmaxf(M, __ldcg(slot_ptr(p, s, c2) + rows * D + tid));
+                    float lsum = 0.f;
+                    if (M != neg_inf()) {
+#pragma unroll 8
+                        for (int c2 = c_first; c2 <= c_last; ++c2) {
+                            const float *sl = slot_ptr(p, s, c2);
+                            lsum += fast_exp2(__ldcg(sl + rows * D + tid) - M) *
+                                    __ldcg(sl + rows * D + rows + tid);
+                        }
+                    }
+                    m_s[tid] = M;
+                    l_s[tid] = lsum > 0.f ? 1.f / lsum : 0.f;
+                }
+                __syncthreads();
+                float o[Ly::PV_RMAX][8];
+#pragma unroll
+                for (int k = 0; k < Ly::PV_RMAX; ++k)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[k][e] = 0.f;
+                // Rows clamped into range (weight 0 beyond `rows`): every load
+                // is unconditional, so one piece's loads are all in flight.
+                int rr[Ly::PV_RMAX];
+                float mr[Ly::PV_RMAX];
+#pragma unroll
+                for (int k = 0; k < Ly::PV_RMAX; ++k) {
+                    const int r = rg + Ly::PV_RG * k;
+                    rr[k] = r < rows ? r : rows - 1;
+                    mr[k] = r < rows ? m_s[rr[k]] : neg_inf();
+                }
+#pragma unroll 2
+                for (int c2 = c_first; c2 <= c_last; ++c2) {
+                    const float *sl = slot_ptr(p, s, c2);
+#pragma unroll
+                    for (int k = 0; k < Ly::PV_RMAX; ++k) {
+                        const float mv = __ldcg(sl + rows * D + rr[k]);
+                        const float4 a = __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + cg * 8));
+                        const float4 bq = __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + cg * 8 + 4));
+                        const float w = mr[k] == neg_inf() ? 0.f : fast_exp2(mv - mr[k]);
+                        o[k][0] += w * a.x; o[k][1] += w * a.y; o[k][2] += w * a.z; o[k][3] += w * a.w;
+                        o[k][4] += w * bq.x; o[k][5] += w * bq.y; o[k][6] += w * bq.z; o[k][7] += w * bq.w;
+                    }
+                }
 #pragma unroll
                 for (int k = 0; k < Ly::PV_RMAX; ++k) {
                     const int r = rg + Ly::PV_RG * k;
                     if (r < rows) {
-                        float M = neg_inf();
-                        for (int c2 = c_first; c2 <= c_last; ++c2)
-                            M = fmaxf(M, __ldcg(slot_ptr(p, s, c2) + rows * D + r));
-                        float o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                        if (M != neg_inf()) {
-                            float lsum = 0.f;
-                            for (int c2 = c_first; c2 <= c_last; ++c2) {
-                                const float *sl = slot_ptr(p, s, c2);
-                                const float w = fast_exp2(__ldcg(sl + rows * D + r) - M);
-                                lsum += w * __ldcg(sl + rows * D + rows + r);
-                                const float4 a = __ldcg(reinterpret_cast<const float4 *>(sl + r * D + cg * 8));
-                                const float4 bq = __ldcg(reinterpret_cast<const float4 *>(sl + r * D + cg * 8 + 4));
-                                o[0] += w * a.x; o[1] += w * a.y; o[2] += w * a.z; o[3] += w * a.w;
-                                o[4] += w * bq.x; o[5] += w * bq.y; o[6] += w * bq.z; o[7] += w * bq.w;
-                            }
-                            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                        const float inv = l_s[r];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) o[e] *= inv;
-                        }
-                        store_out8(p, row_of(p, s, r), cg * 8, o);
+                        for (int e = 0; e < 8; ++e) o[k][e] *= inv;
+                        store_out8(p, row_of(p, s, r), cg * 8, o[k]);
                     }
                 }
                 if (tid == 0) p.counters[s] = 0;

@@ -21,10 +21,11 @@
 //               and stores, or hands a split partial to the in-launch
 //               combine (last block to arrive merges; comfy-kitchen #239,
 //               "GQA decode").
-// Rows of V at or past the length are zeroed in shared memory before the PV
-// product, so garbage in the unused tail of the cache never reaches the
-// arithmetic.  Every wait is bounded (2 s); a timeout sets FD_DEV_INTERNAL
-// in the status word and the block drains its copies and MMAs and exits.
+// The last tile of a segment is loaded right-aligned (ending at the length),
+// so no row of the unused tail is ever read; positions the previous tile
+// already covered are masked.  Every wait is bounded (2 s); a timeout sets
+// FD_DEV_INTERNAL in the status word, records where it waited, and the block
+// drains its copies and MMAs and exits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -42,6 +43,10 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kDevTimeout = 4;          // mirrors FD_DEV_INTERNAL
+// Scores (log2 units) may exceed a row's running maximum by this much before
+// the maximum is refreshed and O rescaled; P is then at most 2^8, which fp32
+// accumulators and the hi/lo bf16 split of P carry without loss.
+constexpr float kRescaleSlack = 8.f;
 
 struct TcArgs {   // CUtensorMap members carry their own alignment
     CUtensorMap tk;
@@ -57,7 +62,7 @@ struct Cfg {
     static constexpr uint32_t SLOT = KB * BOX;   // one K or V tile
     static constexpr uint32_t QB = N * 128;      // one 64-column box of Q or P
     static constexpr uint32_t QBYTES = KB * QB;
-    static constexpr uint32_t PPLANE = 2 * QB;   // one bf16 plane of P (128 positions)
+    static constexpr uint32_t PPLANE = 2 * QB;   // one bf16 plane of P (128 positions x N)
     static constexpr uint32_t PSTAGE = 2 * PPLANE;   // P = hi plane + lo plane
     // Barriers and the reduction scratch come first, then 1024-byte aligned
     // operand buffers.
@@ -78,7 +83,10 @@ struct Cfg {
     static constexpr uint32_t COLS = 2 * N + DC * N;
     static constexpr uint32_t TMEM_COLS = COLS <= 32 ? 32 : COLS <= 64 ? 64 : COLS <= 128 ? 128 : 256;
     static constexpr uint32_t IDESC_QK = ptx::idesc_bf16(128, N, 0, 0);
-    static constexpr uint32_t IDESC_PV = ptx::idesc_bf16(128, N, 1, 0);
+    static constexpr uint32_t IDESC_PV = ptx::idesc_bf16(128, N, 1, 1);
+    // P planes are MN-major (query rows contiguous per position) with 32-byte
+    // swizzle: 16-row atoms of TT positions x 32 bytes.
+    static constexpr uint32_t PATOM = TT * 32;
 };
 
 struct Bars {
@@ -90,7 +98,17 @@ struct Bars {
     int last_flag;
     int pad;
     int64_t total;
+    int vote[2][4];
 };
+
+// First cache position loaded for tile tt of a segment of length L: tiles
+// start at tt * TT, except the last, which is right-aligned to end at L (its
+// start may be negative, where TMA fills zeros), so no position past the
+// filled prefix is ever loaded.
+__device__ __forceinline__ int64_t tile_start(int64_t tt, int64_t L) {
+    const int64_t y0 = tt * TT;
+    return y0 + TT > L ? L - TT : y0;
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -112,6 +130,25 @@ __device__ __forceinline__ uint16_t bf16_bits(float x) {
 __device__ __forceinline__ void set_abort(Bars *bs, const Params &p) {
     bs->abort_flag = 1;
     atomicOr(p.status, kDevTimeout);
+}
+
+// A wait that gives up records where (read back by fd_get_device_diagnostics):
+// status[1..3] = site, tile counter and piece index of the first one in the
+// launch; status[4 + 3r .. 6 + 3r] the same for the first failing wait of
+// role r (0 producer, 1 MMA issuer, 2 softmax), so a stall shows what every
+// role was blocked on when the block gave up.
+__device__ __forceinline__ void note_timeout(Bars *bs, const Params &p, int site,
+                                             uint32_t tile, int piece) {
+    if (!bs->abort_flag && atomicCAS(p.status + 1, 0, site) == 0) {
+        p.status[2] = (int)tile;
+        p.status[3] = piece;
+    }
+    const int role = site == 1 ? 0 : (site <= 7 ? 1 : 2);
+    if (atomicCAS(p.status + 4 + 3 * role, 0, site) == 0) {
+        p.status[5 + 3 * role] = (int)tile;
+        p.status[6 + 3 * role] = piece;
+    }
+    set_abort(bs, p);
 }
 
 template <int D, int N>
@@ -195,11 +232,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             if (s < 0) break;
             const int64_t piece_end = min(t_end, pos.first + pos.ntiles);
             const int b = (int)(s / p.Hkv), hk = (int)(s % p.Hkv);
+            const int64_t L = seq_len(p, b);
             for (int64_t tt = t - pos.first; tt < piece_end - pos.first && ok; ++tt) {
+                const int ys = (int)tile_start(tt, L);
                 for (int kv = 0; kv < 2 && ok; ++kv) {
                     const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
                     if (lane == 0) {
                         ok = ptx::mbar_wait(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+                        if (!ok) note_timeout(bs, p, 1, issued, 0);
                         if (ok) {
                             ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
                             unsigned char *dst = smem + C::OFF_SLOTS + slot * C::SLOT;
@@ -207,10 +247,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                             for (int cb = 0; cb < C::KB; ++cb)
                                 ptx::tma_load_4d(dst + cb * C::BOX, kv ? (const void *)&a.tv
                                                                        : (const void *)&a.tk,
-                                                 &bs->slot_full[slot], cb * 64, (int)(tt * TT),
-                                                 hk, b);
-                        } else {
-                            set_abort(bs, p);
+                                                 &bs->slot_full[slot], cb * 64, ys, hk, b);
                         }
                     }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -234,73 +271,98 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         int piece = 0;
         bool ok = true;
         bool issued_any = false;
+        // S^T[pos, row] = sum_d K[pos, d] Q[row, d] for tile number tc.
+        auto issue_qk = [&](uint32_t tc) -> bool {
+            const uint32_t sb = tc & 1, u = tc >> 1, ki = 2 * tc, ks = ki % C::NS;
+            if (!ptx::mbar_wait(&bs->slot_full[ks], (ki / C::NS) & 1, abort_flag, kWaitNs)) {
+                note_timeout(bs, p, 3, tc, piece);
+                return false;
+            }
+            if (!ptx::mbar_wait(&bs->s_free[sb], (u & 1) ^ 1, abort_flag, kWaitNs)) {
+                note_timeout(bs, p, 4, tc, piece);
+                return false;
+            }
+            ptx::tc_fence_after();
+            const uint32_t k_addr = smem_base + C::OFF_SLOTS + ks * C::SLOT;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t da = ptx::smem_desc(k_addr + (kk >> 2) * C::BOX + (kk & 3) * 32, 16,
+                                                   1024, ptx::kLayoutSwizzle128);
+                const uint64_t db = ptx::smem_desc(q_addr + (kk >> 2) * C::QB + (kk & 3) * 32, 16,
+                                                   1024, ptx::kLayoutSwizzle128);
+                ptx::mma_f16_ss(tmem + sb * N, da, db, C::IDESC_QK, kk > 0);
+            }
+            ptx::mma_commit(&bs->slot_empty[ks]);
+            ptx::mma_commit(&bs->s_full[sb]);
+            issued_any = true;
+            return true;
+        };
+        // O^T[dim, row] += sum_pos V[pos, dim] (P_hi + P_lo)[row, pos] for tile tc.
+        auto issue_pv = [&](uint32_t tc, bool first) -> bool {
+            const uint32_t vi = 2 * tc + 1, vs = vi % C::NS;
+            const uint32_t ps = tc % C::PST, pu = tc / C::PST;
+            if (!ptx::mbar_wait(&bs->slot_full[vs], (vi / C::NS) & 1, abort_flag, kWaitNs)) {
+                note_timeout(bs, p, 6, tc, piece);
+                return false;
+            }
+            if (!ptx::mbar_wait(&bs->p_full[ps], pu & 1, abort_flag, kWaitNs)) {
+                note_timeout(bs, p, 7, tc, piece);
+                return false;
+            }
+            ptx::tc_fence_after();
+            const uint32_t v_addr = smem_base + C::OFF_SLOTS + vs * C::SLOT;
+            const uint32_t pb = p_addr + ps * C::PSTAGE;
+#pragma unroll
+            for (int dc = 0; dc < C::DC; ++dc) {
+#pragma unroll
+                for (int kt = 0; kt < TT / 16; ++kt) {
+                    const uint64_t da = ptx::smem_desc(v_addr + (2 * dc) * C::BOX + kt * 2048,
+                                                       C::BOX, 1024, ptx::kLayoutSwizzle128);
+#pragma unroll
+                    for (int plane = 0; plane < 2; ++plane) {
+                        const uint64_t db = ptx::smem_desc(pb + plane * C::PPLANE + kt * 512,
+                                                           C::PATOM, 256, ptx::kLayoutSwizzle32);
+                        ptx::mma_f16_ss(tmem + 2 * N + dc * N, da, db, C::IDESC_PV,
+                                        (!first || kt > 0 || plane > 0) ? 1u : 0u);
+                    }
+                }
+            }
+            ptx::mma_commit(&bs->slot_empty[vs]);
+            ptx::mma_commit(&bs->p_free[ps]);
+            ptx::mma_commit(&bs->o_done);
+            return true;
+        };
         int64_t t = t_begin;
         while (t < t_end && ok) {
             SegPos pos;
             const int64_t s = seg_of_tile_warp(p, t, &pos);
             if (s < 0) break;
             const int64_t piece_end = min(t_end, pos.first + pos.ntiles);
-            const int64_t n_in = piece_end - t;
+            const uint32_t n_in = (uint32_t)(piece_end - t);
             if (lane == 0) {
+                // Software pipeline: QK of tile j+1 is issued before PV of
+                // tile j, so the next scores are ready when softmax finishes.
                 ok = ptx::mbar_wait(&bs->q_full, piece & 1, abort_flag, kWaitNs);
-                if (ok && piece > 0)
-                    ok = ptx::mbar_wait(&bs->o_free, (piece - 1) & 1, abort_flag, kWaitNs);
+                if (!ok) note_timeout(bs, p, 2, tile_ctr, piece);
                 ptx::tc_fence_after();
-                for (int64_t j = 0; j < n_in && ok; ++j) {
-                    const uint32_t sb = tile_ctr & 1, u = tile_ctr >> 1;
-                    const uint32_t ki = 2 * tile_ctr, vi = 2 * tile_ctr + 1;
-                    const uint32_t ks = ki % C::NS, vs = vi % C::NS;
-                    ok = ptx::mbar_wait(&bs->slot_full[ks], (ki / C::NS) & 1, abort_flag, kWaitNs) &&
-                         ptx::mbar_wait(&bs->s_free[sb], (u & 1) ^ 1, abort_flag, kWaitNs);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    // S^T[pos, row] = sum_d K[pos, d] Q[row, d]
-                    const uint32_t k_addr = smem_base + C::OFF_SLOTS + ks * C::SLOT;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t da = ptx::smem_desc(k_addr + (kk >> 2) * C::BOX + (kk & 3) * 32,
-                                                           16, 1024, ptx::kLayoutSwizzle128);
-                        const uint64_t db = ptx::smem_desc(q_addr + (kk >> 2) * C::QB + (kk & 3) * 32,
-                                                           16, 1024, ptx::kLayoutSwizzle128);
-                        ptx::mma_f16_ss(tmem + sb * N, da, db, C::IDESC_QK, kk > 0);
+                ok = ok && issue_qk(tile_ctr);
+                if (ok && n_in == 1) ptx::mma_commit(&bs->q_free);
+                for (uint32_t j = 0; j < n_in && ok; ++j) {
+                    if (j + 1 < n_in) {
+                        ok = issue_qk(tile_ctr + j + 1);
+                        if (!ok) break;
+                        if (j + 2 == n_in) ptx::mma_commit(&bs->q_free);
                     }
-                    ptx::mma_commit(&bs->slot_empty[ks]);
-                    ptx::mma_commit(&bs->s_full[sb]);
-                    if (j == n_in - 1) ptx::mma_commit(&bs->q_free);
-                    issued_any = true;
-                    const uint32_t ps = tile_ctr % C::PST, pu = tile_ctr / C::PST;
-                    ok = ptx::mbar_wait(&bs->slot_full[vs], (vi / C::NS) & 1, abort_flag, kWaitNs) &&
-                         ptx::mbar_wait(&bs->p_full[ps], pu & 1, abort_flag, kWaitNs);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-                    // O^T[dim, row] += sum_pos V[pos, dim] (P_hi + P_lo)[row, pos]
-                    const uint32_t v_addr = smem_base + C::OFF_SLOTS + vs * C::SLOT;
-                    const uint32_t pb = p_addr + ps * C::PSTAGE;
-#pragma unroll
-                    for (int dc = 0; dc < C::DC; ++dc) {
-#pragma unroll
-                        for (int kt = 0; kt < TT / 16; ++kt) {
-                            const uint64_t da = ptx::smem_desc(v_addr + (2 * dc) * C::BOX + kt * 2048,
-                                                               C::BOX, 1024, ptx::kLayoutSwizzle128);
-#pragma unroll
-                            for (int plane = 0; plane < 2; ++plane) {
-                                const uint64_t db = ptx::smem_desc(
-                                    pb + plane * C::PPLANE + (kt >> 2) * C::QB + (kt & 3) * 32, 16,
-                                    1024, ptx::kLayoutSwizzle128);
-                                ptx::mma_f16_ss(tmem + 2 * N + dc * N, da, db, C::IDESC_PV,
-                                                (j > 0 || kt > 0 || plane > 0) ? 1u : 0u);
-                            }
-                        }
+                    if (j == 0 && piece > 0) {
+                        ok = ptx::mbar_wait(&bs->o_free, (piece - 1) & 1, abort_flag, kWaitNs);
+                        if (!ok) note_timeout(bs, p, 5, tile_ctr, piece);
                     }
-                    ptx::mma_commit(&bs->slot_empty[vs]);
-                    ptx::mma_commit(&bs->p_free[ps]);
-                    ptx::mma_commit(&bs->o_done);
-                    ++tile_ctr;
+                    ok = ok && issue_pv(tile_ctr + j, j == 0);
                 }
                 if (!ok) set_abort(bs, p);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            tile_ctr = __shfl_sync(0xffffffffu, tile_ctr, 0);
+            tile_ctr += n_in;
             t = piece_end;
             ++piece;
         }
@@ -321,13 +383,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         // parity test never aliases with a phase two steps ahead or behind.
         auto wait_pv = [&](uint32_t k) -> bool {
             for (; o_seen <= k; ++o_seen)
-                if (!ptx::mbar_wait(&bs->o_done, o_seen & 1, abort_flag, kWaitNs)) return false;
+                if (!ptx::mbar_wait(&bs->o_done, o_seen & 1, abort_flag, kWaitNs)) {
+                    note_timeout(bs, p, 11, tile_ctr, piece);
+                    return false;
+                }
             return true;
         };
         // Barrier over the 128 softmax threads with a bounded wait.
         auto wg_sync = [&]() -> bool {
             ptx::mbar_arrive(&bs->wg_bar);
-            return ptx::mbar_wait(&bs->wg_bar, (wg_ctr++) & 1, abort_flag, kWaitNs);
+            if (ptx::mbar_wait(&bs->wg_bar, (wg_ctr++) & 1, abort_flag, kWaitNs)) return true;
+            note_timeout(bs, p, 10, tile_ctr, piece);
+            return false;
         };
         int64_t t = t_begin;
         while (t < t_end && ok) {
@@ -343,7 +410,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 
             // Q rows of this segment -> shared memory (K-major, 128-byte swizzle).
             if (piece > 0) ok = ptx::mbar_wait(&bs->q_free, (piece - 1) & 1, abort_flag, kWaitNs);
-            if (!ok) { set_abort(bs, p); break; }
+            if (!ok) { note_timeout(bs, p, 8, tile_ctr, piece); break; }
             for (int e = tid; e < N * (D / 8); e += 128) {
                 const int r = e / (D / 8), cc = e % (D / 8);
                 uint32_t w[4] = {0, 0, 0, 0};
@@ -368,10 +435,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 
             for (int64_t j = 0; j < n_in && ok; ++j) {
                 const int64_t y0 = (tt0 + j) * TT;
-                const int64_t token = y0 + tid;
+                const int64_t token = tile_start(tt0 + j, L) + tid;
                 const uint32_t sb = tile_ctr & 1, u = tile_ctr >> 1;
                 ok = ptx::mbar_wait(&bs->s_full[sb], u & 1, abort_flag, kWaitNs);
-                if (!ok) break;
+                if (!ok) { note_timeout(bs, p, 9, tile_ctr, piece); break; }
                 ptx::tc_fence_after();
                 float sv[N];
 #pragma unroll
@@ -381,91 +448,109 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&bs->s_free[sb]);
 
-                // Visibility: inside the filled prefix and, for causal windows,
-                // at or before L - n_q + i for the row's query index i.
-                const bool in_len = token < L;
+                // Visibility: a position this tile owns (the right-aligned last
+                // tile also holds positions the previous tile covered), inside
+                // the filled prefix and, for causal windows, at or before
+                // L - n_q + i for the row's query index i.
+                const bool in_len = token >= y0 && token < L;
 #pragma unroll
                 for (int r = 0; r < N; ++r) {
                     bool vis = in_len && r < rows;
                     if (p.causal) vis = vis && token <= L - p.n_q + (r % p.n_q);
                     sv[r] = vis ? sv[r] * p.scale_log2 : neg_inf();
                 }
-                // Column maxima over the 128 positions of the tile.
-                float *rb = red + (tile_ctr & 1) * (4 * N);
+                // Refresh the running maxima only when some score passes
+                // mrun + kRescaleSlack (always on a segment's first tile).
+                bool need = false;
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    const float mx = warp_max(sv[r]);
-                    if (lane == 0) rb[warp * N + r] = mx;
-                }
+                for (int r = 0; r < N; ++r) need = need || (sv[r] > mrun[r] + kRescaleSlack);
+                need = __any_sync(0xffffffffu, need);
+                if (lane == 0) bs->vote[tile_ctr & 1][warp] = need;
                 ok = wg_sync();
                 if (!ok) break;
-                float alpha[N];
-                bool grow = false;
+                const int *vt = bs->vote[tile_ctr & 1];
+                if (vt[0] | vt[1] | vt[2] | vt[3]) {
+                    // Column maxima over the 128 positions of the tile.
+                    float *rb = red + (tile_ctr & 1) * (4 * N);
+#pragma unroll
+                    for (int r = 0; r < N; ++r) {
+                        const float mx = warp_max(sv[r]);
+                        if (lane == 0) rb[warp * N + r] = mx;
+                    }
+                    ok = wg_sync();
+                    if (!ok) break;
+                    float alpha[N];
+                    bool grow = false;
+#pragma unroll
+                    for (int r = 0; r < N; ++r) {
+                        const float tmax = fmaxf(fmaxf(rb[r], rb[N + r]), fmaxf(rb[2 * N + r], rb[3 * N + r]));
+                        const float mnew = fmaxf(mrun[r], tmax);
+                        const float muse = mnew == neg_inf() ? 0.f : mnew;
+                        alpha[r] = fast_exp2(mrun[r] - muse);
+                        grow = grow || (alpha[r] < 1.f);
+                        mrun[r] = mnew;
+                        lpart[r] *= alpha[r];
+                    }
+                    // Rescale the running O in TMEM (after the previous PV landed).
+                    if (grow && j > 0) {
+                        ok = wait_pv(tile_ctr - 1);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+#pragma unroll
+                        for (int dc = 0; dc < C::DC; ++dc) {
+#pragma unroll
+                            for (int cb = 0; cb < N / 16; ++cb) {
+                                float o[16];
+                                const uint32_t ta = tmem + lane_base + 2 * N + dc * N + cb * 16;
+                                ptx::tmem_ld16(ta, o);
+                                ptx::tmem_wait_ld();
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) o[k] *= alpha[cb * 16 + k];
+                                ptx::tmem_st16(ta, o);
+                            }
+                        }
+                        ptx::tmem_wait_st();
+                    }
+                }
 #pragma unroll
                 for (int r = 0; r < N; ++r) {
-                    const float tmax = fmaxf(fmaxf(rb[r], rb[N + r]), fmaxf(rb[2 * N + r], rb[3 * N + r]));
-                    const float mnew = fmaxf(mrun[r], tmax);
-                    const float muse = mnew == neg_inf() ? 0.f : mnew;
-                    alpha[r] = fast_exp2(mrun[r] - muse);
-                    grow = grow || (alpha[r] < 1.f);
-                    mrun[r] = mnew;
+                    const float muse = mrun[r] == neg_inf() ? 0.f : mrun[r];
                     const float pr = fast_exp2(sv[r] - muse);
-                    lpart[r] = lpart[r] * alpha[r] + pr;
+                    lpart[r] += pr;
                     sv[r] = pr;
-                }
-                // Rescale the running O in TMEM (after the previous PV landed).
-                if (grow && j > 0) {
-                    ok = wait_pv(tile_ctr - 1);
-                    if (!ok) break;
-                    ptx::tc_fence_after();
-#pragma unroll
-                    for (int dc = 0; dc < C::DC; ++dc) {
-#pragma unroll
-                        for (int cb = 0; cb < N / 16; ++cb) {
-                            float o[16];
-                            const uint32_t ta = tmem + lane_base + 2 * N + dc * N + cb * 16;
-                            ptx::tmem_ld16(ta, o);
-                            ptx::tmem_wait_ld();
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) o[k] *= alpha[cb * 16 + k];
-                            ptx::tmem_st16(ta, o);
-                        }
-                    }
-                    ptx::tmem_wait_st();
-                }
-                // Zero the V rows at or past the length in the segment's last tile.
-                if (y0 + TT > L) {
-                    const uint32_t vi = 2 * tile_ctr + 1;
-                    ok = ptx::mbar_wait(&bs->slot_full[vi % C::NS], (vi / C::NS) & 1, abort_flag,
-                                        kWaitNs);
-                    if (!ok) break;
-                    if (!in_len) {
-                        unsigned char *row = smem + C::OFF_SLOTS + (vi % C::NS) * C::SLOT + tid * 128;
-#pragma unroll
-                        for (int cb = 0; cb < C::KB; ++cb)
-#pragma unroll
-                            for (int k = 0; k < 8; ++k)
-                                *reinterpret_cast<uint4 *>(row + cb * C::BOX + k * 16) =
-                                    make_uint4(0, 0, 0, 0);
-                    }
                 }
                 // P^T (rows x positions, K-major) for the PV product.
                 const uint32_t ps = tile_ctr % C::PST, pu = tile_ctr / C::PST;
                 ok = ptx::mbar_wait(&bs->p_free[ps], (pu & 1) ^ 1, abort_flag, kWaitNs);
-                if (!ok) break;
+                if (!ok) { note_timeout(bs, p, 13, tile_ctr, piece); break; }
+                // PV of the previous tile must have completed before P of this
+                // tile is published: o_done is then exactly one phase behind or
+                // level, so its parity test cannot alias.
+                if (tile_ctr > 0) {
+                    ok = wait_pv(tile_ctr - 1);
+                    if (!ok) break;
+                }
                 {
                     // P = hi + lo, both bf16: hi = rn(p), lo = rn(p - hi), so the
-                    // PV product sees p to about 2^-17 relative.
-                    unsigned char *pbuf = smem + C::OFF_P + ps * C::PSTAGE + (tid >> 6) * C::QB;
-                    const int ch = (tid & 63) >> 3, el = tid & 7;
+                    // PV product sees p to about 2^-17 relative.  Thread tid
+                    // writes its position's row: 8 query rows per 16-byte chunk,
+                    // chunk c of a 16-row atom stored at c ^ bit 2 of tid.
+                    unsigned char *prow = smem + C::OFF_P + ps * C::PSTAGE + tid * 32;
+                    const int sw = (tid >> 2) & 1;
 #pragma unroll
-                    for (int r = 0; r < N; ++r) {
-                        const uint16_t hi = bf16_bits(sv[r]);
-                        const float hf = __uint_as_float((uint32_t)hi << 16);
-                        const uint16_t lo = bf16_bits(sv[r] - hf);
-                        const uint32_t off = r * 128 + ((ch ^ (r & 7)) << 4) + el * 2;
-                        *reinterpret_cast<uint16_t *>(pbuf + off) = hi;
-                        *reinterpret_cast<uint16_t *>(pbuf + C::PPLANE + off) = lo;
+                    for (int a8 = 0; a8 < N / 8; ++a8) {
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float p0 = sv[a8 * 8 + 2 * e], p1 = sv[a8 * 8 + 2 * e + 1];
+                            const uint32_t h = pack_bf16x2(p0, p1);
+                            hw[e] = h;
+                            lw[e] = pack_bf16x2(p0 - bf16lo(h), p1 - bf16hi(h));
+                        }
+                        const uint32_t off = (a8 >> 1) * C::PATOM + (((a8 & 1) ^ sw) << 4);
+                        *reinterpret_cast<uint4 *>(prow + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4 *>(prow + C::PPLANE + off) =
+                            make_uint4(lw[0], lw[1], lw[2], lw[3]);
                     }
                 }
                 ptx::fence_proxy_async_smem();
@@ -548,37 +633,85 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 if (!ok) { set_abort(bs, p); break; }
                 if (bs->last_flag) {
                     __threadfence();
-                    for (int r = 0; r < rows; ++r) {
+                    // Merge the pieces' partials.  Loads are arranged so that
+                    // none depends on another: per-row maxima and sums by one
+                    // thread per row, then piece by piece for 16 rows at a time.
+                    float *cm = red;          // row maxima over the pieces
+                    float *ci = red + N;      // 1 / merged row sums
+                    if (tid < rows) {
                         float M = neg_inf();
+#pragma unroll 8
                         for (int c2 = c_first; c2 <= c_last; ++c2)
-                            M = fmaxf(M, __ldcg(slot_ptr(p, s, c2) + rows * D + r));
-                        float acc[C::DC];
-#pragma unroll
-                        for (int dc = 0; dc < C::DC; ++dc) acc[dc] = 0.f;
+                            M = fmaxf(M, __ldcg(slot_ptr(p, s, c2) + rows * D + tid));
                         float ls = 0.f;
                         if (M != neg_inf()) {
+#pragma unroll 8
                             for (int c2 = c_first; c2 <= c_last; ++c2) {
                                 const float *sl = slot_ptr(p, s, c2);
-                                const float w = fast_exp2(__ldcg(sl + rows * D + r) - M);
-                                ls += w * __ldcg(sl + rows * D + rows + r);
-#pragma unroll
-                                for (int dc = 0; dc < C::DC; ++dc)
-                                    acc[dc] += w * __ldcg(sl + r * D + dc * 128 + tid);
+                                ls += fast_exp2(__ldcg(sl + rows * D + tid) - M) *
+                                      __ldcg(sl + rows * D + rows + tid);
                             }
                         }
-                        const float inv = ls > 0.f ? 1.f / ls : 0.f;
-                        const RowMap m = row_of(p, s, r);
-                        const int64_t off = (int64_t)m.b * p.os[0] + (int64_t)m.i * p.os[1] +
-                                            (int64_t)m.h * p.os[2];
+                        cm[tid] = M;
+                        ci[tid] = ls > 0.f ? 1.f / ls : 0.f;
+                    }
+                    ok = wg_sync();
+                    if (!ok) { set_abort(bs, p); break; }
+                    // Thread -> 4 consecutive dims of rows rg, rg + RG, ...  Row
+                    // indices are clamped into range (weight 0 beyond `rows`) so
+                    // every load is unconditional and a chunk's loads for two
+                    // pieces are all in flight together.
+                    constexpr int TPR = D / 4, RG = 128 / TPR, RPT = N / RG;
+                    constexpr int CH = RPT < 8 ? RPT : 8;
+                    const int dq = (tid % TPR) * 4, rg = tid / TPR;
+#pragma unroll 1
+                    for (int k0 = 0; k0 < RPT && rg + RG * k0 < rows; k0 += CH) {
+                        float4 acc[CH];
+                        float mr[CH];
+                        int rr[CH];
 #pragma unroll
-                        for (int dc = 0; dc < C::DC; ++dc) {
-                            const float val = acc[dc] * inv;
-                            if (p.out_f32)
-                                reinterpret_cast<float *>(p.out)[off + dc * 128 + tid] = val;
-                            else
-                                reinterpret_cast<uint16_t *>(p.out)[off + dc * 128 + tid] = bf16_bits(val);
+                        for (int k = 0; k < CH; ++k) {
+                            const int r = rg + RG * (k0 + k);
+                            rr[k] = r < rows ? r : rows - 1;
+                            mr[k] = r < rows ? cm[rr[k]] : neg_inf();
+                            acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll 2
+                        for (int c2 = c_first; c2 <= c_last; ++c2) {
+                            const float *sl = slot_ptr(p, s, c2);
+#pragma unroll
+                            for (int k = 0; k < CH; ++k) {
+                                const float mv = __ldcg(sl + rows * D + rr[k]);
+                                const float4 v =
+                                    __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + dq));
+                                const float w = mr[k] == neg_inf() ? 0.f : fast_exp2(mv - mr[k]);
+                                acc[k].x += w * v.x; acc[k].y += w * v.y;
+                                acc[k].z += w * v.z; acc[k].w += w * v.w;
+                            }
+                        }
+#pragma unroll
+                        for (int k = 0; k < CH; ++k) {
+                            const int r = rg + RG * (k0 + k);
+                            if (r < rows) {
+                                const RowMap m = row_of(p, s, r);
+                                const int64_t off = (int64_t)m.b * p.os[0] +
+                                                    (int64_t)m.i * p.os[1] + (int64_t)m.h * p.os[2] + dq;
+                                const float inv = ci[r];
+                                const float o4[4] = {acc[k].x * inv, acc[k].y * inv, acc[k].z * inv,
+                                                     acc[k].w * inv};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    if (p.out_f32)
+                                        reinterpret_cast<float *>(p.out)[off + e] = o4[e];
+                                    else
+                                        reinterpret_cast<uint16_t *>(p.out)[off + e] = bf16_bits(o4[e]);
+                                }
+                            }
                         }
                     }
+                    // cm / ci live in the reduction scratch the next tile reuses.
+                    ok = wg_sync();
+                    if (!ok) { set_abort(bs, p); break; }
                     if (tid == 0) p.counters[s] = 0;
                 }
             }

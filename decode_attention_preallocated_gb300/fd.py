@@ -81,6 +81,7 @@ _SIGNATURES = [
     ("fd_workspace_reset", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     ("fd_workspace_destroy", ctypes.c_int, [ctypes.c_void_p]),
     ("fd_get_device_status", ctypes.c_int, [ctypes.c_void_p, _P(ctypes.c_int32)]),
+    ("fd_get_device_diagnostics", ctypes.c_int, [ctypes.c_void_p, _P(ctypes.c_int32)]),
     ("fd_auto_num_ctas", ctypes.c_int32,
      [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64]),
     ("fd_tile_tokens", ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
@@ -179,6 +180,12 @@ class Workspace:
             _check(lib().fd_get_device_status(self.handle, ctypes.byref(st)),
                    "fd_get_device_status")
         return int(st.value)
+
+    def diagnostics(self):
+        w = (ctypes.c_int32 * 13)()
+        with torch.cuda.device(self.device):
+            _check(lib().fd_get_device_diagnostics(self.handle, w), "fd_get_device_diagnostics")
+        return list(w)
 
     def close(self):
         if getattr(self, "handle", None) is not None and self.handle.value:

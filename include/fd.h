@@ -205,6 +205,12 @@ int fd_workspace_reset(fd_workspace *ws, void *stream);
 int fd_workspace_destroy(fd_workspace *ws);
 /* Synchronously reads the sticky status word (FD_DEV_* bits). */
 int fd_get_device_status(fd_workspace *ws, int32_t *status);
+/* Synchronously reads 13 words: the status word; then, if FD_DEV_INTERNAL was
+ * set by the tensor-core kernel, the id, tile counter and piece index of the
+ * first internal wait that gave up; then the same three for the first wait
+ * that gave up in each role (TMA producer, MMA issuer, softmax).  Zero where
+ * nothing gave up.  Cleared by fd_workspace_reset. */
+int fd_get_device_diagnostics(fd_workspace *ws, int32_t *words);
 
 /* Number of thread blocks an auto launch of a dense call with this cache
  * dtype would use on the current device (host query; 0 on error). */

@@ -33,18 +33,36 @@ def to_dev(inp, device="cuda"):
 
 def run_gpu(inp, out_dtype=torch.bfloat16, num_ctas=0, kernel=fd.FD_KERNEL_AUTO,
             workspace=None):
+    """One call through the C ABI.  Without an explicit workspace the call gets
+    a fresh one, and afterwards its status word must not report an internal
+    error (a bounded wait that gave up)."""
+    own = workspace is None
+    if own:
+        B, n_q, Hq, d = inp.q.shape
+        Hkv = inp.k.shape[1]
+        workspace = fd.Workspace(B * n_q * Hkv, min(64, (Hq // Hkv) * n_q), 256,
+                                 max(2048, num_ctas))
     if inp.idx is not None:
-        return fd.decode_gather(inp.q, inp.k, inp.v, inp.idx, scale=inp.scale,
-                                out_dtype=out_dtype, num_ctas=num_ctas, kernel=kernel,
-                                workspace=workspace)
-    if inp.k.dtype == torch.int8:
-        return fd.decode_int8(inp.q, inp.k, inp.v, inp.k_scale, inp.v_scale,
-                              inp.kv_lengths, n_q=inp.n_q, causal=inp.causal,
-                              scale=inp.scale, out_dtype=out_dtype, num_ctas=num_ctas,
-                              kernel=kernel, workspace=workspace)
-    return fd.decode(inp.q, inp.k, inp.v, inp.kv_lengths, n_q=inp.n_q,
-                     causal=inp.causal, scale=inp.scale, out_dtype=out_dtype,
-                     num_ctas=num_ctas, kernel=kernel, workspace=workspace)
+        out = fd.decode_gather(inp.q, inp.k, inp.v, inp.idx, scale=inp.scale,
+                               out_dtype=out_dtype, num_ctas=num_ctas, kernel=kernel,
+                               workspace=workspace)
+    elif inp.k.dtype == torch.int8:
+        out = fd.decode_int8(inp.q, inp.k, inp.v, inp.k_scale, inp.v_scale,
+                             inp.kv_lengths, n_q=inp.n_q, causal=inp.causal,
+                             scale=inp.scale, out_dtype=out_dtype, num_ctas=num_ctas,
+                             kernel=kernel, workspace=workspace)
+    else:
+        out = fd.decode(inp.q, inp.k, inp.v, inp.kv_lengths, n_q=inp.n_q,
+                        causal=inp.causal, scale=inp.scale, out_dtype=out_dtype,
+                        num_ctas=num_ctas, kernel=kernel, workspace=workspace)
+    if own:
+        torch.cuda.synchronize()
+        st = workspace.diagnostics()
+        assert not st[0] & fd.FD_DEV_INTERNAL, (
+            "kernel %d reported an internal error: wait site %d, tile %d, piece %d"
+            % (kernel, st[1], st[2], st[3]))
+        workspace.close()
+    return out
 
 
 def run_oracle(inp):
