@@ -153,8 +153,24 @@ class ClockSampler:
 
 # -------------------------------------------------------------- workloads
 def make_inputs(name, seed, device):
+    """A named workload, or "sweep:L,B,Hq,Hkv,d,n_q": B sequences all of
+    length L in a cache of capacity L + 1000 (causal when n_q > 1)."""
     from decode_attention_preallocated_gb300 import workloads as W
+    if name.startswith("sweep:"):
+        L, B, Hq, Hkv, d, nq = (int(x) for x in name[6:].split(","))
+        return W.dense_inputs(B, nq, Hq, Hkv, d, L + 1000, [L] * B, seed, nq > 1,
+                              device=device, name=name)
     return W.workload(name, seed=seed, device=device)
+
+
+def workload_desc(name):
+    if name == WORKLOAD:
+        return WORKLOAD_DESC
+    if name.startswith("sweep:"):
+        L, B, Hq, Hkv, d, nq = name[6:].split(",")
+        return ("uniform decode: B=%s, kv_len=%s, cap=kv_len+1000, n_q=%s%s, Hq=%s, Hkv=%s, "
+                "head_dim=%s, bf16 K/V" % (B, L, nq, " causal" if int(nq) > 1 else "", Hq, Hkv, d))
+    return name
 
 
 def call_fn(inp, out, ws, kernel, num_ctas=0):
@@ -364,7 +380,7 @@ def run_fd(args):
               "tc": fd.FD_KERNEL_TC}[args.kernel]
     peak, peak_kind = peaks()
 
-    inp = make_inputs(WORKLOAD, seed=1 + rank, device=device)
+    inp = make_inputs(args.workload, seed=1 + rank, device=device)
     nbytes = algorithmic_bytes(inp)
     ws = workspace_for(inp, device)
     out = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=device)
@@ -455,7 +471,7 @@ def run_fd(args):
             "steps": steps, "warmup": warm, "ms_per_step": round(ms_max, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "seed": 1,
+            "config": {"workload": workload_desc(args.workload), "seed": 1,
                        "kv_lengths": inp.lengths_host,
                        "kv_bytes_per_step": nbytes, "us_per_call": round(ms_step * 1e3, 2),
                        "l2": "inputs larger than L2 (no flush)",
@@ -463,7 +479,7 @@ def run_fd(args):
                        "kernel": args.kernel},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": recorded_traffic(WORKLOAD),
+                         "traffic": recorded_traffic(args.workload),
                          "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                          if peak_kind == "measured" else "fallback 6.8 TB/s"},
             "cpu_baseline": cpu,
@@ -490,6 +506,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--kernel", choices=["auto", "simt", "tc"], default="auto")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="ragged (default), dense_1k, mtp_verify, gather, int8, "
+                         "or sweep:L,B,Hq,Hkv,d,n_q")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -101,6 +101,16 @@ struct Bars {
     int vote[2][4];
 };
 
+// Ring fill index of the K and V tiles of tile number tc in a piece whose
+// first and last tiles are pa and pb, for the fill order K(pa), K(pa+1),
+// V(pa), K(pa+2), V(pa+1), ..., V(pb).
+__device__ __forceinline__ uint32_t k_fill(uint32_t tc, uint32_t pa) {
+    return tc == pa ? 2 * tc : 2 * tc - 1;
+}
+__device__ __forceinline__ uint32_t v_fill(uint32_t tc, uint32_t pb) {
+    return tc == pb ? 2 * tc + 1 : 2 * tc + 2;
+}
+
 // First cache position loaded for tile tt of a segment of length L: tiles
 // start at tt * TT, except the last, which is right-aligned to end at L (its
 // start may be negative, where TMA fills zeros), so no position past the
@@ -233,26 +243,34 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             const int64_t piece_end = min(t_end, pos.first + pos.ntiles);
             const int b = (int)(s / p.Hkv), hk = (int)(s % p.Hkv);
             const int64_t L = seq_len(p, b);
-            for (int64_t tt = t - pos.first; tt < piece_end - pos.first && ok; ++tt) {
-                const int ys = (int)tile_start(tt, L);
-                for (int kv = 0; kv < 2 && ok; ++kv) {
-                    const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
-                    if (lane == 0) {
-                        ok = ptx::mbar_wait(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
-                        if (!ok) note_timeout(bs, p, 1, issued, 0);
-                        if (ok) {
-                            ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
-                            unsigned char *dst = smem + C::OFF_SLOTS + slot * C::SLOT;
+            // Fill order = MMA consumption order: K(a); then K(t+1), V(t) for
+            // t = a .. b-1; then V(b) (a, b: first and last tile of the piece).
+            // The ring is then a plain FIFO, and each K tile is requested one
+            // tile period before its QK needs it.
+            const int64_t n_in = piece_end - t, tt0 = t - pos.first;
+            for (int64_t step = 0; step < 2 * n_in && ok; ++step) {
+                int64_t j;
+                int kv;
+                if (step == 0) { j = 0; kv = 0; }
+                else if (step == 2 * n_in - 1) { j = n_in - 1; kv = 1; }
+                else { j = (step + 1) / 2 - (step & 1 ? 0 : 1); kv = step & 1 ? 0 : 1; }
+                const int ys = (int)tile_start(tt0 + j, L);
+                const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
+                if (lane == 0) {
+                    ok = ptx::mbar_wait(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+                    if (!ok) note_timeout(bs, p, 1, issued, 0);
+                    if (ok) {
+                        ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
+                        unsigned char *dst = smem + C::OFF_SLOTS + slot * C::SLOT;
 #pragma unroll
-                            for (int cb = 0; cb < C::KB; ++cb)
-                                ptx::tma_load_4d(dst + cb * C::BOX, kv ? (const void *)&a.tv
-                                                                       : (const void *)&a.tk,
-                                                 &bs->slot_full[slot], cb * 64, ys, hk, b);
-                        }
+                        for (int cb = 0; cb < C::KB; ++cb)
+                            ptx::tma_load_4d(dst + cb * C::BOX, kv ? (const void *)&a.tv
+                                                                   : (const void *)&a.tk,
+                                             &bs->slot_full[slot], cb * 64, ys, hk, b);
                     }
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (ok) ++issued;
                 }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (ok) ++issued;
             }
             t = piece_end;
         }
@@ -271,9 +289,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         int piece = 0;
         bool ok = true;
         bool issued_any = false;
+        uint32_t pa = 0, pb = 0;   // first and last tile number of the current piece
         // S^T[pos, row] = sum_d K[pos, d] Q[row, d] for tile number tc.
         auto issue_qk = [&](uint32_t tc) -> bool {
-            const uint32_t sb = tc & 1, u = tc >> 1, ki = 2 * tc, ks = ki % C::NS;
+            const uint32_t sb = tc & 1, u = tc >> 1, ki = k_fill(tc, pa), ks = ki % C::NS;
             if (!ptx::mbar_wait(&bs->slot_full[ks], (ki / C::NS) & 1, abort_flag, kWaitNs)) {
                 note_timeout(bs, p, 3, tc, piece);
                 return false;
@@ -299,7 +318,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         };
         // O^T[dim, row] += sum_pos V[pos, dim] (P_hi + P_lo)[row, pos] for tile tc.
         auto issue_pv = [&](uint32_t tc, bool first) -> bool {
-            const uint32_t vi = 2 * tc + 1, vs = vi % C::NS;
+            const uint32_t vi = v_fill(tc, pb), vs = vi % C::NS;
             const uint32_t ps = tc % C::PST, pu = tc / C::PST;
             if (!ptx::mbar_wait(&bs->slot_full[vs], (vi / C::NS) & 1, abort_flag, kWaitNs)) {
                 note_timeout(bs, p, 6, tc, piece);
@@ -339,6 +358,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             if (s < 0) break;
             const int64_t piece_end = min(t_end, pos.first + pos.ntiles);
             const uint32_t n_in = (uint32_t)(piece_end - t);
+            pa = tile_ctr;
+            pb = tile_ctr + n_in - 1;
             if (lane == 0) {
                 // Software pipeline: QK of tile j+1 is issued before PV of
                 // tile j, so the next scores are ready when softmax finishes.
