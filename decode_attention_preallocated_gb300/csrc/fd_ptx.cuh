@@ -160,6 +160,41 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
         : "memory");
 }
 
+// 32 lanes x 8 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float *v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                     taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
+}
+
+// NC consecutive columns (a multiple of 8) in x16 / x8 pieces.
+template <int NC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float *v) {
+#pragma unroll
+    for (int c = 0; c + 16 <= NC; c += 16) tmem_ld16(taddr + c, v + c);
+    if (NC % 16) tmem_ld8(taddr + (NC / 16) * 16, v + (NC / 16) * 16);
+}
+
+template <int NC>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float *v) {
+#pragma unroll
+    for (int c = 0; c + 16 <= NC; c += 16) tmem_st16(taddr + c, v + c);
+    if (NC % 16) tmem_st8(taddr + (NC / 16) * 16, v + (NC / 16) * 16);
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

@@ -3,24 +3,26 @@
 //
 // Work split: the same balanced tile partition as the CUDA-core kernel
 // (fd_internal.h), with 128-position tiles and one block per SM.  Roles
-// inside a block (192 threads):
-//   warp 4      TMA producer: streams K and V tiles of the block's range into
+// inside a block (320 threads):
+//   warp 8      TMA producer: streams K and V tiles of the block's range into
 //               a ring of shared-memory slots (4-D tensor maps, 128-byte
-//               swizzle, out-of-capacity rows zero-filled).
-//   warp 5      MMA issuer (one thread): S^T = K . Q^T   (M = 128 positions,
+//               swizzle), in the order the MMAs consume them.
+//   warp 9      MMA issuer (one thread): S^T = K . Q^T   (M = 128 positions,
 //               N = padded query rows, K = head_dim) into TMEM, then
 //               O^T += V^T . P^T (M = 128 dims per chunk, N = rows,
 //               K = 128 positions) into TMEM; completion via tcgen05.commit.
-//   warps 0-3   softmax and epilogue: thread i owns TMEM lane i = cache
-//               position i of the tile (scores) and dim i of each 128-dim
-//               chunk (output).  Per tile: mask (length, causal window),
-//               column max over the 128 positions (warp shuffles + shared
-//               memory), online-softmax rescale of O in TMEM when a row's
-//               maximum grows, P = 2^(s - m) written to shared memory in the
-//               MMA operand layout.  At the end of a segment it normalises
-//               and stores, or hands a split partial to the in-launch
-//               combine (last block to arrive merges; comfy-kitchen #239,
-//               "GQA decode").
+//               QK of tile t+1 is issued before PV of tile t.
+//   warps 0-7   softmax and epilogue, two warpgroups that split the query
+//               rows.  Thread i of a group owns TMEM lane i = cache position
+//               i of the tile (scores) and dim i of each 128-dim chunk
+//               (output).  Per tile: mask (length, causal window), running
+//               row maxima refreshed when a score passes them by 2^8 (column
+//               max over the 128 positions by warp shuffles + shared memory),
+//               O rescaled in TMEM then, P = 2^(s - m) written to shared
+//               memory as two bf16 planes in the MMA operand layout.  At the
+//               end of a segment piece it normalises and stores, or hands a
+//               split partial to the in-launch combine (last block to arrive
+//               merges; comfy-kitchen #239, "GQA decode").
 // The last tile of a segment is loaded right-aligned (ending at the length),
 // so no row of the unused tail is ever read; positions the previous tile
 // already covered are masked.  Every wait is bounded (2 s); a timeout sets
@@ -38,9 +40,11 @@ namespace fd {
 namespace {
 
 constexpr int TT = 128;                 // cache positions per tile (MMA M)
-constexpr int kThreadsTC = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kSoftmaxGroups = 2;       // warpgroups splitting the query rows
+constexpr int kSoftmaxThreads = 128 * kSoftmaxGroups;
+constexpr int kThreadsTC = kSoftmaxThreads + 64;
+constexpr int kProducerWarp = kSoftmaxThreads / 32;
+constexpr int kMmaWarp = kProducerWarp + 1;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kDevTimeout = 4;          // mirrors FD_DEV_INTERNAL
 // Scores (log2 units) may exceed a row's running maximum by this much before
@@ -64,9 +68,13 @@ struct Cfg {
     static constexpr uint32_t QBYTES = KB * QB;
     static constexpr uint32_t PPLANE = 2 * QB;   // one bf16 plane of P (128 positions x N)
     static constexpr uint32_t PSTAGE = 2 * PPLANE;   // P = hi plane + lo plane
+    // Query rows per softmax warpgroup.
+    static constexpr int NH = N / kSoftmaxGroups;
+    static_assert(NH % 8 == 0, "rows per group must be a multiple of 8");
     // Barriers and the reduction scratch come first, then 1024-byte aligned
-    // operand buffers.
-    static constexpr uint32_t RED = 2 * 4 * N * 4;
+    // operand buffers.  Scratch per group: [2 tiles][4 warps][NH] floats.
+    static constexpr uint32_t RED_GROUP = 2 * 4 * NH;   // floats
+    static constexpr uint32_t RED = kSoftmaxGroups * RED_GROUP * 4;
     static constexpr uint32_t MISC = ((512 + RED) + 1023) / 1024 * 1024;
     static constexpr uint32_t BUDGET = 232448;   // max dynamic shared memory per block
     // Two P stages when that still leaves three K/V slots, else one.
@@ -89,16 +97,17 @@ struct Cfg {
     static constexpr uint32_t PATOM = TT * 32;
 };
 
-struct Bars {
+struct Bars {   // at the start of shared memory; the reduction scratch follows at 512
     uint64_t slot_full[8], slot_empty[8];
     uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
-    uint64_t q_full, q_free, o_done, o_free, exit_mma, wg_bar;
+    uint64_t q_full, q_free, o_done, o_free, exit_mma, sm_bar;
+    uint64_t wg_bar[kSoftmaxGroups];
     uint32_t tmem_base;
     int abort_flag;
     int last_flag;
     int pad;
     int64_t total;
-    int vote[2][4];
+    int vote[kSoftmaxGroups][2][4];
 };
 
 // Ring fill index of the K and V tiles of tile number tc in a piece whose
@@ -119,6 +128,8 @@ __device__ __forceinline__ int64_t tile_start(int64_t tt, int64_t L) {
     const int64_t y0 = tt * TT;
     return y0 + TT > L ? L - TT : y0;
 }
+
+static_assert(sizeof(Bars) <= 512, "barrier block overlaps the reduction scratch");
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -168,7 +179,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t smem_base = ptx::smem_u32(smem);
     Bars *bs = reinterpret_cast<Bars *>(smem);
-    float *red = reinterpret_cast<float *>(smem + 512);   // [2][4][N]
+    float *red = reinterpret_cast<float *>(smem + 512);   // per group [2][4][NH]
     volatile int *abort_flag = &bs->abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -203,16 +214,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&bs->s_full[i], 1);
-            ptx::mbar_init(&bs->s_free[i], 128);
-            ptx::mbar_init(&bs->p_full[i], 128);
+            ptx::mbar_init(&bs->s_free[i], kSoftmaxThreads);
+            ptx::mbar_init(&bs->p_full[i], kSoftmaxThreads);
             ptx::mbar_init(&bs->p_free[i], 1);
         }
-        ptx::mbar_init(&bs->q_full, 128);
+        ptx::mbar_init(&bs->q_full, kSoftmaxThreads);
         ptx::mbar_init(&bs->q_free, 1);
         ptx::mbar_init(&bs->o_done, 1);
-        ptx::mbar_init(&bs->o_free, 128);
+        ptx::mbar_init(&bs->o_free, kSoftmaxThreads);
         ptx::mbar_init(&bs->exit_mma, 1);
-        ptx::mbar_init(&bs->wg_bar, 128);
+        ptx::mbar_init(&bs->sm_bar, kSoftmaxThreads);
+        for (int g = 0; g < kSoftmaxGroups; ++g) ptx::mbar_init(&bs->wg_bar[g], 128);
         bs->abort_flag = 0;
         ptx::mbar_fence_init();
     }
@@ -394,14 +406,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         }
     } else {
         // ------------------------------------------- softmax and epilogue
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        // Two warpgroups split the query rows: group wg owns rows
+        // [wg*NH, wg*NH + NH), i.e. those columns of S^T, O^T and P.  Thread
+        // wt of a group owns TMEM lane wt: cache position wt of the tile.
+        constexpr int NH = C::NH;
+        const int wg = warp >> 2, wwarp = warp & 3, wt = tid & 127;
+        const int cb0 = wg * NH;                  // first row (column) of the group
+        const uint32_t lane_base = (uint32_t)(wwarp * 32) << 16;
+        float *gred = red + wg * C::RED_GROUP;    // the group's reduction scratch
         uint32_t tile_ctr = 0;
         uint32_t o_seen = 0;      // o_done phases observed, consumed strictly in order
         uint32_t wg_ctr = 0;      // uses of the group barrier
+        uint32_t sm_ctr = 0;      // uses of the two-group barrier
         int piece = 0;
         bool ok = true;
-        // Completion of PV number k (k = 0, 1, ...): wait phase by phase, so a
-        // parity test never aliases with a phase two steps ahead or behind.
+        // Completion of PV number k (k = 0, 1, ...), phase by phase.  Every
+        // tile consumes the previous tile's phase before publishing its own P,
+        // so the barrier is never more than one phase ahead of this wait and
+        // the parity test cannot alias.
         auto wait_pv = [&](uint32_t k) -> bool {
             for (; o_seen <= k; ++o_seen)
                 if (!ptx::mbar_wait(&bs->o_done, o_seen & 1, abort_flag, kWaitNs)) {
@@ -410,11 +432,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 }
             return true;
         };
-        // Barrier over the 128 softmax threads with a bounded wait.
+        // Barrier over this warpgroup's 128 threads, bounded.
         auto wg_sync = [&]() -> bool {
-            ptx::mbar_arrive(&bs->wg_bar);
-            if (ptx::mbar_wait(&bs->wg_bar, (wg_ctr++) & 1, abort_flag, kWaitNs)) return true;
+            ptx::mbar_arrive(&bs->wg_bar[wg]);
+            if (ptx::mbar_wait(&bs->wg_bar[wg], (wg_ctr++) & 1, abort_flag, kWaitNs)) return true;
             note_timeout(bs, p, 10, tile_ctr, piece);
+            return false;
+        };
+        // Barrier over both warpgroups, bounded.
+        auto sm_sync = [&]() -> bool {
+            ptx::mbar_arrive(&bs->sm_bar);
+            if (ptx::mbar_wait(&bs->sm_bar, (sm_ctr++) & 1, abort_flag, kWaitNs)) return true;
+            note_timeout(bs, p, 14, tile_ctr, piece);
             return false;
         };
         int64_t t = t_begin;
@@ -432,7 +461,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             // Q rows of this segment -> shared memory (K-major, 128-byte swizzle).
             if (piece > 0) ok = ptx::mbar_wait(&bs->q_free, (piece - 1) & 1, abort_flag, kWaitNs);
             if (!ok) { note_timeout(bs, p, 8, tile_ctr, piece); break; }
-            for (int e = tid; e < N * (D / 8); e += 128) {
+            for (int e = tid; e < N * (D / 8); e += kSoftmaxThreads) {
                 const int r = e / (D / 8), cc = e % (D / 8);
                 uint32_t w[4] = {0, 0, 0, 0};
                 if (r < rows) {
@@ -450,21 +479,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(&bs->q_full);
 
-            float mrun[N], lpart[N];
+            float mrun[NH], lpart[NH];
 #pragma unroll
-            for (int r = 0; r < N; ++r) { mrun[r] = neg_inf(); lpart[r] = 0.f; }
+            for (int r = 0; r < NH; ++r) { mrun[r] = neg_inf(); lpart[r] = 0.f; }
 
             for (int64_t j = 0; j < n_in && ok; ++j) {
                 const int64_t y0 = (tt0 + j) * TT;
-                const int64_t token = tile_start(tt0 + j, L) + tid;
+                const int64_t token = tile_start(tt0 + j, L) + wt;
                 const uint32_t sb = tile_ctr & 1, u = tile_ctr >> 1;
                 ok = ptx::mbar_wait(&bs->s_full[sb], u & 1, abort_flag, kWaitNs);
                 if (!ok) { note_timeout(bs, p, 9, tile_ctr, piece); break; }
                 ptx::tc_fence_after();
-                float sv[N];
-#pragma unroll
-                for (int cb = 0; cb < N / 16; ++cb)
-                    ptx::tmem_ld16(tmem + lane_base + sb * N + cb * 16, sv + cb * 16);
+                float sv[NH];
+                ptx::tmem_ld_cols<NH>(tmem + lane_base + sb * N + cb0, sv);
                 ptx::tmem_wait_ld();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&bs->s_free[sb]);
@@ -475,36 +502,37 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 // L - n_q + i for the row's query index i.
                 const bool in_len = token >= y0 && token < L;
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    bool vis = in_len && r < rows;
-                    if (p.causal) vis = vis && token <= L - p.n_q + (r % p.n_q);
+                for (int r = 0; r < NH; ++r) {
+                    bool vis = in_len && cb0 + r < rows;
+                    if (p.causal) vis = vis && token <= L - p.n_q + ((cb0 + r) % p.n_q);
                     sv[r] = vis ? sv[r] * p.scale_log2 : neg_inf();
                 }
                 // Refresh the running maxima only when some score passes
                 // mrun + kRescaleSlack (always on a segment's first tile).
                 bool need = false;
 #pragma unroll
-                for (int r = 0; r < N; ++r) need = need || (sv[r] > mrun[r] + kRescaleSlack);
+                for (int r = 0; r < NH; ++r) need = need || (sv[r] > mrun[r] + kRescaleSlack);
                 need = __any_sync(0xffffffffu, need);
-                if (lane == 0) bs->vote[tile_ctr & 1][warp] = need;
+                if (lane == 0) bs->vote[wg][tile_ctr & 1][wwarp] = need;
                 ok = wg_sync();
                 if (!ok) break;
-                const int *vt = bs->vote[tile_ctr & 1];
+                const int *vt = bs->vote[wg][tile_ctr & 1];
                 if (vt[0] | vt[1] | vt[2] | vt[3]) {
                     // Column maxima over the 128 positions of the tile.
-                    float *rb = red + (tile_ctr & 1) * (4 * N);
+                    float *rb = gred + (tile_ctr & 1) * (4 * NH);
 #pragma unroll
-                    for (int r = 0; r < N; ++r) {
+                    for (int r = 0; r < NH; ++r) {
                         const float mx = warp_max(sv[r]);
-                        if (lane == 0) rb[warp * N + r] = mx;
+                        if (lane == 0) rb[wwarp * NH + r] = mx;
                     }
                     ok = wg_sync();
                     if (!ok) break;
-                    float alpha[N];
+                    float alpha[NH];
                     bool grow = false;
 #pragma unroll
-                    for (int r = 0; r < N; ++r) {
-                        const float tmax = fmaxf(fmaxf(rb[r], rb[N + r]), fmaxf(rb[2 * N + r], rb[3 * N + r]));
+                    for (int r = 0; r < NH; ++r) {
+                        const float tmax = fmaxf(fmaxf(rb[r], rb[NH + r]),
+                                                 fmaxf(rb[2 * NH + r], rb[3 * NH + r]));
                         const float mnew = fmaxf(mrun[r], tmax);
                         const float muse = mnew == neg_inf() ? 0.f : mnew;
                         alpha[r] = fast_exp2(mrun[r] - muse);
@@ -512,58 +540,56 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         mrun[r] = mnew;
                         lpart[r] *= alpha[r];
                     }
-                    // Rescale the running O in TMEM (after the previous PV landed).
+                    // Rescale this group's columns of the running O in TMEM
+                    // (after the previous PV landed).
                     if (grow && j > 0) {
                         ok = wait_pv(tile_ctr - 1);
                         if (!ok) break;
                         ptx::tc_fence_after();
 #pragma unroll
                         for (int dc = 0; dc < C::DC; ++dc) {
+                            float o[NH];
+                            const uint32_t ta = tmem + lane_base + 2 * N + dc * N + cb0;
+                            ptx::tmem_ld_cols<NH>(ta, o);
+                            ptx::tmem_wait_ld();
 #pragma unroll
-                            for (int cb = 0; cb < N / 16; ++cb) {
-                                float o[16];
-                                const uint32_t ta = tmem + lane_base + 2 * N + dc * N + cb * 16;
-                                ptx::tmem_ld16(ta, o);
-                                ptx::tmem_wait_ld();
-#pragma unroll
-                                for (int k = 0; k < 16; ++k) o[k] *= alpha[cb * 16 + k];
-                                ptx::tmem_st16(ta, o);
-                            }
+                            for (int k = 0; k < NH; ++k) o[k] *= alpha[k];
+                            ptx::tmem_st_cols<NH>(ta, o);
                         }
                         ptx::tmem_wait_st();
                     }
                 }
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
+                for (int r = 0; r < NH; ++r) {
                     const float muse = mrun[r] == neg_inf() ? 0.f : mrun[r];
                     const float pr = fast_exp2(sv[r] - muse);
                     lpart[r] += pr;
                     sv[r] = pr;
                 }
-                // P^T (rows x positions, K-major) for the PV product.
+                // P^T for the PV product.
                 const uint32_t ps = tile_ctr % C::PST, pu = tile_ctr / C::PST;
                 ok = ptx::mbar_wait(&bs->p_free[ps], (pu & 1) ^ 1, abort_flag, kWaitNs);
                 if (!ok) { note_timeout(bs, p, 13, tile_ctr, piece); break; }
                 // PV of the previous tile must have completed before P of this
-                // tile is published: o_done is then exactly one phase behind or
-                // level, so its parity test cannot alias.
+                // tile is published (see wait_pv).
                 if (tile_ctr > 0) {
                     ok = wait_pv(tile_ctr - 1);
                     if (!ok) break;
                 }
                 {
                     // P = hi + lo, both bf16: hi = rn(p), lo = rn(p - hi), so the
-                    // PV product sees p to about 2^-17 relative.  Thread tid
+                    // PV product sees p to about 2^-17 relative.  Thread wt
                     // writes its position's row: 8 query rows per 16-byte chunk,
-                    // chunk c of a 16-row atom stored at c ^ bit 2 of tid.
-                    unsigned char *prow = smem + C::OFF_P + ps * C::PSTAGE + tid * 32;
-                    const int sw = (tid >> 2) & 1;
+                    // chunk c of a 16-row atom stored at c ^ bit 2 of wt.
+                    unsigned char *prow = smem + C::OFF_P + ps * C::PSTAGE + wt * 32;
+                    const int sw = (wt >> 2) & 1;
 #pragma unroll
-                    for (int a8 = 0; a8 < N / 8; ++a8) {
+                    for (int l8 = 0; l8 < NH / 8; ++l8) {
+                        const int a8 = cb0 / 8 + l8;      // global 8-row group
                         uint32_t hw[4], lw[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float p0 = sv[a8 * 8 + 2 * e], p1 = sv[a8 * 8 + 2 * e + 1];
+                            const float p0 = sv[l8 * 8 + 2 * e], p1 = sv[l8 * 8 + 2 * e + 1];
                             const uint32_t h = pack_bf16x2(p0, p1);
                             hw[e] = h;
                             lw[e] = pack_bf16x2(p0 - bf16lo(h), p1 - bf16hi(h));
@@ -585,36 +611,34 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             ok = wait_pv(tile_ctr - 1);
             if (!ok) { set_abort(bs, p); break; }
             ptx::tc_fence_after();
-            float o[C::DC][N];
+            float o[C::DC][NH];
 #pragma unroll
             for (int dc = 0; dc < C::DC; ++dc)
-#pragma unroll
-                for (int cb = 0; cb < N / 16; ++cb)
-                    ptx::tmem_ld16(tmem + lane_base + 2 * N + dc * N + cb * 16, &o[dc][cb * 16]);
+                ptx::tmem_ld_cols<NH>(tmem + lane_base + 2 * N + dc * N + cb0, o[dc]);
             ptx::tmem_wait_ld();
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bs->o_free);
 
-            // Row sums of P over the segment piece.
-            float *lb = red + (tile_ctr & 1) * (4 * N);
+            // Row sums of P over the segment piece (this group's rows).
+            float *lb = gred + (tile_ctr & 1) * (4 * NH);
 #pragma unroll
-            for (int r = 0; r < N; ++r) {
+            for (int r = 0; r < NH; ++r) {
                 const float v = warp_sum(lpart[r]);
-                if (lane == 0) lb[warp * N + r] = v;
+                if (lane == 0) lb[wwarp * NH + r] = v;
             }
             ok = wg_sync();
-            float lsum[N];
+            float lsum[NH];
 #pragma unroll
-            for (int r = 0; r < N; ++r) lsum[r] = lb[r] + lb[N + r] + lb[2 * N + r] + lb[3 * N + r];
+            for (int r = 0; r < NH; ++r) lsum[r] = lb[r] + lb[NH + r] + lb[2 * NH + r] + lb[3 * NH + r];
             ok = ok && wg_sync();
             if (!ok) { set_abort(bs, p); break; }
 
             const int c_first = sp.owner(pos.first), c_last = sp.owner(pos.first + pos.ntiles - 1);
             if (c_first == c_last) {
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    if (r < rows) {
-                        const RowMap m = row_of(p, s, r);
+                for (int r = 0; r < NH; ++r) {
+                    if (cb0 + r < rows) {
+                        const RowMap m = row_of(p, s, cb0 + r);
                         const float inv = lsum[r] > 0.f ? 1.f / lsum[r] : 0.f;
                         const int64_t off = (int64_t)m.b * p.os[0] + (int64_t)m.i * p.os[1] +
                                             (int64_t)m.h * p.os[2];
@@ -622,79 +646,78 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         for (int dc = 0; dc < C::DC; ++dc) {
                             const float val = o[dc][r] * inv;
                             if (p.out_f32)
-                                reinterpret_cast<float *>(p.out)[off + dc * 128 + tid] = val;
+                                reinterpret_cast<float *>(p.out)[off + dc * 128 + wt] = val;
                             else
-                                reinterpret_cast<uint16_t *>(p.out)[off + dc * 128 + tid] = bf16_bits(val);
+                                reinterpret_cast<uint16_t *>(p.out)[off + dc * 128 + wt] = bf16_bits(val);
                         }
                     }
                 }
             } else {
                 float *slot = slot_ptr(p, s, c);
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    if (r < rows) {
+                for (int r = 0; r < NH; ++r) {
+                    if (cb0 + r < rows) {
 #pragma unroll
-                        for (int dc = 0; dc < C::DC; ++dc) slot[r * D + dc * 128 + tid] = o[dc][r];
+                        for (int dc = 0; dc < C::DC; ++dc)
+                            slot[(cb0 + r) * D + dc * 128 + wt] = o[dc][r];
                     }
                 }
-                if (tid < rows) {
-                    // lane tid of every thread holds the same mrun/lsum values
+                // every thread of the group holds the same mrun / lsum values
 #pragma unroll
-                    for (int r = 0; r < N; ++r) {
-                        if (r == tid) {
-                            slot[rows * D + r] = mrun[r];
-                            slot[rows * D + rows + r] = lsum[r];
-                        }
+                for (int r = 0; r < NH; ++r) {
+                    if (r == wt && cb0 + r < rows) {
+                        slot[rows * D + cb0 + r] = mrun[r];
+                        slot[rows * D + rows + cb0 + r] = lsum[r];
                     }
                 }
                 __threadfence();
-                ok = wg_sync();
+                ok = sm_sync();
                 if (tid == 0 && ok) bs->last_flag = atomicAdd(p.counters + s, 1) == c_last - c_first;
-                ok = ok && wg_sync();
+                ok = ok && sm_sync();
                 if (!ok) { set_abort(bs, p); break; }
-                if (bs->last_flag) {
+                const int r1w = min(cb0 + NH, rows);       // this group merges rows cb0 .. r1w-1
+                if (bs->last_flag && r1w > cb0) {
                     __threadfence();
-                    // Merge the pieces' partials.  Loads are arranged so that
-                    // none depends on another: per-row maxima and sums by one
-                    // thread per row, then piece by piece for 16 rows at a time.
-                    float *cm = red;          // row maxima over the pieces
-                    float *ci = red + N;      // 1 / merged row sums
-                    if (tid < rows) {
+                    // Merge the pieces' partials.  Row maxima and merged sums by
+                    // one thread per row; then every load is unconditional (row
+                    // indices clamped into range, weight 0 beyond) so a chunk's
+                    // loads for two pieces are all in flight together.
+                    float *cm = gred;          // row maxima over the pieces
+                    float *ci = gred + NH;     // 1 / merged row sums
+                    if (wt < r1w - cb0) {
+                        const int r = cb0 + wt;
                         float M = neg_inf();
 #pragma unroll 8
                         for (int c2 = c_first; c2 <= c_last; ++c2)
-                            M = fmaxf(M, __ldcg(slot_ptr(p, s, c2) + rows * D + tid));
+                            M = fmaxf(M, __ldcg(slot_ptr(p, s, c2) + rows * D + r));
                         float ls = 0.f;
                         if (M != neg_inf()) {
 #pragma unroll 8
                             for (int c2 = c_first; c2 <= c_last; ++c2) {
                                 const float *sl = slot_ptr(p, s, c2);
-                                ls += fast_exp2(__ldcg(sl + rows * D + tid) - M) *
-                                      __ldcg(sl + rows * D + rows + tid);
+                                ls += fast_exp2(__ldcg(sl + rows * D + r) - M) *
+                                      __ldcg(sl + rows * D + rows + r);
                             }
                         }
-                        cm[tid] = M;
-                        ci[tid] = ls > 0.f ? 1.f / ls : 0.f;
+                        cm[wt] = M;
+                        ci[wt] = ls > 0.f ? 1.f / ls : 0.f;
                     }
                     ok = wg_sync();
                     if (!ok) { set_abort(bs, p); break; }
-                    // Thread -> 4 consecutive dims of rows rg, rg + RG, ...  Row
-                    // indices are clamped into range (weight 0 beyond `rows`) so
-                    // every load is unconditional and a chunk's loads for two
-                    // pieces are all in flight together.
-                    constexpr int TPR = D / 4, RG = 128 / TPR, RPT = N / RG;
+                    // Thread -> 4 consecutive dims of rows cb0 + rg + RG*k.
+                    constexpr int TPR = D / 4, RG = 128 / TPR, RPT = NH / RG;
                     constexpr int CH = RPT < 8 ? RPT : 8;
-                    const int dq = (tid % TPR) * 4, rg = tid / TPR;
+                    const int dq = (wt % TPR) * 4, rg = wt / TPR;
 #pragma unroll 1
-                    for (int k0 = 0; k0 < RPT && rg + RG * k0 < rows; k0 += CH) {
+                    for (int k0 = 0; k0 < RPT && cb0 + rg + RG * k0 < r1w; k0 += CH) {
                         float4 acc[CH];
                         float mr[CH];
                         int rr[CH];
 #pragma unroll
                         for (int k = 0; k < CH; ++k) {
-                            const int r = rg + RG * (k0 + k);
-                            rr[k] = r < rows ? r : rows - 1;
-                            mr[k] = r < rows ? cm[rr[k]] : neg_inf();
+                            const int r = cb0 + rg + RG * (k0 + k);
+                            rr[k] = r < r1w ? r : r1w - 1;
+                            mr[k] = r < r1w ? cm[rr[k] - cb0] : neg_inf();
                             acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
                         }
 #pragma unroll 2
@@ -712,12 +735,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         }
 #pragma unroll
                         for (int k = 0; k < CH; ++k) {
-                            const int r = rg + RG * (k0 + k);
-                            if (r < rows) {
+                            const int r = cb0 + rg + RG * (k0 + k);
+                            if (r < r1w) {
                                 const RowMap m = row_of(p, s, r);
                                 const int64_t off = (int64_t)m.b * p.os[0] +
                                                     (int64_t)m.i * p.os[1] + (int64_t)m.h * p.os[2] + dq;
-                                const float inv = ci[r];
+                                const float inv = ci[r - cb0];
                                 const float o4[4] = {acc[k].x * inv, acc[k].y * inv, acc[k].z * inv,
                                                      acc[k].w * inv};
 #pragma unroll
@@ -733,8 +756,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     // cm / ci live in the reduction scratch the next tile reuses.
                     ok = wg_sync();
                     if (!ok) { set_abort(bs, p); break; }
-                    if (tid == 0) p.counters[s] = 0;
                 }
+                if (bs->last_flag && tid == 0) p.counters[s] = 0;
             }
             t = piece_end;
             ++piece;
