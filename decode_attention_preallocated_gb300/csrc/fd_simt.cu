@@ -328,41 +328,21 @@ simt_kernel(const __grid_constant__ Params p) {
             __syncthreads();
             if (sh_last) {
                 __threadfence();
-                // Merge the pieces' partials with independent loads: per-row
-                // maxima and merged sums first (one thread per row, kept in
-                // m_s / l_s), then piece by piece for every row of the thread.
-                if (tid < rows) {
-                    float M = neg_inf();
-#pragma unroll 8
-                    for (int c2 = c_first; c2 <= c_last; ++c2)
-                        M = fmaxf(M, __ldcg(slot_ptr(p, s, c2) + rows * D + tid));
-                    float lsum = 0.f;
-                    if (M != neg_inf()) {
-#pragma unroll 8
-                        for (int c2 = c_first; c2 <= c_last; ++c2) {
-                            const float *sl = slot_ptr(p, s, c2);
-                            lsum += fast_exp2(__ldcg(sl + rows * D + tid) - M) *
-                                    __ldcg(sl + rows * D + rows + tid);
-                        }
-                    }
-                    m_s[tid] = M;
-                    l_s[tid] = lsum > 0.f ? 1.f / lsum : 0.f;
-                }
-                __syncthreads();
-                float o[Ly::PV_RMAX][8];
-#pragma unroll
-                for (int k = 0; k < Ly::PV_RMAX; ++k)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[k][e] = 0.f;
-                // Rows clamped into range (weight 0 beyond `rows`): every load
-                // is unconditional, so one piece's loads are all in flight.
+                // Merge the pieces' partials in one pass per row: running
+                // maximum, merged sum and accumulator rescaled as each piece
+                // arrives.  Rows are clamped into range (weight 0 beyond
+                // `rows`), so every load is unconditional and one piece's loads
+                // are all in flight together.
                 int rr[Ly::PV_RMAX];
-                float mr[Ly::PV_RMAX];
+                float M[Ly::PV_RMAX], Ls[Ly::PV_RMAX], o[Ly::PV_RMAX][8];
 #pragma unroll
                 for (int k = 0; k < Ly::PV_RMAX; ++k) {
                     const int r = rg + Ly::PV_RG * k;
                     rr[k] = r < rows ? r : rows - 1;
-                    mr[k] = r < rows ? m_s[rr[k]] : neg_inf();
+                    M[k] = neg_inf();
+                    Ls[k] = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[k][e] = 0.f;
                 }
 #pragma unroll 2
                 for (int c2 = c_first; c2 <= c_last; ++c2) {
@@ -370,18 +350,24 @@ simt_kernel(const __grid_constant__ Params p) {
 #pragma unroll
                     for (int k = 0; k < Ly::PV_RMAX; ++k) {
                         const float mv = __ldcg(sl + rows * D + rr[k]);
-                        const float4 a = __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + cg * 8));
-                        const float4 bq = __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + cg * 8 + 4));
-                        const float w = mr[k] == neg_inf() ? 0.f : fast_exp2(mv - mr[k]);
-                        o[k][0] += w * a.x; o[k][1] += w * a.y; o[k][2] += w * a.z; o[k][3] += w * a.w;
-                        o[k][4] += w * bq.x; o[k][5] += w * bq.y; o[k][6] += w * bq.z; o[k][7] += w * bq.w;
+                        const float lv = __ldcg(sl + rows * D + rows + rr[k]);
+                        const float4 a4 = __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + cg * 8));
+                        const float4 b4 = __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + cg * 8 + 4));
+                        const float mn = fmaxf(M[k], mv);
+                        const float mu = mn == neg_inf() ? 0.f : mn;
+                        const float a = fast_exp2(M[k] - mu), w = fast_exp2(mv - mu);
+                        M[k] = mn;
+                        Ls[k] = Ls[k] * a + w * lv;
+                        const float v[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[k][e] = o[k][e] * a + w * v[e];
                     }
                 }
 #pragma unroll
                 for (int k = 0; k < Ly::PV_RMAX; ++k) {
                     const int r = rg + Ly::PV_RG * k;
                     if (r < rows) {
-                        const float inv = l_s[r];
+                        const float inv = Ls[k] > 0.f ? 1.f / Ls[k] : 0.f;
 #pragma unroll
                         for (int e = 0; e < 8; ++e) o[k][e] *= inv;
                         store_out8(p, row_of(p, s, r), cg * 8, o[k]);

@@ -75,7 +75,10 @@ struct Cfg {
     // operand buffers.  Scratch per group: [2 tiles][4 warps][NH] floats.
     static constexpr uint32_t RED_GROUP = 2 * 4 * NH;   // floats
     static constexpr uint32_t RED = kSoftmaxGroups * RED_GROUP * 4;
-    static constexpr uint32_t MISC = ((512 + RED) + 1023) / 1024 * 1024;
+    // Per-row element offsets of q and out for the current segment (int64).
+    static constexpr uint32_t OFF_TBL = 512 + RED;
+    static constexpr uint32_t TBL = 2 * N * 8;
+    static constexpr uint32_t MISC = ((OFF_TBL + TBL) + 1023) / 1024 * 1024;
     static constexpr uint32_t BUDGET = 232448;   // max dynamic shared memory per block
     // Two P stages when that still leaves three K/V slots, else one.
     static constexpr int NS2 = (int)((BUDGET - MISC - QBYTES - 2 * PSTAGE) / SLOT);
@@ -180,6 +183,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
     const uint32_t smem_base = ptx::smem_u32(smem);
     Bars *bs = reinterpret_cast<Bars *>(smem);
     float *red = reinterpret_cast<float *>(smem + 512);   // per group [2][4][NH]
+    // Row tables: qoff[r], ooff[r] = element offsets of packed row r in q / out.
+    int64_t *qoff = reinterpret_cast<int64_t *>(smem + C::OFF_TBL);
+    int64_t *ooff = qoff + N;
     volatile int *abort_flag = &bs->abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -458,16 +464,33 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             const int64_t L = seq_len(p, b);
             const int rows = p.rows;
 
-            // Q rows of this segment -> shared memory (K-major, 128-byte swizzle).
+            // Row tables for this group's rows (one division sequence per row,
+            // so the unrolled per-row code below needs none), the causal
+            // limit of each row, then the group's Q rows -> shared memory
+            // (K-major, 128-byte swizzle).
+            if (wt < NH && cb0 + wt < rows) {
+                const RowMap m = row_of(p, s, cb0 + wt);
+                qoff[cb0 + wt] = (int64_t)m.b * p.qs[0] + (int64_t)m.i * p.qs[1] + (int64_t)m.h * p.qs[2];
+                ooff[cb0 + wt] = (int64_t)m.b * p.os[0] + (int64_t)m.i * p.os[1] + (int64_t)m.h * p.os[2];
+            }
+            int lim[NH];    // last visible position of each row
+            {
+                int qi = cb0 % p.n_q;
+#pragma unroll
+                for (int r = 0; r < NH; ++r) {
+                    lim[r] = p.causal ? (int)(L - p.n_q + qi) : (int)(L - 1);
+                    if (++qi == p.n_q) qi = 0;
+                }
+            }
             if (piece > 0) ok = ptx::mbar_wait(&bs->q_free, (piece - 1) & 1, abort_flag, kWaitNs);
             if (!ok) { note_timeout(bs, p, 8, tile_ctr, piece); break; }
-            for (int e = tid; e < N * (D / 8); e += kSoftmaxThreads) {
-                const int r = e / (D / 8), cc = e % (D / 8);
+            ok = wg_sync();
+            if (!ok) break;
+            for (int e = wt; e < NH * (D / 8); e += 128) {
+                const int r = cb0 + e / (D / 8), cc = e % (D / 8);
                 uint32_t w[4] = {0, 0, 0, 0};
                 if (r < rows) {
-                    const RowMap m = row_of(p, s, r);
-                    const uint16_t *src = p.q + (int64_t)m.b * p.qs[0] + (int64_t)m.i * p.qs[1] +
-                                          (int64_t)m.h * p.qs[2] + cc * 8;
+                    const uint16_t *src = p.q + qoff[r] + cc * 8;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         w[k] = (uint32_t)src[2 * k] | ((uint32_t)src[2 * k + 1] << 16);
@@ -503,8 +526,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 const bool in_len = token >= y0 && token < L;
 #pragma unroll
                 for (int r = 0; r < NH; ++r) {
-                    bool vis = in_len && cb0 + r < rows;
-                    if (p.causal) vis = vis && token <= L - p.n_q + ((cb0 + r) % p.n_q);
+                    const bool vis = in_len && cb0 + r < rows && token <= lim[r];
                     sv[r] = vis ? sv[r] * p.scale_log2 : neg_inf();
                 }
                 // Refresh the running maxima only when some score passes
@@ -638,10 +660,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 #pragma unroll
                 for (int r = 0; r < NH; ++r) {
                     if (cb0 + r < rows) {
-                        const RowMap m = row_of(p, s, cb0 + r);
                         const float inv = lsum[r] > 0.f ? 1.f / lsum[r] : 0.f;
-                        const int64_t off = (int64_t)m.b * p.os[0] + (int64_t)m.i * p.os[1] +
-                                            (int64_t)m.h * p.os[2];
+                        const int64_t off = ooff[cb0 + r];
 #pragma unroll
                         for (int dc = 0; dc < C::DC; ++dc) {
                             const float val = o[dc][r] * inv;
@@ -678,47 +698,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 const int r1w = min(cb0 + NH, rows);       // this group merges rows cb0 .. r1w-1
                 if (bs->last_flag && r1w > cb0) {
                     __threadfence();
-                    // Merge the pieces' partials.  Row maxima and merged sums by
-                    // one thread per row; then every load is unconditional (row
-                    // indices clamped into range, weight 0 beyond) so a chunk's
-                    // loads for two pieces are all in flight together.
-                    float *cm = gred;          // row maxima over the pieces
-                    float *ci = gred + NH;     // 1 / merged row sums
-                    if (wt < r1w - cb0) {
-                        const int r = cb0 + wt;
-                        float M = neg_inf();
-#pragma unroll 8
-                        for (int c2 = c_first; c2 <= c_last; ++c2)
-                            M = fmaxf(M, __ldcg(slot_ptr(p, s, c2) + rows * D + r));
-                        float ls = 0.f;
-                        if (M != neg_inf()) {
-#pragma unroll 8
-                            for (int c2 = c_first; c2 <= c_last; ++c2) {
-                                const float *sl = slot_ptr(p, s, c2);
-                                ls += fast_exp2(__ldcg(sl + rows * D + r) - M) *
-                                      __ldcg(sl + rows * D + rows + r);
-                            }
-                        }
-                        cm[wt] = M;
-                        ci[wt] = ls > 0.f ? 1.f / ls : 0.f;
-                    }
-                    ok = wg_sync();
-                    if (!ok) { set_abort(bs, p); break; }
-                    // Thread -> 4 consecutive dims of rows cb0 + rg + RG*k.
+                    // Merge the pieces' partials in one pass per row: running
+                    // maximum M, merged sum Ls and accumulator rescaled as each
+                    // piece arrives.  Thread -> 4 consecutive dims of rows
+                    // cb0 + rg + RG*k; row indices are clamped into range
+                    // (weight 0 beyond) so every load is unconditional and two
+                    // pieces' loads are in flight together.
                     constexpr int TPR = D / 4, RG = 128 / TPR, RPT = NH / RG;
                     constexpr int CH = RPT < 8 ? RPT : 8;
                     const int dq = (wt % TPR) * 4, rg = wt / TPR;
 #pragma unroll 1
                     for (int k0 = 0; k0 < RPT && cb0 + rg + RG * k0 < r1w; k0 += CH) {
                         float4 acc[CH];
-                        float mr[CH];
+                        float M[CH], Ls[CH];
                         int rr[CH];
 #pragma unroll
                         for (int k = 0; k < CH; ++k) {
                             const int r = cb0 + rg + RG * (k0 + k);
                             rr[k] = r < r1w ? r : r1w - 1;
-                            mr[k] = r < r1w ? cm[rr[k] - cb0] : neg_inf();
                             acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            M[k] = neg_inf();
+                            Ls[k] = 0.f;
                         }
 #pragma unroll 2
                         for (int c2 = c_first; c2 <= c_last; ++c2) {
@@ -726,21 +726,26 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 #pragma unroll
                             for (int k = 0; k < CH; ++k) {
                                 const float mv = __ldcg(sl + rows * D + rr[k]);
+                                const float lv = __ldcg(sl + rows * D + rows + rr[k]);
                                 const float4 v =
                                     __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + dq));
-                                const float w = mr[k] == neg_inf() ? 0.f : fast_exp2(mv - mr[k]);
-                                acc[k].x += w * v.x; acc[k].y += w * v.y;
-                                acc[k].z += w * v.z; acc[k].w += w * v.w;
+                                const float mn = fmaxf(M[k], mv);
+                                const float mu = mn == neg_inf() ? 0.f : mn;
+                                const float a = fast_exp2(M[k] - mu), w = fast_exp2(mv - mu);
+                                M[k] = mn;
+                                Ls[k] = Ls[k] * a + w * lv;
+                                acc[k].x = acc[k].x * a + w * v.x;
+                                acc[k].y = acc[k].y * a + w * v.y;
+                                acc[k].z = acc[k].z * a + w * v.z;
+                                acc[k].w = acc[k].w * a + w * v.w;
                             }
                         }
 #pragma unroll
                         for (int k = 0; k < CH; ++k) {
                             const int r = cb0 + rg + RG * (k0 + k);
                             if (r < r1w) {
-                                const RowMap m = row_of(p, s, r);
-                                const int64_t off = (int64_t)m.b * p.os[0] +
-                                                    (int64_t)m.i * p.os[1] + (int64_t)m.h * p.os[2] + dq;
-                                const float inv = ci[r - cb0];
+                                const int64_t off = ooff[r] + dq;
+                                const float inv = Ls[k] > 0.f ? 1.f / Ls[k] : 0.f;
                                 const float o4[4] = {acc[k].x * inv, acc[k].y * inv, acc[k].z * inv,
                                                      acc[k].w * inv};
 #pragma unroll
@@ -753,9 +758,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                             }
                         }
                     }
-                    // cm / ci live in the reduction scratch the next tile reuses.
-                    ok = wg_sync();
-                    if (!ok) { set_abort(bs, p); break; }
                 }
                 if (bs->last_flag && tid == 0) p.counters[s] = 0;
             }
