@@ -92,11 +92,14 @@ int kernel_tile(int32_t kernel) {
 // Blocks for an auto launch: one per SM for the tensor-core kernel (its
 // shared-memory ring fills an SM), two per SM for the CUDA-core kernel;
 // never more than the largest possible tile count.
-int32_t auto_ctas(int32_t kernel, int64_t max_tiles) {
+// max_units: the most work units the launch can have for its capacity
+// (tiles plus the per-segment charge), so that the block count, and with it
+// the split, never depends on the capacity when the units outnumber it.
+int32_t auto_ctas(int32_t kernel, int64_t max_units) {
     const int sms = sm_count_current();
     if (sms <= 0) return 0;
     int64_t g = (int64_t)sms * (kernel == FD_KERNEL_TC ? 1 : 2);
-    if (max_tiles > 0 && g > max_tiles) g = max_tiles;
+    if (max_units > 0 && g > max_units) g = max_units;
     return (int32_t)(g < 1 ? 1 : g);
 }
 
@@ -175,15 +178,20 @@ int run(const Call &c) {
     const int64_t nseg = c.mode == fd::kGather ? B * n_q * Hkv : B * Hkv;
     // Kernel choice: the tensor-core kernel serves the dense bf16 modes; the
     // CUDA-core kernel serves every mode.
-    const bool tc_ok = c.mode == fd::kDense && !c.kv_int8 && cap < ((int64_t)1 << 31);
+    // (Q is loaded through a tensor map there: 16-byte aligned base and strides.)
+    bool q_tma = aligned16(c.q->data);
+    for (int i = 0; i < 3; ++i) q_tma = q_tma && (c.q->stride[i] * 2) % 16 == 0;
+    const bool tc_ok = c.mode == fd::kDense && !c.kv_int8 && cap < ((int64_t)1 << 31) && q_tma;
     int32_t kernel = o.kernel == FD_KERNEL_AUTO ? (tc_ok ? FD_KERNEL_TC : FD_KERNEL_SIMT) : o.kernel;
     if (kernel == FD_KERNEL_TC && !tc_ok) return FD_ERR_UNSUPPORTED;
     const int tile = kernel_tile(kernel);
-    const int64_t max_tiles =
-        c.mode == fd::kGather ? nseg * fd::ceil_div(c.idx_len, tile) : nseg * fd::ceil_div(cap, tile);
+    const int32_t seg_units = kernel == FD_KERNEL_TC ? fd_seg_units(FD_KERNEL_TC, (int32_t)d) : 0;
+    const int64_t max_units =
+        c.mode == fd::kGather ? nseg * fd::ceil_div(c.idx_len, tile)
+                              : nseg * (fd::ceil_div(cap, tile) + seg_units);
     int32_t G = o.num_ctas;
     if (G == 0) {
-        G = auto_ctas(kernel, max_tiles);
+        G = auto_ctas(kernel, max_units);
         if (G <= 0) return FD_ERR_CUDA;
     }
     if (nseg > ws->max_segments || rows > ws->max_rows || d > ws->head_dim || G > ws->max_ctas)
@@ -216,6 +224,8 @@ int run(const Call &c) {
     p.counters = ws->counters;
     p.status = ws->status;
     p.partials = ws->partials;
+
+    p.seg_units = seg_units;
 
     cudaStream_t st = static_cast<cudaStream_t>(o.stream);
     rc = kernel == FD_KERNEL_TC ? fd::launch_tc(p, G, st) : fd::launch_simt(p, G, st);
@@ -321,9 +331,9 @@ int fd_get_device_diagnostics(fd_workspace *ws, int32_t *words) {
 }
 
 int32_t fd_auto_num_ctas(int32_t kernel, int32_t head_dim, int32_t kv_dtype, int32_t rows,
-                         int64_t max_tiles) {
+                         int64_t max_units) {
     (void)head_dim; (void)kv_dtype; (void)rows;
-    return auto_ctas(resolve(kernel, kv_dtype), max_tiles);
+    return auto_ctas(resolve(kernel, kv_dtype), max_units);
 }
 
 int32_t fd_tile_tokens(int32_t kernel, int32_t head_dim, int32_t kv_dtype) {
@@ -332,29 +342,41 @@ int32_t fd_tile_tokens(int32_t kernel, int32_t head_dim, int32_t kv_dtype) {
 }
 
 int64_t fd_plan(const int64_t *seg_len, int64_t nseg, int32_t tile_tokens, int32_t num_ctas,
-                int32_t *first_cta, int32_t *n_pieces) {
-    if (!seg_len || nseg < 0 || tile_tokens < 1 || num_ctas < 1 || !first_cta || !n_pieces)
+                int32_t seg_units, int32_t *first_cta, int32_t *n_pieces) {
+    if (!seg_len || nseg < 0 || tile_tokens < 1 || num_ctas < 1 || seg_units < 0 ||
+        !first_cta || !n_pieces)
         return FD_ERR_ARG;
     int64_t total = 0;
     for (int64_t s = 0; s < nseg; ++s) {
         if (seg_len[s] < 0) return FD_ERR_ARG;
-        total += fd::ceil_div(seg_len[s], tile_tokens);
+        const int64_t n = fd::ceil_div(seg_len[s], tile_tokens);
+        total += n > 0 ? n + seg_units : 0;
     }
     const fd::Split sp{total, fd::working_blocks(total, num_ctas)};
-    int64_t first = 0;
+    int64_t first = 0;   // unit index where segment s starts
     for (int64_t s = 0; s < nseg; ++s) {
         const int64_t n = fd::ceil_div(seg_len[s], tile_tokens);
         if (n == 0) {
             first_cta[s] = (int32_t)(s % num_ctas);   // block that zeroes it
             n_pieces[s] = 0;
         } else {
-            const int32_t a = sp.owner(first), b = sp.owner(first + n - 1);
+            // blocks whose ranges hold the segment's tiles (its units after
+            // the first seg_units)
+            const int32_t a = sp.owner(first + seg_units), b = sp.owner(first + seg_units + n - 1);
             first_cta[s] = a;
             n_pieces[s] = b - a + 1;
+            first += n + seg_units;
         }
-        first += n;
     }
     return total;
+}
+
+int32_t fd_seg_units(int32_t kernel, int32_t head_dim) {
+    if (kernel != FD_KERNEL_TC || (head_dim != 128 && head_dim != 256)) return 0;
+    fd::Params p;
+    memset(&p, 0, sizeof p);
+    p.d = head_dim;
+    return fd::tc_seg_units(p);
 }
 
 const char *fd_status_string(int status) {

@@ -25,6 +25,8 @@ struct Params {
     int32_t kv_int8;
     int32_t out_f32;
     int32_t tile;          // cache positions per tile
+    int32_t seg_units;     // extra work units the split charges at the start of
+                           // each non-empty segment (0: plain tile split)
     float scale_log2;      // scale * log2(e): scores are kept in the log2 domain
     int32_t idx_len;
     int64_t nseg;          // segments: B*Hkv (dense) or B*n_q*Hkv (gather)

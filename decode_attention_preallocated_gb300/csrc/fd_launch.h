@@ -14,6 +14,8 @@ int launch_simt(const Params &p, int num_ctas, cudaStream_t stream);
 // Tensor-core kernel (fd_tc.cu): dense bf16 prefix (optionally causal),
 // head_dim 128 / 256, up to 64 packed rows; one block per SM.
 int tc_tile_tokens();
+// Work units the split charges per segment start (Params::seg_units).
+int tc_seg_units(const Params &p);
 bool tc_supports(const Params &p);
 int launch_tc(const Params &p, int num_ctas, cudaStream_t stream);
 

@@ -4,9 +4,11 @@
 // Work split: the same balanced tile partition as the CUDA-core kernel
 // (fd_internal.h), with 128-position tiles and one block per SM.  Roles
 // inside a block (320 threads):
-//   warp 8      TMA producer: streams K and V tiles of the block's range into
-//               a ring of shared-memory slots (4-D tensor maps, 128-byte
-//               swizzle), in the order the MMAs consume them.
+//   warp 8      TMA producer: loads each segment's packed Q rows (one box
+//               per 64 columns) as soon as the previous piece's last QK has
+//               read the buffer, and streams K and V tiles of the block's
+//               range into a ring of shared-memory slots (4-D tensor maps,
+//               128-byte swizzle), in the order the MMAs consume them.
 //   warp 9      MMA issuer (one thread): S^T = K . Q^T   (M = 128 positions,
 //               N = padded query rows, K = head_dim) into TMEM, then
 //               O^T += V^T . P^T (M = 128 dims per chunk, N = rows,
@@ -55,6 +57,7 @@ constexpr float kRescaleSlack = 8.f;
 struct TcArgs {   // CUtensorMap members carry their own alignment
     CUtensorMap tk;
     CUtensorMap tv;
+    CUtensorMap tq;
     Params p;
 };
 
@@ -75,7 +78,8 @@ struct Cfg {
     // operand buffers.  Scratch per group: [2 tiles][4 warps][NH] floats.
     static constexpr uint32_t RED_GROUP = 2 * 4 * NH;   // floats
     static constexpr uint32_t RED = kSoftmaxGroups * RED_GROUP * 4;
-    // Per-row element offsets of q and out for the current segment (int64).
+    // Per-row element offsets into out for the current segment (int64), two
+    // tables used by alternate pieces.
     static constexpr uint32_t OFF_TBL = 512 + RED;
     static constexpr uint32_t TBL = 2 * N * 8;
     static constexpr uint32_t MISC = ((OFF_TBL + TBL) + 1023) / 1024 * 1024;
@@ -100,6 +104,94 @@ struct Cfg {
     static constexpr uint32_t PATOM = TT * 32;
 };
 
+// ------------------------------------------------------------------ pieces
+// The split is over work units: a non-empty segment s = b*Hkv + hk holds
+// V = p.seg_units units that stand for the fixed cost of a piece boundary
+// (epilogue, pipeline restart), then one unit per tile.  The block whose
+// range crosses into a segment pays for the boundary with V fewer tiles; a
+// range may start or end inside those V units, which map to no tile.
+// A block's work is a run of consecutive non-empty segments.  The first one
+// is found once per block by a warp scan over the sequence lengths; every
+// later one is the next non-empty segment, so walking needs no division.
+struct Walk {
+    int64_t s;        // segment
+    int64_t first;    // unit index of the segment's first tile
+    int64_t L;        // its sequence length
+    int32_t ntiles;   // its tile count
+    int32_t b, hk;
+};
+
+__device__ __forceinline__ int32_t tiles_of(int64_t L) { return (int32_t)((L + TT - 1) / TT); }
+
+// Units of a segment of n tiles.
+__device__ __forceinline__ int64_t units_of(const Params &p, int64_t n) {
+    return n > 0 ? n + p.seg_units : 0;
+}
+
+// Total work units of the launch (one warp; every lane gets the value).
+__device__ __forceinline__ int64_t total_units_tc(const Params &p) {
+    const int lane = threadIdx.x & 31;
+    int64_t acc = 0;
+    for (int b = lane; b < p.B; b += 32) acc += units_of(p, tiles_of(seq_len(p, b)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc * p.Hkv;
+}
+
+// The segment holding work unit t (one warp; false if t is past the end).
+__device__ __noinline__ bool first_piece_warp(const Params &p, int64_t t, Walk *w) {
+    const int lane = threadIdx.x & 31;
+    int64_t base = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int64_t L = b < p.B ? seq_len(p, b) : 0;
+        const int64_t n = tiles_of(L), u = units_of(p, n);
+        const int64_t wt = (int64_t)p.Hkv * u;
+        int64_t incl = wt;   // inclusive scan over the 32 lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += x;
+        }
+        const int64_t excl = incl - wt;
+        const unsigned m = __ballot_sync(0xffffffffu, wt > 0 && t >= base + excl && t < base + incl);
+        if (m) {
+            const int src = __ffs(m) - 1;
+            const int64_t e = __shfl_sync(0xffffffffu, excl, src);
+            const int64_t nb = __shfl_sync(0xffffffffu, n, src);
+            const int64_t ub = __shfl_sync(0xffffffffu, u, src);
+            const int64_t Lb = __shfl_sync(0xffffffffu, L, src);
+            const int hk = (int)((t - base - e) / ub);
+            w->b = b0 + src;
+            w->hk = hk;
+            w->s = (int64_t)w->b * p.Hkv + hk;
+            w->first = base + e + (int64_t)hk * ub + p.seg_units;
+            w->ntiles = (int32_t)nb;
+            w->L = Lb;
+            return true;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return false;
+}
+
+// Advance to the next segment with at least one tile (false past the end).
+__device__ __forceinline__ bool next_piece(const Params &p, Walk &w) {
+    w.first += w.ntiles;
+    do {
+        if (w.s + 1 >= p.nseg) return false;
+        ++w.s;
+        if (++w.hk == p.Hkv) {
+            w.hk = 0;
+            ++w.b;
+            w.L = seq_len(p, w.b);
+            w.ntiles = tiles_of(w.L);
+        }
+    } while (w.ntiles == 0);
+    w.first += p.seg_units;
+    return true;
+}
+
 struct Bars {   // at the start of shared memory; the reduction scratch follows at 512
     uint64_t slot_full[8], slot_empty[8];
     uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
@@ -111,6 +203,9 @@ struct Bars {   // at the start of shared memory; the reduction scratch follows 
     int pad;
     int64_t total;
     int vote[kSoftmaxGroups][2][4];
+    int64_t t_begin, t_end;   // the block's range of work units
+    Walk walk;                // its first piece
+    int has_work;
 };
 
 // Ring fill index of the K and V tiles of tile number tc in a piece whose
@@ -167,7 +262,7 @@ __device__ __forceinline__ void note_timeout(Bars *bs, const Params &p, int site
         p.status[2] = (int)tile;
         p.status[3] = piece;
     }
-    const int role = site == 1 ? 0 : (site <= 7 ? 1 : 2);
+    const int role = (site == 1 || site == 8) ? 0 : (site <= 7 ? 1 : 2);
     if (atomicCAS(p.status + 4 + 3 * role, 0, site) == 0) {
         p.status[5 + 3 * role] = (int)tile;
         p.status[6 + 3 * role] = piece;
@@ -183,9 +278,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
     const uint32_t smem_base = ptx::smem_u32(smem);
     Bars *bs = reinterpret_cast<Bars *>(smem);
     float *red = reinterpret_cast<float *>(smem + 512);   // per group [2][4][NH]
-    // Row tables: qoff[r], ooff[r] = element offsets of packed row r in q / out.
-    int64_t *qoff = reinterpret_cast<int64_t *>(smem + C::OFF_TBL);
-    int64_t *ooff = qoff + N;
+    // Row tables: element offset of packed row r in out, one table per piece
+    // parity (a group may start the next piece while a lagging warp of it
+    // still stores the previous one).
+    int64_t *otbl = reinterpret_cast<int64_t *>(smem + C::OFF_TBL);
     volatile int *abort_flag = &bs->abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -200,19 +296,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 
     // Segments with nothing to attend still need their output rows zeroed.
     for (int64_t s = c; s < p.nseg; s += G)
-        if (seg_tiles(p, s) == 0) zero_segment(p, s);
-    if (warp == 0) {
-        const int64_t tot = total_tiles_warp(p);
-        if (lane == 0) bs->total = tot;
+        if (tiles_of(seq_len(p, (int)(s / p.Hkv))) == 0) zero_segment(p, s);
+    // The producer warp finds the block's tile range and first piece while
+    // the others set up barriers and TMEM.
+    if (warp == kProducerWarp) {
+        const int64_t tot = total_units_tc(p);
+        Walk w{};
+        int64_t tb = 0, te = 0;
+        bool has = false;
+        if (tot > 0) {
+            const int32_t Gw = working_blocks(tot, G);
+            if (c < Gw) {
+                const Split sp{tot, Gw};
+                tb = sp.start(c);
+                te = sp.start(c + 1);
+                has = tb < te && first_piece_warp(p, tb, &w) && w.first < te;
+            }
+        }
+        if (lane == 0) {
+            bs->total = tot;
+            bs->t_begin = tb;
+            bs->t_end = te;
+            bs->walk = w;
+            bs->has_work = has;
+        }
     }
-    __syncthreads();
-    const int64_t total = bs->total;
-    if (total == 0) return;
-    const int32_t Gw = working_blocks(total, G);
-    if (c >= Gw) return;
-    const Split sp{total, Gw};
-    const int64_t t_begin = sp.start(c), t_end = sp.start(c + 1);
-
     if (tid == 0) {
         for (int i = 0; i < C::NS; ++i) {
             ptx::mbar_init(&bs->slot_full[i], 1);
@@ -224,7 +332,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             ptx::mbar_init(&bs->p_full[i], kSoftmaxThreads);
             ptx::mbar_init(&bs->p_free[i], 1);
         }
-        ptx::mbar_init(&bs->q_full, kSoftmaxThreads);
+        ptx::mbar_init(&bs->q_full, 1);
         ptx::mbar_init(&bs->q_free, 1);
         ptx::mbar_init(&bs->o_done, 1);
         ptx::mbar_init(&bs->o_free, kSoftmaxThreads);
@@ -239,33 +347,69 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         ptx::tmem_relinquish();
     }
     if (warp == kProducerWarp && lane == 0) {
+        ptx::prefetch_tmap(&a.tq);
         ptx::prefetch_tmap(&a.tk);
         ptx::prefetch_tmap(&a.tv);
+    }
+    // Padding rows (p.rows .. N-1) of the Q operand stay zero: the Q copies
+    // write only the segment's rows.
+    if (tid < kSoftmaxThreads && p.rows < N) {
+        const int per = (N - p.rows) * 8;    // 16-byte chunks per 64-column box
+        for (int e = tid; e < C::KB * per; e += kSoftmaxThreads) {
+            const int cb = e / per, rem = e - cb * per;
+            *reinterpret_cast<uint4 *>(smem + C::OFF_Q + cb * C::QB + (p.rows + rem / 8) * 128 +
+                                       (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        ptx::fence_proxy_async_smem();
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bs->tmem_base;
+    const bool has_work = bs->has_work != 0;
+    const int64_t t_begin = bs->t_begin, t_end = bs->t_end;
+    const Split sp{bs->total, has_work ? working_blocks(bs->total, G) : 1};
     const uint32_t q_addr = smem_base + C::OFF_Q;
     const uint32_t p_addr = smem_base + C::OFF_P;
 
-    if (warp == kProducerWarp) {
+    if (!has_work) {
+        // nothing to stream: straight to the exit
+    } else if (warp == kProducerWarp) {
         // ------------------------------------------------------ TMA producer
         uint32_t issued = 0;
         bool ok = true;
-        int64_t t = t_begin;
-        while (t < t_end && ok) {
-            SegPos pos;
-            const int64_t s = seg_of_tile_warp(p, t, &pos);
-            if (s < 0) break;
-            const int64_t piece_end = min(t_end, pos.first + pos.ntiles);
-            const int b = (int)(s / p.Hkv), hk = (int)(s % p.Hkv);
-            const int64_t L = seq_len(p, b);
+        int piece = 0;
+        Walk w = bs->walk;
+        int64_t t = max(t_begin, w.first);
+        while (ok) {
+            const int64_t piece_end = min(t_end, w.first + w.ntiles);
+            const int b = w.b, hk = w.hk;
+            const int64_t L = w.L;
+            // The segment's Q rows, once the previous piece's last QK has read
+            // the buffer: one box per 64 columns covering query indices
+            // 0..n_q-1 of query heads hk*g .. hk*g+g-1, which lands row
+            // r = (head offset) * n_q + (query index), K-major with the
+            // 128-byte swizzle the QK descriptors expect.
+            if (lane == 0) {
+                if (piece > 0) {
+                    ok = ptx::mbar_wait(&bs->q_free, (piece - 1) & 1, abort_flag, kWaitNs);
+                    if (!ok) note_timeout(bs, p, 8, issued, piece);
+                }
+                if (ok) {
+                    ptx::mbar_arrive_expect_tx(&bs->q_full, (uint32_t)(C::KB * p.rows * 128));
+#pragma unroll
+                    for (int cb = 0; cb < C::KB; ++cb)
+                        ptx::tma_load_4d(smem + C::OFF_Q + cb * C::QB, &a.tq, &bs->q_full, cb * 64,
+                                         0, hk * p.g, b);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
             // Fill order = MMA consumption order: K(a); then K(t+1), V(t) for
             // t = a .. b-1; then V(b) (a, b: first and last tile of the piece).
             // The ring is then a plain FIFO, and each K tile is requested one
             // tile period before its QK needs it.
-            const int64_t n_in = piece_end - t, tt0 = t - pos.first;
+            const int64_t n_in = piece_end - t, tt0 = t - w.first;
             for (int64_t step = 0; step < 2 * n_in && ok; ++step) {
                 int64_t j;
                 int kv;
@@ -290,7 +434,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (ok) ++issued;
             }
-            t = piece_end;
+            ++piece;
+            if (piece_end >= t_end || !next_piece(p, w) || w.first >= t_end) break;
+            t = w.first;
         }
         // Drain: every issued copy must land before the block exits.
         if (lane == 0) {
@@ -369,12 +515,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             ptx::mma_commit(&bs->o_done);
             return true;
         };
-        int64_t t = t_begin;
-        while (t < t_end && ok) {
-            SegPos pos;
-            const int64_t s = seg_of_tile_warp(p, t, &pos);
-            if (s < 0) break;
-            const int64_t piece_end = min(t_end, pos.first + pos.ntiles);
+        Walk w = bs->walk;
+        int64_t t = max(t_begin, w.first);
+        while (ok) {
+            const int64_t piece_end = min(t_end, w.first + w.ntiles);
             const uint32_t n_in = (uint32_t)(piece_end - t);
             pa = tile_ctr;
             pb = tile_ctr + n_in - 1;
@@ -402,8 +546,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             tile_ctr += n_in;
-            t = piece_end;
             ++piece;
+            if (piece_end >= t_end || !next_piece(p, w) || w.first >= t_end) break;
+            t = w.first;
         }
         // Drain: all MMAs issued by this thread complete before TMEM is freed.
         if (lane == 0 && issued_any) {
@@ -452,26 +597,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             note_timeout(bs, p, 14, tile_ctr, piece);
             return false;
         };
-        int64_t t = t_begin;
-        while (t < t_end && ok) {
-            SegPos pos;
-            const int64_t s = seg_of_tile_warp(p, t, &pos);
-            if (s < 0) break;
-            const int64_t piece_end = min(t_end, pos.first + pos.ntiles);
+        Walk w = bs->walk;
+        int64_t t = max(t_begin, w.first);
+        while (ok) {
+            const int64_t s = w.s;
+            const int64_t piece_end = min(t_end, w.first + w.ntiles);
             const int64_t n_in = piece_end - t;
-            const int64_t tt0 = t - pos.first;
-            const int b = (int)(s / p.Hkv);
-            const int64_t L = seq_len(p, b);
+            const int64_t tt0 = t - w.first;
+            const int64_t L = w.L;
             const int rows = p.rows;
 
-            // Row tables for this group's rows (one division sequence per row,
-            // so the unrolled per-row code below needs none), the causal
-            // limit of each row, then the group's Q rows -> shared memory
-            // (K-major, 128-byte swizzle).
+            // Output offsets of this group's rows (one division sequence per
+            // row, so the unrolled per-row code below needs none) and the
+            // causal limit of each row.  The Q rows arrive by TMA.
+            int64_t *ooff = otbl + (piece & 1) * N;
             if (wt < NH && cb0 + wt < rows) {
-                const RowMap m = row_of(p, s, cb0 + wt);
-                qoff[cb0 + wt] = (int64_t)m.b * p.qs[0] + (int64_t)m.i * p.qs[1] + (int64_t)m.h * p.qs[2];
-                ooff[cb0 + wt] = (int64_t)m.b * p.os[0] + (int64_t)m.i * p.os[1] + (int64_t)m.h * p.os[2];
+                const int r = cb0 + wt, i = r % p.n_q, h = w.hk * p.g + r / p.n_q;
+                ooff[r] = (int64_t)w.b * p.os[0] + (int64_t)i * p.os[1] + (int64_t)h * p.os[2];
             }
             int lim[NH];    // last visible position of each row
             {
@@ -482,25 +624,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     if (++qi == p.n_q) qi = 0;
                 }
             }
-            if (piece > 0) ok = ptx::mbar_wait(&bs->q_free, (piece - 1) & 1, abort_flag, kWaitNs);
-            if (!ok) { note_timeout(bs, p, 8, tile_ctr, piece); break; }
-            ok = wg_sync();
-            if (!ok) break;
-            for (int e = wt; e < NH * (D / 8); e += 128) {
-                const int r = cb0 + e / (D / 8), cc = e % (D / 8);
-                uint32_t w[4] = {0, 0, 0, 0};
-                if (r < rows) {
-                    const uint16_t *src = p.q + qoff[r] + cc * 8;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        w[k] = (uint32_t)src[2 * k] | ((uint32_t)src[2 * k + 1] << 16);
-                }
-                unsigned char *dst = smem + C::OFF_Q + (cc >> 3) * C::QB + r * 128 +
-                                     (((cc & 7) ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(&bs->q_full);
 
             float mrun[NH], lpart[NH];
 #pragma unroll
@@ -555,7 +678,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     for (int r = 0; r < NH; ++r) {
                         const float tmax = fmaxf(fmaxf(rb[r], rb[NH + r]),
                                                  fmaxf(rb[2 * NH + r], rb[3 * NH + r]));
-                        const float mnew = fmaxf(mrun[r], tmax);
+                        // Only rows that passed their own threshold move,
+                        // so a row's arithmetic never depends on another
+                        // row's scores.
+                        const float mnew = tmax > mrun[r] + kRescaleSlack ? tmax : mrun[r];
                         const float muse = mnew == neg_inf() ? 0.f : mnew;
                         alpha[r] = fast_exp2(mrun[r] - muse);
                         grow = grow || (alpha[r] < 1.f);
@@ -655,7 +781,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             ok = ok && wg_sync();
             if (!ok) { set_abort(bs, p); break; }
 
-            const int c_first = sp.owner(pos.first), c_last = sp.owner(pos.first + pos.ntiles - 1);
+            // Blocks sharing the segment (owner() only where the piece is
+            // cut at this block's range boundary).
+            const int c_first = w.first >= t_begin ? c : sp.owner(w.first);
+            const int c_last = w.first + w.ntiles <= t_end ? c : sp.owner(w.first + w.ntiles - 1);
             if (c_first == c_last) {
 #pragma unroll
                 for (int r = 0; r < NH; ++r) {
@@ -761,8 +890,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 }
                 if (bs->last_flag && tid == 0) p.counters[s] = 0;
             }
-            t = piece_end;
             ++piece;
+            if (piece_end >= t_end || !next_piece(p, w) || w.first >= t_end) break;
+            t = w.first;
         }
     }
 
@@ -807,6 +937,21 @@ bool make_map(CUtensorMap *m, const void *base, const int64_t *st, const Params 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [B, n_q, Hq, d] queries -> 4-D map (d, n_q, Hq, B), box (64, n_q, g, 1):
+// one box holds a segment's packed rows for 64 columns.
+bool make_qmap(CUtensorMap *m, const Params &p) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)p.n_q, (cuuint64_t)p.Hq, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {(cuuint64_t)p.qs[1] * 2, (cuuint64_t)p.qs[2] * 2,
+                             (cuuint64_t)p.qs[0] * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)p.n_q, (cuuint32_t)p.g, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(p.q), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int N>
 int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
     using C = Cfg<D, N>;
@@ -831,9 +976,18 @@ int launch_d(const TcArgs &args, int G, cudaStream_t st) {
 
 int tc_tile_tokens() { return TT; }
 
+// Work units charged per segment start: about the cost of a piece boundary
+// (epilogue of one piece, restart of the pipeline on the next) in tile times.
+// A tile of head_dim 256 streams twice the bytes of one of head_dim 128.
+int tc_seg_units(const Params &p) { return p.d == 256 ? 6 : 9; }
+
 bool tc_supports(const Params &p) {
+    // Q goes through a tensor map: 16-byte aligned base and strides.
+    const bool q_aligned = (reinterpret_cast<uintptr_t>(p.q) & 15) == 0 && p.qs[0] % 8 == 0 &&
+                           p.qs[1] % 8 == 0 && p.qs[2] % 8 == 0;
     return p.mode == kDense && !p.kv_int8 && (p.d == 128 || p.d == 256) && p.rows >= 1 &&
-           p.rows <= 64 && p.cap < (int64_t)1 << 31 && p.B < (1 << 30) && p.Hkv < (1 << 30);
+           p.rows <= 64 && p.cap < (int64_t)1 << 31 && p.B < (1 << 30) && p.Hkv < (1 << 30) &&
+           q_aligned;
 }
 
 int launch_tc(const Params &p, int G, cudaStream_t st) {
@@ -841,7 +995,9 @@ int launch_tc(const Params &p, int G, cudaStream_t st) {
     TcArgs args;
     memset(&args, 0, sizeof args);
     args.p = p;
-    if (!make_map(&args.tk, p.k, p.ks, p) || !make_map(&args.tv, p.v, p.vs, p)) return -5;
+    if (!make_map(&args.tk, p.k, p.ks, p) || !make_map(&args.tv, p.v, p.vs, p) ||
+        !make_qmap(&args.tq, p))
+        return -5;
     if (p.d == 128) return launch_d<128>(args, G, st);
     return launch_d<256>(args, G, st);
 }

@@ -86,8 +86,9 @@ _SIGNATURES = [
      [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64]),
     ("fd_tile_tokens", ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     ("fd_plan", ctypes.c_int64,
-     [_P(ctypes.c_int64), ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+     [_P(ctypes.c_int64), ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
       _P(ctypes.c_int32), _P(ctypes.c_int32)]),
+    ("fd_seg_units", ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32]),
     ("fd_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("fd_version", ctypes.c_int32, []),
 ]
@@ -234,17 +235,23 @@ def tile_tokens(kernel=FD_KERNEL_AUTO, head_dim=128, kv_dtype=FD_BF16) -> int:
     return int(lib().fd_tile_tokens(kernel, head_dim, kv_dtype))
 
 
-def plan(seg_len, tile, num_ctas):
-    """Host mirror of the device partitioner: (total tiles, first block of
-    each segment, number of blocks sharing each segment)."""
+def plan(seg_len, tile, num_ctas, seg_units=0):
+    """Host mirror of the device partitioner: (total work units, first block
+    of each segment, number of blocks sharing each segment).  Each non-empty
+    segment is charged `seg_units` units before its tiles."""
     n = len(seg_len)
     arr = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in seg_len])
     first = (ctypes.c_int32 * max(n, 1))()
     pieces = (ctypes.c_int32 * max(n, 1))()
-    total = lib().fd_plan(arr, n, int(tile), int(num_ctas), first, pieces)
+    total = lib().fd_plan(arr, n, int(tile), int(num_ctas), int(seg_units), first, pieces)
     if total < 0:
         raise FdError(int(total), "fd_plan")
     return int(total), list(first)[:n], list(pieces)[:n]
+
+
+def seg_units(kernel, head_dim):
+    """Work units a launch of `kernel` charges per segment start."""
+    return int(lib().fd_seg_units(int(kernel), int(head_dim)))
 
 
 # ---------------------------------------------------------- torch wrappers

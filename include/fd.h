@@ -85,11 +85,13 @@ extern "C" {
                                     call's output is not valid              */
 
 /* kernel selection (fd_opts.kernel); AUTO takes the tensor-core kernel for
- * the dense bf16 modes and the CUDA-core kernel otherwise */
+ * the dense bf16 modes when q's base pointer and strides are 16-byte aligned
+ * (q is read through a TMA tensor map there), the CUDA-core kernel otherwise */
 #define FD_KERNEL_AUTO 0
 #define FD_KERNEL_SIMT 1         /* CUDA-core kernel, every mode           */
 #define FD_KERNEL_TC 2           /* tensor-core (tcgen05) kernel, dense
-                                    bf16 modes only (else FD_ERR_UNSUPPORTED) */
+                                    bf16 modes with 16-byte aligned q only
+                                    (else FD_ERR_UNSUPPORTED)              */
 
 #define FD_MAX_ROWS 64           /* query rows per kv head per launch unit */
 
@@ -213,21 +215,30 @@ int fd_get_device_status(fd_workspace *ws, int32_t *status);
 int fd_get_device_diagnostics(fd_workspace *ws, int32_t *words);
 
 /* Number of thread blocks an auto launch of a dense call with this cache
- * dtype would use on the current device (host query; 0 on error). */
+ * dtype would use on the current device (host query; 0 on error).  max_units
+ * bounds the launch's work units (tiles for the capacity plus fd_seg_units
+ * per segment); 0 for no bound. */
 int32_t fd_auto_num_ctas(int32_t kernel, int32_t head_dim, int32_t kv_dtype,
-                         int32_t rows, int64_t max_tiles);
+                         int32_t rows, int64_t max_units);
 /* Cache positions per K/V tile for a kernel / head_dim / cache dtype. */
 int32_t fd_tile_tokens(int32_t kernel, int32_t head_dim, int32_t kv_dtype);
 
 /*
  * Host mirror of the device split partitioner, for inspection and tests.
- * For segment lengths seg_len[0..nseg) (positions), tile size and num_ctas,
- * writes for every segment the first thread block that works on it and the
- * number of blocks that share it (0 for an empty segment).  Returns the total
- * tile count, or a negative FD_ERR_* code.
+ * The split is over work units: each non-empty segment holds seg_units units
+ * (the fixed cost of a piece boundary, mapped to no tile) followed by one
+ * unit per tile; num_ctas blocks take balanced consecutive unit ranges.
+ * For segment lengths seg_len[0..nseg) (positions), tile size, num_ctas and
+ * seg_units, writes for every segment the first thread block that works on
+ * its tiles and the number of blocks that share them (0 for an empty
+ * segment).  Returns the total unit count, or a negative FD_ERR_* code.
  */
 int64_t fd_plan(const int64_t *seg_len, int64_t nseg, int32_t tile_tokens,
-                int32_t num_ctas, int32_t *first_cta, int32_t *n_pieces);
+                int32_t num_ctas, int32_t seg_units, int32_t *first_cta,
+                int32_t *n_pieces);
+/* seg_units a launch of this kernel and head_dim uses (0 for the CUDA-core
+ * kernel; AUTO is not resolved here). */
+int32_t fd_seg_units(int32_t kernel, int32_t head_dim);
 
 const char *fd_status_string(int status);
 int32_t fd_version(void);

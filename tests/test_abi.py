@@ -148,34 +148,37 @@ def test_partition_covers_each_tile_once(L, seed):
     maxlen = 5000 if seed % 2 else 300           # odd seeds: more blocks than tiles
     lens = [rnd.choice([0, rnd.randint(1, maxlen)]) for _ in range(nseg)]
     grid = rnd.randint(1, 400)
-    total, first, pieces = fd.plan(lens, tile, grid)
+    V = rnd.choice([0, 0, 1, 4, 6])      # units charged per segment start
+    total, first, pieces = fd.plan(lens, tile, grid, V)
     ntiles = [-(-x // tile) for x in lens]
-    assert total == sum(ntiles)
+    units = [n + V if n else 0 for n in ntiles]
+    assert total == sum(units)
     if total == 0:
         assert all(p == 0 for p in pieces)
         return
-    G = min(grid, total)          # blocks beyond the tile count get no work
+    G = min(grid, total)          # blocks beyond the unit count get no work
     starts = [c * total // G for c in range(G + 1)]
     assert all(starts[c + 1] > starts[c] for c in range(G))
-    # balanced: block ranges differ by at most one tile
+    # balanced: block ranges differ by at most one unit
     sizes = [starts[c + 1] - starts[c] for c in range(G)]
     assert max(sizes) - min(sizes) <= 1
-    seen = [0] * total
+    seen = {}
     slots = set()
-    t = 0
+    u = 0                          # unit where segment s starts
     for s in range(nseg):
         if ntiles[s] == 0:
             assert pieces[s] == 0
             continue
-        blocks = [c for c in range(G)
-                  if starts[c] < t + ntiles[s] and starts[c + 1] > t]
+        t0, t1 = u + V, u + units[s]     # units that carry the segment's tiles
+        blocks = [c for c in range(G) if starts[c] < t1 and starts[c + 1] > t0]
         assert blocks == list(range(first[s], first[s] + pieces[s]))
         for c in blocks:
-            lo, hi = max(starts[c], t), min(starts[c + 1], t + ntiles[s])
-            for x in range(lo, hi):
-                seen[x] += 1
+            lo, hi = max(starts[c], t0), min(starts[c + 1], t1)
+            for x in range(lo - t0, hi - t0):
+                seen[(s, x)] = seen.get((s, x), 0) + 1
             assert s + c not in slots          # workspace slot is unique
             slots.add(s + c)
             assert s + c < nseg + G - 1
-        t += ntiles[s]
-    assert all(x == 1 for x in seen)
+        u += units[s]
+    # every tile of every segment is covered exactly once
+    assert len(seen) == sum(ntiles) and all(x == 1 for x in seen.values())
