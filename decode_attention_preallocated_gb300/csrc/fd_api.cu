@@ -106,7 +106,7 @@ int32_t auto_ctas(int32_t kernel, int64_t max_units) {
 // The kernel an auto request runs for a dense call with this cache dtype.
 int32_t resolve(int32_t kernel, int32_t kv_dtype) {
     if (kernel != FD_KERNEL_AUTO) return kernel;
-    return kv_dtype == FD_BF16 ? FD_KERNEL_TC : FD_KERNEL_SIMT;
+    return kv_dtype == FD_BF16 || kv_dtype == FD_I8 ? FD_KERNEL_TC : FD_KERNEL_SIMT;
 }
 
 // Shared validation and launch for the three entry points.
@@ -181,11 +181,14 @@ int run(const Call &c) {
     // (Q is loaded through a tensor map there: 16-byte aligned base and strides.)
     bool q_tma = aligned16(c.q->data);
     for (int i = 0; i < 3; ++i) q_tma = q_tma && (c.q->stride[i] * 2) % 16 == 0;
-    const bool tc_ok = c.mode == fd::kDense && !c.kv_int8 && cap < ((int64_t)1 << 31) && q_tma;
+    // (int8 caches: head_dim 128 and up to 32 rows there.)
+    const bool tc_ok = c.mode == fd::kDense && cap < ((int64_t)1 << 31) && q_tma &&
+                       (!c.kv_int8 || (d == 128 && rows <= 32));
     int32_t kernel = o.kernel == FD_KERNEL_AUTO ? (tc_ok ? FD_KERNEL_TC : FD_KERNEL_SIMT) : o.kernel;
     if (kernel == FD_KERNEL_TC && !tc_ok) return FD_ERR_UNSUPPORTED;
     const int tile = kernel_tile(kernel);
-    const int32_t seg_units = kernel == FD_KERNEL_TC ? fd_seg_units(FD_KERNEL_TC, (int32_t)d) : 0;
+    const int32_t seg_units =
+        kernel == FD_KERNEL_TC ? fd_seg_units(FD_KERNEL_TC, (int32_t)d, kvdt) : 0;
     const int64_t max_units =
         c.mode == fd::kGather ? nseg * fd::ceil_div(c.idx_len, tile)
                               : nseg * (fd::ceil_div(cap, tile) + seg_units);
@@ -371,11 +374,12 @@ int64_t fd_plan(const int64_t *seg_len, int64_t nseg, int32_t tile_tokens, int32
     return total;
 }
 
-int32_t fd_seg_units(int32_t kernel, int32_t head_dim) {
+int32_t fd_seg_units(int32_t kernel, int32_t head_dim, int32_t kv_dtype) {
     if (kernel != FD_KERNEL_TC || (head_dim != 128 && head_dim != 256)) return 0;
     fd::Params p;
     memset(&p, 0, sizeof p);
     p.d = head_dim;
+    p.kv_int8 = kv_dtype == FD_I8;
     return fd::tc_seg_units(p);
 }
 

@@ -31,6 +31,7 @@
 // FD_DEV_INTERNAL in the status word, records where it waited, and the block
 // drains its copies and MMAs and exits.
 #include <cuda.h>
+#include <type_traits>
 #include <cuda_runtime.h>
 
 #include "fd_device.cuh"
@@ -42,11 +43,10 @@ namespace fd {
 namespace {
 
 constexpr int TT = 128;                 // cache positions per tile (MMA M)
-constexpr int kSoftmaxGroups = 2;       // warpgroups splitting the query rows
-constexpr int kSoftmaxThreads = 128 * kSoftmaxGroups;
-constexpr int kThreadsTC = kSoftmaxThreads + 64;
-constexpr int kProducerWarp = kSoftmaxThreads / 32;
-constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kMaxGroups = 2;           // softmax warpgroups (bf16 caches)
+constexpr int kThreadsTC = 320;         // warps 0-7, producer, MMA issuer
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kDevTimeout = 4;          // mirrors FD_DEV_INTERNAL
 // Scores (log2 units) may exceed a row's running maximum by this much before
@@ -55,14 +55,20 @@ constexpr int kDevTimeout = 4;          // mirrors FD_DEV_INTERNAL
 constexpr float kRescaleSlack = 8.f;
 
 struct TcArgs {   // CUtensorMap members carry their own alignment
+    // (int8 caches: tk / tv map the int8 codes)
     CUtensorMap tk;
     CUtensorMap tv;
     CUtensorMap tq;
     Params p;
 };
 
-template <int D, int N>
+template <int D, int N, bool I8, int NV>
 struct Cfg {
+    // bf16 caches: two softmax warpgroups split the rows (warps 0-7).  int8
+    // caches: one softmax warpgroup (warps 0-3); warps 4-7 widen the int8
+    // tiles to bf16 for the MMAs.
+    static constexpr int GROUPS = I8 ? 1 : 2;
+    static constexpr int SMT = 128 * GROUPS;     // softmax threads
     static constexpr int KB = D / 64;            // 128-byte boxes per cache row
     static constexpr int DC = D / 128;           // 128-dim chunks of O
     static constexpr uint32_t BOX = TT * 128;    // bytes of one box of a slot
@@ -72,28 +78,37 @@ struct Cfg {
     static constexpr uint32_t PPLANE = 2 * QB;   // one bf16 plane of P (128 positions x N)
     static constexpr uint32_t PSTAGE = 2 * PPLANE;   // P = hi plane + lo plane
     // Query rows per softmax warpgroup.
-    static constexpr int NH = N / kSoftmaxGroups;
+    // Rows the softmax handles: NV (<= N, a multiple of 8) bounds the packed
+    // rows; the MMAs still run N columns, and P rows NV..N-1 stay zero.
+    static_assert(NV <= N && NV % 8 == 0, "valid-row bound");
+    static constexpr int NH = NV / GROUPS;
     static_assert(NH % 8 == 0, "rows per group must be a multiple of 8");
     // Barriers and the reduction scratch come first, then 1024-byte aligned
     // operand buffers.  Scratch per group: [2 tiles][4 warps][NH] floats.
     static constexpr uint32_t RED_GROUP = 2 * 4 * NH;   // floats
-    static constexpr uint32_t RED = kSoftmaxGroups * RED_GROUP * 4;
+    static constexpr uint32_t RED = GROUPS * RED_GROUP * 4;
     // Per-row element offsets into out for the current segment (int64), two
     // tables used by alternate pieces.
     static constexpr uint32_t OFF_TBL = 512 + RED;
     static constexpr uint32_t TBL = 2 * N * 8;
     static constexpr uint32_t MISC = ((OFF_TBL + TBL) + 1023) / 1024 * 1024;
     static constexpr uint32_t BUDGET = 232448;   // max dynamic shared memory per block
+    // int8 caches: a ring of NR raw tiles (TT positions x D codes, as TMA
+    // lands them) in front of the bf16 slots the MMAs read.
+    static constexpr uint32_t RAW = I8 ? TT * D : 0;
+    static constexpr int NR = I8 ? 6 : 0;
+    static constexpr int NRX = I8 ? NR : 1;   // ring length for index arithmetic
     // Two P stages when that still leaves three K/V slots, else one.
-    static constexpr int NS2 = (int)((BUDGET - MISC - QBYTES - 2 * PSTAGE) / SLOT);
+    static constexpr int NS2 = (int)((BUDGET - MISC - QBYTES - 2 * PSTAGE - NR * RAW) / SLOT);
     static constexpr int PST = NS2 >= 3 ? 2 : 1;
-    static constexpr int NS_RAW = (int)((BUDGET - MISC - QBYTES - PST * PSTAGE) / SLOT);
+    static constexpr int NS_RAW = (int)((BUDGET - MISC - QBYTES - PST * PSTAGE - NR * RAW) / SLOT);
     static constexpr int NS = NS_RAW > 8 ? 8 : NS_RAW;
     static_assert(NS >= 2, "need two K/V slots");
     static constexpr uint32_t OFF_SLOTS = MISC;
     static constexpr uint32_t OFF_Q = OFF_SLOTS + NS * SLOT;
     static constexpr uint32_t OFF_P = OFF_Q + QBYTES;
-    static constexpr uint32_t SMEM = OFF_P + PST * PSTAGE;
+    static constexpr uint32_t OFF_RAW = OFF_P + PST * PSTAGE;
+    static constexpr uint32_t SMEM = OFF_RAW + NR * RAW;
     static_assert(SMEM <= BUDGET, "shared memory budget");
     static constexpr uint32_t COLS = 2 * N + DC * N;
     static constexpr uint32_t TMEM_COLS = COLS <= 32 ? 32 : COLS <= 64 ? 64 : COLS <= 128 ? 128 : 256;
@@ -196,13 +211,14 @@ struct Bars {   // at the start of shared memory; the reduction scratch follows 
     uint64_t slot_full[8], slot_empty[8];
     uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
     uint64_t q_full, q_free, o_done, o_free, exit_mma, sm_bar;
-    uint64_t wg_bar[kSoftmaxGroups];
+    uint64_t wg_bar[kMaxGroups];
+    uint64_t raw_full[6], raw_empty[6];   // int8 caches: raw tile ring
     uint32_t tmem_base;
     int abort_flag;
     int last_flag;
     int pad;
     int64_t total;
-    int vote[kSoftmaxGroups][2][4];
+    int vote[kMaxGroups][2][4];
     int64_t t_begin, t_end;   // the block's range of work units
     Walk walk;                // its first piece
     int has_work;
@@ -241,6 +257,18 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Two int8 codes (bytes k and k+1 of w) -> two bf16 holding the same integers,
+// exactly: byte ^ 0x80 = code + 128 in [0, 255] becomes the low mantissa
+// byte of the float 1.5 * 2^23 + code + 128, from which the constant is
+// subtracted exactly; integers of magnitude <= 128 are exact in bf16.
+__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int k) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float base = 12582912.f + 128.f;
+    const float f0 = __uint_as_float(__byte_perm(u, 0x4B400000u, 0x7650 | k)) - base;
+    const float f1 = __uint_as_float(__byte_perm(u, 0x4B400000u, 0x7650 | (k + 1))) - base;
+    return pack_bf16x2(f0, f1);
+}
+
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
     __nv_bfloat16 h = __float2bfloat16_rn(x);
     return *reinterpret_cast<uint16_t *>(&h);
@@ -270,9 +298,10 @@ __device__ __forceinline__ void note_timeout(Bars *bs, const Params &p, int site
     set_abort(bs, p);
 }
 
-template <int D, int N>
+template <int D, int N, bool I8, int NV>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant__ TcArgs a) {
-    using C = Cfg<D, N>;
+    using C = Cfg<D, N, I8, NV>;
+    constexpr int kSoftmaxThreads = C::SMT;
     const Params &p = a.p;
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t smem_base = ptx::smem_u32(smem);
@@ -322,9 +351,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         }
     }
     if (tid == 0) {
+        // bf16 slots are filled by TMA (one arrival plus bytes) or, for int8
+        // caches, by the 128 widening threads.
         for (int i = 0; i < C::NS; ++i) {
-            ptx::mbar_init(&bs->slot_full[i], 1);
+            ptx::mbar_init(&bs->slot_full[i], I8 ? 128 : 1);
             ptx::mbar_init(&bs->slot_empty[i], 1);
+        }
+        for (int i = 0; i < C::NR; ++i) {
+            ptx::mbar_init(&bs->raw_full[i], 1);
+            ptx::mbar_init(&bs->raw_empty[i], 128);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&bs->s_full[i], 1);
@@ -338,7 +373,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         ptx::mbar_init(&bs->o_free, kSoftmaxThreads);
         ptx::mbar_init(&bs->exit_mma, 1);
         ptx::mbar_init(&bs->sm_bar, kSoftmaxThreads);
-        for (int g = 0; g < kSoftmaxGroups; ++g) ptx::mbar_init(&bs->wg_bar[g], 128);
+        for (int g = 0; g < C::GROUPS; ++g) ptx::mbar_init(&bs->wg_bar[g], 128);
         bs->abort_flag = 0;
         ptx::mbar_fence_init();
     }
@@ -350,6 +385,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         ptx::prefetch_tmap(&a.tq);
         ptx::prefetch_tmap(&a.tk);
         ptx::prefetch_tmap(&a.tv);
+    }
+    // P rows NV..N-1 are never written: zero them once.
+    if (NV < N && tid < kSoftmaxThreads) {
+        for (uint32_t e = tid; e < C::PST * C::PSTAGE / 16; e += kSoftmaxThreads)
+            *reinterpret_cast<uint4 *>(smem + C::OFF_P + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+        ptx::fence_proxy_async_smem();
     }
     // Padding rows (p.rows .. N-1) of the Q operand stay zero: the Q copies
     // write only the segment's rows.
@@ -417,8 +458,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 else if (step == 2 * n_in - 1) { j = n_in - 1; kv = 1; }
                 else { j = (step + 1) / 2 - (step & 1 ? 0 : 1); kv = step & 1 ? 0 : 1; }
                 const int ys = (int)tile_start(tt0 + j, L);
-                const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
-                if (lane == 0) {
+                if (lane == 0 && I8) {
+                    // int8 codes -> raw ring (one box of TT positions x D codes)
+                    const uint32_t rs = issued % C::NRX, ph = (issued / C::NRX) & 1;
+                    ok = ptx::mbar_wait(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
+                    if (!ok) note_timeout(bs, p, 1, issued, 0);
+                    if (ok) {
+                        ptx::mbar_arrive_expect_tx(&bs->raw_full[rs], C::RAW);
+                        ptx::tma_load_4d(smem + C::OFF_RAW + rs * C::RAW,
+                                         kv ? (const void *)&a.tv : (const void *)&a.tk,
+                                         &bs->raw_full[rs], 0, ys, hk, b);
+                    }
+                } else if (lane == 0) {
+                    const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
                     ok = ptx::mbar_wait(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
                     if (!ok) note_timeout(bs, p, 1, issued, 0);
                     if (ok) {
@@ -440,11 +492,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         }
         // Drain: every issued copy must land before the block exits.
         if (lane == 0) {
-            const uint32_t n = issued < (uint32_t)C::NS ? issued : (uint32_t)C::NS;
+            constexpr uint32_t RING = I8 ? (uint32_t)C::NRX : (uint32_t)C::NS;
+            const uint32_t n = issued < RING ? issued : RING;
             for (uint32_t k = 0; k < n; ++k) {
                 const uint32_t idx = issued - 1 - k;
-                ptx::mbar_wait(&bs->slot_full[idx % C::NS], (idx / C::NS) & 1, abort_flag,
-                               kWaitNs);
+                ptx::mbar_wait(I8 ? &bs->raw_full[idx % RING] : &bs->slot_full[idx % RING],
+                               (idx / RING) & 1, abort_flag, kWaitNs);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -495,21 +548,28 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             ptx::tc_fence_after();
             const uint32_t v_addr = smem_base + C::OFF_SLOTS + vs * C::SLOT;
             const uint32_t pb = p_addr + ps * C::PSTAGE;
+            const bool two_planes = p.out_f32 != 0;
+            // O^T += V^T P_hi^T (+ V^T P_lo^T for fp32 outputs)
+            auto pv_tiles = [&](auto planes) {
+                constexpr int NP = decltype(planes)::value;
 #pragma unroll
-            for (int dc = 0; dc < C::DC; ++dc) {
+                for (int dc = 0; dc < C::DC; ++dc) {
 #pragma unroll
-                for (int kt = 0; kt < TT / 16; ++kt) {
-                    const uint64_t da = ptx::smem_desc(v_addr + (2 * dc) * C::BOX + kt * 2048,
-                                                       C::BOX, 1024, ptx::kLayoutSwizzle128);
+                    for (int kt = 0; kt < TT / 16; ++kt) {
+                        const uint64_t da = ptx::smem_desc(v_addr + (2 * dc) * C::BOX + kt * 2048,
+                                                           C::BOX, 1024, ptx::kLayoutSwizzle128);
 #pragma unroll
-                    for (int plane = 0; plane < 2; ++plane) {
-                        const uint64_t db = ptx::smem_desc(pb + plane * C::PPLANE + kt * 512,
-                                                           C::PATOM, 256, ptx::kLayoutSwizzle32);
-                        ptx::mma_f16_ss(tmem + 2 * N + dc * N, da, db, C::IDESC_PV,
-                                        (!first || kt > 0 || plane > 0) ? 1u : 0u);
+                        for (int pl = 0; pl < NP; ++pl) {
+                            const uint64_t db = ptx::smem_desc(pb + pl * C::PPLANE + kt * 512,
+                                                               C::PATOM, 256, ptx::kLayoutSwizzle32);
+                            ptx::mma_f16_ss(tmem + 2 * N + dc * N, da, db, C::IDESC_PV,
+                                            (first && kt == 0 && pl == 0) ? 0u : 1u);
+                        }
                     }
                 }
-            }
+            };
+            if (two_planes) pv_tiles(std::integral_constant<int, 2>());
+            else pv_tiles(std::integral_constant<int, 1>());
             ptx::mma_commit(&bs->slot_empty[vs]);
             ptx::mma_commit(&bs->p_free[ps]);
             ptx::mma_commit(&bs->o_done);
@@ -554,6 +614,69 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         if (lane == 0 && issued_any) {
             ptx::mma_commit(&bs->exit_mma);
             ptx::mbar_wait(&bs->exit_mma, 0, abort_flag, kWaitNs);
+        }
+    } else if (I8 && warp >= 4) {
+        // ------------------------------------- int8 -> bf16 widening (warps 4-7)
+        // Fill f of the raw ring becomes fill f of the bf16 slot ring, in the
+        // producer's order.  Codes widen exactly (|code| <= 127 has 8
+        // significant bits); the per-position scales are applied to the
+        // scores and to P by the softmax group, so nothing here rounds.
+        // Raw tile: row-major [TT][D] codes.  bf16 tile: KB boxes of
+        // [TT][64] with the 128-byte swizzle (16-byte chunk c of position r
+        // at c ^ (r & 7)), exactly what a TMA load of a bf16 cache produces.
+        const int ct = tid - 128;
+        uint32_t f = 0;
+        bool ok = true;
+        int piece = 0;
+        Walk w = bs->walk;
+        int64_t t = max(t_begin, w.first);
+        while (ok) {
+            const int64_t piece_end = min(t_end, w.first + w.ntiles);
+            const int64_t n_fill = 2 * (piece_end - t);
+            for (int64_t k = 0; k < n_fill && ok; ++k, ++f) {
+                const uint32_t rs = f % C::NRX, ss = f % C::NS;
+                ok = ptx::mbar_wait(&bs->raw_full[rs], (f / C::NRX) & 1, abort_flag, kWaitNs);
+                if (!ok) { note_timeout(bs, p, 17, f, piece); break; }
+                // Thread ct takes 16 codes (dims 16*q .. 16*q+15, q = ct % QPR)
+                // of positions ct / QPR + RSTEP*k: one 16-byte load and two
+                // swizzled 16-byte stores each, all loads issued first.
+                constexpr int QPR = D / 16, RSTEP = 128 / QPR, NK = TT / RSTEP;
+                const int q16 = ct % QPR, r0 = ct / QPR;
+                // (raw rows are 128 bytes with the 128-byte swizzle: chunk q16 of
+                // row r sits at q16 ^ (r & 7), and r & 7 == r0 & 7 here)
+                static_assert(!I8 || D == 128, "int8 tiles: one 128-byte row per position");
+                const unsigned char *raw = smem + C::OFF_RAW + rs * C::RAW + r0 * D + ((q16 ^ (r0 & 7)) << 4);
+                unsigned char *dst = smem + C::OFF_SLOTS + ss * C::SLOT + (q16 >> 2) * C::BOX +
+                                     r0 * 128;
+                // (r0 + RSTEP*k) & 7 == r0 & 7: the swizzled chunk offsets are per thread
+                const int sw0 = (((2 * q16) & 7) ^ (r0 & 7)) << 4, sw1 = (((2 * q16 + 1) & 7) ^ (r0 & 7)) << 4;
+                uint4 cw[NK];
+#pragma unroll
+                for (int k = 0; k < NK; ++k)
+                    cw[k] = *reinterpret_cast<const uint4 *>(raw + k * RSTEP * D);
+                // The raw slot is free for the next copy once the codes are
+                // in registers; then wait for a bf16 slot the MMAs released.
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(&bs->raw_empty[rs]);
+                ok = ptx::mbar_wait(&bs->slot_empty[ss], ((f / C::NS) & 1) ^ 1, abort_flag, kWaitNs);
+                if (!ok) { note_timeout(bs, p, 18, f, piece); break; }
+#pragma unroll
+                for (int k = 0; k < NK; ++k) {
+                    unsigned char *row = dst + k * RSTEP * 128;
+                    *reinterpret_cast<uint4 *>(row + sw0) =
+                        make_uint4(i8x2_to_bf16x2(cw[k].x, 0), i8x2_to_bf16x2(cw[k].x, 2),
+                                   i8x2_to_bf16x2(cw[k].y, 0), i8x2_to_bf16x2(cw[k].y, 2));
+                    *reinterpret_cast<uint4 *>(row + sw1) =
+                        make_uint4(i8x2_to_bf16x2(cw[k].z, 0), i8x2_to_bf16x2(cw[k].z, 2),
+                                   i8x2_to_bf16x2(cw[k].w, 0), i8x2_to_bf16x2(cw[k].w, 2));
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(&bs->slot_full[ss]);
+            }
+            if (!ok) { set_abort(bs, p); break; }
+            ++piece;
+            if (piece_end >= t_end || !next_piece(p, w) || w.first >= t_end) break;
+            t = w.first;
         }
     } else {
         // ------------------------------------------- softmax and epilogue
@@ -629,10 +752,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 #pragma unroll
             for (int r = 0; r < NH; ++r) { mrun[r] = neg_inf(); lpart[r] = 0.f; }
 
+            // int8 caches: this segment's per-position scales, read one tile
+            // ahead (k scale multiplies the scores, v scale multiplies P but
+            // not the row sums; nothing outside the filled prefix is read).
+            const float *ksrow = I8 ? p.k_scale + (int64_t)w.b * p.kss[0] + (int64_t)w.hk * p.kss[1] : nullptr;
+            const float *vsrow = I8 ? p.v_scale + (int64_t)w.b * p.vss[0] + (int64_t)w.hk * p.vss[1] : nullptr;
+            float ksc_n = 1.f, vsc_n = 1.f;
+            auto load_scales = [&](int64_t jj) {
+                const int64_t tok = tile_start(tt0 + jj, L) + wt;
+                if (tok >= (tt0 + jj) * TT && tok < L) {
+                    ksc_n = __ldg(ksrow + tok * p.kss[2]);
+                    vsc_n = __ldg(vsrow + tok * p.vss[2]);
+                }
+            };
+            if (I8) load_scales(0);
             for (int64_t j = 0; j < n_in && ok; ++j) {
                 const int64_t y0 = (tt0 + j) * TT;
                 const int64_t token = tile_start(tt0 + j, L) + wt;
                 const uint32_t sb = tile_ctr & 1, u = tile_ctr >> 1;
+                // Visibility: a position this tile owns (the right-aligned last
+                // tile also holds positions the previous tile covered), inside
+                // the filled prefix and, for causal windows, at or before
+                // L - n_q + i for the row's query index i.
+                const bool in_len = token >= y0 && token < L;
+                const float ksc = ksc_n, vsc = vsc_n;
+                if (I8 && j + 1 < n_in) load_scales(j + 1);
                 ok = ptx::mbar_wait(&bs->s_full[sb], u & 1, abort_flag, kWaitNs);
                 if (!ok) { note_timeout(bs, p, 9, tile_ctr, piece); break; }
                 ptx::tc_fence_after();
@@ -642,15 +786,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&bs->s_free[sb]);
 
-                // Visibility: a position this tile owns (the right-aligned last
-                // tile also holds positions the previous tile covered), inside
-                // the filled prefix and, for causal windows, at or before
-                // L - n_q + i for the row's query index i.
-                const bool in_len = token >= y0 && token < L;
+                const float sl = I8 ? p.scale_log2 * ksc : p.scale_log2;
 #pragma unroll
                 for (int r = 0; r < NH; ++r) {
                     const bool vis = in_len && cb0 + r < rows && token <= lim[r];
-                    sv[r] = vis ? sv[r] * p.scale_log2 : neg_inf();
+                    sv[r] = vis ? sv[r] * sl : neg_inf();
                 }
                 // Refresh the running maxima only when some score passes
                 // mrun + kRescaleSlack (always on a segment's first tile).
@@ -712,7 +852,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     const float muse = mrun[r] == neg_inf() ? 0.f : mrun[r];
                     const float pr = fast_exp2(sv[r] - muse);
                     lpart[r] += pr;
-                    sv[r] = pr;
+                    sv[r] = I8 ? pr * vsc : pr;
                 }
                 // P^T for the PV product.
                 const uint32_t ps = tile_ctr % C::PST, pu = tile_ctr / C::PST;
@@ -726,7 +866,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 }
                 {
                     // P = hi + lo, both bf16: hi = rn(p), lo = rn(p - hi), so the
-                    // PV product sees p to about 2^-17 relative.  Thread wt
+                    // PV product sees p to about 2^-17 relative, which fp32
+                    // outputs need; bf16 outputs (2^-9 themselves) take P_hi
+                    // alone, which halves the PV MMAs.  Thread wt
                     // writes its position's row: 8 query rows per 16-byte chunk,
                     // chunk c of a 16-row atom stored at c ^ bit 2 of wt.
                     unsigned char *prow = smem + C::OFF_P + ps * C::PSTAGE + wt * 32;
@@ -744,8 +886,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         }
                         const uint32_t off = (a8 >> 1) * C::PATOM + (((a8 & 1) ^ sw) << 4);
                         *reinterpret_cast<uint4 *>(prow + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4 *>(prow + C::PPLANE + off) =
-                            make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        if (p.out_f32)
+                            *reinterpret_cast<uint4 *>(prow + C::PPLANE + off) =
+                                make_uint4(lw[0], lw[1], lw[2], lw[3]);
                     }
                 }
                 ptx::fence_proxy_async_smem();
@@ -923,17 +1066,24 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [B, Hkv, cap, d] cache -> 4-D map (d, cap, Hkv, B), box (64, 128, 1, 1),
-// 128-byte swizzle, rows past the capacity read as zeros.
+// [B, Hkv, cap, d] cache -> 4-D map (d, cap, Hkv, B); rows past the capacity
+// (or before 0) read as zeros.  bf16: box (64, 128, 1, 1) with the 128-byte
+// swizzle the MMA descriptors expect.  int8 (d = 128): the same 128-byte rows
+// (64 pairs of codes), also 128-byte swizzled (the widening threads read it).
 bool make_map(CUtensorMap *m, const void *base, const int64_t *st, const Params &p) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)p.cap, (cuuint64_t)p.Hkv, (cuuint64_t)p.B};
-    cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
-    cuuint32_t box[4] = {64, (cuuint32_t)TT, 1, 1};
+    // (int8 codes are moved as pairs: 16-bit elements, d / 2 per row)
+    const int es = p.kv_int8 ? 1 : 2;
+    const cuuint64_t row_elems = p.kv_int8 ? (cuuint64_t)p.d / 2 : (cuuint64_t)p.d;
+    cuuint64_t dims[4] = {row_elems, (cuuint64_t)p.cap, (cuuint64_t)p.Hkv, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {(cuuint64_t)(st[2] * es), (cuuint64_t)(st[1] * es),
+                             (cuuint64_t)(st[0] * es)};
+    cuuint32_t box[4] = {64u, (cuuint32_t)TT, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return fn(m, p.kv_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -952,23 +1102,23 @@ bool make_qmap(CUtensorMap *m, const Params &p) {
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int N>
+template <int D, int N, bool I8, int NV = N>
 int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
-    using C = Cfg<D, N>;
-    if (cudaFuncSetAttribute(tc_kernel<D, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    using C = Cfg<D, N, I8, NV>;
+    if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::SMEM) != cudaSuccess)
         return -5;
-    tc_kernel<D, N><<<G, kThreadsTC, C::SMEM, st>>>(args);
+    tc_kernel<D, N, I8, NV><<<G, kThreadsTC, C::SMEM, st>>>(args);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 
 template <int D>
 int launch_d(const TcArgs &args, int G, cudaStream_t st) {
     const int rows = args.p.rows;
-    if (rows <= 16) return launch_dn<D, 16>(args, G, st);
-    if (rows <= 32) return launch_dn<D, 32>(args, G, st);
-    if (rows <= 48) return launch_dn<D, 48>(args, G, st);
-    if (rows <= 64) return launch_dn<D, 64>(args, G, st);
+    if (rows <= 16) return launch_dn<D, 16, false>(args, G, st);
+    if (rows <= 32) return launch_dn<D, 32, false>(args, G, st);
+    if (rows <= 48) return launch_dn<D, 48, false>(args, G, st);
+    if (rows <= 64) return launch_dn<D, 64, false>(args, G, st);
     return -2;
 }
 
@@ -979,15 +1129,18 @@ int tc_tile_tokens() { return TT; }
 // Work units charged per segment start: about the cost of a piece boundary
 // (epilogue of one piece, restart of the pipeline on the next) in tile times.
 // A tile of head_dim 256 streams twice the bytes of one of head_dim 128.
-int tc_seg_units(const Params &p) { return p.d == 256 ? 6 : 9; }
+// int8 tiles (codes and scales) stream about half the bytes of bf16 ones.
+int tc_seg_units(const Params &p) { return p.kv_int8 ? 14 : (p.d == 256 ? 6 : 9); }
 
 bool tc_supports(const Params &p) {
     // Q goes through a tensor map: 16-byte aligned base and strides.
     const bool q_aligned = (reinterpret_cast<uintptr_t>(p.q) & 15) == 0 && p.qs[0] % 8 == 0 &&
                            p.qs[1] % 8 == 0 && p.qs[2] % 8 == 0;
-    return p.mode == kDense && !p.kv_int8 && (p.d == 128 || p.d == 256) && p.rows >= 1 &&
-           p.rows <= 64 && p.cap < (int64_t)1 << 31 && p.B < (1 << 30) && p.Hkv < (1 << 30) &&
-           q_aligned;
+    // int8 caches: head_dim 128 and up to 32 rows (one softmax warpgroup).
+    const bool shape = p.kv_int8 ? (p.d == 128 && p.rows <= 32)
+                                 : ((p.d == 128 || p.d == 256) && p.rows <= 64);
+    return p.mode == kDense && shape && p.rows >= 1 && p.cap < (int64_t)1 << 31 &&
+           p.B < (1 << 30) && p.Hkv < (1 << 30) && q_aligned;
 }
 
 int launch_tc(const Params &p, int G, cudaStream_t st) {
@@ -998,6 +1151,10 @@ int launch_tc(const Params &p, int G, cudaStream_t st) {
     if (!make_map(&args.tk, p.k, p.ks, p) || !make_map(&args.tv, p.v, p.vs, p) ||
         !make_qmap(&args.tq, p))
         return -5;
+    if (p.kv_int8)
+        return p.rows <= 8    ? launch_dn<128, 16, true, 8>(args, G, st)
+               : p.rows <= 16 ? launch_dn<128, 16, true>(args, G, st)
+                              : launch_dn<128, 32, true>(args, G, st);
     if (p.d == 128) return launch_d<128>(args, G, st);
     return launch_d<256>(args, G, st);
 }

@@ -88,7 +88,7 @@ _SIGNATURES = [
     ("fd_plan", ctypes.c_int64,
      [_P(ctypes.c_int64), ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
       _P(ctypes.c_int32), _P(ctypes.c_int32)]),
-    ("fd_seg_units", ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32]),
+    ("fd_seg_units", ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     ("fd_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("fd_version", ctypes.c_int32, []),
 ]
@@ -249,9 +249,9 @@ def plan(seg_len, tile, num_ctas, seg_units=0):
     return int(total), list(first)[:n], list(pieces)[:n]
 
 
-def seg_units(kernel, head_dim):
+def seg_units(kernel, head_dim, kv_dtype=FD_BF16):
     """Work units a launch of `kernel` charges per segment start."""
-    return int(lib().fd_seg_units(int(kernel), int(head_dim)))
+    return int(lib().fd_seg_units(int(kernel), int(head_dim), int(kv_dtype)))
 
 
 # ---------------------------------------------------------- torch wrappers

@@ -85,12 +85,15 @@ extern "C" {
                                     call's output is not valid              */
 
 /* kernel selection (fd_opts.kernel); AUTO takes the tensor-core kernel for
- * the dense bf16 modes when q's base pointer and strides are 16-byte aligned
- * (q is read through a TMA tensor map there), the CUDA-core kernel otherwise */
+ * the dense modes it serves when q's base pointer and strides are 16-byte
+ * aligned (q is read through a TMA tensor map there), the CUDA-core kernel
+ * otherwise */
 #define FD_KERNEL_AUTO 0
 #define FD_KERNEL_SIMT 1         /* CUDA-core kernel, every mode           */
-#define FD_KERNEL_TC 2           /* tensor-core (tcgen05) kernel, dense
-                                    bf16 modes with 16-byte aligned q only
+#define FD_KERNEL_TC 2           /* tensor-core (tcgen05) kernel: dense
+                                    bf16 caches (head_dim 128/256, up to 64
+                                    rows) and dense int8 caches (head_dim
+                                    128, up to 32 rows), 16-byte aligned q
                                     (else FD_ERR_UNSUPPORTED)              */
 
 #define FD_MAX_ROWS 64           /* query rows per kv head per launch unit */
@@ -236,9 +239,9 @@ int32_t fd_tile_tokens(int32_t kernel, int32_t head_dim, int32_t kv_dtype);
 int64_t fd_plan(const int64_t *seg_len, int64_t nseg, int32_t tile_tokens,
                 int32_t num_ctas, int32_t seg_units, int32_t *first_cta,
                 int32_t *n_pieces);
-/* seg_units a launch of this kernel and head_dim uses (0 for the CUDA-core
- * kernel; AUTO is not resolved here). */
-int32_t fd_seg_units(int32_t kernel, int32_t head_dim);
+/* seg_units a launch of this kernel, head_dim and cache dtype uses (0 for
+ * the CUDA-core kernel; AUTO is not resolved here). */
+int32_t fd_seg_units(int32_t kernel, int32_t head_dim, int32_t kv_dtype);
 
 const char *fd_status_string(int status);
 int32_t fd_version(void);

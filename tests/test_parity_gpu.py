@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
 
 KERNELS = [fd.FD_KERNEL_SIMT]
 DENSE_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]
+INT8_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]   # tensor cores: head_dim 128, <= 32 rows
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -41,8 +42,8 @@ def check(inp_cpu, out_dtype=torch.bfloat16, num_ctas=0, kernel=fd.FD_KERNEL_AUT
 @pytest.mark.parametrize("kernel", DENSE_KERNELS)
 def test_golden_fixture_on_gpu(name, d, kernel):
     fx = load_fixture(name, pad_d=d)
-    if kernel == fd.FD_KERNEL_TC and (fx["mode"] == "gather" or fx.get("int8")):
-        pytest.skip("the tensor-core kernel serves the dense bf16 modes")
+    if kernel == fd.FD_KERNEL_TC and (fx["mode"] == "gather" or (fx.get("int8") and d != 128)):
+        pytest.skip("the tensor-core kernel serves dense bf16 and head_dim-128 int8 caches")
     dev = lambda t: None if t is None else t.cuda()
     for out_dtype in (torch.float32, torch.bfloat16):
         if fx["mode"] == "gather":
@@ -226,7 +227,7 @@ def test_gather_empty_list(kernel):
 
 
 # -------------------------------------------------------------------- int8
-@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kernel", INT8_KERNELS)
 @pytest.mark.parametrize("causal,n_q", [(False, 1), (True, 4)])
 def test_int8_small(kernel, causal, n_q):
     inp = W.dense_inputs(3, n_q, 32, 8, 128, 640, [640, 200, 1], 24, causal, int8=True)
@@ -234,10 +235,30 @@ def test_int8_small(kernel, causal, n_q):
     check(inp, torch.float32, kernel=kernel)
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
-def test_int8_poisoned_tail_scales(kernel):
-    inp = W.dense_inputs(2, 1, 16, 4, 256, 300, [150, 299], 25, False, int8=True, tail="nan")
+@pytest.mark.parametrize("kernel", INT8_KERNELS)
+@pytest.mark.parametrize("d", [128, 256])
+def test_int8_poisoned_tail_scales(kernel, d):
+    if kernel == fd.FD_KERNEL_TC and d != 128:
+        pytest.skip("tensor-core int8 path: head_dim 128")
+    inp = W.dense_inputs(2, 1, 16, 4, d, 300, [150, 299], 25, False, int8=True, tail="nan")
     check(inp, torch.float32, kernel=kernel)
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 19, 300])
+def test_int8_tensor_core_splits_and_32_rows(ctas):
+    # 32 packed rows (8 heads per group x 4 causal rows), ragged lengths, the
+    # segments cut into many split pieces
+    inp = W.dense_inputs(3, 4, 32, 4, 128, 1500, [1500, 611, 129], 26, True, int8=True)
+    check(inp, torch.float32, kernel=fd.FD_KERNEL_TC, num_ctas=ctas)
+    check(inp, torch.bfloat16, kernel=fd.FD_KERNEL_TC, num_ctas=ctas)
+
+
+def test_int8_tensor_core_rejects_unserved_shapes():
+    # more than 32 rows: the tensor-core kernel declines, AUTO takes the CUDA-core one
+    inp = to_dev(W.dense_inputs(1, 2, 32, 1, 128, 200, [150], 27, True, int8=True))
+    with pytest.raises(fd.FdError):
+        run_gpu(inp, torch.float32, kernel=fd.FD_KERNEL_TC)
+    compare(run_gpu(inp, torch.float32), run_oracle(inp), torch.float32, "int8 rows 64 auto")
 
 
 # ------------------------------------------------------------- CUDA graphs
@@ -297,7 +318,7 @@ def test_mtp_verify_capacity_independent_output(kernel):
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kernel", INT8_KERNELS)
 def test_int8_workload_full_size_sampled(kernel):
     # full int8 workload (4 x 131072 tokens, 32/8 heads): generated on the GPU,
     # every output row checked against the oracle on the same bits
