@@ -1,9 +1,11 @@
-// fd_tc.cu -- tensor-core (tcgen05) decode kernel for the dense bf16 prefix
-// mode (optionally causal), head_dim 128 / 256, up to 64 packed query rows.
+// fd_tc.cu -- tensor-core (tcgen05) decode kernel for the dense prefix mode
+// (optionally causal): bf16 caches at head_dim 128 / 256 with up to 64 packed
+// query rows, int8 caches at head_dim 128 with up to 32.
 //
-// Work split: the same balanced tile partition as the CUDA-core kernel
-// (fd_internal.h), with 128-position tiles and one block per SM.  Roles
-// inside a block (320 threads):
+// Work split: balanced consecutive ranges of work units over one block per
+// SM, where a segment is its tiles (128 positions) plus a few units for the
+// fixed cost of a piece boundary (see Walk).  Roles inside a block
+// (320 threads):
 //   warp 8      TMA producer: loads each segment's packed Q rows (one box
 //               per 64 columns) as soon as the previous piece's last QK has
 //               read the buffer, and streams K and V tiles of the block's
@@ -15,16 +17,20 @@
 //               K = 128 positions) into TMEM; completion via tcgen05.commit.
 //               QK of tile t+1 is issued before PV of tile t.
 //   warps 0-7   softmax and epilogue, two warpgroups that split the query
-//               rows.  Thread i of a group owns TMEM lane i = cache position
-//               i of the tile (scores) and dim i of each 128-dim chunk
-//               (output).  Per tile: mask (length, causal window), running
-//               row maxima refreshed when a score passes them by 2^8 (column
-//               max over the 128 positions by warp shuffles + shared memory),
-//               O rescaled in TMEM then, P = 2^(s - m) written to shared
-//               memory as two bf16 planes in the MMA operand layout.  At the
-//               end of a segment piece it normalises and stores, or hands a
-//               split partial to the in-launch combine (last block to arrive
-//               merges; comfy-kitchen #239, "GQA decode").
+//               rows (bf16 caches).  Thread i of a group owns TMEM lane i =
+//               cache position i of the tile (scores) and dim i of each
+//               128-dim chunk (output).  Per tile: mask (length, causal
+//               window), running row maxima refreshed when a score passes
+//               them by 2^8 (column max over the 128 positions by warp
+//               shuffles + shared memory), O rescaled in TMEM then,
+//               P = 2^(s - m) written to shared memory in the MMA operand
+//               layout (one bf16 plane, or hi + lo planes for fp32 outputs).
+//               At the end of a segment piece it normalises and stores, or
+//               hands a split partial to the in-launch combine (last block
+//               to arrive merges; comfy-kitchen #239, "GQA decode").
+//   int8 caches: warps 0-3 are the one softmax group and warps 4-7 widen the
+//               int8 tiles the producer loads into the bf16 slots the MMAs
+//               read; the per-position scales multiply scores and P.
 // The last tile of a segment is loaded right-aligned (ending at the length),
 // so no row of the unused tail is ever read; positions the previous tile
 // already covered are masked.  Every wait is bounded (2 s); a timeout sets
