@@ -176,38 +176,12 @@ int run(const Call &c) {
     fd_workspace *ws = o.ws;
     if (!ws) return FD_ERR_WORKSPACE;
     const int64_t nseg = c.mode == fd::kGather ? B * n_q * Hkv : B * Hkv;
-    // Kernel choice: the tensor-core kernel serves the dense bf16 modes; the
-    // CUDA-core kernel serves every mode.
-    // (Q is loaded through a tensor map there: 16-byte aligned base and strides.)
-    bool q_tma = aligned16(c.q->data);
-    for (int i = 0; i < 3; ++i) q_tma = q_tma && (c.q->stride[i] * 2) % 16 == 0;
-    // (int8 caches: head_dim 128 and up to 32 rows there.)
-    const bool tc_ok = c.mode == fd::kDense && cap < ((int64_t)1 << 31) && q_tma &&
-                       (!c.kv_int8 || (d == 128 && rows <= 32));
-    int32_t kernel = o.kernel == FD_KERNEL_AUTO ? (tc_ok ? FD_KERNEL_TC : FD_KERNEL_SIMT) : o.kernel;
-    if (kernel == FD_KERNEL_TC && !tc_ok) return FD_ERR_UNSUPPORTED;
-    const int tile = kernel_tile(kernel);
-    const int32_t seg_units =
-        kernel == FD_KERNEL_TC ? fd_seg_units(FD_KERNEL_TC, (int32_t)d, kvdt) : 0;
-    const int64_t max_units =
-        c.mode == fd::kGather ? nseg * fd::ceil_div(c.idx_len, tile)
-                              : nseg * (fd::ceil_div(cap, tile) + seg_units);
-    int32_t G = o.num_ctas;
-    if (G == 0) {
-        G = auto_ctas(kernel, max_units);
-        if (G <= 0) return FD_ERR_CUDA;
-    }
-    if (nseg > ws->max_segments || rows > ws->max_rows || d > ws->head_dim || G > ws->max_ctas)
-        return FD_ERR_WORKSPACE;
-    if ((size_t)(nseg + G) * (size_t)fd::slot_floats(rows, d) > ws->partial_floats)
-        return FD_ERR_WORKSPACE;
-
     fd::Params p;
     memset(&p, 0, sizeof p);
     p.B = (int32_t)B; p.n_q = (int32_t)n_q; p.Hq = (int32_t)Hq; p.Hkv = (int32_t)Hkv;
     p.g = (int32_t)g; p.d = (int32_t)d; p.cap = cap; p.rows = (int32_t)rows;
     p.mode = c.mode; p.causal = c.mode == fd::kDense ? c.causal : 0;
-    p.kv_int8 = c.kv_int8; p.out_f32 = c.out->dtype == FD_F32; p.tile = tile;
+    p.kv_int8 = c.kv_int8; p.out_f32 = c.out->dtype == FD_F32;
     p.scale_log2 = c.scale * 1.4426950408889634f;
     p.idx_len = c.idx_len; p.nseg = nseg;
     p.q = static_cast<const uint16_t *>(c.q->data);
@@ -228,6 +202,29 @@ int run(const Call &c) {
     p.status = ws->status;
     p.partials = ws->partials;
 
+    // Kernel choice: the tensor-core kernel serves what fd::tc_supports
+    // accepts (dense bf16 and head_dim-128 int8 caches, bf16 gather over a
+    // strided cache; q read through a TMA map); the CUDA-core kernel serves
+    // every mode.
+    const bool tc_ok = fd::tc_supports(p);
+    int32_t kernel = o.kernel == FD_KERNEL_AUTO ? (tc_ok ? FD_KERNEL_TC : FD_KERNEL_SIMT) : o.kernel;
+    if (kernel == FD_KERNEL_TC && !tc_ok) return FD_ERR_UNSUPPORTED;
+    const int tile = kernel_tile(kernel);
+    const int32_t seg_units =
+        kernel == FD_KERNEL_TC ? fd_seg_units(FD_KERNEL_TC, (int32_t)d, kvdt) : 0;
+    const int64_t max_units =
+        c.mode == fd::kGather ? nseg * (fd::ceil_div(c.idx_len, tile) + seg_units)
+                              : nseg * (fd::ceil_div(cap, tile) + seg_units);
+    int32_t G = o.num_ctas;
+    if (G == 0) {
+        G = auto_ctas(kernel, max_units);
+        if (G <= 0) return FD_ERR_CUDA;
+    }
+    if (nseg > ws->max_segments || rows > ws->max_rows || d > ws->head_dim || G > ws->max_ctas)
+        return FD_ERR_WORKSPACE;
+    if ((size_t)(nseg + G) * (size_t)fd::slot_floats(rows, d) > ws->partial_floats)
+        return FD_ERR_WORKSPACE;
+    p.tile = tile;
     p.seg_units = seg_units;
 
     cudaStream_t st = static_cast<cudaStream_t>(o.stream);

@@ -77,6 +77,18 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// Four rows (r0..r3, one box-wide row each) of a 2-D tensor map gathered into
+// consecutive rows of shared memory; a row outside the tensor reads as zeros.
+__device__ __forceinline__ void tma_gather4(void *dst, const void *tmap, uint64_t *bar, int c0,
+                                            int r0, int r1, int r2, int r3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }

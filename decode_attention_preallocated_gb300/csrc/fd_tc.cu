@@ -61,14 +61,16 @@ constexpr int kDevTimeout = 4;          // mirrors FD_DEV_INTERNAL
 constexpr float kRescaleSlack = 8.f;
 
 struct TcArgs {   // CUtensorMap members carry their own alignment
-    // (int8 caches: tk / tv map the int8 codes)
+    // (int8 caches: tk / tv map the int8 codes; gather: 2-D maps of cache rows)
     CUtensorMap tk;
     CUtensorMap tv;
     CUtensorMap tq;
     Params p;
+    // gather: cache row (b, hk, pos) is row b*gs0 + hk*gs1 + pos*gs2 of tk / tv
+    int64_t gs0, gs1, gs2;
 };
 
-template <int D, int N, bool I8, int NV>
+template <int D, int N, bool I8, int NV, bool GA = false>
 struct Cfg {
     // bf16 caches: two softmax warpgroups split the rows (warps 0-7).  int8
     // caches: one softmax warpgroup (warps 0-3); warps 4-7 widen the int8
@@ -134,12 +136,15 @@ struct Cfg {
 // A block's work is a run of consecutive non-empty segments.  The first one
 // is found once per block by a warp scan over the sequence lengths; every
 // later one is the next non-empty segment, so walking needs no division.
+// Gather launches: segment s = (b*n_q + i)*Hkv + hk is one index list (all of
+// length idx_len) seen by the g query heads of kv head hk.
 struct Walk {
     int64_t s;        // segment
     int64_t first;    // unit index of the segment's first tile
-    int64_t L;        // its sequence length
+    int64_t L;        // its sequence length (gather: the list length)
     int32_t ntiles;   // its tile count
     int32_t b, hk;
+    int32_t i;        // gather: query row of the list (dense: 0)
 };
 
 __device__ __forceinline__ int32_t tiles_of(int64_t L) { return (int32_t)((L + TT - 1) / TT); }
@@ -151,6 +156,7 @@ __device__ __forceinline__ int64_t units_of(const Params &p, int64_t n) {
 
 // Total work units of the launch (one warp; every lane gets the value).
 __device__ __forceinline__ int64_t total_units_tc(const Params &p) {
+    if (p.mode == kGather) return p.nseg * units_of(p, tiles_of(p.idx_len));
     const int lane = threadIdx.x & 31;
     int64_t acc = 0;
     for (int b = lane; b < p.B; b += 32) acc += units_of(p, tiles_of(seq_len(p, b)));
@@ -161,6 +167,19 @@ __device__ __forceinline__ int64_t total_units_tc(const Params &p) {
 
 // The segment holding work unit t (one warp; false if t is past the end).
 __device__ __noinline__ bool first_piece_warp(const Params &p, int64_t t, Walk *w) {
+    if (p.mode == kGather) {   // equal segments: closed form
+        const int64_t n = tiles_of(p.idx_len), u = units_of(p, n);
+        if (u == 0 || t >= p.nseg * u) return false;
+        const int64_t s = t / u, bi = s / p.Hkv;
+        w->s = s;
+        w->hk = (int)(s % p.Hkv);
+        w->b = (int)(bi / p.n_q);
+        w->i = (int)(bi % p.n_q);
+        w->first = s * u + p.seg_units;
+        w->ntiles = (int32_t)n;
+        w->L = p.idx_len;
+        return true;
+    }
     const int lane = threadIdx.x & 31;
     int64_t base = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
@@ -185,6 +204,7 @@ __device__ __noinline__ bool first_piece_warp(const Params &p, int64_t t, Walk *
             const int hk = (int)((t - base - e) / ub);
             w->b = b0 + src;
             w->hk = hk;
+            w->i = 0;
             w->s = (int64_t)w->b * p.Hkv + hk;
             w->first = base + e + (int64_t)hk * ub + p.seg_units;
             w->ntiles = (int32_t)nb;
@@ -199,6 +219,19 @@ __device__ __noinline__ bool first_piece_warp(const Params &p, int64_t t, Walk *
 // Advance to the next segment with at least one tile (false past the end).
 __device__ __forceinline__ bool next_piece(const Params &p, Walk &w) {
     w.first += w.ntiles;
+    if (p.mode == kGather) {
+        if (w.s + 1 >= p.nseg) return false;
+        ++w.s;
+        if (++w.hk == p.Hkv) {
+            w.hk = 0;
+            if (++w.i == p.n_q) {
+                w.i = 0;
+                ++w.b;
+            }
+        }
+        w.first += p.seg_units;
+        return true;
+    }
     do {
         if (w.s + 1 >= p.nseg) return false;
         ++w.s;
@@ -304,9 +337,9 @@ __device__ __forceinline__ void note_timeout(Bars *bs, const Params &p, int site
     set_abort(bs, p);
 }
 
-template <int D, int N, bool I8, int NV>
+template <int D, int N, bool I8, int NV, bool GA>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant__ TcArgs a) {
-    using C = Cfg<D, N, I8, NV>;
+    using C = Cfg<D, N, I8, NV, GA>;
     constexpr int kSoftmaxThreads = C::SMT;
     const Params &p = a.p;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -331,7 +364,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 
     // Segments with nothing to attend still need their output rows zeroed.
     for (int64_t s = c; s < p.nseg; s += G)
-        if (tiles_of(seq_len(p, (int)(s / p.Hkv))) == 0) zero_segment(p, s);
+        if ((GA ? tiles_of(p.idx_len) : tiles_of(seq_len(p, (int)(s / p.Hkv)))) == 0)
+            zero_segment(p, s);
     // The producer warp finds the block's tile range and first piece while
     // the others set up barriers and TMEM.
     if (warp == kProducerWarp) {
@@ -443,11 +477,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     if (!ok) note_timeout(bs, p, 8, issued, piece);
                 }
                 if (ok) {
+                    // (gather: the list's one query row, box (64, 1, g, 1))
                     ptx::mbar_arrive_expect_tx(&bs->q_full, (uint32_t)(C::KB * p.rows * 128));
 #pragma unroll
                     for (int cb = 0; cb < C::KB; ++cb)
                         ptx::tma_load_4d(smem + C::OFF_Q + cb * C::QB, &a.tq, &bs->q_full, cb * 64,
-                                         0, hk * p.g, b);
+                                         GA ? w.i : 0, hk * p.g, b);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -457,6 +492,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             // The ring is then a plain FIFO, and each K tile is requested one
             // tile period before its QK needs it.
             const int64_t n_in = piece_end - t, tt0 = t - w.first;
+            // gather: lane l fetches positions 4l .. 4l+3 of each tile, rows of
+            // the 2-D cache maps (-1, read as zeros, for padding, cells past the
+            // list or out of range); the next K tile's rows are read ahead.
+            const int32_t *ilist = GA ? p.idx + ((int64_t)b * p.n_q + w.i) * p.idx_len : nullptr;
+            const int64_t segrow = GA ? (int64_t)b * a.gs0 + (int64_t)hk * a.gs1 : 0;
+            int yk[4] = {-1, -1, -1, -1}, yv0[4] = {-1, -1, -1, -1}, yv1[4] = {-1, -1, -1, -1};
+            auto list_rows = [&](int64_t tile, int *y) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int64_t pos = tile * TT + 4 * lane + r;
+                    y[r] = -1;
+                    if (pos < p.idx_len) {
+                        const int x = __ldg(ilist + pos);
+                        if (x >= 0 && x < p.cap) y[r] = (int)(segrow + (int64_t)x * a.gs2);
+                    }
+                }
+            };
+            if (GA) list_rows(tt0, yk);
             for (int64_t step = 0; step < 2 * n_in && ok; ++step) {
                 int64_t j;
                 int kv;
@@ -464,7 +517,37 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 else if (step == 2 * n_in - 1) { j = n_in - 1; kv = 1; }
                 else { j = (step + 1) / 2 - (step & 1 ? 0 : 1); kv = step & 1 ? 0 : 1; }
                 const int ys = (int)tile_start(tt0 + j, L);
-                if (lane == 0 && I8) {
+                if (GA) {
+                    // rows of this fill: K(j) takes the prefetched rows (kept
+                    // for V(j)), then the next tile's are requested
+                    int y[4];
+                    if (kv == 0) {
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            y[r] = yk[r];
+                            if (j & 1) yv1[r] = yk[r]; else yv0[r] = yk[r];
+                        }
+                        if (j + 1 < n_in) list_rows(tt0 + j + 1, yk);
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) y[r] = (j & 1) ? yv1[r] : yv0[r];
+                    }
+                    const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
+                    if (lane == 0) {
+                        ok = ptx::mbar_wait(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+                        if (!ok) note_timeout(bs, p, 1, issued, 0);
+                        else ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (ok) {
+                        unsigned char *dst = smem + C::OFF_SLOTS + slot * C::SLOT + 4 * lane * 128;
+#pragma unroll
+                        for (int cb = 0; cb < C::KB; ++cb)
+                            ptx::tma_gather4(dst + cb * C::BOX, kv ? (const void *)&a.tv
+                                                                   : (const void *)&a.tk,
+                                             &bs->slot_full[slot], cb * 64, y[0], y[1], y[2], y[3]);
+                    }
+                } else if (lane == 0 && I8) {
                     // int8 codes -> raw ring (one box of TT positions x D codes)
                     const uint32_t rs = issued % C::NRX, ph = (issued / C::NRX) & 1;
                     ok = ptx::mbar_wait(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
@@ -741,7 +824,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             // causal limit of each row.  The Q rows arrive by TMA.
             int64_t *ooff = otbl + (piece & 1) * N;
             if (wt < NH && cb0 + wt < rows) {
-                const int r = cb0 + wt, i = r % p.n_q, h = w.hk * p.g + r / p.n_q;
+                // (gather: the list's query row, head offset r)
+                const int r = cb0 + wt;
+                const int i = GA ? w.i : r % p.n_q, h = w.hk * p.g + (GA ? r : r / p.n_q);
                 ooff[r] = (int64_t)w.b * p.os[0] + (int64_t)i * p.os[1] + (int64_t)h * p.os[2];
             }
             int lim[NH];    // last visible position of each row
@@ -772,15 +857,32 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 }
             };
             if (I8) load_scales(0);
+            // gather: the list cell this lane's position holds, read one tile
+            // ahead; a cell is visible if 0 <= cell < cap (cap or more is
+            // flagged FD_DEV_BAD_INDEX, negative is padding).
+            const int32_t *ilist = GA ? p.idx + ((int64_t)w.b * p.n_q + w.i) * p.idx_len : nullptr;
+            int cell_n = -1;
+            auto load_cell = [&](int64_t jj) {
+                const int64_t pos = (tt0 + jj) * TT + wt;
+                cell_n = pos < p.idx_len ? __ldg(ilist + pos) : -1;
+            };
+            if (GA) load_cell(0);
             for (int64_t j = 0; j < n_in && ok; ++j) {
                 const int64_t y0 = (tt0 + j) * TT;
-                const int64_t token = tile_start(tt0 + j, L) + wt;
+                const int64_t token = GA ? y0 + wt : tile_start(tt0 + j, L) + wt;
                 const uint32_t sb = tile_ctr & 1, u = tile_ctr >> 1;
                 // Visibility: a position this tile owns (the right-aligned last
                 // tile also holds positions the previous tile covered), inside
                 // the filled prefix and, for causal windows, at or before
-                // L - n_q + i for the row's query index i.
-                const bool in_len = token >= y0 && token < L;
+                // L - n_q + i for the row's query index i.  Gather: a valid
+                // cell of the list.
+                bool in_len = token >= y0 && token < L;
+                if (GA) {
+                    const int cell = cell_n;
+                    if (j + 1 < n_in) load_cell(j + 1);
+                    if (cell >= p.cap) atomicOr(p.status, kDevBadIndex);
+                    in_len = in_len && cell >= 0 && cell < p.cap;
+                }
                 const float ksc = ksc_n, vsc = vsc_n;
                 if (I8 && j + 1 < n_in) load_scales(j + 1);
                 ok = ptx::mbar_wait(&bs->s_full[sb], u & 1, abort_flag, kWaitNs);
@@ -1094,27 +1196,59 @@ bool make_map(CUtensorMap *m, const void *base, const int64_t *st, const Params 
 }
 
 // [B, n_q, Hq, d] queries -> 4-D map (d, n_q, Hq, B), box (64, n_q, g, 1):
-// one box holds a segment's packed rows for 64 columns.
+// one box holds a segment's packed rows for 64 columns (gather: box
+// (64, 1, g, 1), the g heads of one query row).
 bool make_qmap(CUtensorMap *m, const Params &p) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)p.n_q, (cuuint64_t)p.Hq, (cuuint64_t)p.B};
     cuuint64_t strides[3] = {(cuuint64_t)p.qs[1] * 2, (cuuint64_t)p.qs[2] * 2,
                              (cuuint64_t)p.qs[0] * 2};
-    cuuint32_t box[4] = {64, (cuuint32_t)p.n_q, (cuuint32_t)p.g, 1};
+    cuuint32_t box[4] = {64, p.mode == kGather ? 1u : (cuuint32_t)p.n_q, (cuuint32_t)p.g, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(p.q), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int N, bool I8, int NV = N>
+// Gather: the cache seen as 2-D rows (d, Y) of stride rs elements, with rs
+// the smallest of the three outer strides (each a multiple of it); gather4
+// loads read one 64-column, one-row box per listed cell.
+bool gather_rows(const Params &p, int64_t *rs, int64_t *Y, int64_t g[3]) {
+    const int64_t *st = p.ks;
+    if (p.vs[0] != st[0] || p.vs[1] != st[1] || p.vs[2] != st[2]) return false;
+    int64_t r = st[0];
+    for (int k = 1; k < 3; ++k) r = st[k] < r ? st[k] : r;
+    if (r < p.d) return false;
+    for (int k = 0; k < 3; ++k)
+        if (st[k] % r) return false;
+    g[0] = st[0] / r;
+    g[1] = st[1] / r;
+    g[2] = st[2] / r;
+    *rs = r;
+    *Y = (int64_t)(p.B - 1) * g[0] + (int64_t)(p.Hkv - 1) * g[1] + (p.cap - 1) * g[2] + 1;
+    return *Y < ((int64_t)1 << 31);
+}
+
+bool make_gmap(CUtensorMap *m, const void *base, const Params &p, int64_t rs, int64_t Y) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)p.d, (cuuint64_t)Y};
+    cuuint64_t strides[1] = {(cuuint64_t)rs * 2};
+    cuuint32_t box[2] = {64, 1};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int N, bool I8, int NV = N, bool GA = false>
 int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
-    using C = Cfg<D, N, I8, NV>;
-    if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::SMEM) != cudaSuccess)
+    using C = Cfg<D, N, I8, NV, GA>;
+    if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV, GA>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess)
         return -5;
-    tc_kernel<D, N, I8, NV><<<G, kThreadsTC, C::SMEM, st>>>(args);
+    tc_kernel<D, N, I8, NV, GA><<<G, kThreadsTC, C::SMEM, st>>>(args);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 
@@ -1145,8 +1279,12 @@ bool tc_supports(const Params &p) {
     // int8 caches: head_dim 128 and up to 32 rows (one softmax warpgroup).
     const bool shape = p.kv_int8 ? (p.d == 128 && p.rows <= 32)
                                  : ((p.d == 128 || p.d == 256) && p.rows <= 64);
-    return p.mode == kDense && shape && p.rows >= 1 && p.cap < (int64_t)1 << 31 &&
-           p.B < (1 << 30) && p.Hkv < (1 << 30) && q_aligned;
+    // gather: bf16 caches whose rows form one strided 2-D array
+    int64_t rs, Y, g[3];
+    const bool mode = p.mode == kDense || (p.mode == kGather && !p.kv_int8 &&
+                                           gather_rows(p, &rs, &Y, g));
+    return mode && shape && p.rows >= 1 && p.cap < (int64_t)1 << 31 && p.B < (1 << 30) &&
+           p.Hkv < (1 << 30) && q_aligned;
 }
 
 int launch_tc(const Params &p, int G, cudaStream_t st) {
@@ -1154,6 +1292,24 @@ int launch_tc(const Params &p, int G, cudaStream_t st) {
     TcArgs args;
     memset(&args, 0, sizeof args);
     args.p = p;
+    if (p.mode == kGather) {
+        int64_t rs, Y, g[3];
+        gather_rows(p, &rs, &Y, g);
+        args.gs0 = g[0];
+        args.gs1 = g[1];
+        args.gs2 = g[2];
+        if (!make_gmap(&args.tk, p.k, p, rs, Y) || !make_gmap(&args.tv, p.v, p, rs, Y) ||
+            !make_qmap(&args.tq, p))
+            return -5;
+        const int rows = p.rows;
+        if (p.d == 128)
+            return rows <= 16   ? launch_dn<128, 16, false, 16, true>(args, G, st)
+                   : rows <= 32 ? launch_dn<128, 32, false, 32, true>(args, G, st)
+                                : launch_dn<128, 64, false, 64, true>(args, G, st);
+        return rows <= 16   ? launch_dn<256, 16, false, 16, true>(args, G, st)
+               : rows <= 32 ? launch_dn<256, 32, false, 32, true>(args, G, st)
+                            : launch_dn<256, 64, false, 64, true>(args, G, st);
+    }
     if (!make_map(&args.tk, p.k, p.ks, p) || !make_map(&args.tv, p.v, p.vs, p) ||
         !make_qmap(&args.tq, p))
         return -5;

@@ -18,6 +18,7 @@ pytestmark = pytest.mark.gpu
 KERNELS = [fd.FD_KERNEL_SIMT]
 DENSE_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]
 INT8_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]   # tensor cores: head_dim 128, <= 32 rows
+GATHER_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -42,8 +43,8 @@ def check(inp_cpu, out_dtype=torch.bfloat16, num_ctas=0, kernel=fd.FD_KERNEL_AUT
 @pytest.mark.parametrize("kernel", DENSE_KERNELS)
 def test_golden_fixture_on_gpu(name, d, kernel):
     fx = load_fixture(name, pad_d=d)
-    if kernel == fd.FD_KERNEL_TC and (fx["mode"] == "gather" or (fx.get("int8") and d != 128)):
-        pytest.skip("the tensor-core kernel serves dense bf16 and head_dim-128 int8 caches")
+    if kernel == fd.FD_KERNEL_TC and fx.get("int8") and d != 128:
+        pytest.skip("the tensor-core kernel serves head_dim-128 int8 caches")
     dev = lambda t: None if t is None else t.cuda()
     for out_dtype in (torch.float32, torch.bfloat16):
         if fx["mode"] == "gather":
@@ -173,7 +174,7 @@ def test_causal_row_ignores_later_drafts(kernel):
 
 
 # ------------------------------------------------------------------ gather
-@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kernel", GATHER_KERNELS)
 @pytest.mark.parametrize("n_q", [1, 3])
 def test_gather_small(kernel, n_q):
     inp = W.gather_inputs(2, n_q, 32, 4, 128, 3000, 200, 16, 20)
@@ -183,7 +184,7 @@ def test_gather_small(kernel, n_q):
     check(inp, torch.bfloat16, kernel=kernel)
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kernel", GATHER_KERNELS)
 def test_gather_prefix_equals_dense(kernel):
     L = 333
     inp = W.dense_inputs(1, 1, 8, 2, 128, 400, [L], 21, False)
@@ -192,14 +193,17 @@ def test_gather_prefix_equals_dense(kernel):
     idx = torch.arange(L, dtype=torch.int32, device="cuda").view(1, 1, L)
     g = fd.decode_gather(dev.q, dev.k, dev.v, idx, scale=inp.scale,
                          out_dtype=torch.float32, kernel=kernel)
-    torch.testing.assert_close(g, dense, rtol=0, atol=2e-6)
+    # the same cells in other tiles: rounding-level differences only (P is
+    # carried to ~2^-17 on the tensor cores, fp32 on the CUDA cores)
+    tol = 2e-6 if kernel == fd.FD_KERNEL_SIMT else 1e-4
+    torch.testing.assert_close(g, dense, rtol=0, atol=tol)
     perm = idx[:, :, torch.randperm(L, device="cuda")].contiguous()
     g2 = fd.decode_gather(dev.q, dev.k, dev.v, perm, scale=inp.scale,
                           out_dtype=torch.float32, kernel=kernel)
-    torch.testing.assert_close(g2, dense, rtol=0, atol=2e-6)
+    torch.testing.assert_close(g2, dense, rtol=0, atol=tol)
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kernel", GATHER_KERNELS)
 def test_gather_out_of_range_index_is_skipped_and_flagged(kernel):
     inp = W.gather_inputs(1, 1, 8, 2, 128, 500, 64, 4, 22)
     dev = to_dev(inp)
@@ -214,7 +218,7 @@ def test_gather_out_of_range_index_is_skipped_and_flagged(kernel):
     compare(got, run_oracle(inp), torch.float32, "gather skip")
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("kernel", GATHER_KERNELS)
 def test_gather_empty_list(kernel):
     inp = W.gather_inputs(1, 2, 8, 2, 128, 100, 8, 2, 23)
     dev = to_dev(inp)
@@ -224,6 +228,21 @@ def test_gather_empty_list(kernel):
     idx0 = torch.empty((1, 2, 0), dtype=torch.int32, device="cuda")
     got = fd.decode_gather(dev.q, dev.k, dev.v, idx0, out_dtype=torch.float32, kernel=kernel)
     assert torch.count_nonzero(got) == 0
+
+
+@pytest.mark.parametrize("ctas", [1, 5, 64, 300])
+@pytest.mark.parametrize("d", [128, 256])
+def test_gather_tensor_core_splits_token_major(ctas, d):
+    # lists of 700 cells over a token-major cache, many split pieces
+    inp = W.gather_inputs(2, 2, 16, 4, d, 4000, 700, 64, 28)
+    inp.idx[1, 1, 33] = -1
+    tm = to_dev(inp)
+    k = tm.k.transpose(1, 2).contiguous().transpose(1, 2)   # [B, cap, Hkv, d] storage
+    v = tm.v.transpose(1, 2).contiguous().transpose(1, 2)
+    for od in (torch.float32, torch.bfloat16):
+        got = fd.decode_gather(tm.q, k, v, tm.idx, scale=inp.scale, out_dtype=od,
+                               kernel=fd.FD_KERNEL_TC, num_ctas=ctas)
+        compare(got, run_oracle(inp), od, "gather tc token-major")
 
 
 # -------------------------------------------------------------------- int8
@@ -291,8 +310,6 @@ def test_graph_capture_and_replay_with_new_lengths(kernel):
 @pytest.mark.parametrize("kernel", DENSE_KERNELS)
 @pytest.mark.parametrize("name", ["dense_1k", "mtp_verify", "gather", "ragged"])
 def test_named_workload_full_size(kernel, name):
-    if kernel == fd.FD_KERNEL_TC and name == "gather":
-        pytest.skip("the tensor-core kernel serves the dense bf16 modes")
     inp = W.workload(name, seed=1)
     check(inp, torch.bfloat16, kernel=kernel)
     if name == "dense_1k":
