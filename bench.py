@@ -215,6 +215,39 @@ def time_calls(fn, n, stream):
     return a.elapsed_time(b) / n
 
 
+GRAPH_CALLS = 50   # decode calls captured per CUDA graph
+
+
+def capture(fn, calls, stream):
+    """A CUDA graph of `calls` back-to-back calls of fn on `stream` (the
+    library allocates nothing and reads no device data on the host, so a
+    call captures as-is; a decode loop replays its step graph the same way)."""
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, calls, replays, stream):
+    """Average ms per call over `replays` replays of a `calls`-call graph."""
+    g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(replays):
+            g.replay()
+        b.record(stream)
+    b.synchronize()
+    return a.elapsed_time(b) / (calls * replays)
+
+
 def workspace_for(inp, device):
     from decode_attention_preallocated_gb300 import fd
     B, n_q, Hq, d = inp.q.shape
@@ -324,7 +357,9 @@ def run_reference(args):
 
 def extras(args, device, stream, peak, kernel):
     """Per-mode timings beside the headline: the other workloads, the
-    capacity-independence check and the depth sweep (µs/call and GB/s)."""
+    capacity-independence check and the depth sweep (µs/call and GB/s from
+    CUDA graph replay; us_python_loop: the same calls launched one by one
+    from Python, which host overhead bounds for the small workloads)."""
     from decode_attention_preallocated_gb300 import workloads as W
     res = {}
 
@@ -334,10 +369,15 @@ def extras(args, device, stream, peak, kernel):
         fn = call_fn(inp, out, ws, kernel)
         for _ in range(5):
             fn()
-        ms = time_calls(fn, n, stream)
+        ms_host = time_calls(fn, n, stream)         # each call launched from Python
+        calls = min(n, GRAPH_CALLS)
+        g = capture(fn, calls, stream)
+        ms = time_graph(g, calls, max(1, n // calls), stream)   # graph replay: GPU time
+        del g
         nbytes = algorithmic_bytes(inp)
         res[tag] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
-                    "frac": round(nbytes / ms / 1e6 / peak, 4), "bytes": nbytes}
+                    "frac": round(nbytes / ms / 1e6 / peak, 4), "bytes": nbytes,
+                    "us_python_loop": round(ms_host * 1e3, 2)}
         ws.close()
 
     for name in ("dense_1k", "mtp_verify", "gather", "int8"):
@@ -396,6 +436,11 @@ def run_fd(args):
     if steps <= 0:   # auto: about 3 s of timed work so the clock samples mean something
         ms = time_calls(fn, 5, stream)
         steps = int(max(20, min(20000, 3000.0 / max(ms, 1e-3))))
+    # the timed steps run as replays of a captured graph of calls
+    gcalls = max(1, min(GRAPH_CALLS, steps))
+    replays = -(-steps // gcalls)
+    steps = replays * gcalls
+    graph = capture(fn, gcalls, stream)
 
     def barrier():
         if world > 1:
@@ -412,8 +457,8 @@ def run_fd(args):
     ev1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for _ in range(steps):
-            fn()
+        for _ in range(replays):
+            graph.replay()
         ev1.record(stream)
     ev1.synchronize()
     barrier()
@@ -475,6 +520,7 @@ def run_fd(args):
                        "kv_lengths": inp.lengths_host,
                        "kv_bytes_per_step": nbytes, "us_per_call": round(ms_step * 1e3, 2),
                        "l2": "inputs larger than L2 (no flush)",
+                       "launch": "CUDA graph of %d calls, replayed %d times" % (gcalls, replays),
                        "parallelism": "replicas (one batch per GPU, no collective)",
                        "kernel": args.kernel},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,

@@ -10,6 +10,8 @@
 // #239, "GQA decode": splits combined inside the same launch).
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "fd_device.cuh"
 #include "fd_launch.h"
 
@@ -383,10 +385,19 @@ simt_kernel(const __grid_constant__ Params p) {
 template <int D>
 int launch_d(const Params &p, int G, cudaStream_t st) {
     const size_t smem = Layout<D>::smem_bytes(p.rows);
-    cudaError_t e = cudaFuncSetAttribute(simt_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return -5;
+    // the dynamic shared memory opt-in (for the largest row count), once per
+    // device
+    static std::atomic<uint64_t> opted{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -5;
+    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+    if (!bit || !(opted.load(std::memory_order_acquire) & bit)) {
+        const size_t most = Layout<D>::smem_bytes(64) > smem ? Layout<D>::smem_bytes(64) : smem;
+        if (cudaFuncSetAttribute(simt_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)most) != cudaSuccess)
+            return -5;
+        opted.fetch_or(bit, std::memory_order_release);
+    }
     simt_kernel<D><<<G, kThreads, smem, st>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }

@@ -37,6 +37,9 @@
 // FD_DEV_INTERNAL in the status word, records where it waited, and the block
 // drains its copies and MMAs and exits.
 #include <cuda.h>
+#include <atomic>
+#include <cstring>
+#include <mutex>
 #include <type_traits>
 #include <cuda_runtime.h>
 
@@ -1159,6 +1162,60 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+EncodeTiledFn encode_fn();
+
+// Tensor maps are encoded on the host for every launch; a decode loop passes
+// the same caches (and often the same q) each step, so the last encodings
+// are kept, keyed by every argument that goes into one.
+struct MapKey {
+    const void *base;
+    uint32_t dtype, rank, swizzle, pad;
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4];
+};
+
+CUresult encode_cached(CUtensorMap *m, CUtensorMapDataType dtype, cuuint32_t rank, void *base,
+                       const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
+                       const cuuint32_t *estr, CUtensorMapSwizzle swizzle) {
+    MapKey k;
+    memset(&k, 0, sizeof k);
+    k.base = base;
+    k.dtype = (uint32_t)dtype;
+    k.rank = rank;
+    k.swizzle = (uint32_t)swizzle;
+    for (cuuint32_t i = 0; i < rank; ++i) {
+        k.dims[i] = dims[i];
+        k.box[i] = box[i];
+        if (i + 1 < rank) k.strides[i] = strides[i];
+    }
+    constexpr int kEntries = 32;
+    static std::mutex mu;
+    static MapKey keys[kEntries];
+    static CUtensorMap maps[kEntries];
+    static int used = 0, next = 0;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < used; ++i)
+            if (memcmp(&keys[i], &k, sizeof k) == 0) {
+                *m = maps[i];
+                return CUDA_SUCCESS;
+            }
+    }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return CUDA_ERROR_NOT_SUPPORTED;
+    const CUresult r = fn(m, dtype, rank, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+        std::lock_guard<std::mutex> lk(mu);
+        keys[next] = k;
+        maps[next] = *m;
+        next = (next + 1) % kEntries;
+        if (used < kEntries) ++used;
+    }
+    return r;
+}
+
 EncodeTiledFn encode_fn() {
     static EncodeTiledFn fn = nullptr;
     static bool tried = false;
@@ -1179,8 +1236,6 @@ EncodeTiledFn encode_fn() {
 // swizzle the MMA descriptors expect.  int8 (d = 128): the same 128-byte rows
 // (64 pairs of codes), also 128-byte swizzled (the widening threads read it).
 bool make_map(CUtensorMap *m, const void *base, const int64_t *st, const Params &p) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
     // (int8 codes are moved as pairs: 16-bit elements, d / 2 per row)
     const int es = p.kv_int8 ? 1 : 2;
     const cuuint64_t row_elems = p.kv_int8 ? (cuuint64_t)p.d / 2 : (cuuint64_t)p.d;
@@ -1189,26 +1244,22 @@ bool make_map(CUtensorMap *m, const void *base, const int64_t *st, const Params 
                              (cuuint64_t)(st[0] * es)};
     cuuint32_t box[4] = {64u, (cuuint32_t)TT, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(m, p.kv_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_cached(m, p.kv_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         4, const_cast<void *>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
 }
 
 // [B, n_q, Hq, d] queries -> 4-D map (d, n_q, Hq, B), box (64, n_q, g, 1):
 // one box holds a segment's packed rows for 64 columns (gather: box
 // (64, 1, g, 1), the g heads of one query row).
 bool make_qmap(CUtensorMap *m, const Params &p) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
     cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)p.n_q, (cuuint64_t)p.Hq, (cuuint64_t)p.B};
     cuuint64_t strides[3] = {(cuuint64_t)p.qs[1] * 2, (cuuint64_t)p.qs[2] * 2,
                              (cuuint64_t)p.qs[0] * 2};
     cuuint32_t box[4] = {64, p.mode == kGather ? 1u : (cuuint32_t)p.n_q, (cuuint32_t)p.g, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(p.q), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(p.q), dims,
+                         strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
 }
 
 // Gather: the cache seen as 2-D rows (d, Y) of stride rs elements, with rs
@@ -1231,23 +1282,28 @@ bool gather_rows(const Params &p, int64_t *rs, int64_t *Y, int64_t g[3]) {
 }
 
 bool make_gmap(CUtensorMap *m, const void *base, const Params &p, int64_t rs, int64_t Y) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)p.d, (cuuint64_t)Y};
     cuuint64_t strides[1] = {(cuuint64_t)rs * 2};
     cuuint32_t box[2] = {64, 1};
     cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
 }
 
 template <int D, int N, bool I8, int NV = N, bool GA = false>
 int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
     using C = Cfg<D, N, I8, NV, GA>;
-    if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV, GA>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess)
-        return -5;
+    // the dynamic shared memory opt-in, once per device for this instantiation
+    static std::atomic<uint64_t> opted{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -5;
+    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+    if (!bit || !(opted.load(std::memory_order_acquire) & bit)) {
+        if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV, GA>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess)
+            return -5;
+        opted.fetch_or(bit, std::memory_order_release);
+    }
     tc_kernel<D, N, I8, NV, GA><<<G, kThreadsTC, C::SMEM, st>>>(args);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }

@@ -118,24 +118,52 @@ def status_string(code: int) -> str:
 
 # ------------------------------------------------------------- marshalling
 def as_fd_tensor(t: torch.Tensor) -> FdTensor:
-    if t.dtype not in _DTYPES:
+    dt = _DTYPES.get(t.dtype)
+    if dt is None:
         raise TypeError("unsupported dtype %s" % t.dtype)
-    if t.dim() > 4:
+    shape = t.shape
+    n = len(shape)
+    if n > 4:
         raise ValueError("at most 4 dimensions")
     ft = FdTensor()
     ft.data = t.data_ptr()
-    ft.dtype = _DTYPES[t.dtype]
-    ft.ndim = t.dim()
-    for i in range(t.dim()):
-        ft.shape[i] = t.shape[i]
-        ft.stride[i] = t.stride(i)
+    ft.dtype = dt
+    ft.ndim = n
+    ft.shape[:n] = shape
+    ft.stride[:n] = t.stride()
     return ft
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
-    if stream is None:
-        stream = torch.cuda.current_stream(device)
-    return stream.cuda_stream
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(device.index)
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+class _on_device:
+    """Makes `device` current for the C call, unless it already is."""
+
+    __slots__ = ("device", "prev")
+
+    def __init__(self, device):
+        self.device = device
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.device.index:
+            self.prev = cur
+            torch.cuda.set_device(self.device)
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+        return False
 
 
 def _check(code: int, what: str):
@@ -272,13 +300,13 @@ def _prepare(q, k, out, out_dtype, segments, rows, num_ctas, kernel, stream, ws)
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=device)
     sh = _stream_handle(stream, device)
-    ctas = num_ctas
-    if ctas == 0:
-        # an upper bound on what either kernel picks for an auto launch
-        with torch.cuda.device(device):
-            ctas = max(auto_num_ctas(FD_KERNEL_SIMT, q.shape[-1], FD_BF16, rows, 0),
-                       auto_num_ctas(FD_KERNEL_TC, q.shape[-1], FD_BF16, rows, 0))
     if ws is None:
+        ctas = num_ctas
+        if ctas == 0:
+            # an upper bound on what either kernel picks for an auto launch
+            with torch.cuda.device(device):
+                ctas = max(auto_num_ctas(FD_KERNEL_SIMT, q.shape[-1], FD_BF16, rows, 0),
+                           auto_num_ctas(FD_KERNEL_TC, q.shape[-1], FD_BF16, rows, 0))
         ws = workspace_for(device, sh, segments, rows, q.shape[-1], max(ctas, 1))
     return out, sh, ws
 
@@ -298,7 +326,7 @@ def decode(q, k_cache, v_cache, kv_lengths, n_q=None, causal=False, scale=None,
                            kernel, stream, workspace)
     tq, tk, tv, to = map(as_fd_tensor, (q, k_cache, v_cache, out))
     o = _opts(sh, ws, num_ctas, kernel)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = lib().fd_decode(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
                              kv_lengths.data_ptr(), int(n_q), int(bool(causal)),
                              float(scale), ctypes.byref(to), ctypes.byref(o))
@@ -320,7 +348,7 @@ def decode_int8(q, k_cache, v_cache, k_scale, v_scale, kv_lengths, n_q=None,
                            kernel, stream, workspace)
     tq, tk, tv, tks, tvs, to = map(as_fd_tensor, (q, k_cache, v_cache, k_scale, v_scale, out))
     o = _opts(sh, ws, num_ctas, kernel)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = lib().fd_decode_int8(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
                                   ctypes.byref(tks), ctypes.byref(tvs),
                                   kv_lengths.data_ptr(), int(n_q), int(bool(causal)),
@@ -343,7 +371,7 @@ def decode_gather(q, k_cache, v_cache, idx, scale=None, out=None,
                            kernel, stream, workspace)
     tq, tk, tv, to = map(as_fd_tensor, (q, k_cache, v_cache, out))
     o = _opts(sh, ws, num_ctas, kernel, 0.0 if scale is None else scale)
-    with torch.cuda.device(q.device):
+    with _on_device(q.device):
         rc = lib().fd_decode_gather(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
                                     idx.data_ptr(), int(idx.shape[2]), ctypes.byref(to),
                                     ctypes.byref(o))
