@@ -729,11 +729,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 const uint32_t rs = f % C::NRX, ss = f % C::NS;
                 ok = ptx::mbar_wait(&bs->raw_full[rs], (f / C::NRX) & 1, abort_flag, kWaitNs);
                 if (!ok) { note_timeout(bs, p, 17, f, piece); break; }
-                // Thread ct takes 16 codes (dims 16*q .. 16*q+15, q = ct % QPR)
-                // of positions ct / QPR + RSTEP*k: one 16-byte load and two
-                // swizzled 16-byte stores each, all loads issued first.
+                // Thread ct takes 16 codes (dims 16*q16 .. 16*q16+15) of
+                // positions r0 + RSTEP*k: one 16-byte load and two swizzled
+                // 16-byte stores each, all loads issued first.  Each group of
+                // 8 threads covers half of two rows, its low half of one and
+                // high half of the other, so its 8 loads and each of its two
+                // sets of 8 stores fall in 8 different bank groups.
                 constexpr int QPR = D / 16, RSTEP = 128 / QPR, NK = TT / RSTEP;
-                const int q16 = ct % QPR, r0 = ct / QPR;
+                static_assert(!I8 || QPR == 8, "widening layout is for 128-code rows");
+                const int quarter = ct >> 3, tq = ct & 7;
+                const int r0 = 2 * (quarter >> 1) + (tq >> 2);
+                const int q16 = (tq & 3) + 4 * ((tq >> 2) ^ (quarter & 1));
                 // (raw rows are 128 bytes with the 128-byte swizzle: chunk q16 of
                 // row r sits at q16 ^ (r & 7), and r & 7 == r0 & 7 here)
                 static_assert(!I8 || D == 128, "int8 tiles: one 128-byte row per position");
