@@ -27,6 +27,8 @@ struct Params {
     int32_t tile;          // cache positions per tile
     int32_t seg_units;     // extra work units the split charges at the start of
                            // each non-empty segment (0: plain tile split)
+    int32_t coop;          // tensor-core kernel launched cooperatively (all
+                           // blocks resident): split segments may share merges
     float scale_log2;      // scale * log2(e): scores are kept in the log2 domain
     int32_t idx_len;
     int64_t nseg;          // segments: B*Hkv (dense) or B*n_q*Hkv (gather)

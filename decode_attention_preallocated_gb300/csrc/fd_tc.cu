@@ -255,7 +255,12 @@ struct Bars {   // at the start of shared memory; the reduction scratch follows 
     uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
     uint64_t q_full, q_free, o_done, o_free, exit_mma, sm_bar;
     uint64_t wg_bar[kMaxGroups];
-    uint64_t raw_full[6], raw_empty[6];   // int8 caches: raw tile ring
+    union {
+        struct {
+            uint64_t raw_full[6], raw_empty[6];   // int8 caches: raw tile ring
+        };
+        Walk walk_last;   // shared merges (bf16 caches): the last piece worked on
+    };
     uint32_t tmem_base;
     int abort_flag;
     int last_flag;
@@ -312,6 +317,12 @@ __device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int k) {
     return pack_bf16x2(f0, f1);
 }
 
+__device__ __forceinline__ int ld_acquire(const int32_t *ptr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint16_t bf16_bits(float x) {
     __nv_bfloat16 h = __float2bfloat16_rn(x);
     return *reinterpret_cast<uint16_t *>(&h);
@@ -341,7 +352,84 @@ __device__ __forceinline__ void note_timeout(Bars *bs, const Params &p, int site
     set_abort(bs, p);
 }
 
-template <int D, int N, bool I8, int NV, bool GA>
+// One block's share of the merge of split segment sw.s (blocks c0 .. c1 hold
+// its pieces) in a cooperative launch: wait until every piece has arrived,
+// merge units [share*U/P, (share+1)*U/P) of the rows x (D/4) float4 units from
+// the pieces' workspace slots (running maximum per row, pieces in order),
+// store them, and count the share done (the last one resets the counter).
+// Kept out of line so that its registers do not weigh on the tile loop.
+template <int D, bool GA, int SMT>
+__device__ __noinline__ bool share_merge_segment(const Params &p, Bars *bs, Walk sw, int c0, int c1,
+                                                 int c, int tid, uint32_t &sm_ctr, int k, int piece) {
+    volatile int *abort_flag = &bs->abort_flag;
+    auto sm_sync = [&]() -> bool {
+        ptx::mbar_arrive(&bs->sm_bar);
+        if (ptx::mbar_wait(&bs->sm_bar, (sm_ctr++) & 1, abort_flag, kWaitNs)) return true;
+        note_timeout(bs, p, 14, 0, piece);
+        return false;
+    };
+    const int64_t sg = sw.s;
+    const int P = c1 - c0 + 1, share = c - c0;
+    const int kSoftmaxThreads = SMT;
+    bool ok;
+    if (tid == 0) {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        for (uint32_t n = 0; ld_acquire(p.counters + sg) < P; ++n) {
+            __nanosleep(64);
+            if ((n & 63) == 63 &&
+                (*abort_flag || ptx::globaltimer_ns() - t0 > kWaitNs)) {
+                note_timeout(bs, p, 15, (uint32_t)k, piece);
+                break;
+            }
+        }
+    }
+    ok = sm_sync() && !*abort_flag;
+    if (!ok) return false;
+    __threadfence();
+    const int rows = p.rows;
+    constexpr int UPR = D / 4;                    // float4 units per row
+    const int64_t U = (int64_t)rows * UPR;
+    const int64_t u0 = U * share / P, u1 = U * (share + 1) / P;
+    for (int64_t u = u0 + tid; u < u1; u += kSoftmaxThreads) {
+        const int r = (int)(u / UPR), dq = (int)(u % UPR) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float M = neg_inf(), Ls = 0.f;
+#pragma unroll 4
+        for (int c2 = c0; c2 <= c1; ++c2) {
+            const float *sl = slot_ptr(p, sg, c2);
+            const float mv = __ldcg(sl + rows * D + r), lv = __ldcg(sl + rows * D + rows + r);
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(sl + r * D + dq));
+            const float mn = fmaxf(M, mv);
+            const float mu = mn == neg_inf() ? 0.f : mn;
+            const float a = fast_exp2(M - mu), wv = fast_exp2(mv - mu);
+            // (the same roundings as the last arriver's merge, bit for bit)
+            M = mn;
+            Ls = __fmaf_rn(wv, lv, Ls * a);
+            acc.x = __fmaf_rn(wv, v.x, acc.x * a);
+            acc.y = __fmaf_rn(wv, v.y, acc.y * a);
+            acc.z = __fmaf_rn(wv, v.z, acc.z * a);
+            acc.w = __fmaf_rn(wv, v.w, acc.w * a);
+        }
+        const int qi = GA ? sw.i : r % p.n_q, h = sw.hk * p.g + (GA ? r : r / p.n_q);
+        const int64_t off = (int64_t)sw.b * p.os[0] + (int64_t)qi * p.os[1] +
+                            (int64_t)h * p.os[2] + dq;
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        const float o4[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (p.out_f32)
+                reinterpret_cast<float *>(p.out)[off + e] = o4[e];
+            else
+                reinterpret_cast<uint16_t *>(p.out)[off + e] = bf16_bits(o4[e]);
+        }
+    }
+    ok = sm_sync();
+    if (!ok) return false;
+    if (tid == 0 && atomicAdd(p.counters + sg, 1) == 2 * P - 1) p.counters[sg] = 0;
+    return true;
+}
+
+template <int D, int N, bool I8, int NV, bool GA, bool SH>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant__ TcArgs a) {
     using C = Cfg<D, N, I8, NV, GA>;
     constexpr int kSoftmaxThreads = C::SMT;
@@ -454,6 +542,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
     const bool has_work = bs->has_work != 0;
     const int64_t t_begin = bs->t_begin, t_end = bs->t_end;
     const Split sp{bs->total, has_work ? working_blocks(bs->total, G) : 1};
+    // Shared merges (SH instantiations, cooperative launch): every block of a
+    // split segment merges a share of it, which pays off when blocks stream
+    // few tiles each (the last arriver's merge of many small pieces would be
+    // the launch's tail); with longer ranges the last arriver merges.
+    const bool share_merge = SH && p.coop && sp.total <= 4 * (int64_t)sp.G;
     const uint32_t q_addr = smem_base + C::OFF_Q;
     const uint32_t p_addr = smem_base + C::OFF_P;
 
@@ -833,6 +926,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             // row, so the unrolled per-row code below needs none) and the
             // causal limit of each row.  The Q rows arrive by TMA.
             int64_t *ooff = otbl + (piece & 1) * N;
+            if (share_merge && tid == 0) bs->walk_last = w;
             if (wt < NH && cb0 + wt < rows) {
                 // (gather: the list's query row, head offset r)
                 const int r = cb0 + wt;
@@ -1086,7 +1180,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 ok = ok && sm_sync();
                 if (!ok) { set_abort(bs, p); break; }
                 const int r1w = min(cb0 + NH, rows);       // this group merges rows cb0 .. r1w-1
-                if (bs->last_flag && r1w > cb0) {
+                if (!share_merge && bs->last_flag && r1w > cb0) {
                     __threadfence();
                     // Merge the pieces' partials in one pass per row: running
                     // maximum M, merged sum Ls and accumulator rescaled as each
@@ -1125,12 +1219,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                                 const float mn = fmaxf(M[k], mv);
                                 const float mu = mn == neg_inf() ? 0.f : mn;
                                 const float a = fast_exp2(M[k] - mu), w = fast_exp2(mv - mu);
+                                // (explicit roundings: the shared merge computes
+                                // the same values bit for bit)
                                 M[k] = mn;
-                                Ls[k] = Ls[k] * a + w * lv;
-                                acc[k].x = acc[k].x * a + w * v.x;
-                                acc[k].y = acc[k].y * a + w * v.y;
-                                acc[k].z = acc[k].z * a + w * v.z;
-                                acc[k].w = acc[k].w * a + w * v.w;
+                                Ls[k] = __fmaf_rn(w, lv, Ls[k] * a);
+                                acc[k].x = __fmaf_rn(w, v.x, acc[k].x * a);
+                                acc[k].y = __fmaf_rn(w, v.y, acc[k].y * a);
+                                acc[k].z = __fmaf_rn(w, v.z, acc[k].z * a);
+                                acc[k].w = __fmaf_rn(w, v.w, acc[k].w * a);
                             }
                         }
 #pragma unroll
@@ -1152,11 +1248,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         }
                     }
                 }
-                if (bs->last_flag && tid == 0) p.counters[s] = 0;
+                if (!share_merge && bs->last_flag && tid == 0) p.counters[s] = 0;
             }
             ++piece;
             if (piece_end >= t_end || !next_piece(p, w) || w.first >= t_end) break;
             t = w.first;
+        }
+        // Cooperative launch: merge this block's share of each split segment
+        // it worked on (only a range's first and last pieces can be split),
+        // once every piece of it has arrived.  Arrivals never wait and all
+        // blocks are resident, so every wait ends.  The segment counter then
+        // counts the finished shares; the last one resets it.
+        if (ok && share_merge) ok = sm_sync();   // both groups see walk_last
+#pragma unroll 1
+        for (int k = 0; k < 2 && ok && share_merge; ++k) {
+            if (k == 1 && piece < 2) break;
+            const Walk sw = k == 0 ? bs->walk : bs->walk_last;
+            if (sw.first >= t_begin && sw.first + sw.ntiles <= t_end) continue;   // whole
+            const int c0 = sw.first >= t_begin ? c : sp.owner(sw.first);
+            const int c1 = sw.first + sw.ntiles <= t_end ? c : sp.owner(sw.first + sw.ntiles - 1);
+            ok = share_merge_segment<D, GA, kSoftmaxThreads>(p, bs, sw, c0, c1, c, tid, sm_ctr, k, piece);
+            if (!ok) { set_abort(bs, p); break; }
         }
     }
 
@@ -1300,27 +1412,67 @@ bool make_gmap(CUtensorMap *m, const void *base, const Params &p, int64_t rs, in
                          strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
 }
 
-template <int D, int N, bool I8, int NV = N, bool GA = false>
+// Blocks of this instantiation that can be resident at once on the current
+// device (0 on error); sets the dynamic shared memory opt-in the first time.
+template <int D, int N, bool I8, int NV, bool GA, bool SH>
+int resident_blocks() {
+    using C = Cfg<D, N, I8, NV, GA>;
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int n = cached[dev].load(std::memory_order_acquire);
+    if (n > 0) return n;
+    int per_sm = 0, sms = 0;
+    if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV, GA, SH>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_kernel<D, N, I8, NV, GA, SH>,
+                                                      kThreadsTC, C::SMEM) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    n = per_sm * sms;
+    cached[dev].store(n, std::memory_order_release);
+    return n;
+}
+
+template <int D, int N, bool I8, int NV = N, bool GA = false, bool SH = false>
 int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
     using C = Cfg<D, N, I8, NV, GA>;
-    // the dynamic shared memory opt-in, once per device for this instantiation
-    static std::atomic<uint64_t> opted{0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return -5;
-    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
-    if (!bit || !(opted.load(std::memory_order_acquire) & bit)) {
-        if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV, GA>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess)
-            return -5;
-        opted.fetch_or(bit, std::memory_order_release);
+    if (resident_blocks<D, N, I8, NV, GA, SH>() <= 0) return -5;
+    if (!SH) {
+        tc_kernel<D, N, I8, NV, GA, SH><<<G, kThreadsTC, C::SMEM, st>>>(args);
+        return cudaGetLastError() == cudaSuccess ? 0 : -5;
     }
-    tc_kernel<D, N, I8, NV, GA><<<G, kThreadsTC, C::SMEM, st>>>(args);
-    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+    // shared merges: a cooperative launch (the caller checked the grid fits)
+    TcArgs ca = args;
+    ca.p.coop = 1;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)G);
+    cfg.blockDim = dim3(kThreadsTC);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_kernel<D, N, I8, NV, GA, SH>, ca) == cudaSuccess ? 0 : -5;
 }
 
 template <int D>
 int launch_d(const TcArgs &args, int G, cudaStream_t st) {
     const int rows = args.p.rows;
+    // Short launches at head_dim 256 (work units for the capacity at most 8
+    // per block, so ranges of a few tiles and merges of many pieces) take the
+    // shared-merge kernels when the grid fits on the device at once.
+    const Params &p = args.p;
+    const int64_t max_units = p.nseg * ((p.cap + TT - 1) / TT + p.seg_units);
+    if (D == 256 && max_units <= 8 * (int64_t)G) {
+        if (rows <= 16 && G <= resident_blocks<D, 16, false, 16, false, true>())
+            return launch_dn<D, 16, false, 16, false, true>(args, G, st);
+        if (rows > 16 && rows <= 32 && G <= resident_blocks<D, 32, false, 32, false, true>())
+            return launch_dn<D, 32, false, 32, false, true>(args, G, st);
+    }
     if (rows <= 16) return launch_dn<D, 16, false>(args, G, st);
     if (rows <= 32) return launch_dn<D, 32, false>(args, G, st);
     if (rows <= 48) return launch_dn<D, 48, false>(args, G, st);
