@@ -347,3 +347,39 @@ def test_int8_workload_full_size_sampled(kernel):
                          scale=inp.scale, k_scale=inp.k_scale.cpu(),
                          v_scale=inp.v_scale.cpu())
     compare(got, run_oracle(cpu), torch.bfloat16, "int8 full")
+
+
+# -------------------------------------------------- kernel choice by layout
+def test_tensor_core_kernel_declines_unaligned_q():
+    # q whose base is 2 bytes off a 16-byte boundary cannot be read through a
+    # TMA map: the tensor-core kernel declines, AUTO takes the CUDA-core one
+    inp = W.dense_inputs(2, 1, 8, 2, 128, 300, [300, 41], 29, False)
+    dev = to_dev(inp)
+    buf = torch.empty(dev.q.numel() + 1, dtype=torch.bfloat16, device="cuda")
+    q = buf[1:].view(dev.q.shape)
+    q.copy_(dev.q)
+    assert q.data_ptr() % 16 != 0
+    with pytest.raises(fd.FdError):
+        fd.decode(q, dev.k, dev.v, dev.kv_lengths, n_q=1, scale=inp.scale,
+                  out_dtype=torch.float32, kernel=fd.FD_KERNEL_TC)
+    got = fd.decode(q, dev.k, dev.v, dev.kv_lengths, n_q=1, scale=inp.scale,
+                    out_dtype=torch.float32)
+    compare(got, run_oracle(inp), torch.float32, "unaligned q, auto")
+
+
+def test_inputs_changed_in_place_between_calls():
+    # the same tensors (so the same cached tensor maps) with new contents
+    inp = W.dense_inputs(2, 4, 16, 4, 256, 900, [900, 333], 30, True)
+    dev = to_dev(inp)
+    ws = fd.Workspace(8, 16, 256, 1024)
+    out = torch.empty(dev.q.shape, dtype=torch.float32, device="cuda")
+    for step in range(3):
+        fd.decode(dev.q, dev.k, dev.v, dev.kv_lengths, n_q=4, causal=True, scale=inp.scale,
+                  out=out, workspace=ws, kernel=fd.FD_KERNEL_TC)
+        torch.cuda.synchronize()
+        compare(out, run_oracle(inp), torch.float32, "step %d" % step)
+        g = torch.Generator().manual_seed(100 + step)
+        inp.q = torch.randn(inp.q.shape, generator=g).to(torch.bfloat16)
+        inp.k = torch.randn(inp.k.shape, generator=g).to(torch.bfloat16)
+        dev.q.copy_(inp.q)
+        dev.k.copy_(inp.k)
