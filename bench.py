@@ -50,6 +50,21 @@ def rank_info():
     return rank, world, local
 
 
+def max_over_ranks(x, world, device=None):
+    """The largest x over the ranks (the slowest replica's time)."""
+    if world <= 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_rank, world, ms_max):
+    """Whole-job GB/s: every replica's bytes over the slowest replica's time."""
+    return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -464,13 +479,9 @@ def run_fd(args):
     barrier()
     clocks = sampler.stop()
     ms_step = ev0.elapsed_time(ev1) / steps
-    t = torch.tensor([ms_step], device=device, dtype=torch.float64)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms_step, world, device)
     all_bytes = nbytes * world
-    value = all_bytes / (ms_max * 1e-3) / 1e9
+    value = aggregate_gbs(nbytes, world, ms_max)
 
     # end to end through the public call with host buffers: every step copies
     # q, both caches and kv_lengths from pinned host memory, decodes, and reads
@@ -496,11 +507,7 @@ def run_fd(args):
             e2e_step()
         barrier()
         e_ms = time_calls(e2e_step, e2e_steps, stream)
-        et = torch.tensor([e_ms], device=device, dtype=torch.float64)
-        if world > 1:
-            import torch.distributed as dist
-            dist.all_reduce(et, op=dist.ReduceOp.MAX)
-        e2e_value = round(all_bytes / (float(et.item()) * 1e-3) / 1e9, 3)
+        e2e_value = round(aggregate_gbs(nbytes, world, max_over_ranks(e_ms, world, device)), 3)
 
     result = None
     if rank == 0:
