@@ -404,6 +404,13 @@ def extras(args, device, stream, peak, kernel):
         inp = W.dense_inputs(1, 4, 16, 4, 256, cap, [3000], 1, True, device=device)
         measure("mtp_verify_cap%d" % cap, inp)
         del inp
+    # gather: time follows the list length, not the capacity
+    for K in (512, 2048, 8192):
+        for cap in (8192, 32768, 131072):
+            inp = W.gather_inputs(1, 1, 32, 4, 128, cap, K, 128, 1, device=device)
+            measure("gather_K%d_cap%d" % (K, cap), inp, 100)
+            del inp
+    torch.cuda.empty_cache()
     inp = W.dense_inputs(1, 1, 32, 4, 128, 131072, [131072], 1, False, device=device)
     measure("dense_scan_131k_32q4kv", inp, 50)
     del inp

@@ -1462,12 +1462,13 @@ int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
 template <int D>
 int launch_d(const TcArgs &args, int G, cudaStream_t st) {
     const int rows = args.p.rows;
-    // Short launches at head_dim 256 (work units for the capacity at most 8
-    // per block, so ranges of a few tiles and merges of many pieces) take the
-    // shared-merge kernels when the grid fits on the device at once.
+    // Launches of few segments at head_dim 256 take the shared-merge kernels
+    // (when the grid fits on the device at once); inside, a short launch
+    // (a few tiles per block) shares its merges and a long one keeps the
+    // last-arriver merge.  The choice depends on shapes only, never on the
+    // capacity.
     const Params &p = args.p;
-    const int64_t max_units = p.nseg * ((p.cap + TT - 1) / TT + p.seg_units);
-    if (D == 256 && max_units <= 8 * (int64_t)G) {
+    if (D == 256 && p.nseg * 8 <= (int64_t)G) {
         if (rows <= 16 && G <= resident_blocks<D, 16, false, 16, false, true>())
             return launch_dn<D, 16, false, 16, false, true>(args, G, st);
         if (rows > 16 && rows <= 32 && G <= resident_blocks<D, 32, false, 32, false, true>())
