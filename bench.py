@@ -190,6 +190,11 @@ def workload_desc(name):
 
 def call_fn(inp, out, ws, kernel, num_ctas=0):
     from decode_attention_preallocated_gb300 import fd
+    if inp.block_table is not None:
+        return lambda: fd.decode_paged(inp.q, inp.k, inp.v, inp.block_table, inp.kv_lengths,
+                                       n_q=inp.n_q, causal=inp.causal, scale=inp.scale,
+                                       k_scale=inp.k_scale, v_scale=inp.v_scale, out=out,
+                                       workspace=ws, kernel=kernel, num_ctas=num_ctas)
     if inp.idx is not None:
         return lambda: fd.decode_gather(inp.q, inp.k, inp.v, inp.idx, scale=inp.scale, out=out,
                                         workspace=ws, kernel=kernel, num_ctas=num_ctas)
@@ -411,6 +416,14 @@ def extras(args, device, stream, peak, kernel):
             measure("gather_K%d_cap%d" % (K, cap), inp, 100)
             del inp
     torch.cuda.empty_cache()
+    # paged caches: the ragged and int8 workloads with their pages scattered
+    # over a pool (bytes: the same K/V rows as the flat caches)
+    for name in ("paged_ps16", "paged_ps64", "paged_ps256", "paged_int8_ps64",
+                 "paged_int8_ps256"):
+        inp = W.workload(name, seed=1, device=device)
+        measure(name, inp, 50)
+        del inp
+        torch.cuda.empty_cache()
     inp = W.dense_inputs(1, 1, 32, 4, 128, 131072, [131072], 1, False, device=device)
     measure("dense_scan_131k_32q4kv", inp, 50)
     del inp
@@ -491,19 +504,19 @@ def run_fd(args):
     value = aggregate_gbs(nbytes, world, ms_max)
 
     # end to end through the public call with host buffers: every step copies
-    # q, both caches and kv_lengths from pinned host memory, decodes, and reads
-    # the output back
-    host = {} if args.no_e2e else {
-        n: getattr(inp, n).cpu().pin_memory() for n in ("q", "k", "v", "kv_lengths")}
+    # q, both caches, kv_lengths (and the scales, index lists or block table
+    # the workload has) from pinned host memory, decodes, and reads the output
+    # back
+    names = [n for n in ("q", "k", "v", "kv_lengths", "k_scale", "v_scale", "idx", "block_table")
+             if getattr(inp, n) is not None]
+    host = {} if args.no_e2e else {n: getattr(inp, n).cpu().pin_memory() for n in names}
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in host.values())
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
-        inp.q.copy_(host["q"], non_blocking=True)
-        inp.k.copy_(host["k"], non_blocking=True)
-        inp.v.copy_(host["v"], non_blocking=True)
-        inp.kv_lengths.copy_(host["kv_lengths"], non_blocking=True)
+        for n, x in host.items():
+            getattr(inp, n).copy_(x, non_blocking=True)
         fn()
         out_host.copy_(out, non_blocking=True)
 

@@ -115,6 +115,8 @@ struct Call {
     const int32_t *kv_lengths;
     const int32_t *idx;
     int32_t idx_len;
+    const int32_t *block_table;   // paged mode: [B, max_pages]
+    int32_t max_pages;
     int32_t n_q, causal;
     float scale;
     int mode;         // fd::Mode
@@ -137,14 +139,21 @@ int run(const Call &c) {
     if (c.q->dtype != FD_BF16 || c.k->dtype != kvdt || c.v->dtype != kvdt) return FD_ERR_ARG;
     if (c.out->dtype != FD_BF16 && c.out->dtype != FD_F32) return FD_ERR_ARG;
 
+    const bool paged = c.mode == fd::kPaged;
     const int64_t B = c.q->shape[0], n_q = c.q->shape[1], Hq = c.q->shape[2], d = c.q->shape[3];
-    const int64_t Hkv = c.k->shape[1], cap = c.k->shape[2];
+    // paged: k / v are pools [num_pages, Hkv, page_size, d] and the logical
+    // capacity is max_pages * page_size
+    const int64_t Hkv = c.k->shape[1], rows_per = c.k->shape[2];
+    if (paged && (!c.block_table || c.max_pages < 1 || rows_per < 1 || c.k->shape[0] < 1))
+        return FD_ERR_ARG;
+    const int64_t cap = paged ? (int64_t)c.max_pages * rows_per : rows_per;
+    if (paged && cap >= ((int64_t)1 << 31)) return FD_ERR_UNSUPPORTED;
     if (n_q != c.n_q) return FD_ERR_ARG;
     for (int i = 0; i < 4; ++i) {
         if (c.k->shape[i] != c.v->shape[i]) return FD_ERR_ARG;
         if (c.out->shape[i] != c.q->shape[i]) return FD_ERR_ARG;
     }
-    if (c.k->shape[0] != B || c.k->shape[3] != d) return FD_ERR_ARG;
+    if ((!paged && c.k->shape[0] != B) || c.k->shape[3] != d) return FD_ERR_ARG;
     if (B < 1 || Hq < 1 || Hkv < 1 || B > (1 << 24) || Hq > 4096 || cap > ((int64_t)1 << 40))
         return FD_ERR_ARG;
     if (Hq % Hkv != 0) return FD_ERR_ARG;
@@ -165,11 +174,11 @@ int run(const Call &c) {
     if (c.kv_int8) {
         if ((rc = check_tensor(c.ks, 3)) || (rc = check_tensor(c.vs, 3))) return rc;
         if (c.ks->dtype != FD_F32 || c.vs->dtype != FD_F32) return FD_ERR_ARG;
-        const int64_t want[3] = {B, Hkv, cap};
+        const int64_t want[3] = {c.k->shape[0], Hkv, rows_per};
         for (int i = 0; i < 3; ++i)
             if (c.ks->shape[i] != want[i] || c.vs->shape[i] != want[i]) return FD_ERR_ARG;
     }
-    if (c.mode == fd::kDense && !c.kv_lengths) return FD_ERR_ARG;
+    if (c.mode != fd::kGather && !c.kv_lengths) return FD_ERR_ARG;
     if (c.mode == fd::kGather && (c.idx_len < 0 || (!c.idx && c.idx_len > 0))) return FD_ERR_ARG;
     if (c.causal != 0 && c.causal != 1) return FD_ERR_ARG;
 
@@ -180,7 +189,7 @@ int run(const Call &c) {
     memset(&p, 0, sizeof p);
     p.B = (int32_t)B; p.n_q = (int32_t)n_q; p.Hq = (int32_t)Hq; p.Hkv = (int32_t)Hkv;
     p.g = (int32_t)g; p.d = (int32_t)d; p.cap = cap; p.rows = (int32_t)rows;
-    p.mode = c.mode; p.causal = c.mode == fd::kDense ? c.causal : 0;
+    p.mode = c.mode; p.causal = c.mode != fd::kGather ? c.causal : 0;
     p.kv_int8 = c.kv_int8; p.out_f32 = c.out->dtype == FD_F32;
     p.scale_log2 = c.scale * 1.4426950408889634f;
     p.idx_len = c.idx_len; p.nseg = nseg;
@@ -197,6 +206,12 @@ int run(const Call &c) {
     }
     p.kv_lengths = c.kv_lengths;
     p.idx = c.idx;
+    if (paged) {
+        p.block_table = c.block_table;
+        p.page_size = (int32_t)rows_per;
+        p.max_pages = c.max_pages;
+        p.num_pages = c.k->shape[0];
+    }
     p.out = c.out->data;
     p.counters = ws->counters;
     p.status = ws->status;
@@ -239,7 +254,7 @@ extern "C" {
 int fd_decode(const fd_tensor *q, const fd_tensor *k_cache, const fd_tensor *v_cache,
               const int32_t *kv_lengths, int32_t n_q, int32_t causal, float scale,
               const fd_tensor *out, const fd_opts *opts) {
-    Call c{q, k_cache, v_cache, nullptr, nullptr, out, kv_lengths, nullptr, 0,
+    Call c{q, k_cache, v_cache, nullptr, nullptr, out, kv_lengths, nullptr, 0, nullptr, 0,
            n_q, causal, scale, fd::kDense, 0, opts};
     return run(c);
 }
@@ -248,7 +263,7 @@ int fd_decode_int8(const fd_tensor *q, const fd_tensor *k_cache, const fd_tensor
                    const fd_tensor *k_scale, const fd_tensor *v_scale,
                    const int32_t *kv_lengths, int32_t n_q, int32_t causal, float scale,
                    const fd_tensor *out, const fd_opts *opts) {
-    Call c{q, k_cache, v_cache, k_scale, v_scale, out, kv_lengths, nullptr, 0,
+    Call c{q, k_cache, v_cache, k_scale, v_scale, out, kv_lengths, nullptr, 0, nullptr, 0,
            n_q, causal, scale, fd::kDense, 1, opts};
     return run(c);
 }
@@ -259,8 +274,21 @@ int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache, const fd_tens
     if (!q || !opts) return FD_ERR_ARG;
     float scale = opts->scale;
     if (scale == 0.f && q->ndim == 4 && q->shape[3] > 0) scale = 1.f / sqrtf((float)q->shape[3]);
-    Call c{q, k_cache, v_cache, nullptr, nullptr, out, nullptr, idx, idx_len,
+    Call c{q, k_cache, v_cache, nullptr, nullptr, out, nullptr, idx, idx_len, nullptr, 0,
            q->ndim == 4 ? (int32_t)q->shape[1] : 0, 0, scale, fd::kGather, 0, opts};
+    return run(c);
+}
+
+int fd_decode_paged(const fd_tensor *q, const fd_tensor *k_pages, const fd_tensor *v_pages,
+                    const fd_tensor *k_scale, const fd_tensor *v_scale,
+                    const int32_t *block_table, int32_t max_pages, const int32_t *kv_lengths,
+                    int32_t n_q, int32_t causal, float scale, const fd_tensor *out,
+                    const fd_opts *opts) {
+    if (!k_pages) return FD_ERR_ARG;
+    const int int8 = k_pages->dtype == FD_I8;
+    if (!int8 && (k_scale || v_scale)) return FD_ERR_ARG;
+    Call c{q, k_pages, v_pages, k_scale, v_scale, out, kv_lengths, nullptr, 0, block_table,
+           max_pages, n_q, causal, scale, fd::kPaged, int8, opts};
     return run(c);
 }
 

@@ -51,6 +51,18 @@ __device__ __forceinline__ int64_t seq_len(const Params &p, int b) {
     return clamp_len(L, p.cap);
 }
 
+// Paged caches: the pool page that holds logical position pos (< cap) of
+// sequence b, or -1, with FD_DEV_BAD_INDEX set, when the table entry names no
+// page of the pool (the position is then skipped).
+__device__ __forceinline__ int32_t page_of(const Params &p, int b, int32_t pos) {
+    const int32_t e = __ldg(p.block_table + (int64_t)b * p.max_pages + pos / p.page_size);
+    if (e < 0 || e >= p.num_pages) {
+        atomicOr(p.status, kDevBadIndex);
+        return -1;
+    }
+    return e;
+}
+
 __device__ __forceinline__ int64_t seg_tiles(const Params &p, int64_t s) {
     if (p.mode == kGather) return ceil_div(p.idx_len, p.tile);
     return ceil_div(seq_len(p, (int)(s / p.Hkv)), p.tile);

@@ -12,7 +12,10 @@
 
 namespace fd {
 
-enum Mode : int32_t { kDense = 0, kGather = 1 };
+// kPaged: the dense prefix mode over a paged cache (a pool of fixed-size
+// pages and a per-sequence block table); it shares the dense mode's segments,
+// tiles and masks and differs only in where a position's row lives.
+enum Mode : int32_t { kDense = 0, kGather = 1, kPaged = 2 };
 
 // Everything a kernel needs, passed by value as one __grid_constant__ block.
 struct Params {
@@ -40,6 +43,12 @@ struct Params {
     const float *v_scale;  int64_t vss[3];
     const int32_t *kv_lengths;
     const int32_t *idx;
+    // paged caches: logical position j of sequence b lives at row j % page_size
+    // of pool page block_table[b * max_pages + j / page_size]; the caches'
+    // strides are then (page, kv head, row in page); cap = max_pages * page_size
+    const int32_t *block_table;
+    int32_t page_size, max_pages;
+    int64_t num_pages;
     void *out;             int64_t os[4];
     // workspace
     int32_t *counters;     // [nseg], zero between launches

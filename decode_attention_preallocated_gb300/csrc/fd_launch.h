@@ -11,12 +11,17 @@ namespace fd {
 int simt_tile_tokens();
 int launch_simt(const Params &p, int num_ctas, cudaStream_t stream);
 
-// Tensor-core kernel (fd_tc.cu): dense bf16 prefix (optionally causal),
-// head_dim 128 / 256, up to 64 packed rows; one block per SM.
+// Tensor-core kernel (fd_tc.cu, fd_tc_paged.cu): dense prefix (optionally
+// causal) over flat or paged caches and index gather; bf16 caches at head_dim
+// 128 / 256 with up to 64 packed rows, int8 at head_dim 128 with up to 32;
+// one block per SM.
 int tc_tile_tokens();
 // Work units the split charges per segment start (Params::seg_units).
 int tc_seg_units(const Params &p);
 bool tc_supports(const Params &p);
 int launch_tc(const Params &p, int num_ctas, cudaStream_t stream);
+// Paged caches (fd_tc_paged.cu); tc_supports covers them.
+bool tc_supports_paged(const Params &p);
+int launch_tc_paged(const Params &p, int num_ctas, cudaStream_t stream);
 
 }  // namespace fd

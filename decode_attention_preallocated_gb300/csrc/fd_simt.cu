@@ -1,5 +1,5 @@
 // fd_simt.cu -- CUDA-core decode kernel: every mode (dense prefix, causal
-// window, index gather, int8 cache), head_dim 128 and 256.
+// window, index gather, paged cache, int8 cache), head_dim 128 and 256.
 //
 // One thread block walks a contiguous range of 32-position tiles chosen by
 // the balanced split partitioner (fd_internal.h).  Per tile it stages K and
@@ -33,7 +33,8 @@ struct Layout {
     static size_t smem_bytes(int rows) {
         return (size_t)rows * D * 4          // Q (fp32)
                + 2 * (size_t)T * KST * 2     // K, V tiles (bf16)
-               + (size_t)T * 8               // positions (int64, 8-byte aligned here)
+               + 3 * (size_t)T * 8           // positions, K and V row offsets (int64,
+                                             // 8-byte aligned here)
                + (size_t)rows * (T + 1) * 4  // P
                + 3 * (size_t)T * 4           // k scale, v scale, valid
                + 3 * (size_t)rows * 4;       // m, l, alpha
@@ -64,7 +65,8 @@ simt_kernel(const __grid_constant__ Params p) {
     uint16_t *Ks = reinterpret_cast<uint16_t *>(Qs + rows * D);
     uint16_t *Vs = Ks + T * Ly::KST;
     int64_t *tpos = reinterpret_cast<int64_t *>(Vs + T * Ly::KST);
-    float *Ps = reinterpret_cast<float *>(tpos + T);
+    int64_t *tko = tpos + T, *tvo = tko + T;   // element offsets of the K / V rows
+    float *Ps = reinterpret_cast<float *>(tvo + T);
     float *ksc = Ps + rows * (T + 1);
     float *vsc = ksc + T;
     int *tval = reinterpret_cast<int *>(vsc + T);
@@ -140,9 +142,6 @@ simt_kernel(const __grid_constant__ Params p) {
 
         const char *kbase = reinterpret_cast<const char *>(p.k);
         const char *vbase = reinterpret_cast<const char *>(p.v);
-        const int esz = p.kv_int8 ? 1 : 2;
-        const int64_t kb_off = (int64_t)b * p.ks[0] + (int64_t)hk * p.ks[1];
-        const int64_t vb_off = (int64_t)b * p.vs[0] + (int64_t)hk * p.vs[1];
 
         for (int64_t tt = t - first; tt < piece_end - first; ++tt) {
             const int64_t j0 = tt * T;
@@ -157,12 +156,23 @@ simt_kernel(const __grid_constant__ Params p) {
                     ok = cell >= 0 && cell < p.cap;
                     pos = cell;
                 }
+                // Where the position's row lives: (sequence, kv head, position)
+                // of a flat cache, (page, kv head, row in page) of a paged one.
+                int64_t o0 = b, o2 = pos;
+                if (ok && p.mode == kPaged) {
+                    const int32_t pg = page_of(p, b, (int32_t)pos);
+                    ok = pg >= 0;
+                    o0 = pg;
+                    o2 = pos % p.page_size;
+                }
                 tpos[tid] = ok ? pos : 0;
                 tval[tid] = ok;
+                tko[tid] = o0 * p.ks[0] + (int64_t)hk * p.ks[1] + o2 * p.ks[2];
+                tvo[tid] = o0 * p.vs[0] + (int64_t)hk * p.vs[1] + o2 * p.vs[2];
                 float kscale = 1.f, vscale = 1.f;
                 if (ok && p.kv_int8) {
-                    kscale = p.k_scale[(int64_t)b * p.kss[0] + (int64_t)hk * p.kss[1] + pos * p.kss[2]];
-                    vscale = p.v_scale[(int64_t)b * p.vss[0] + (int64_t)hk * p.vss[1] + pos * p.vss[2]];
+                    kscale = p.k_scale[o0 * p.kss[0] + (int64_t)hk * p.kss[1] + o2 * p.kss[2]];
+                    vscale = p.v_scale[o0 * p.vss[0] + (int64_t)hk * p.vss[1] + o2 * p.vss[2]];
                 }
                 ksc[tid] = kscale;
                 vsc[tid] = vscale;
@@ -176,9 +186,8 @@ simt_kernel(const __grid_constant__ Params p) {
                     const int jj = (e / CPR) % T, cc = e % CPR;
                     uint4 w = make_uint4(0, 0, 0, 0);
                     if (tval[jj]) {
-                        const char *src = which
-                            ? vbase + (vb_off + tpos[jj] * p.vs[2] + cc * 8) * 2
-                            : kbase + (kb_off + tpos[jj] * p.ks[2] + cc * 8) * 2;
+                        const char *src = which ? vbase + (tvo[jj] + cc * 8) * 2
+                                                : kbase + (tko[jj] + cc * 8) * 2;
                         w = ldg_stream(src);
                     }
                     uint16_t *dst = (which ? Vs : Ks) + jj * Ly::KST + cc * 8;
@@ -191,9 +200,8 @@ simt_kernel(const __grid_constant__ Params p) {
                     const int jj = (e / CPR) % T, cc = e % CPR;
                     uint4 w = make_uint4(0, 0, 0, 0);
                     if (tval[jj]) {
-                        const char *src = which
-                            ? vbase + (vb_off + tpos[jj] * p.vs[2] + cc * 16)
-                            : kbase + (kb_off + tpos[jj] * p.ks[2] + cc * 16);
+                        const char *src = which ? vbase + (tvo[jj] + cc * 16)
+                                                : kbase + (tko[jj] + cc * 16);
                         w = ldg_stream(src);
                     }
                     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -209,7 +217,6 @@ simt_kernel(const __grid_constant__ Params p) {
                     *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(o[4], o[5], o[6], o[7]);
                 }
             }
-            (void)esz;
             __syncthreads();
 
             // Scores: warp w owns rows w, w+8, ...; lane = position in tile.
@@ -237,7 +244,7 @@ simt_kernel(const __grid_constant__ Params p) {
                 const int r = warp + kWarps * k;
                 if (r < rows) {
                     bool vis = tval[lane] != 0;
-                    if (p.causal && p.mode == kDense) {
+                    if (p.causal && p.mode != kGather) {
                         const int i = r % p.n_q;
                         vis = vis && tpos[lane] <= len - p.n_q + i;
                     }

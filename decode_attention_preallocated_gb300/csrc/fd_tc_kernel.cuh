@@ -1,0 +1,1524 @@
+// fd_tc_kernel.cuh -- the tensor-core (tcgen05) decode kernel template and
+// its host-side helpers (tensor-map encoding, occupancy, launch), included
+// by the translation units that instantiate it: fd_tc.cu (flat caches,
+// index gather) and fd_tc_paged.cu (paged caches).
+//
+// Modes: the dense prefix (optionally causal) over flat or paged caches, and
+// index gather; bf16 caches at head_dim 128 / 256 with up to 64 packed query
+// rows, int8 caches at head_dim 128 with up to 32.
+//
+// Work split: balanced consecutive ranges of work units over one block per
+// SM, where a segment is its tiles (128 positions) plus a few units for the
+// fixed cost of a piece boundary (see Walk).  Roles inside a block
+// (320 threads):
+//   warp 8      TMA producer: loads each segment's packed Q rows (one box
+//               per 64 columns) as soon as the previous piece's last QK has
+//               read the buffer, and streams K and V tiles of the block's
+//               range into a ring of shared-memory slots (4-D tensor maps,
+//               128-byte swizzle), in the order the MMAs consume them.
+//   warp 9      MMA issuer (one thread): S^T = K . Q^T   (M = 128 positions,
+//               N = padded query rows, K = head_dim) into TMEM, then
+//               O^T += V^T . P^T (M = 128 dims per chunk, N = rows,
+//               K = 128 positions) into TMEM; completion via tcgen05.commit.
+//               QK of tile t+1 is issued before PV of tile t.
+//   warps 0-7   softmax and epilogue, two warpgroups that split the query
+//               rows (bf16 caches).  Thread i of a group owns TMEM lane i =
+//               cache position i of the tile (scores) and dim i of each
+//               128-dim chunk (output).  Per tile: mask (length, causal
+//               window), running row maxima refreshed when a score passes
+//               them by 2^8 (column max over the 128 positions by warp
+//               shuffles + shared memory), O rescaled in TMEM then,
+//               P = 2^(s - m) written to shared memory in the MMA operand
+//               layout (one bf16 plane, or hi + lo planes for fp32 outputs).
+//               At the end of a segment piece it normalises and stores, or
+//               hands a split partial to the in-launch combine (last block
+//               to arrive merges; comfy-kitchen #239, "GQA decode").
+//   int8 caches: warps 0-3 are the one softmax group and warps 4-7 widen the
+//               int8 tiles the producer loads into the bf16 slots the MMAs
+//               read; the per-position scales multiply scores and P.
+// Flat caches: the last tile of a segment is loaded right-aligned (ending at
+// the length), so no row of the unused tail is ever read; positions the
+// previous tile already covered are masked.  Paged caches (PG) and index
+// gather (GA): tiles start at multiples of 128 and each producer lane fetches
+// four rows per tile with tile::gather4 (rows past the length, or of a bad
+// page or cell, are row -1 and read as zeros; the softmax masks them).  Every wait is bounded (2 s); a timeout sets
+// FD_DEV_INTERNAL in the status word, records where it waited, and the block
+// drains its copies and MMAs and exits.
+#pragma once
+
+#include <cuda.h>
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+#include <cuda_runtime.h>
+
+#include "fd_device.cuh"
+#include "fd_launch.h"
+#include "fd_ptx.cuh"
+
+namespace fd {
+
+// ------------------------------------------------------ tensor-map encoding
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Tensor maps are encoded on the host for every launch; a decode loop passes
+// the same caches (and often the same q) each step, so the last encodings
+// are kept, keyed by every argument that goes into one.
+struct MapKey {
+    const void *base;
+    uint32_t dtype, rank, swizzle, pad;
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4];
+};
+
+inline EncodeTiledFn encode_fn();
+
+inline CUresult encode_cached(CUtensorMap *m, CUtensorMapDataType dtype, cuuint32_t rank, void *base,
+                       const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
+                       const cuuint32_t *estr, CUtensorMapSwizzle swizzle) {
+    MapKey k;
+    memset(&k, 0, sizeof k);
+    k.base = base;
+    k.dtype = (uint32_t)dtype;
+    k.rank = rank;
+    k.swizzle = (uint32_t)swizzle;
+    for (cuuint32_t i = 0; i < rank; ++i) {
+        k.dims[i] = dims[i];
+        k.box[i] = box[i];
+        if (i + 1 < rank) k.strides[i] = strides[i];
+    }
+    constexpr int kEntries = 32;
+    static std::mutex mu;
+    static MapKey keys[kEntries];
+    static CUtensorMap maps[kEntries];
+    static int used = 0, next = 0;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < used; ++i)
+            if (memcmp(&keys[i], &k, sizeof k) == 0) {
+                *m = maps[i];
+                return CUDA_SUCCESS;
+            }
+    }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return CUDA_ERROR_NOT_SUPPORTED;
+    const CUresult r = fn(m, dtype, rank, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+        std::lock_guard<std::mutex> lk(mu);
+        keys[next] = k;
+        maps[next] = *m;
+        next = (next + 1) % kEntries;
+        if (used < kEntries) ++used;
+    }
+    return r;
+}
+
+inline EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+namespace {
+
+constexpr int TT = 128;                 // cache positions per tile (MMA M)
+constexpr int kMaxGroups = 2;           // softmax warpgroups (bf16 caches)
+constexpr int kThreadsTC = 320;         // warps 0-7, producer, MMA issuer
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kDevTimeout = 4;          // mirrors FD_DEV_INTERNAL
+// Scores (log2 units) may exceed a row's running maximum by this much before
+// the maximum is refreshed and O rescaled; P is then at most 2^8, which fp32
+// accumulators and the hi/lo bf16 split of P carry without loss.
+constexpr float kRescaleSlack = 8.f;
+
+struct TcArgs {   // CUtensorMap members carry their own alignment
+    // (int8 caches: tk / tv map the int8 codes; gather and paged caches: 2-D
+    // maps of cache rows)
+    CUtensorMap tk;
+    CUtensorMap tv;
+    CUtensorMap tq;
+    Params p;
+    // gather: cache row (b, hk, pos) is row b*gs0 + hk*gs1 + pos*gs2 of tk / tv;
+    // paged: pool row (page, hk, r) is row page*gs0 + hk*gs1 + r*gs2
+    int64_t gs0, gs1, gs2;
+};
+
+template <int D, int N, bool I8, int NV, bool GA = false>
+struct Cfg {
+    // bf16 caches: two softmax warpgroups split the rows (warps 0-7).  int8
+    // caches: one softmax warpgroup (warps 0-3); warps 4-7 widen the int8
+    // tiles to bf16 for the MMAs.
+    static constexpr int GROUPS = I8 ? 1 : 2;
+    static constexpr int SMT = 128 * GROUPS;     // softmax threads
+    static constexpr int KB = D / 64;            // 128-byte boxes per cache row
+    static constexpr int DC = D / 128;           // 128-dim chunks of O
+    static constexpr uint32_t BOX = TT * 128;    // bytes of one box of a slot
+    static constexpr uint32_t SLOT = KB * BOX;   // one K or V tile
+    static constexpr uint32_t QB = N * 128;      // one 64-column box of Q or P
+    static constexpr uint32_t QBYTES = KB * QB;
+    static constexpr uint32_t PPLANE = 2 * QB;   // one bf16 plane of P (128 positions x N)
+    static constexpr uint32_t PSTAGE = 2 * PPLANE;   // P = hi plane + lo plane
+    // Query rows per softmax warpgroup.
+    // Rows the softmax handles: NV (<= N, a multiple of 8) bounds the packed
+    // rows; the MMAs still run N columns, and P rows NV..N-1 stay zero.
+    static_assert(NV <= N && NV % 8 == 0, "valid-row bound");
+    static constexpr int NH = NV / GROUPS;
+    static_assert(NH % 8 == 0, "rows per group must be a multiple of 8");
+    // Barriers and the reduction scratch come first, then 1024-byte aligned
+    // operand buffers.  Scratch per group: [2 tiles][4 warps][NH] floats.
+    static constexpr uint32_t RED_GROUP = 2 * 4 * NH;   // floats
+    static constexpr uint32_t RED = GROUPS * RED_GROUP * 4;
+    // Per-row element offsets into out for the current segment (int64), two
+    // tables used by alternate pieces.
+    static constexpr uint32_t OFF_TBL = 512 + RED;
+    static constexpr uint32_t TBL = 2 * N * 8;
+    static constexpr uint32_t MISC = ((OFF_TBL + TBL) + 1023) / 1024 * 1024;
+    static constexpr uint32_t BUDGET = 232448;   // max dynamic shared memory per block
+    // int8 caches: a ring of NR raw tiles (TT positions x D codes, as TMA
+    // lands them) in front of the bf16 slots the MMAs read.
+    static constexpr uint32_t RAW = I8 ? TT * D : 0;
+    static constexpr int NR = I8 ? 6 : 0;
+    static constexpr int NRX = I8 ? NR : 1;   // ring length for index arithmetic
+    // Two P stages when that still leaves three K/V slots, else one.
+    static constexpr int NS2 = (int)((BUDGET - MISC - QBYTES - 2 * PSTAGE - NR * RAW) / SLOT);
+    static constexpr int PST = NS2 >= 3 ? 2 : 1;
+    static constexpr int NS_RAW = (int)((BUDGET - MISC - QBYTES - PST * PSTAGE - NR * RAW) / SLOT);
+    static constexpr int NS = NS_RAW > 8 ? 8 : NS_RAW;
+    static_assert(NS >= 2, "need two K/V slots");
+    static constexpr uint32_t OFF_SLOTS = MISC;
+    static constexpr uint32_t OFF_Q = OFF_SLOTS + NS * SLOT;
+    static constexpr uint32_t OFF_P = OFF_Q + QBYTES;
+    static constexpr uint32_t OFF_RAW = OFF_P + PST * PSTAGE;
+    static constexpr uint32_t SMEM = OFF_RAW + NR * RAW;
+    static_assert(SMEM <= BUDGET, "shared memory budget");
+    static constexpr uint32_t COLS = 2 * N + DC * N;
+    static constexpr uint32_t TMEM_COLS = COLS <= 32 ? 32 : COLS <= 64 ? 64 : COLS <= 128 ? 128 : 256;
+    static constexpr int MERGE_UNROLL = (D == 256 && NV >= 32 && !I8) ? 1 : 2;
+    static constexpr uint32_t IDESC_QK = ptx::idesc_bf16(128, N, 0, 0);
+    static constexpr uint32_t IDESC_PV = ptx::idesc_bf16(128, N, 1, 1);
+    // P planes are MN-major (query rows contiguous per position) with 32-byte
+    // swizzle: 16-row atoms of TT positions x 32 bytes.
+    static constexpr uint32_t PATOM = TT * 32;
+};
+
+// ------------------------------------------------------------------ pieces
+// The split is over work units: a non-empty segment s = b*Hkv + hk holds
+// V = p.seg_units units that stand for the fixed cost of a piece boundary
+// (epilogue, pipeline restart), then one unit per tile.  The block whose
+// range crosses into a segment pays for the boundary with V fewer tiles; a
+// range may start or end inside those V units, which map to no tile.
+// A block's work is a run of consecutive non-empty segments.  The first one
+// is found once per block by a warp scan over the sequence lengths; every
+// later one is the next non-empty segment, so walking needs no division.
+// Gather launches: segment s = (b*n_q + i)*Hkv + hk is one index list (all of
+// length idx_len) seen by the g query heads of kv head hk.
+struct Walk {
+    int64_t s;        // segment
+    int64_t first;    // unit index of the segment's first tile
+    int64_t L;        // its sequence length (gather: the list length)
+    int32_t ntiles;   // its tile count
+    int32_t b, hk;
+    int32_t i;        // gather: query row of the list (dense: 0)
+};
+
+__device__ __forceinline__ int32_t tiles_of(int64_t L) { return (int32_t)((L + TT - 1) / TT); }
+
+// Units of a segment of n tiles.
+__device__ __forceinline__ int64_t units_of(const Params &p, int64_t n) {
+    return n > 0 ? n + p.seg_units : 0;
+}
+
+// Total work units of the launch (one warp; every lane gets the value).
+__device__ __forceinline__ int64_t total_units_tc(const Params &p) {
+    if (p.mode == kGather) return p.nseg * units_of(p, tiles_of(p.idx_len));
+    const int lane = threadIdx.x & 31;
+    int64_t acc = 0;
+    for (int b = lane; b < p.B; b += 32) acc += units_of(p, tiles_of(seq_len(p, b)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc * p.Hkv;
+}
+
+// The segment holding work unit t (one warp; false if t is past the end).
+__device__ __noinline__ bool first_piece_warp(const Params &p, int64_t t, Walk *w) {
+    if (p.mode == kGather) {   // equal segments: closed form
+        const int64_t n = tiles_of(p.idx_len), u = units_of(p, n);
+        if (u == 0 || t >= p.nseg * u) return false;
+        const int64_t s = t / u, bi = s / p.Hkv;
+        w->s = s;
+        w->hk = (int)(s % p.Hkv);
+        w->b = (int)(bi / p.n_q);
+        w->i = (int)(bi % p.n_q);
+        w->first = s * u + p.seg_units;
+        w->ntiles = (int32_t)n;
+        w->L = p.idx_len;
+        return true;
+    }
+    const int lane = threadIdx.x & 31;
+    int64_t base = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int64_t L = b < p.B ? seq_len(p, b) : 0;
+        const int64_t n = tiles_of(L), u = units_of(p, n);
+        const int64_t wt = (int64_t)p.Hkv * u;
+        int64_t incl = wt;   // inclusive scan over the 32 lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += x;
+        }
+        const int64_t excl = incl - wt;
+        const unsigned m = __ballot_sync(0xffffffffu, wt > 0 && t >= base + excl && t < base + incl);
+        if (m) {
+            const int src = __ffs(m) - 1;
+            const int64_t e = __shfl_sync(0xffffffffu, excl, src);
+            const int64_t nb = __shfl_sync(0xffffffffu, n, src);
+            const int64_t ub = __shfl_sync(0xffffffffu, u, src);
+            const int64_t Lb = __shfl_sync(0xffffffffu, L, src);
+            const int hk = (int)((t - base - e) / ub);
+            w->b = b0 + src;
+            w->hk = hk;
+            w->i = 0;
+            w->s = (int64_t)w->b * p.Hkv + hk;
+            w->first = base + e + (int64_t)hk * ub + p.seg_units;
+            w->ntiles = (int32_t)nb;
+            w->L = Lb;
+            return true;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return false;
+}
+
+// Advance to the next segment with at least one tile (false past the end).
+__device__ __forceinline__ bool next_piece(const Params &p, Walk &w) {
+    w.first += w.ntiles;
+    if (p.mode == kGather) {
+        if (w.s + 1 >= p.nseg) return false;
+        ++w.s;
+        if (++w.hk == p.Hkv) {
+            w.hk = 0;
+            if (++w.i == p.n_q) {
+                w.i = 0;
+                ++w.b;
+            }
+        }
+        w.first += p.seg_units;
+        return true;
+    }
+    do {
+        if (w.s + 1 >= p.nseg) return false;
+        ++w.s;
+        if (++w.hk == p.Hkv) {
+            w.hk = 0;
+            ++w.b;
+            w.L = seq_len(p, w.b);
+            w.ntiles = tiles_of(w.L);
+        }
+    } while (w.ntiles == 0);
+    w.first += p.seg_units;
+    return true;
+}
+
+struct Bars {   // at the start of shared memory; the reduction scratch follows at 512
+    uint64_t slot_full[8], slot_empty[8];
+    uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+    uint64_t q_full, q_free, o_done, o_free, exit_mma, sm_bar;
+    uint64_t wg_bar[kMaxGroups];
+    union {
+        struct {
+            uint64_t raw_full[6], raw_empty[6];   // int8 caches: raw tile ring
+        };
+        Walk walk_last;   // shared merges (bf16 caches): the last piece worked on
+    };
+    uint32_t tmem_base;
+    int abort_flag;
+    int last_flag;
+    int pad;
+    int64_t total;
+    int vote[kMaxGroups][2][4];
+    int64_t t_begin, t_end;   // the block's range of work units
+    Walk walk;                // its first piece
+    int has_work;
+};
+
+// Ring fill index of the K and V tiles of tile number tc in a piece whose
+// first and last tiles are pa and pb, for the fill order K(pa), K(pa+1),
+// V(pa), K(pa+2), V(pa+1), ..., V(pb).
+__device__ __forceinline__ uint32_t k_fill(uint32_t tc, uint32_t pa) {
+    return tc == pa ? 2 * tc : 2 * tc - 1;
+}
+__device__ __forceinline__ uint32_t v_fill(uint32_t tc, uint32_t pb) {
+    return tc == pb ? 2 * tc + 1 : 2 * tc + 2;
+}
+
+// First cache position loaded for tile tt of a segment of length L: tiles
+// start at tt * TT, except the last, which is right-aligned to end at L (its
+// start may be negative, where TMA fills zeros), so no position past the
+// filled prefix is ever loaded.
+__device__ __forceinline__ int64_t tile_start(int64_t tt, int64_t L) {
+    const int64_t y0 = tt * TT;
+    return y0 + TT > L ? L - TT : y0;
+}
+
+static_assert(sizeof(Bars) <= 512, "barrier block overlaps the reduction scratch");
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Two int8 codes (bytes k and k+1 of w) -> two bf16 holding the same integers,
+// exactly: byte ^ 0x80 = code + 128 in [0, 255] becomes the low mantissa
+// byte of the float 1.5 * 2^23 + code + 128, from which the constant is
+// subtracted exactly; integers of magnitude <= 128 are exact in bf16.
+__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int k) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float base = 12582912.f + 128.f;
+    const float f0 = __uint_as_float(__byte_perm(u, 0x4B400000u, 0x7650 | k)) - base;
+    const float f1 = __uint_as_float(__byte_perm(u, 0x4B400000u, 0x7650 | (k + 1))) - base;
+    return pack_bf16x2(f0, f1);
+}
+
+__device__ __forceinline__ int ld_acquire(const int32_t *ptr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+    __nv_bfloat16 h = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t *>(&h);
+}
+
+__device__ __forceinline__ void set_abort(Bars *bs, const Params &p) {
+    bs->abort_flag = 1;
+    atomicOr(p.status, kDevTimeout);
+}
+
+// A wait that gives up records where (read back by fd_get_device_diagnostics):
+// status[1..3] = site, tile counter and piece index of the first one in the
+// launch; status[4 + 3r .. 6 + 3r] the same for the first failing wait of
+// role r (0 producer, 1 MMA issuer, 2 softmax), so a stall shows what every
+// role was blocked on when the block gave up.
+__device__ __forceinline__ void note_timeout(Bars *bs, const Params &p, int site,
+                                             uint32_t tile, int piece) {
+    if (!bs->abort_flag && atomicCAS(p.status + 1, 0, site) == 0) {
+        p.status[2] = (int)tile;
+        p.status[3] = piece;
+    }
+    const int role = (site == 1 || site == 8) ? 0 : (site <= 7 ? 1 : 2);
+    if (atomicCAS(p.status + 4 + 3 * role, 0, site) == 0) {
+        p.status[5 + 3 * role] = (int)tile;
+        p.status[6 + 3 * role] = piece;
+    }
+    set_abort(bs, p);
+}
+
+// One block's share of the merge of split segment sw.s (blocks c0 .. c1 hold
+// its pieces) in a cooperative launch: wait until every piece has arrived,
+// merge units [share*U/P, (share+1)*U/P) of the rows x (D/4) float4 units from
+// the pieces' workspace slots (running maximum per row, pieces in order),
+// store them, and count the share done (the last one resets the counter).
+// Kept out of line so that its registers do not weigh on the tile loop.
+template <int D, bool GA, int SMT>
+__device__ __noinline__ bool share_merge_segment(const Params &p, Bars *bs, Walk sw, int c0, int c1,
+                                                 int c, int tid, uint32_t &sm_ctr, int k, int piece) {
+    volatile int *abort_flag = &bs->abort_flag;
+    auto sm_sync = [&]() -> bool {
+        ptx::mbar_arrive(&bs->sm_bar);
+        if (ptx::mbar_wait(&bs->sm_bar, (sm_ctr++) & 1, abort_flag, kWaitNs)) return true;
+        note_timeout(bs, p, 14, 0, piece);
+        return false;
+    };
+    const int64_t sg = sw.s;
+    const int P = c1 - c0 + 1, share = c - c0;
+    const int kSoftmaxThreads = SMT;
+    bool ok;
+    if (tid == 0) {
+        const uint64_t t0 = ptx::globaltimer_ns();
+        for (uint32_t n = 0; ld_acquire(p.counters + sg) < P; ++n) {
+            __nanosleep(64);
+            if ((n & 63) == 63 &&
+                (*abort_flag || ptx::globaltimer_ns() - t0 > kWaitNs)) {
+                note_timeout(bs, p, 15, (uint32_t)k, piece);
+                break;
+            }
+        }
+    }
+    ok = sm_sync() && !*abort_flag;
+    if (!ok) return false;
+    __threadfence();
+    const int rows = p.rows;
+    constexpr int UPR = D / 4;                    // float4 units per row
+    const int64_t U = (int64_t)rows * UPR;
+    const int64_t u0 = U * share / P, u1 = U * (share + 1) / P;
+    for (int64_t u = u0 + tid; u < u1; u += kSoftmaxThreads) {
+        const int r = (int)(u / UPR), dq = (int)(u % UPR) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float M = neg_inf(), Ls = 0.f;
+#pragma unroll 4
+        for (int c2 = c0; c2 <= c1; ++c2) {
+            const float *sl = slot_ptr(p, sg, c2);
+            const float mv = __ldcg(sl + rows * D + r), lv = __ldcg(sl + rows * D + rows + r);
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(sl + r * D + dq));
+            const float mn = fmaxf(M, mv);
+            const float mu = mn == neg_inf() ? 0.f : mn;
+            const float a = fast_exp2(M - mu), wv = fast_exp2(mv - mu);
+            // (the same roundings as the last arriver's merge, bit for bit)
+            M = mn;
+            Ls = __fmaf_rn(wv, lv, Ls * a);
+            acc.x = __fmaf_rn(wv, v.x, acc.x * a);
+            acc.y = __fmaf_rn(wv, v.y, acc.y * a);
+            acc.z = __fmaf_rn(wv, v.z, acc.z * a);
+            acc.w = __fmaf_rn(wv, v.w, acc.w * a);
+        }
+        const int qi = GA ? sw.i : r % p.n_q, h = sw.hk * p.g + (GA ? r : r / p.n_q);
+        const int64_t off = (int64_t)sw.b * p.os[0] + (int64_t)qi * p.os[1] +
+                            (int64_t)h * p.os[2] + dq;
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        const float o4[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (p.out_f32)
+                reinterpret_cast<float *>(p.out)[off + e] = o4[e];
+            else
+                reinterpret_cast<uint16_t *>(p.out)[off + e] = bf16_bits(o4[e]);
+        }
+    }
+    ok = sm_sync();
+    if (!ok) return false;
+    if (tid == 0 && atomicAdd(p.counters + sg, 1) == 2 * P - 1) p.counters[sg] = 0;
+    return true;
+}
+
+template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG>
+__global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant__ TcArgs a) {
+    static_assert(!(GA && PG), "gather and paged loads are separate modes");
+    using C = Cfg<D, N, I8, NV, GA>;
+    constexpr int kSoftmaxThreads = C::SMT;
+    const Params &p = a.p;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const uint32_t smem_base = ptx::smem_u32(smem);
+    Bars *bs = reinterpret_cast<Bars *>(smem);
+    float *red = reinterpret_cast<float *>(smem + 512);   // per group [2][4][NH]
+    // Row tables: element offset of packed row r in out, one table per piece
+    // parity (a group may start the next piece while a lagging warp of it
+    // still stores the previous one).
+    int64_t *otbl = reinterpret_cast<int64_t *>(smem + C::OFF_TBL);
+    volatile int *abort_flag = &bs->abort_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x, c = blockIdx.x;
+    // The swizzled operand layouts need 1024-byte aligned buffers; the
+    // dynamic shared window starts aligned, and a block that finds otherwise
+    // reports it instead of computing.
+    if (smem_base & 1023u) {
+        if (tid == 0) atomicOr(p.status, kDevTimeout);
+        return;
+    }
+
+    // Segments with nothing to attend still need their output rows zeroed.
+    for (int64_t s = c; s < p.nseg; s += G)
+        if ((GA ? tiles_of(p.idx_len) : tiles_of(seq_len(p, (int)(s / p.Hkv)))) == 0)
+            zero_segment(p, s);
+    // The producer warp finds the block's tile range and first piece while
+    // the others set up barriers and TMEM.
+    if (warp == kProducerWarp) {
+        const int64_t tot = total_units_tc(p);
+        Walk w{};
+        int64_t tb = 0, te = 0;
+        bool has = false;
+        if (tot > 0) {
+            const int32_t Gw = working_blocks(tot, G);
+            if (c < Gw) {
+                const Split sp{tot, Gw};
+                tb = sp.start(c);
+                te = sp.start(c + 1);
+                has = tb < te && first_piece_warp(p, tb, &w) && w.first < te;
+            }
+        }
+        if (lane == 0) {
+            bs->total = tot;
+            bs->t_begin = tb;
+            bs->t_end = te;
+            bs->walk = w;
+            bs->has_work = has;
+        }
+    }
+    if (tid == 0) {
+        // bf16 slots are filled by TMA (one arrival plus bytes) or, for int8
+        // caches, by the 128 widening threads.
+        for (int i = 0; i < C::NS; ++i) {
+            ptx::mbar_init(&bs->slot_full[i], I8 ? 128 : 1);
+            ptx::mbar_init(&bs->slot_empty[i], 1);
+        }
+        for (int i = 0; i < C::NR; ++i) {
+            ptx::mbar_init(&bs->raw_full[i], 1);
+            ptx::mbar_init(&bs->raw_empty[i], 128);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&bs->s_full[i], 1);
+            ptx::mbar_init(&bs->s_free[i], kSoftmaxThreads);
+            ptx::mbar_init(&bs->p_full[i], kSoftmaxThreads);
+            ptx::mbar_init(&bs->p_free[i], 1);
+        }
+        ptx::mbar_init(&bs->q_full, 1);
+        ptx::mbar_init(&bs->q_free, 1);
+        ptx::mbar_init(&bs->o_done, 1);
+        ptx::mbar_init(&bs->o_free, kSoftmaxThreads);
+        ptx::mbar_init(&bs->exit_mma, 1);
+        ptx::mbar_init(&bs->sm_bar, kSoftmaxThreads);
+        for (int g = 0; g < C::GROUPS; ++g) ptx::mbar_init(&bs->wg_bar[g], 128);
+        bs->abort_flag = 0;
+        ptx::mbar_fence_init();
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(&bs->tmem_base, C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        ptx::prefetch_tmap(&a.tq);
+        ptx::prefetch_tmap(&a.tk);
+        ptx::prefetch_tmap(&a.tv);
+    }
+    // P rows NV..N-1 are never written: zero them once.
+    if (NV < N && tid < kSoftmaxThreads) {
+        for (uint32_t e = tid; e < C::PST * C::PSTAGE / 16; e += kSoftmaxThreads)
+            *reinterpret_cast<uint4 *>(smem + C::OFF_P + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+        ptx::fence_proxy_async_smem();
+    }
+    // Padding rows (p.rows .. N-1) of the Q operand stay zero: the Q copies
+    // write only the segment's rows.
+    if (tid < kSoftmaxThreads && p.rows < N) {
+        const int per = (N - p.rows) * 8;    // 16-byte chunks per 64-column box
+        for (int e = tid; e < C::KB * per; e += kSoftmaxThreads) {
+            const int cb = e / per, rem = e - cb * per;
+            *reinterpret_cast<uint4 *>(smem + C::OFF_Q + cb * C::QB + (p.rows + rem / 8) * 128 +
+                                       (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        ptx::fence_proxy_async_smem();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bs->tmem_base;
+    const bool has_work = bs->has_work != 0;
+    const int64_t t_begin = bs->t_begin, t_end = bs->t_end;
+    const Split sp{bs->total, has_work ? working_blocks(bs->total, G) : 1};
+    // Shared merges (SH instantiations, cooperative launch): every block of a
+    // split segment merges a share of it, which pays off when blocks stream
+    // few tiles each (the last arriver's merge of many small pieces would be
+    // the launch's tail); with longer ranges the last arriver merges.
+    const bool share_merge = SH && p.coop && sp.total <= 4 * (int64_t)sp.G;
+    const uint32_t q_addr = smem_base + C::OFF_Q;
+    const uint32_t p_addr = smem_base + C::OFF_P;
+
+    if (!has_work) {
+        // nothing to stream: straight to the exit
+    } else if (warp == kProducerWarp) {
+        // ------------------------------------------------------ TMA producer
+        uint32_t issued = 0;
+        bool ok = true;
+        int piece = 0;
+        Walk w = bs->walk;
+        int64_t t = max(t_begin, w.first);
+        while (ok) {
+            const int64_t piece_end = min(t_end, w.first + w.ntiles);
+            const int b = w.b, hk = w.hk;
+            const int64_t L = w.L;
+            // The segment's Q rows, once the previous piece's last QK has read
+            // the buffer: one box per 64 columns covering query indices
+            // 0..n_q-1 of query heads hk*g .. hk*g+g-1, which lands row
+            // r = (head offset) * n_q + (query index), K-major with the
+            // 128-byte swizzle the QK descriptors expect.
+            if (lane == 0) {
+                if (piece > 0) {
+                    ok = ptx::mbar_wait(&bs->q_free, (piece - 1) & 1, abort_flag, kWaitNs);
+                    if (!ok) note_timeout(bs, p, 8, issued, piece);
+                }
+                if (ok) {
+                    // (gather: the list's one query row, box (64, 1, g, 1))
+                    ptx::mbar_arrive_expect_tx(&bs->q_full, (uint32_t)(C::KB * p.rows * 128));
+#pragma unroll
+                    for (int cb = 0; cb < C::KB; ++cb)
+                        ptx::tma_load_4d(smem + C::OFF_Q + cb * C::QB, &a.tq, &bs->q_full, cb * 64,
+                                         GA ? w.i : 0, hk * p.g, b);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            // Fill order = MMA consumption order: K(a); then K(t+1), V(t) for
+            // t = a .. b-1; then V(b) (a, b: first and last tile of the piece).
+            // The ring is then a plain FIFO, and each K tile is requested one
+            // tile period before its QK needs it.
+            const int64_t n_in = piece_end - t, tt0 = t - w.first;
+            // gather: lane l fetches positions 4l .. 4l+3 of each tile, rows of
+            // the 2-D cache maps (-1, read as zeros, for padding, cells past the
+            // list or out of range); the next K tile's rows are read ahead.
+            // paged: the same, with the rows of positions 4l .. 4l+3 found
+            // through the block table (-1 past the length or for a bad page).
+            const int32_t *ilist = GA ? p.idx + ((int64_t)b * p.n_q + w.i) * p.idx_len : nullptr;
+            const int64_t segrow = GA ? (int64_t)b * a.gs0 + (int64_t)hk * a.gs1 : (int64_t)hk * a.gs1;
+            int yk[4] = {-1, -1, -1, -1}, yv0[4] = {-1, -1, -1, -1}, yv1[4] = {-1, -1, -1, -1};
+            auto list_rows = [&](int64_t tile, int *y) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int64_t pos = tile * TT + 4 * lane + r;
+                    y[r] = -1;
+                    if (GA && pos < p.idx_len) {
+                        const int x = __ldg(ilist + pos);
+                        if (x >= 0 && x < p.cap) y[r] = (int)(segrow + (int64_t)x * a.gs2);
+                    }
+                    if (PG && pos < L) {
+                        const int32_t pg = page_of(p, b, (int32_t)pos);
+                        if (pg >= 0)
+                            y[r] = (int)(segrow + (int64_t)pg * a.gs0 +
+                                         (int64_t)((int32_t)pos % p.page_size) * a.gs2);
+                    }
+                }
+            };
+            if (GA || PG) list_rows(tt0, yk);
+            for (int64_t step = 0; step < 2 * n_in && ok; ++step) {
+                int64_t j;
+                int kv;
+                if (step == 0) { j = 0; kv = 0; }
+                else if (step == 2 * n_in - 1) { j = n_in - 1; kv = 1; }
+                else { j = (step + 1) / 2 - (step & 1 ? 0 : 1); kv = step & 1 ? 0 : 1; }
+                const int ys = (int)tile_start(tt0 + j, L);
+                if (GA || PG) {
+                    // rows of this fill: K(j) takes the prefetched rows (kept
+                    // for V(j)), then the next tile's are requested
+                    int y[4];
+                    if (kv == 0) {
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            y[r] = yk[r];
+                            if (j & 1) yv1[r] = yk[r]; else yv0[r] = yk[r];
+                        }
+                        if (j + 1 < n_in) list_rows(tt0 + j + 1, yk);
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) y[r] = (j & 1) ? yv1[r] : yv0[r];
+                    }
+                    if (!I8) {
+                        const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
+                        if (lane == 0) {
+                            ok = ptx::mbar_wait(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+                            if (!ok) note_timeout(bs, p, 1, issued, 0);
+                            else ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
+                        }
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (ok) {
+                            unsigned char *dst = smem + C::OFF_SLOTS + slot * C::SLOT + 4 * lane * 128;
+#pragma unroll
+                            for (int cb = 0; cb < C::KB; ++cb)
+                                ptx::tma_gather4(dst + cb * C::BOX, kv ? (const void *)&a.tv
+                                                                       : (const void *)&a.tk,
+                                                 &bs->slot_full[slot], cb * 64, y[0], y[1], y[2], y[3]);
+                        }
+                    } else {
+                        // int8 pages: the four rows' codes (one 128-byte box
+                        // each) into the raw ring
+                        const uint32_t rs = issued % C::NRX, ph = (issued / C::NRX) & 1;
+                        if (lane == 0) {
+                            ok = ptx::mbar_wait(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
+                            if (!ok) note_timeout(bs, p, 1, issued, 0);
+                            else ptx::mbar_arrive_expect_tx(&bs->raw_full[rs], C::RAW);
+                        }
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (ok)
+                            ptx::tma_gather4(smem + C::OFF_RAW + rs * C::RAW + 4 * lane * 128,
+                                             kv ? (const void *)&a.tv : (const void *)&a.tk,
+                                             &bs->raw_full[rs], 0, y[0], y[1], y[2], y[3]);
+                    }
+                } else if (lane == 0 && I8) {
+                    // int8 codes -> raw ring (one box of TT positions x D codes)
+                    const uint32_t rs = issued % C::NRX, ph = (issued / C::NRX) & 1;
+                    ok = ptx::mbar_wait(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
+                    if (!ok) note_timeout(bs, p, 1, issued, 0);
+                    if (ok) {
+                        ptx::mbar_arrive_expect_tx(&bs->raw_full[rs], C::RAW);
+                        ptx::tma_load_4d(smem + C::OFF_RAW + rs * C::RAW,
+                                         kv ? (const void *)&a.tv : (const void *)&a.tk,
+                                         &bs->raw_full[rs], 0, ys, hk, b);
+                    }
+                } else if (lane == 0) {
+                    const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
+                    ok = ptx::mbar_wait(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+                    if (!ok) note_timeout(bs, p, 1, issued, 0);
+                    if (ok) {
+                        ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
+                        unsigned char *dst = smem + C::OFF_SLOTS + slot * C::SLOT;
+#pragma unroll
+                        for (int cb = 0; cb < C::KB; ++cb)
+                            ptx::tma_load_4d(dst + cb * C::BOX, kv ? (const void *)&a.tv
+                                                                   : (const void *)&a.tk,
+                                             &bs->slot_full[slot], cb * 64, ys, hk, b);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (ok) ++issued;
+            }
+            ++piece;
+            if (piece_end >= t_end || !next_piece(p, w) || w.first >= t_end) break;
+            t = w.first;
+        }
+        // Drain: every issued copy must land before the block exits.
+        if (lane == 0) {
+            constexpr uint32_t RING = I8 ? (uint32_t)C::NRX : (uint32_t)C::NS;
+            const uint32_t n = issued < RING ? issued : RING;
+            for (uint32_t k = 0; k < n; ++k) {
+                const uint32_t idx = issued - 1 - k;
+                ptx::mbar_wait(I8 ? &bs->raw_full[idx % RING] : &bs->slot_full[idx % RING],
+                               (idx / RING) & 1, abort_flag, kWaitNs);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // -------------------------------------------------------- MMA issuer
+        uint32_t tile_ctr = 0;
+        int piece = 0;
+        bool ok = true;
+        bool issued_any = false;
+        uint32_t pa = 0, pb = 0;   // first and last tile number of the current piece
+        // S^T[pos, row] = sum_d K[pos, d] Q[row, d] for tile number tc.
+        auto issue_qk = [&](uint32_t tc) -> bool {
+            const uint32_t sb = tc & 1, u = tc >> 1, ki = k_fill(tc, pa), ks = ki % C::NS;
+            if (!ptx::mbar_wait(&bs->slot_full[ks], (ki / C::NS) & 1, abort_flag, kWaitNs)) {
+                note_timeout(bs, p, 3, tc, piece);
+                return false;
+            }
+            if (!ptx::mbar_wait(&bs->s_free[sb], (u & 1) ^ 1, abort_flag, kWaitNs)) {
+                note_timeout(bs, p, 4, tc, piece);
+                return false;
+            }
+            ptx::tc_fence_after();
+            const uint32_t k_addr = smem_base + C::OFF_SLOTS + ks * C::SLOT;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t da = ptx::smem_desc(k_addr + (kk >> 2) * C::BOX + (kk & 3) * 32, 16,
+                                                   1024, ptx::kLayoutSwizzle128);
+                const uint64_t db = ptx::smem_desc(q_addr + (kk >> 2) * C::QB + (kk & 3) * 32, 16,
+                                                   1024, ptx::kLayoutSwizzle128);
+                ptx::mma_f16_ss(tmem + sb * N, da, db, C::IDESC_QK, kk > 0);
+            }
+            ptx::mma_commit(&bs->slot_empty[ks]);
+            ptx::mma_commit(&bs->s_full[sb]);
+            issued_any = true;
+            return true;
+        };
+        // O^T[dim, row] += sum_pos V[pos, dim] (P_hi + P_lo)[row, pos] for tile tc.
+        auto issue_pv = [&](uint32_t tc, bool first) -> bool {
+            const uint32_t vi = v_fill(tc, pb), vs = vi % C::NS;
+            const uint32_t ps = tc % C::PST, pu = tc / C::PST;
+            if (!ptx::mbar_wait(&bs->slot_full[vs], (vi / C::NS) & 1, abort_flag, kWaitNs)) {
+                note_timeout(bs, p, 6, tc, piece);
+                return false;
+            }
+            if (!ptx::mbar_wait(&bs->p_full[ps], pu & 1, abort_flag, kWaitNs)) {
+                note_timeout(bs, p, 7, tc, piece);
+                return false;
+            }
+            ptx::tc_fence_after();
+            const uint32_t v_addr = smem_base + C::OFF_SLOTS + vs * C::SLOT;
+            const uint32_t pb = p_addr + ps * C::PSTAGE;
+            const bool two_planes = p.out_f32 != 0;
+            // O^T += V^T P_hi^T (+ V^T P_lo^T for fp32 outputs)
+            auto pv_tiles = [&](auto planes) {
+                constexpr int NP = decltype(planes)::value;
+#pragma unroll
+                for (int dc = 0; dc < C::DC; ++dc) {
+#pragma unroll
+                    for (int kt = 0; kt < TT / 16; ++kt) {
+                        const uint64_t da = ptx::smem_desc(v_addr + (2 * dc) * C::BOX + kt * 2048,
+                                                           C::BOX, 1024, ptx::kLayoutSwizzle128);
+#pragma unroll
+                        for (int pl = 0; pl < NP; ++pl) {
+                            const uint64_t db = ptx::smem_desc(pb + pl * C::PPLANE + kt * 512,
+                                                               C::PATOM, 256, ptx::kLayoutSwizzle32);
+                            ptx::mma_f16_ss(tmem + 2 * N + dc * N, da, db, C::IDESC_PV,
+                                            (first && kt == 0 && pl == 0) ? 0u : 1u);
+                        }
+                    }
+                }
+            };
+            if (two_planes) pv_tiles(std::integral_constant<int, 2>());
+            else pv_tiles(std::integral_constant<int, 1>());
+            ptx::mma_commit(&bs->slot_empty[vs]);
+            ptx::mma_commit(&bs->p_free[ps]);
+            ptx::mma_commit(&bs->o_done);
+            return true;
+        };
+        Walk w = bs->walk;
+        int64_t t = max(t_begin, w.first);
+        while (ok) {
+            const int64_t piece_end = min(t_end, w.first + w.ntiles);
+            const uint32_t n_in = (uint32_t)(piece_end - t);
+            pa = tile_ctr;
+            pb = tile_ctr + n_in - 1;
+            if (lane == 0) {
+                // Software pipeline: QK of tile j+1 is issued before PV of
+                // tile j, so the next scores are ready when softmax finishes.
+                ok = ptx::mbar_wait(&bs->q_full, piece & 1, abort_flag, kWaitNs);
+                if (!ok) note_timeout(bs, p, 2, tile_ctr, piece);
+                ptx::tc_fence_after();
+                ok = ok && issue_qk(tile_ctr);
+                if (ok && n_in == 1) ptx::mma_commit(&bs->q_free);
+                for (uint32_t j = 0; j < n_in && ok; ++j) {
+                    if (j + 1 < n_in) {
+                        ok = issue_qk(tile_ctr + j + 1);
+                        if (!ok) break;
+                        if (j + 2 == n_in) ptx::mma_commit(&bs->q_free);
+                    }
+                    if (j == 0 && piece > 0) {
+                        ok = ptx::mbar_wait(&bs->o_free, (piece - 1) & 1, abort_flag, kWaitNs);
+                        if (!ok) note_timeout(bs, p, 5, tile_ctr, piece);
+                    }
+                    ok = ok && issue_pv(tile_ctr + j, j == 0);
+                }
+                if (!ok) set_abort(bs, p);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            tile_ctr += n_in;
+            ++piece;
+            if (piece_end >= t_end || !next_piece(p, w) || w.first >= t_end) break;
+            t = w.first;
+        }
+        // Drain: all MMAs issued by this thread complete before TMEM is freed.
+        if (lane == 0 && issued_any) {
+            ptx::mma_commit(&bs->exit_mma);
+            ptx::mbar_wait(&bs->exit_mma, 0, abort_flag, kWaitNs);
+        }
+    } else if (I8 && warp >= 4) {
+        // ------------------------------------- int8 -> bf16 widening (warps 4-7)
+        // Fill f of the raw ring becomes fill f of the bf16 slot ring, in the
+        // producer's order.  Codes widen exactly (|code| <= 127 has 8
+        // significant bits); the per-position scales are applied to the
+        // scores and to P by the softmax group, so nothing here rounds.
+        // Raw tile: row-major [TT][D] codes.  bf16 tile: KB boxes of
+        // [TT][64] with the 128-byte swizzle (16-byte chunk c of position r
+        // at c ^ (r & 7)), exactly what a TMA load of a bf16 cache produces.
+        const int ct = tid - 128;
+        uint32_t f = 0;
+        bool ok = true;
+        int piece = 0;
+        Walk w = bs->walk;
+        int64_t t = max(t_begin, w.first);
+        while (ok) {
+            const int64_t piece_end = min(t_end, w.first + w.ntiles);
+            const int64_t n_fill = 2 * (piece_end - t);
+            for (int64_t k = 0; k < n_fill && ok; ++k, ++f) {
+                const uint32_t rs = f % C::NRX, ss = f % C::NS;
+                ok = ptx::mbar_wait(&bs->raw_full[rs], (f / C::NRX) & 1, abort_flag, kWaitNs);
+                if (!ok) { note_timeout(bs, p, 17, f, piece); break; }
+                // Thread ct takes 16 codes (dims 16*q16 .. 16*q16+15) of
+                // positions r0 + RSTEP*k: one 16-byte load and two swizzled
+                // 16-byte stores each, all loads issued first.  Each group of
+                // 8 threads covers half of two rows, its low half of one and
+                // high half of the other, so its 8 loads and each of its two
+                // sets of 8 stores fall in 8 different bank groups.
+                constexpr int QPR = D / 16, RSTEP = 128 / QPR, NK = TT / RSTEP;
+                static_assert(!I8 || QPR == 8, "widening layout is for 128-code rows");
+                const int quarter = ct >> 3, tq = ct & 7;
+                const int r0 = 2 * (quarter >> 1) + (tq >> 2);
+                const int q16 = (tq & 3) + 4 * ((tq >> 2) ^ (quarter & 1));
+                // (raw rows are 128 bytes with the 128-byte swizzle: chunk q16 of
+                // row r sits at q16 ^ (r & 7), and r & 7 == r0 & 7 here)
+                static_assert(!I8 || D == 128, "int8 tiles: one 128-byte row per position");
+                const unsigned char *raw = smem + C::OFF_RAW + rs * C::RAW + r0 * D + ((q16 ^ (r0 & 7)) << 4);
+                unsigned char *dst = smem + C::OFF_SLOTS + ss * C::SLOT + (q16 >> 2) * C::BOX +
+                                     r0 * 128;
+                // (r0 + RSTEP*k) & 7 == r0 & 7: the swizzled chunk offsets are per thread
+                const int sw0 = (((2 * q16) & 7) ^ (r0 & 7)) << 4, sw1 = (((2 * q16 + 1) & 7) ^ (r0 & 7)) << 4;
+                uint4 cw[NK];
+#pragma unroll
+                for (int k = 0; k < NK; ++k)
+                    cw[k] = *reinterpret_cast<const uint4 *>(raw + k * RSTEP * D);
+                // The raw slot is free for the next copy once the codes are
+                // in registers; then wait for a bf16 slot the MMAs released.
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(&bs->raw_empty[rs]);
+                ok = ptx::mbar_wait(&bs->slot_empty[ss], ((f / C::NS) & 1) ^ 1, abort_flag, kWaitNs);
+                if (!ok) { note_timeout(bs, p, 18, f, piece); break; }
+#pragma unroll
+                for (int k = 0; k < NK; ++k) {
+                    unsigned char *row = dst + k * RSTEP * 128;
+                    *reinterpret_cast<uint4 *>(row + sw0) =
+                        make_uint4(i8x2_to_bf16x2(cw[k].x, 0), i8x2_to_bf16x2(cw[k].x, 2),
+                                   i8x2_to_bf16x2(cw[k].y, 0), i8x2_to_bf16x2(cw[k].y, 2));
+                    *reinterpret_cast<uint4 *>(row + sw1) =
+                        make_uint4(i8x2_to_bf16x2(cw[k].z, 0), i8x2_to_bf16x2(cw[k].z, 2),
+                                   i8x2_to_bf16x2(cw[k].w, 0), i8x2_to_bf16x2(cw[k].w, 2));
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(&bs->slot_full[ss]);
+            }
+            if (!ok) { set_abort(bs, p); break; }
+            ++piece;
+            if (piece_end >= t_end || !next_piece(p, w) || w.first >= t_end) break;
+            t = w.first;
+        }
+    } else {
+        // ------------------------------------------- softmax and epilogue
+        // Two warpgroups split the query rows: group wg owns rows
+        // [wg*NH, wg*NH + NH), i.e. those columns of S^T, O^T and P.  Thread
+        // wt of a group owns TMEM lane wt: cache position wt of the tile.
+        constexpr int NH = C::NH;
+        const int wg = warp >> 2, wwarp = warp & 3, wt = tid & 127;
+        const int cb0 = wg * NH;                  // first row (column) of the group
+        const uint32_t lane_base = (uint32_t)(wwarp * 32) << 16;
+        float *gred = red + wg * C::RED_GROUP;    // the group's reduction scratch
+        uint32_t tile_ctr = 0;
+        uint32_t o_seen = 0;      // o_done phases observed, consumed strictly in order
+        uint32_t wg_ctr = 0;      // uses of the group barrier
+        uint32_t sm_ctr = 0;      // uses of the two-group barrier
+        int piece = 0;
+        bool ok = true;
+        // Completion of PV number k (k = 0, 1, ...), phase by phase.  Every
+        // tile consumes the previous tile's phase before publishing its own P,
+        // so the barrier is never more than one phase ahead of this wait and
+        // the parity test cannot alias.
+        auto wait_pv = [&](uint32_t k) -> bool {
+            for (; o_seen <= k; ++o_seen)
+                if (!ptx::mbar_wait(&bs->o_done, o_seen & 1, abort_flag, kWaitNs)) {
+                    note_timeout(bs, p, 11, tile_ctr, piece);
+                    return false;
+                }
+            return true;
+        };
+        // Barrier over this warpgroup's 128 threads, bounded.
+        auto wg_sync = [&]() -> bool {
+            ptx::mbar_arrive(&bs->wg_bar[wg]);
+            if (ptx::mbar_wait(&bs->wg_bar[wg], (wg_ctr++) & 1, abort_flag, kWaitNs)) return true;
+            note_timeout(bs, p, 10, tile_ctr, piece);
+            return false;
+        };
+        // Barrier over both warpgroups, bounded.
+        auto sm_sync = [&]() -> bool {
+            ptx::mbar_arrive(&bs->sm_bar);
+            if (ptx::mbar_wait(&bs->sm_bar, (sm_ctr++) & 1, abort_flag, kWaitNs)) return true;
+            note_timeout(bs, p, 14, tile_ctr, piece);
+            return false;
+        };
+        Walk w = bs->walk;
+        int64_t t = max(t_begin, w.first);
+        while (ok) {
+            const int64_t s = w.s;
+            const int64_t piece_end = min(t_end, w.first + w.ntiles);
+            const int64_t n_in = piece_end - t;
+            const int64_t tt0 = t - w.first;
+            const int64_t L = w.L;
+            const int rows = p.rows;
+
+            // Output offsets of this group's rows (one division sequence per
+            // row, so the unrolled per-row code below needs none) and the
+            // causal limit of each row.  The Q rows arrive by TMA.
+            int64_t *ooff = otbl + (piece & 1) * N;
+            if (share_merge && tid == 0) bs->walk_last = w;
+            if (wt < NH && cb0 + wt < rows) {
+                // (gather: the list's query row, head offset r)
+                const int r = cb0 + wt;
+                const int i = GA ? w.i : r % p.n_q, h = w.hk * p.g + (GA ? r : r / p.n_q);
+                ooff[r] = (int64_t)w.b * p.os[0] + (int64_t)i * p.os[1] + (int64_t)h * p.os[2];
+            }
+            int lim[NH];    // last visible position of each row
+            {
+                int qi = cb0 % p.n_q;
+#pragma unroll
+                for (int r = 0; r < NH; ++r) {
+                    lim[r] = p.causal ? (int)(L - p.n_q + qi) : (int)(L - 1);
+                    if (++qi == p.n_q) qi = 0;
+                }
+            }
+
+            float mrun[NH], lpart[NH];
+#pragma unroll
+            for (int r = 0; r < NH; ++r) { mrun[r] = neg_inf(); lpart[r] = 0.f; }
+
+            // int8 caches: this segment's per-position scales, read one tile
+            // ahead (k scale multiplies the scores, v scale multiplies P but
+            // not the row sums; nothing outside the filled prefix is read).
+            // (paged: scales live beside their rows, page pg_n, row tok % page_size)
+            const int64_t sb0 = PG ? 0 : (int64_t)w.b;
+            const float *ksrow = I8 ? p.k_scale + sb0 * p.kss[0] + (int64_t)w.hk * p.kss[1] : nullptr;
+            const float *vsrow = I8 ? p.v_scale + sb0 * p.vss[0] + (int64_t)w.hk * p.vss[1] : nullptr;
+            // paged: the pool page of this thread's position, read one tile
+            // ahead (-1 past the length, or for a table entry outside the pool)
+            int pg_n = -1;
+            auto load_page = [&](int64_t jj) {
+                const int64_t tok = (tt0 + jj) * TT + wt;
+                pg_n = tok < L ? page_of(p, w.b, (int32_t)tok) : -1;
+            };
+            if (PG) load_page(0);
+            float ksc_n = 1.f, vsc_n = 1.f;
+            auto load_scales = [&](int64_t jj) {
+                if (PG) {
+                    const int64_t tok = (tt0 + jj) * TT + wt;
+                    if (pg_n >= 0) {
+                        const int64_t r = (int32_t)tok % p.page_size;
+                        ksc_n = __ldg(ksrow + (int64_t)pg_n * p.kss[0] + r * p.kss[2]);
+                        vsc_n = __ldg(vsrow + (int64_t)pg_n * p.vss[0] + r * p.vss[2]);
+                    }
+                } else {
+                    const int64_t tok = tile_start(tt0 + jj, L) + wt;
+                    if (tok >= (tt0 + jj) * TT && tok < L) {
+                        ksc_n = __ldg(ksrow + tok * p.kss[2]);
+                        vsc_n = __ldg(vsrow + tok * p.vss[2]);
+                    }
+                }
+            };
+            if (I8) load_scales(0);
+            // gather: the list cell this lane's position holds, read one tile
+            // ahead; a cell is visible if 0 <= cell < cap (cap or more is
+            // flagged FD_DEV_BAD_INDEX, negative is padding).
+            const int32_t *ilist = GA ? p.idx + ((int64_t)w.b * p.n_q + w.i) * p.idx_len : nullptr;
+            int cell_n = -1;
+            auto load_cell = [&](int64_t jj) {
+                const int64_t pos = (tt0 + jj) * TT + wt;
+                cell_n = pos < p.idx_len ? __ldg(ilist + pos) : -1;
+            };
+            if (GA) load_cell(0);
+            for (int64_t j = 0; j < n_in && ok; ++j) {
+                const int64_t y0 = (tt0 + j) * TT;
+                const int64_t token = (GA || PG) ? y0 + wt : tile_start(tt0 + j, L) + wt;
+                const uint32_t sb = tile_ctr & 1, u = tile_ctr >> 1;
+                // Visibility: a position this tile owns (the right-aligned last
+                // tile also holds positions the previous tile covered), inside
+                // the filled prefix and, for causal windows, at or before
+                // L - n_q + i for the row's query index i.  Gather: a valid
+                // cell of the list.  Paged: a position on a page of the pool.
+                bool in_len = token >= y0 && token < L;
+                if (GA) {
+                    const int cell = cell_n;
+                    if (j + 1 < n_in) load_cell(j + 1);
+                    if (cell >= p.cap) atomicOr(p.status, kDevBadIndex);
+                    in_len = in_len && cell >= 0 && cell < p.cap;
+                }
+                if (PG) {
+                    in_len = in_len && pg_n >= 0;
+                    if (j + 1 < n_in) load_page(j + 1);
+                }
+                const float ksc = ksc_n, vsc = vsc_n;
+                if (I8 && j + 1 < n_in) load_scales(j + 1);
+                ok = ptx::mbar_wait(&bs->s_full[sb], u & 1, abort_flag, kWaitNs);
+                if (!ok) { note_timeout(bs, p, 9, tile_ctr, piece); break; }
+                ptx::tc_fence_after();
+                float sv[NH];
+                ptx::tmem_ld_cols<NH>(tmem + lane_base + sb * N + cb0, sv);
+                ptx::tmem_wait_ld();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&bs->s_free[sb]);
+
+                const float sl = I8 ? p.scale_log2 * ksc : p.scale_log2;
+#pragma unroll
+                for (int r = 0; r < NH; ++r) {
+                    const bool vis = in_len && cb0 + r < rows && token <= lim[r];
+                    sv[r] = vis ? sv[r] * sl : neg_inf();
+                }
+                // Refresh the running maxima only when some score passes
+                // mrun + kRescaleSlack (always on a segment's first tile).
+                bool need = false;
+#pragma unroll
+                for (int r = 0; r < NH; ++r) need = need || (sv[r] > mrun[r] + kRescaleSlack);
+                need = __any_sync(0xffffffffu, need);
+                if (lane == 0) bs->vote[wg][tile_ctr & 1][wwarp] = need;
+                ok = wg_sync();
+                if (!ok) break;
+                const int *vt = bs->vote[wg][tile_ctr & 1];
+                if (vt[0] | vt[1] | vt[2] | vt[3]) {
+                    // Column maxima over the 128 positions of the tile.
+                    float *rb = gred + (tile_ctr & 1) * (4 * NH);
+#pragma unroll
+                    for (int r = 0; r < NH; ++r) {
+                        const float mx = warp_max(sv[r]);
+                        if (lane == 0) rb[wwarp * NH + r] = mx;
+                    }
+                    ok = wg_sync();
+                    if (!ok) break;
+                    float alpha[NH];
+                    bool grow = false;
+#pragma unroll
+                    for (int r = 0; r < NH; ++r) {
+                        const float tmax = fmaxf(fmaxf(rb[r], rb[NH + r]),
+                                                 fmaxf(rb[2 * NH + r], rb[3 * NH + r]));
+                        // Only rows that passed their own threshold move,
+                        // so a row's arithmetic never depends on another
+                        // row's scores.
+                        const float mnew = tmax > mrun[r] + kRescaleSlack ? tmax : mrun[r];
+                        const float muse = mnew == neg_inf() ? 0.f : mnew;
+                        alpha[r] = fast_exp2(mrun[r] - muse);
+                        grow = grow || (alpha[r] < 1.f);
+                        mrun[r] = mnew;
+                        lpart[r] *= alpha[r];
+                    }
+                    // Rescale this group's columns of the running O in TMEM
+                    // (after the previous PV landed).
+                    if (grow && j > 0) {
+                        ok = wait_pv(tile_ctr - 1);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+#pragma unroll
+                        for (int dc = 0; dc < C::DC; ++dc) {
+                            float o[NH];
+                            const uint32_t ta = tmem + lane_base + 2 * N + dc * N + cb0;
+                            ptx::tmem_ld_cols<NH>(ta, o);
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < NH; ++k) o[k] *= alpha[k];
+                            ptx::tmem_st_cols<NH>(ta, o);
+                        }
+                        ptx::tmem_wait_st();
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < NH; ++r) {
+                    const float muse = mrun[r] == neg_inf() ? 0.f : mrun[r];
+                    const float pr = fast_exp2(sv[r] - muse);
+                    lpart[r] += pr;
+                    sv[r] = I8 ? pr * vsc : pr;
+                }
+                // P^T for the PV product.
+                const uint32_t ps = tile_ctr % C::PST, pu = tile_ctr / C::PST;
+                ok = ptx::mbar_wait(&bs->p_free[ps], (pu & 1) ^ 1, abort_flag, kWaitNs);
+                if (!ok) { note_timeout(bs, p, 13, tile_ctr, piece); break; }
+                // PV of the previous tile must have completed before P of this
+                // tile is published (see wait_pv).
+                if (tile_ctr > 0) {
+                    ok = wait_pv(tile_ctr - 1);
+                    if (!ok) break;
+                }
+                {
+                    // P = hi + lo, both bf16: hi = rn(p), lo = rn(p - hi), so the
+                    // PV product sees p to about 2^-17 relative, which fp32
+                    // outputs need; bf16 outputs (2^-9 themselves) take P_hi
+                    // alone, which halves the PV MMAs.  Thread wt
+                    // writes its position's row: 8 query rows per 16-byte chunk,
+                    // chunk c of a 16-row atom stored at c ^ bit 2 of wt.
+                    unsigned char *prow = smem + C::OFF_P + ps * C::PSTAGE + wt * 32;
+                    const int sw = (wt >> 2) & 1;
+#pragma unroll
+                    for (int l8 = 0; l8 < NH / 8; ++l8) {
+                        const int a8 = cb0 / 8 + l8;      // global 8-row group
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float p0 = sv[l8 * 8 + 2 * e], p1 = sv[l8 * 8 + 2 * e + 1];
+                            const uint32_t h = pack_bf16x2(p0, p1);
+                            hw[e] = h;
+                            lw[e] = pack_bf16x2(p0 - bf16lo(h), p1 - bf16hi(h));
+                        }
+                        const uint32_t off = (a8 >> 1) * C::PATOM + (((a8 & 1) ^ sw) << 4);
+                        *reinterpret_cast<uint4 *>(prow + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        if (p.out_f32)
+                            *reinterpret_cast<uint4 *>(prow + C::PPLANE + off) =
+                                make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&bs->p_full[ps]);
+                ++tile_ctr;
+            }
+            if (!ok) { set_abort(bs, p); break; }
+
+            // ------------------------------------------ segment epilogue
+            ok = wait_pv(tile_ctr - 1);
+            if (!ok) { set_abort(bs, p); break; }
+            ptx::tc_fence_after();
+            float o[C::DC][NH];
+#pragma unroll
+            for (int dc = 0; dc < C::DC; ++dc)
+                ptx::tmem_ld_cols<NH>(tmem + lane_base + 2 * N + dc * N + cb0, o[dc]);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bs->o_free);
+
+            // Row sums of P over the segment piece (this group's rows).
+            float *lb = gred + (tile_ctr & 1) * (4 * NH);
+#pragma unroll
+            for (int r = 0; r < NH; ++r) {
+                const float v = warp_sum(lpart[r]);
+                if (lane == 0) lb[wwarp * NH + r] = v;
+            }
+            ok = wg_sync();
+            float lsum[NH];
+#pragma unroll
+            for (int r = 0; r < NH; ++r) lsum[r] = lb[r] + lb[NH + r] + lb[2 * NH + r] + lb[3 * NH + r];
+            ok = ok && wg_sync();
+            if (!ok) { set_abort(bs, p); break; }
+
+            // Blocks sharing the segment (owner() only where the piece is
+            // cut at this block's range boundary).
+            const int c_first = w.first >= t_begin ? c : sp.owner(w.first);
+            const int c_last = w.first + w.ntiles <= t_end ? c : sp.owner(w.first + w.ntiles - 1);
+            if (c_first == c_last) {
+#pragma unroll
+                for (int r = 0; r < NH; ++r) {
+                    if (cb0 + r < rows) {
+                        const float inv = lsum[r] > 0.f ? 1.f / lsum[r] : 0.f;
+                        const int64_t off = ooff[cb0 + r];
+#pragma unroll
+                        for (int dc = 0; dc < C::DC; ++dc) {
+                            const float val = o[dc][r] * inv;
+                            if (p.out_f32)
+                                reinterpret_cast<float *>(p.out)[off + dc * 128 + wt] = val;
+                            else
+                                reinterpret_cast<uint16_t *>(p.out)[off + dc * 128 + wt] = bf16_bits(val);
+                        }
+                    }
+                }
+            } else {
+                float *slot = slot_ptr(p, s, c);
+#pragma unroll
+                for (int r = 0; r < NH; ++r) {
+                    if (cb0 + r < rows) {
+#pragma unroll
+                        for (int dc = 0; dc < C::DC; ++dc)
+                            slot[(cb0 + r) * D + dc * 128 + wt] = o[dc][r];
+                    }
+                }
+                // every thread of the group holds the same mrun / lsum values
+#pragma unroll
+                for (int r = 0; r < NH; ++r) {
+                    if (r == wt && cb0 + r < rows) {
+                        slot[rows * D + cb0 + r] = mrun[r];
+                        slot[rows * D + rows + cb0 + r] = lsum[r];
+                    }
+                }
+                __threadfence();
+                ok = sm_sync();
+                if (tid == 0 && ok) bs->last_flag = atomicAdd(p.counters + s, 1) == c_last - c_first;
+                ok = ok && sm_sync();
+                if (!ok) { set_abort(bs, p); break; }
+                const int r1w = min(cb0 + NH, rows);       // this group merges rows cb0 .. r1w-1
+                if (!share_merge && bs->last_flag && r1w > cb0) {
+                    __threadfence();
+                    // Merge the pieces' partials in one pass per row: running
+                    // maximum M, merged sum Ls and accumulator rescaled as each
+                    // piece arrives.  Thread -> 4 consecutive dims of rows
+                    // cb0 + rg + RG*k; row indices are clamped into range
+                    // (weight 0 beyond) so every load is unconditional and two
+                    // pieces' loads are in flight together.
+                    constexpr int TPR = D / 4, RG = 128 / TPR, RPT = NH / RG;
+                    constexpr int CH = RPT < 8 ? RPT : 8;
+                    const int dq = (wt % TPR) * 4, rg = wt / TPR;
+#pragma unroll 1
+                    for (int k0 = 0; k0 < RPT && cb0 + rg + RG * k0 < r1w; k0 += CH) {
+                        float4 acc[CH];
+                        float M[CH], Ls[CH];
+                        int rr[CH];
+#pragma unroll
+                        for (int k = 0; k < CH; ++k) {
+                            const int r = cb0 + rg + RG * (k0 + k);
+                            rr[k] = r < r1w ? r : r1w - 1;
+                            acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            M[k] = neg_inf();
+                            Ls[k] = 0.f;
+                        }
+                        // (one piece per iteration where the rows are many: the
+                        // merge runs once, from cold instruction caches, and a
+                        // smaller loop body measured faster there)
+#pragma unroll(C::MERGE_UNROLL)
+                        for (int c2 = c_first; c2 <= c_last; ++c2) {
+                            const float *sl = slot_ptr(p, s, c2);
+#pragma unroll
+                            for (int k = 0; k < CH; ++k) {
+                                const float mv = __ldcg(sl + rows * D + rr[k]);
+                                const float lv = __ldcg(sl + rows * D + rows + rr[k]);
+                                const float4 v =
+                                    __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + dq));
+                                const float mn = fmaxf(M[k], mv);
+                                const float mu = mn == neg_inf() ? 0.f : mn;
+                                const float a = fast_exp2(M[k] - mu), w = fast_exp2(mv - mu);
+                                // (explicit roundings: the shared merge computes
+                                // the same values bit for bit)
+                                M[k] = mn;
+                                Ls[k] = __fmaf_rn(w, lv, Ls[k] * a);
+                                acc[k].x = __fmaf_rn(w, v.x, acc[k].x * a);
+                                acc[k].y = __fmaf_rn(w, v.y, acc[k].y * a);
+                                acc[k].z = __fmaf_rn(w, v.z, acc[k].z * a);
+                                acc[k].w = __fmaf_rn(w, v.w, acc[k].w * a);
+                            }
+                        }
+#pragma unroll
+                        for (int k = 0; k < CH; ++k) {
+                            const int r = cb0 + rg + RG * (k0 + k);
+                            if (r < r1w) {
+                                const int64_t off = ooff[r] + dq;
+                                const float inv = Ls[k] > 0.f ? 1.f / Ls[k] : 0.f;
+                                const float o4[4] = {acc[k].x * inv, acc[k].y * inv, acc[k].z * inv,
+                                                     acc[k].w * inv};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    if (p.out_f32)
+                                        reinterpret_cast<float *>(p.out)[off + e] = o4[e];
+                                    else
+                                        reinterpret_cast<uint16_t *>(p.out)[off + e] = bf16_bits(o4[e]);
+                                }
+                            }
+                        }
+                    }
+                }
+                if (!share_merge && bs->last_flag && tid == 0) p.counters[s] = 0;
+            }
+            ++piece;
+            if (piece_end >= t_end || !next_piece(p, w) || w.first >= t_end) break;
+            t = w.first;
+        }
+        // Cooperative launch: merge this block's share of each split segment
+        // it worked on (only a range's first and last pieces can be split),
+        // once every piece of it has arrived.  Arrivals never wait and all
+        // blocks are resident, so every wait ends.  The segment counter then
+        // counts the finished shares; the last one resets it.
+        if (ok && share_merge) ok = sm_sync();   // both groups see walk_last
+#pragma unroll 1
+        for (int k = 0; k < 2 && ok && share_merge; ++k) {
+            if (k == 1 && piece < 2) break;
+            const Walk sw = k == 0 ? bs->walk : bs->walk_last;
+            if (sw.first >= t_begin && sw.first + sw.ntiles <= t_end) continue;   // whole
+            const int c0 = sw.first >= t_begin ? c : sp.owner(sw.first);
+            const int c1 = sw.first + sw.ntiles <= t_end ? c : sp.owner(sw.first + sw.ntiles - 1);
+            ok = share_merge_segment<D, GA, kSoftmaxThreads>(p, bs, sw, c0, c1, c, tid, sm_ctr, k, piece);
+            if (!ok) { set_abort(bs, p); break; }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ------------------------------------------------------------- host side
+// [B, Hkv, cap, d] cache -> 4-D map (d, cap, Hkv, B); rows past the capacity
+// (or before 0) read as zeros.  bf16: box (64, 128, 1, 1) with the 128-byte
+// swizzle the MMA descriptors expect.  int8 (d = 128): the same 128-byte rows
+// (64 pairs of codes), also 128-byte swizzled (the widening threads read it).
+inline bool make_map(CUtensorMap *m, const void *base, const int64_t *st, const Params &p) {
+    // (int8 codes are moved as pairs: 16-bit elements, d / 2 per row)
+    const int es = p.kv_int8 ? 1 : 2;
+    const cuuint64_t row_elems = p.kv_int8 ? (cuuint64_t)p.d / 2 : (cuuint64_t)p.d;
+    cuuint64_t dims[4] = {row_elems, (cuuint64_t)p.cap, (cuuint64_t)p.Hkv, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {(cuuint64_t)(st[2] * es), (cuuint64_t)(st[1] * es),
+                             (cuuint64_t)(st[0] * es)};
+    cuuint32_t box[4] = {64u, (cuuint32_t)TT, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return encode_cached(m, p.kv_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         4, const_cast<void *>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
+}
+
+// [B, n_q, Hq, d] queries -> 4-D map (d, n_q, Hq, B), box (64, n_q, g, 1):
+// one box holds a segment's packed rows for 64 columns (gather: box
+// (64, 1, g, 1), the g heads of one query row).
+inline bool make_qmap(CUtensorMap *m, const Params &p) {
+    cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)p.n_q, (cuuint64_t)p.Hq, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {(cuuint64_t)p.qs[1] * 2, (cuuint64_t)p.qs[2] * 2,
+                             (cuuint64_t)p.qs[0] * 2};
+    cuuint32_t box[4] = {64, p.mode == kGather ? 1u : (cuuint32_t)p.n_q, (cuuint32_t)p.g, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(p.q), dims,
+                         strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
+}
+
+// Gather: the cache seen as 2-D rows (d, Y) of stride rs elements, with rs
+// the smallest of the three outer strides (each a multiple of it); gather4
+// loads read one 64-column, one-row box per listed cell.
+inline bool gather_rows(const Params &p, int64_t *rs, int64_t *Y, int64_t g[3]) {
+    const int64_t *st = p.ks;
+    if (p.vs[0] != st[0] || p.vs[1] != st[1] || p.vs[2] != st[2]) return false;
+    int64_t r = st[0];
+    for (int k = 1; k < 3; ++k) r = st[k] < r ? st[k] : r;
+    if (r < p.d) return false;
+    for (int k = 0; k < 3; ++k)
+        if (st[k] % r) return false;
+    g[0] = st[0] / r;
+    g[1] = st[1] / r;
+    g[2] = st[2] / r;
+    *rs = r;
+    *Y = (int64_t)(p.B - 1) * g[0] + (int64_t)(p.Hkv - 1) * g[1] + (p.cap - 1) * g[2] + 1;
+    return *Y < ((int64_t)1 << 31);
+}
+
+inline bool make_gmap(CUtensorMap *m, const void *base, const Params &p, int64_t rs, int64_t Y) {
+    cuuint64_t dims[2] = {(cuuint64_t)p.d, (cuuint64_t)Y};
+    cuuint64_t strides[1] = {(cuuint64_t)rs * 2};
+    cuuint32_t box[2] = {64, 1};
+    cuuint32_t estr[2] = {1, 1};
+    return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
+}
+
+// Blocks of this instantiation that can be resident at once on the current
+// device (0 on error); sets the dynamic shared memory opt-in the first time.
+template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG>
+int resident_blocks() {
+    using C = Cfg<D, N, I8, NV, GA>;
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int n = cached[dev].load(std::memory_order_acquire);
+    if (n > 0) return n;
+    int per_sm = 0, sms = 0;
+    if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV, GA, SH, PG>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_kernel<D, N, I8, NV, GA, SH, PG>,
+                                                      kThreadsTC, C::SMEM) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    n = per_sm * sms;
+    cached[dev].store(n, std::memory_order_release);
+    return n;
+}
+
+template <int D, int N, bool I8, int NV = N, bool GA = false, bool SH = false, bool PG = false>
+int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
+    using C = Cfg<D, N, I8, NV, GA>;
+    if (resident_blocks<D, N, I8, NV, GA, SH, PG>() <= 0) return -5;
+    if (!SH) {
+        tc_kernel<D, N, I8, NV, GA, SH, PG><<<G, kThreadsTC, C::SMEM, st>>>(args);
+        return cudaGetLastError() == cudaSuccess ? 0 : -5;
+    }
+    // shared merges: a cooperative launch (the caller checked the grid fits)
+    TcArgs ca = args;
+    ca.p.coop = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)G);
+    cfg.blockDim = dim3(kThreadsTC);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_kernel<D, N, I8, NV, GA, SH, PG>, ca) == cudaSuccess ? 0 : -5;
+}
+
+}  // namespace
+
+}  // namespace fd

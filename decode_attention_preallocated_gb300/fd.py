@@ -6,8 +6,9 @@ stream.  There is no fallback: if libfd.so is missing or cannot be loaded,
 every call raises.
 
 Low-level names mirror the C ABI (``fd_decode``, ``fd_decode_int8``,
-``fd_decode_gather``, ``fd_workspace_create`` ...) and take ``FdTensor`` /
-``FdOpts`` structures; ``decode``, ``decode_int8`` and ``decode_gather`` take
+``fd_decode_paged``, ``fd_decode_gather``, ``fd_workspace_create`` ...) and
+take ``FdTensor`` / ``FdOpts`` structures; ``decode``, ``decode_int8``,
+``decode_paged`` and ``decode_gather`` take
 torch tensors, allocate ``out`` with torch when it is not given, and keep one
 workspace per (device, stream).
 """
@@ -70,6 +71,10 @@ _SIGNATURES = [
     ("fd_decode_gather", ctypes.c_int,
      [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_int32,
       _P(FdTensor), _P(FdOpts)]),
+    ("fd_decode_paged", ctypes.c_int,
+     [_P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor),
+      ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+      ctypes.c_float, _P(FdTensor), _P(FdOpts)]),
     ("fd_decode_noalloc", ctypes.c_int,
      [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_int32,
       ctypes.c_int32, ctypes.c_float, _P(FdTensor), ctypes.c_void_p, ctypes.c_int32]),
@@ -354,6 +359,40 @@ def decode_int8(q, k_cache, v_cache, k_scale, v_scale, kv_lengths, n_q=None,
                                   kv_lengths.data_ptr(), int(n_q), int(bool(causal)),
                                   float(scale), ctypes.byref(to), ctypes.byref(o))
     _check(rc, "fd_decode_int8")
+    return out
+
+
+def decode_paged(q, k_pages, v_pages, block_table, kv_lengths, n_q=None,
+                 causal=False, scale=None, k_scale=None, v_scale=None, out=None,
+                 out_dtype=torch.bfloat16, num_ctas=0, kernel=FD_KERNEL_AUTO,
+                 stream=None, workspace: Optional[Workspace] = None):
+    """As ``decode`` (or ``decode_int8``) over a paged cache: pools
+    k_pages / v_pages [num_pages, Hkv, page_size, d] (bf16, or int8 with fp32
+    scales [num_pages, Hkv, page_size]) and block_table [B, max_pages] (int32,
+    contiguous, on the device): position j of sequence b is row
+    j % page_size of page block_table[b, j // page_size]."""
+    B, nq, Hq, d = q.shape
+    n_q = nq if n_q is None else n_q
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if (not block_table.is_contiguous() or block_table.dtype != torch.int32
+            or block_table.dim() != 2 or block_table.shape[0] != B):
+        raise ValueError("block_table must be a contiguous int32 [B, max_pages] tensor")
+    Hkv = k_pages.shape[1]
+    rows = (Hq // max(Hkv, 1)) * nq
+    out, sh, ws = _prepare(q, k_pages, out, out_dtype, B * Hkv, rows, num_ctas,
+                           kernel, stream, workspace)
+    tq, tk, tv, to = map(as_fd_tensor, (q, k_pages, v_pages, out))
+    pks = pvs = None
+    if k_scale is not None or v_scale is not None:
+        tks, tvs = as_fd_tensor(k_scale), as_fd_tensor(v_scale)
+        pks, pvs = ctypes.byref(tks), ctypes.byref(tvs)
+    o = _opts(sh, ws, num_ctas, kernel)
+    with _on_device(q.device):
+        rc = lib().fd_decode_paged(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                   pks, pvs, block_table.data_ptr(), int(block_table.shape[1]),
+                                   kv_lengths.data_ptr(), int(n_q), int(bool(causal)),
+                                   float(scale), ctypes.byref(to), ctypes.byref(o))
+    _check(rc, "fd_decode_paged")
     return out
 
 

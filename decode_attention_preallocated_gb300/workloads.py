@@ -21,6 +21,9 @@ rounded to bf16 with round-to-nearest-even by ``Tensor.to``):
 * ``int8``       -- 4 sequences x 131072 tokens, int8 K/V quantised per
   (token, kv head) with fp32 scales, 1 query row, 32 / 8 heads,
   head_dim 128.
+* ``paged_ps<P>`` / ``paged_int8_ps<P>`` -- the ragged / int8 workloads over
+  a paged cache: pools of P-position pages, every sequence's pages scattered
+  over the pool by a seeded permutation (``paged_inputs``).
 
 The ComfyUI issue's cache is "prompt + max_length + 7" long with only the
 answer-so-far filled ("Qwen3.5 text generation attends over the full KV
@@ -51,12 +54,18 @@ class DecodeInputs:
     idx: Optional[torch.Tensor] = None       # [B, n_q, K] int32 (gather only)
     lengths_host: list = field(default_factory=list)
     name: str = ""
+    # paged caches: k, v (and the scales) are pools [num_pages, Hkv, page_size,
+    # ...]; position j of sequence b is row j % page_size of page
+    # block_table[b, j // page_size]
+    block_table: Optional[torch.Tensor] = None   # [B, max_pages] int32
+    page_size: int = 0
 
     @property
     def shape(self):
         B, n_q, Hq, d = self.q.shape
-        return dict(B=B, n_q=n_q, Hq=Hq, Hkv=self.k.shape[1], d=d,
-                    cap=self.k.shape[2])
+        cap = (self.block_table.shape[1] * self.page_size if self.block_table is not None
+               else self.k.shape[2])
+        return dict(B=B, n_q=n_q, Hq=Hq, Hkv=self.k.shape[1], d=d, cap=cap)
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -177,6 +186,62 @@ def gather_inputs(B, n_q, Hq, Hkv, d, cap, K, recent, seed, device="cpu",
                         idx=idx.to(device), lengths_host=[cap] * B, name=name)
 
 
+def paged_inputs(B, n_q, Hq, Hkv, d, page_size, max_pages, lengths, seed, causal,
+                 device="cpu", layout="bhtd", spare_pages=3, tail="randn",
+                 int8=False, name="") -> DecodeInputs:
+    """Seeded decode inputs over a paged cache.
+
+    Pools k, v: [num_pages, Hkv, page_size, d] with num_pages =
+    B * max_pages + spare_pages (layout "bthd" stores [num_pages, page_size,
+    Hkv, d] and returns the transposed view); int8 pools are written by
+    ``quantize_per_token`` with fp32 scales [num_pages, Hkv, page_size].
+    block_table [B, max_pages]: the first B * max_pages entries of a seeded
+    permutation of the pool's pages, so a sequence's consecutive positions
+    sit on scattered pages and the spare pages belong to no sequence.
+    tail="nan"/"inf" poisons every pool row that holds no position below its
+    sequence's length (the spare pages included).
+    """
+    gen = _gen(seed, "cpu" if str(device) == "cpu" else device)
+    q = randn_bf16((B, n_q, Hq, d), gen, device)
+    P = B * max_pages + spare_pages
+    if int8:
+        src_k = make_cache(P, Hkv, page_size, d, gen, device, layout, torch.float32)
+        src_v = make_cache(P, Hkv, page_size, d, gen, device, layout, torch.float32)
+        k, ks = quantize_per_token(src_k)
+        v, vs = quantize_per_token(src_v)
+        if layout == "bthd":
+            k = k.transpose(1, 2).contiguous().transpose(1, 2)
+            v = v.transpose(1, 2).contiguous().transpose(1, 2)
+        del src_k, src_v
+    else:
+        k = make_cache(P, Hkv, page_size, d, gen, device, layout)
+        v = make_cache(P, Hkv, page_size, d, gen, device, layout)
+        ks = vs = None
+    cpu_gen = _gen(seed + 104729, "cpu")
+    table = torch.randperm(P, generator=cpu_gen)[: B * max_pages].view(B, max_pages)
+    table = table.to(torch.int32)
+    lengths = [int(x) for x in lengths]
+    if tail in ("nan", "inf"):
+        used = torch.zeros((P, page_size), dtype=torch.bool)
+        for b, L in enumerate(lengths):
+            for j in range(max(0, min(L, max_pages * page_size))):
+                used[int(table[b, j // page_size]), j % page_size] = True
+        free = (~used).to(k.device)
+        if int8:
+            # int8 codes cannot hold NaN; poison the scales instead
+            ks[free.unsqueeze(1).expand_as(ks)] = float(tail)
+            vs[free.unsqueeze(1).expand_as(vs)] = float(tail)
+        else:
+            m = free.unsqueeze(1).unsqueeze(-1).expand_as(k)
+            k[m] = float(tail)
+            v[m] = float("nan") if tail == "nan" else -float("inf")
+    lens = torch.tensor(lengths, dtype=torch.int32, device=device)
+    return DecodeInputs(q=q, k=k, v=v, kv_lengths=lens, n_q=n_q, causal=bool(causal),
+                        scale=1.0 / math.sqrt(d), k_scale=ks, v_scale=vs,
+                        lengths_host=lengths, name=name, block_table=table.to(device),
+                        page_size=page_size)
+
+
 def ragged_lengths(B, lo, hi, seed):
     g = _gen(seed, "cpu")
     return torch.randint(lo, hi + 1, (B,), generator=g).tolist()
@@ -202,7 +267,21 @@ def workload(name: str, seed: int = 1, device="cpu", tail="randn",
     if name == "int8":
         return dense_inputs(4, 1, 32, 8, 128, 131072, [131072] * 4, seed, False,
                             device, layout, tail, int8=True, name=name)
+    if name.startswith("paged_ps"):
+        # the ragged workload over a paged cache of page_size positions
+        ps = int(name[len("paged_ps"):])
+        lens = ragged_lengths(8, 1024, 32768, seed)
+        return paged_inputs(8, 6, 16, 4, 256, ps, 32768 // ps, lens, seed, True, device,
+                            layout, tail=tail, name=name)
+    if name.startswith("paged_int8_ps"):
+        # the int8 workload over a paged cache of page_size positions
+        ps = int(name[len("paged_int8_ps"):])
+        return paged_inputs(4, 1, 32, 8, 128, ps, 131072 // ps, [131072] * 4, seed, False,
+                            device, layout, tail=tail, int8=True, name=name)
     raise KeyError(name)
 
 
 WORKLOADS = ("dense_1k", "mtp_verify", "ragged", "gather", "int8")
+# The ragged and int8 workloads over paged caches (page size 64 for bf16,
+# 256 for int8; other page sizes by name, e.g. "paged_ps16").
+PAGED_WORKLOADS = ("paged_ps64", "paged_int8_ps256")

@@ -17,6 +17,7 @@
  *     drafts already written at L-n_q .. L-1) and row i sees 0 .. L-n_q+i
  *     (same issue, list item 2 and "Existing Solutions": a bottom-right
  *     aligned causal window, up to 6 rows).
+ *     fd_decode_paged computes the same over a paged cache.
  *   - fd_decode_gather: V = the cells listed for that (b, i) in idx
  *     ("attend the selected cells instead of masking the window",
  *     llama.cpp #28244, Conversation; "gather-based sparse attention for
@@ -162,6 +163,35 @@ int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache,
                      int32_t idx_len, const fd_tensor *out,
                      const fd_opts *opts);
 
+/*
+ * Dense prefix decode over a paged cache: the same visible set, causal
+ * window and result as fd_decode / fd_decode_int8, but cache position j of
+ * sequence b lives in a pool of fixed-size pages, at row j % page_size of
+ * page block_table[b * max_pages + j / page_size] (comfy-kitchen #239,
+ * commit list and Description: a bounded paged int8 decode cache with
+ * rollback).  Rolling a sequence back needs only a smaller kv_lengths[b];
+ * pages past the length are never read.
+ *   k_pages, v_pages: [num_pages, Hkv, page_size, d] bf16 or int8 (both the
+ *     same), any strides that are multiples of 16 bytes, so the token-major
+ *     pool [num_pages, page_size, Hkv, d] works through a transpose.
+ *   k_scale, v_scale: NULL for bf16 pools; for int8 pools fp32
+ *     [num_pages, Hkv, page_size] (any strides), one scale per cached row.
+ *   block_table: device int32 [B, max_pages], contiguous, caller-owned.
+ *     The logical capacity is cap = max_pages * page_size (below 2^31);
+ *     kv_lengths[b] is clamped to [0, cap] (FD_DEV_BAD_LENGTH).  Only the
+ *     entries of pages that hold positions < kv_lengths[b] are read; such an
+ *     entry outside [0, num_pages) skips that page's positions and sets
+ *     FD_DEV_BAD_INDEX.
+ *   Other arguments as fd_decode.  The tensor-core kernel serves pools whose
+ *   three outer strides are multiples of the smallest, itself at least d
+ *   (every contiguous layout), with the row limits of the flat caches.
+ */
+int fd_decode_paged(const fd_tensor *q, const fd_tensor *k_pages,
+                    const fd_tensor *v_pages, const fd_tensor *k_scale,
+                    const fd_tensor *v_scale, const int32_t *block_table,
+                    int32_t max_pages, const int32_t *kv_lengths, int32_t n_q,
+                    int32_t causal, float scale, const fd_tensor *out,
+                    const fd_opts *opts);
 /*
  * Dense prefix decode that allocates nothing (no counterpart in the paper).
  *

@@ -195,6 +195,67 @@ def dense(q, k, v, kv_lengths, n_q, causal, scale, k_scale=None,
     return out
 
 
+def paged(q, k_pages, v_pages, block_table, kv_lengths, n_q, causal, scale,
+          k_scale=None, v_scale=None, _lib_override=None):
+    """fp64 attention over a paged cache: the dense prefix definition with
+    one indirection (comfy-kitchen #239, commit list and Description: a
+    bounded paged int8 decode cache with rollback).
+
+    Position j of sequence b is row j % page_size of pool page
+    block_table[b, j // page_size].  Pools k_pages, v_pages are
+    [num_pages, Hkv, page_size, d] (bf16, or int8 with fp32 scales
+    [num_pages, Hkv, page_size]); block_table [B, max_pages] int32 and
+    kv_lengths [B] int32 are host values.  The visible positions of query
+    row i are those of ``dense`` -- j < L_b with L_b clamped to
+    [0, max_pages * page_size], and j <= L_b - n_q + i for causal windows --
+    minus the positions on a page whose table entry is outside
+    [0, num_pages).
+
+    Each sequence's logical cache is assembled row by row from the pool,
+    and each (sequence, query row)'s visible positions are handed to
+    ``gather`` as its list.  Returns float64 [B, n_q, Hq, d].
+    """
+    qa = _as_np(q)
+    ka, va, ksa, vsa, int8 = _kv_args(k_pages, v_pages, k_scale, v_scale)
+    B, nq_, Hq, d = qa.shape
+    if nq_ != n_q:
+        raise ValueError("q.shape[1] != n_q")
+    P, Hkv, ps, d2 = ka.shape
+    if d2 != d or va.shape != ka.shape:
+        raise ValueError("shape mismatch")
+    table = np.asarray(_as_np(block_table), dtype=np.int64)
+    if table.ndim != 2 or table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_pages]")
+    max_pages = table.shape[1]
+    cap = max_pages * ps
+    lens = np.clip(np.asarray(_as_np(kv_lengths), dtype=np.int64).reshape(B), 0, cap)
+    # logical caches [B, Hkv, cap, d]: position j <- pool[page(j), :, j % ps, :]
+    j = np.arange(cap)
+    page = table[:, j // ps]                      # [B, cap]
+    on_pool = (page >= 0) & (page < P)
+    pg = np.where(on_pool, page, 0)
+    row = np.broadcast_to(j % ps, pg.shape)
+    k_log = np.ascontiguousarray(np.transpose(ka[pg, :, row, :], (0, 2, 1, 3)))
+    v_log = np.ascontiguousarray(np.transpose(va[pg, :, row, :], (0, 2, 1, 3)))
+    ks_log = vs_log = None
+    if int8:
+        ks_log = np.ascontiguousarray(np.transpose(ksa[pg, :, row], (0, 2, 1)))
+        vs_log = np.ascontiguousarray(np.transpose(vsa[pg, :, row], (0, 2, 1)))
+    # visible positions of each (sequence, query row), padded with -1
+    lists = []
+    for b in range(B):
+        L = int(lens[b])
+        for i in range(n_q):
+            last = L - n_q + i if causal else L - 1
+            lists.append(np.nonzero(on_pool[b, :max(0, min(L, last + 1))])[0])
+    K = max(1, max(len(c) for c in lists))
+    idx = np.full((B * n_q, K), -1, dtype=np.int32)
+    for r, cells in enumerate(lists):
+        idx[r, :len(cells)] = cells
+    return gather(qa, k_log, v_log, idx.reshape(B, n_q, K), scale, ks_log, vs_log,
+                  _lib_override=_lib_override)
+
+
 def gather(q, k, v, idx, scale, k_scale=None, v_scale=None,
            _lib_override=None):
     """fp64 attention over the cache rows named by ``idx`` [B, n_q, K].

@@ -16,7 +16,7 @@ def to_dev(inp, device="cuda"):
     """Copy a DecodeInputs to the GPU (keeping strided cache layouts)."""
     import copy
     out = copy.copy(inp)
-    for name in ("q", "kv_lengths", "k_scale", "v_scale", "idx"):
+    for name in ("q", "kv_lengths", "k_scale", "v_scale", "idx", "block_table"):
         t = getattr(inp, name)
         if t is not None:
             setattr(out, name, t.to(device))
@@ -42,7 +42,12 @@ def run_gpu(inp, out_dtype=torch.bfloat16, num_ctas=0, kernel=fd.FD_KERNEL_AUTO,
         Hkv = inp.k.shape[1]
         workspace = fd.Workspace(B * n_q * Hkv, min(64, (Hq // Hkv) * n_q), 256,
                                  max(2048, num_ctas))
-    if inp.idx is not None:
+    if inp.block_table is not None:
+        out = fd.decode_paged(inp.q, inp.k, inp.v, inp.block_table, inp.kv_lengths,
+                              n_q=inp.n_q, causal=inp.causal, scale=inp.scale,
+                              k_scale=inp.k_scale, v_scale=inp.v_scale, out_dtype=out_dtype,
+                              num_ctas=num_ctas, kernel=kernel, workspace=workspace)
+    elif inp.idx is not None:
         out = fd.decode_gather(inp.q, inp.k, inp.v, inp.idx, scale=inp.scale,
                                out_dtype=out_dtype, num_ctas=num_ctas, kernel=kernel,
                                workspace=workspace)
@@ -66,6 +71,10 @@ def run_gpu(inp, out_dtype=torch.bfloat16, num_ctas=0, kernel=fd.FD_KERNEL_AUTO,
 
 
 def run_oracle(inp):
+    if inp.block_table is not None:
+        return torch.from_numpy(oracle.paged(inp.q, inp.k, inp.v, inp.block_table.cpu(),
+                                             inp.kv_lengths.cpu(), inp.n_q, inp.causal,
+                                             inp.scale, inp.k_scale, inp.v_scale))
     if inp.idx is not None:
         return torch.from_numpy(oracle.gather(inp.q, inp.k, inp.v, inp.idx, inp.scale))
     lens = inp.kv_lengths.cpu()

@@ -132,6 +132,39 @@ def test_int8_and_gather_validation(L):
     assert rc == fd.FD_ERR_ARG
 
 
+def call_paged(q, k, v, out, table=0x400000, max_pages=4, ks=None, vs=None, n_q=1,
+               causal=0, lens=0x200000):
+    op = fd.FdOpts()
+    return fd.lib().fd_decode_paged(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+                                    ctypes.byref(ks) if ks is not None else None,
+                                    ctypes.byref(vs) if vs is not None else None,
+                                    table, max_pages, lens, n_q, causal, 0.1,
+                                    ctypes.byref(out), ctypes.byref(op))
+
+
+def test_paged_validation(L):
+    # pools [num_pages, Hkv, page_size, d]; the batch comes from q
+    q, _, _, o = fake([3, 1, 8, 128]), None, None, fake([3, 1, 8, 128])
+    kp = fake([10, 2, 16, 128])
+    assert call_paged(q, kp, kp, o) == fd.FD_ERR_WORKSPACE        # valid up to the workspace
+    assert call_paged(q, kp, kp, o, table=None) == fd.FD_ERR_ARG
+    assert call_paged(q, kp, kp, o, max_pages=0) == fd.FD_ERR_ARG
+    assert call_paged(q, kp, kp, o, lens=None) == fd.FD_ERR_ARG
+    assert call_paged(q, kp, kp, o, causal=2) == fd.FD_ERR_ARG
+    assert call_paged(q, kp, fake([10, 2, 8, 128]), o) == fd.FD_ERR_ARG   # k / v pools differ
+    assert call_paged(q, fake([0, 2, 16, 128]), fake([0, 2, 16, 128]), o) == fd.FD_ERR_ARG
+    assert call_paged(q, kp, kp, o, max_pages=(1 << 31) // 16) == fd.FD_ERR_UNSUPPORTED
+    ks = fake([10, 2, 16], fd.FD_F32)
+    assert call_paged(q, kp, kp, o, ks=ks, vs=ks) == fd.FD_ERR_ARG    # scales on a bf16 pool
+    k8 = fake([10, 2, 16, 128], fd.FD_I8)
+    assert call_paged(q, k8, k8, o, ks=ks, vs=ks) == fd.FD_ERR_WORKSPACE
+    assert call_paged(q, k8, k8, o) == fd.FD_ERR_ARG                  # int8 pool, no scales
+    bad = fake([10, 2, 15], fd.FD_F32)
+    assert call_paged(q, k8, k8, o, ks=bad, vs=ks) == fd.FD_ERR_ARG
+    k2 = fake([10, 2, 16, 128], strides=[2 * 16 * 132, 16 * 132, 132, 1])
+    assert call_paged(q, k2, k2, o) == fd.FD_ERR_ALIGN
+
+
 def test_workspace_size_formula(L):
     n = L.fd_workspace_bytes(10, 24, 256, 300)
     floats = (10 + 300) * 24 * 258
