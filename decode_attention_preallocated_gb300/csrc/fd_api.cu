@@ -211,6 +211,9 @@ int run(const Call &c) {
         p.page_size = (int32_t)rows_per;
         p.max_pages = c.max_pages;
         p.num_pages = c.k->shape[0];
+        p.page_shift = -1;
+        for (int sh = 0; sh < 31; ++sh)
+            if (((int64_t)1 << sh) == rows_per) p.page_shift = sh;
     }
     p.out = c.out->data;
     p.counters = ws->counters;

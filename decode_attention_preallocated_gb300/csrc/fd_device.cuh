@@ -51,11 +51,20 @@ __device__ __forceinline__ int64_t seq_len(const Params &p, int b) {
     return clamp_len(L, p.cap);
 }
 
-// Paged caches: the pool page that holds logical position pos (< cap) of
-// sequence b, or -1, with FD_DEV_BAD_INDEX set, when the table entry names no
-// page of the pool (the position is then skipped).
+// Paged caches: which page of its sequence logical position pos falls on,
+// and its row in that page (shifts for power-of-two page sizes).
+__device__ __forceinline__ int32_t page_slot(const Params &p, int32_t pos) {
+    return p.page_shift >= 0 ? pos >> p.page_shift : pos / p.page_size;
+}
+__device__ __forceinline__ int32_t page_row(const Params &p, int32_t pos) {
+    return p.page_shift >= 0 ? pos & (p.page_size - 1) : pos % p.page_size;
+}
+
+// The pool page that holds logical position pos (< cap) of sequence b, or
+// -1, with FD_DEV_BAD_INDEX set, when the table entry names no page of the
+// pool (the position is then skipped).
 __device__ __forceinline__ int32_t page_of(const Params &p, int b, int32_t pos) {
-    const int32_t e = __ldg(p.block_table + (int64_t)b * p.max_pages + pos / p.page_size);
+    const int32_t e = __ldg(p.block_table + (int64_t)b * p.max_pages + page_slot(p, pos));
     if (e < 0 || e >= p.num_pages) {
         atomicOr(p.status, kDevBadIndex);
         return -1;

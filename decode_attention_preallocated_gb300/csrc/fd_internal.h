@@ -48,6 +48,7 @@ struct Params {
     // strides are then (page, kv head, row in page); cap = max_pages * page_size
     const int32_t *block_table;
     int32_t page_size, max_pages;
+    int32_t page_shift;    // log2(page_size) when it is a power of two, else -1
     int64_t num_pages;
     void *out;             int64_t os[4];
     // workspace

@@ -163,7 +163,7 @@ simt_kernel(const __grid_constant__ Params p) {
                     const int32_t pg = page_of(p, b, (int32_t)pos);
                     ok = pg >= 0;
                     o0 = pg;
-                    o2 = pos % p.page_size;
+                    o2 = page_row(p, (int32_t)pos);
                 }
                 tpos[tid] = ok ? pos : 0;
                 tval[tid] = ok;

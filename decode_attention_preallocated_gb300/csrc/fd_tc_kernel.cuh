@@ -156,8 +156,14 @@ struct TcArgs {   // CUtensorMap members carry their own alignment
     CUtensorMap tq;
     Params p;
     // gather: cache row (b, hk, pos) is row b*gs0 + hk*gs1 + pos*gs2 of tk / tv;
-    // paged: pool row (page, hk, r) is row page*gs0 + hk*gs1 + r*gs2
+    // paged: pool row (page, hk, r) is row page*gs0 + hk*gs1 + r*gs2 of gk / gv
     int64_t gs0, gs1, gs2;
+    // paged: tk / tv are 4-D maps of the pool (d, page_size, Hkv, num_pages)
+    // with box (64, prow, 1, 1); a tile wholly inside the length is TT / prow
+    // such boxes (prow = 0: every tile is gathered row by row)
+    CUtensorMap gk;
+    CUtensorMap gv;
+    int32_t prow;
 };
 
 template <int D, int N, bool I8, int NV, bool GA = false>
@@ -605,6 +611,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         ptx::prefetch_tmap(&a.tq);
         ptx::prefetch_tmap(&a.tk);
         ptx::prefetch_tmap(&a.tv);
+        if (PG) {
+            ptx::prefetch_tmap(&a.gk);
+            ptx::prefetch_tmap(&a.gv);
+        }
     }
     // P rows NV..N-1 are never written: zero them once.
     if (NV < N && tid < kSoftmaxThreads) {
@@ -681,7 +691,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             // the 2-D cache maps (-1, read as zeros, for padding, cells past the
             // list or out of range); the next K tile's rows are read ahead.
             // paged: the same, with the rows of positions 4l .. 4l+3 found
-            // through the block table (-1 past the length or for a bad page).
+            // through the block table (-1 past the length or for a bad page),
+            // for the segment's partial last tile only; a tile wholly inside
+            // the length is read with tiled box loads, one per run of prow
+            // rows on one page: lane s < TT / prow holds run s's page (-1 for
+            // a bad entry, which reads as zeros) and first row.
             const int32_t *ilist = GA ? p.idx + ((int64_t)b * p.n_q + w.i) * p.idx_len : nullptr;
             const int64_t segrow = GA ? (int64_t)b * a.gs0 + (int64_t)hk * a.gs1 : (int64_t)hk * a.gs1;
             int yk[4] = {-1, -1, -1, -1}, yv0[4] = {-1, -1, -1, -1}, yv1[4] = {-1, -1, -1, -1};
@@ -698,11 +712,28 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         const int32_t pg = page_of(p, b, (int32_t)pos);
                         if (pg >= 0)
                             y[r] = (int)(segrow + (int64_t)pg * a.gs0 +
-                                         (int64_t)((int32_t)pos % p.page_size) * a.gs2);
+                                         (int64_t)page_row(p, (int32_t)pos) * a.gs2);
                     }
                 }
             };
-            if (GA || PG) list_rows(tt0, yk);
+            int rk_pg = -1, rk_rw = 0, rv_pg0 = -1, rv_rw0 = 0, rv_pg1 = -1, rv_rw1 = 0;
+            auto tiled_tile = [&](int64_t tile) { return PG && a.prow > 0 && (tile + 1) * TT <= L; };
+            auto page_runs = [&](int64_t tile) {
+                rk_pg = -1;
+                rk_rw = 0;
+                if (lane < TT / a.prow) {
+                    const int32_t pos = (int32_t)(tile * TT) + lane * a.prow;
+                    const int32_t e = __ldg(p.block_table + (int64_t)b * p.max_pages + page_slot(p, pos));
+                    rk_pg = (uint32_t)e < (uint32_t)p.num_pages ? e : -1;
+                    if (rk_pg < 0) atomicOr(p.status, kDevBadIndex);
+                    rk_rw = page_row(p, pos);
+                }
+            };
+            auto next_rows = [&](int64_t tile) {
+                if (tiled_tile(tile)) page_runs(tile); else list_rows(tile, yk);
+            };
+            if (GA) list_rows(tt0, yk);
+            if (PG) next_rows(tt0);
             for (int64_t step = 0; step < 2 * n_in && ok; ++step) {
                 int64_t j;
                 int kv;
@@ -713,18 +744,30 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 if (GA || PG) {
                     // rows of this fill: K(j) takes the prefetched rows (kept
                     // for V(j)), then the next tile's are requested
-                    int y[4];
+                    int y[4], rpg = -1, rrw = 0;
+                    const bool tl = tiled_tile(tt0 + j);
                     if (kv == 0) {
 #pragma unroll
                         for (int r = 0; r < 4; ++r) {
                             y[r] = yk[r];
                             if (j & 1) yv1[r] = yk[r]; else yv0[r] = yk[r];
                         }
-                        if (j + 1 < n_in) list_rows(tt0 + j + 1, yk);
+                        rpg = rk_pg;
+                        rrw = rk_rw;
+                        if (j & 1) { rv_pg1 = rk_pg; rv_rw1 = rk_rw; } else { rv_pg0 = rk_pg; rv_rw0 = rk_rw; }
+                        if (j + 1 < n_in) {
+                            if (GA) list_rows(tt0 + j + 1, yk);
+                            else next_rows(tt0 + j + 1);
+                        }
                     } else {
 #pragma unroll
                         for (int r = 0; r < 4; ++r) y[r] = (j & 1) ? yv1[r] : yv0[r];
+                        rpg = (j & 1) ? rv_pg1 : rv_pg0;
+                        rrw = (j & 1) ? rv_rw1 : rv_rw0;
                     }
+                    const void *map = tl ? (kv ? (const void *)&a.tv : (const void *)&a.tk)
+                                         : PG ? (kv ? (const void *)&a.gv : (const void *)&a.gk)
+                                              : (kv ? (const void *)&a.tv : (const void *)&a.tk);
                     if (!I8) {
                         const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
                         if (lane == 0) {
@@ -733,13 +776,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                             else ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
                         }
                         ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (ok) {
+                        if (ok && tl) {
+                            if (lane < TT / a.prow) {
+                                unsigned char *dst = smem + C::OFF_SLOTS + slot * C::SLOT + lane * a.prow * 128;
+#pragma unroll
+                                for (int cb = 0; cb < C::KB; ++cb)
+                                    ptx::tma_load_4d(dst + cb * C::BOX, map, &bs->slot_full[slot], cb * 64,
+                                                     rrw, hk, rpg);
+                            }
+                        } else if (ok) {
                             unsigned char *dst = smem + C::OFF_SLOTS + slot * C::SLOT + 4 * lane * 128;
 #pragma unroll
                             for (int cb = 0; cb < C::KB; ++cb)
-                                ptx::tma_gather4(dst + cb * C::BOX, kv ? (const void *)&a.tv
-                                                                       : (const void *)&a.tk,
-                                                 &bs->slot_full[slot], cb * 64, y[0], y[1], y[2], y[3]);
+                                ptx::tma_gather4(dst + cb * C::BOX, map, &bs->slot_full[slot], cb * 64,
+                                                 y[0], y[1], y[2], y[3]);
                         }
                     } else {
                         // int8 pages: the four rows' codes (one 128-byte box
@@ -751,10 +801,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                             else ptx::mbar_arrive_expect_tx(&bs->raw_full[rs], C::RAW);
                         }
                         ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (ok)
-                            ptx::tma_gather4(smem + C::OFF_RAW + rs * C::RAW + 4 * lane * 128,
-                                             kv ? (const void *)&a.tv : (const void *)&a.tk,
+                        if (ok && tl) {
+                            if (lane < TT / a.prow)
+                                ptx::tma_load_4d(smem + C::OFF_RAW + rs * C::RAW + lane * a.prow * 128, map,
+                                                 &bs->raw_full[rs], 0, rrw, hk, rpg);
+                        } else if (ok) {
+                            ptx::tma_gather4(smem + C::OFF_RAW + rs * C::RAW + 4 * lane * 128, map,
                                              &bs->raw_full[rs], 0, y[0], y[1], y[2], y[3]);
+                        }
                     }
                 } else if (lane == 0 && I8) {
                     // int8 codes -> raw ring (one box of TT positions x D codes)
@@ -1066,22 +1120,30 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             const int64_t sb0 = PG ? 0 : (int64_t)w.b;
             const float *ksrow = I8 ? p.k_scale + sb0 * p.kss[0] + (int64_t)w.hk * p.kss[1] : nullptr;
             const float *vsrow = I8 ? p.v_scale + sb0 * p.vss[0] + (int64_t)w.hk * p.vss[1] : nullptr;
-            // paged: the pool page of this thread's position, read one tile
-            // ahead (-1 past the length, or for a table entry outside the pool)
-            int pg_n = -1;
-            auto load_page = [&](int64_t jj) {
-                const int64_t tok = (tt0 + jj) * TT + wt;
-                pg_n = tok < L ? page_of(p, w.b, (int32_t)tok) : -1;
+            // paged: the pool page of this thread's position (-1 past the
+            // length, or for a table entry outside the pool, which the
+            // producer flags), read two tiles ahead so the scale reads of the
+            // next tile need not wait for it: pg_c for tile j, pg_n for j + 1
+            const int32_t *trow = PG ? p.block_table + (int64_t)w.b * p.max_pages : nullptr;
+            auto page_at = [&](int64_t jj) -> int {
+                const int32_t tok = (int32_t)((tt0 + jj) * TT) + wt;
+                if (tok >= (int32_t)L) return -1;
+                const int32_t e = __ldg(trow + page_slot(p, tok));
+                return (uint32_t)e < (uint32_t)p.num_pages ? e : -1;
             };
-            if (PG) load_page(0);
+            int pg_c = -1, pg_n = -1;
+            if (PG) {
+                pg_c = page_at(0);
+                if (n_in > 1) pg_n = page_at(1);
+            }
             float ksc_n = 1.f, vsc_n = 1.f;
-            auto load_scales = [&](int64_t jj) {
+            auto load_scales = [&](int64_t jj, int pg) {
                 if (PG) {
                     const int64_t tok = (tt0 + jj) * TT + wt;
-                    if (pg_n >= 0) {
-                        const int64_t r = (int32_t)tok % p.page_size;
-                        ksc_n = __ldg(ksrow + (int64_t)pg_n * p.kss[0] + r * p.kss[2]);
-                        vsc_n = __ldg(vsrow + (int64_t)pg_n * p.vss[0] + r * p.vss[2]);
+                    if (pg >= 0) {
+                        const int64_t r = page_row(p, (int32_t)tok);
+                        ksc_n = __ldg(ksrow + (int64_t)pg * p.kss[0] + r * p.kss[2]);
+                        vsc_n = __ldg(vsrow + (int64_t)pg * p.vss[0] + r * p.vss[2]);
                     }
                 } else {
                     const int64_t tok = tile_start(tt0 + jj, L) + wt;
@@ -1091,7 +1153,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     }
                 }
             };
-            if (I8) load_scales(0);
+            if (I8) load_scales(0, pg_c);
             // gather: the list cell this lane's position holds, read one tile
             // ahead; a cell is visible if 0 <= cell < cap (cap or more is
             // flagged FD_DEV_BAD_INDEX, negative is padding).
@@ -1118,12 +1180,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     if (cell >= p.cap) atomicOr(p.status, kDevBadIndex);
                     in_len = in_len && cell >= 0 && cell < p.cap;
                 }
+                const int pg_next = pg_n;
                 if (PG) {
-                    in_len = in_len && pg_n >= 0;
-                    if (j + 1 < n_in) load_page(j + 1);
+                    in_len = in_len && pg_c >= 0;
+                    if (j + 2 < n_in) pg_n = page_at(j + 2);
                 }
                 const float ksc = ksc_n, vsc = vsc_n;
-                if (I8 && j + 1 < n_in) load_scales(j + 1);
+                if (I8 && j + 1 < n_in) load_scales(j + 1, pg_next);
+                pg_c = pg_next;
                 ok = ptx::mbar_wait(&bs->s_full[sb], u & 1, abort_flag, kWaitNs);
                 if (!ok) { note_timeout(bs, p, 9, tile_ctr, piece); break; }
                 ptx::tc_fence_after();
