@@ -190,6 +190,13 @@ def workload_desc(name):
 
 def call_fn(inp, out, ws, kernel, num_ctas=0):
     from decode_attention_preallocated_gb300 import fd
+    if getattr(inp, "k_new", None) is not None:
+        # fused append step; the lengths are left as they are, so every timed
+        # call appends the same rows at the same positions
+        return lambda: fd.decode_append(inp.q, inp.k, inp.v, inp.k_new, inp.v_new,
+                                        inp.kv_lengths, causal=inp.causal, scale=inp.scale,
+                                        update_lengths=False, out=out, workspace=ws,
+                                        kernel=kernel, num_ctas=num_ctas)
     if inp.block_table is not None:
         return lambda: fd.decode_paged(inp.q, inp.k, inp.v, inp.block_table, inp.kv_lengths,
                                        n_q=inp.n_q, causal=inp.causal, scale=inp.scale,
@@ -215,6 +222,11 @@ def algorithmic_bytes(inp):
         valid = int(((inp.idx >= 0) & (inp.idx < inp.k.shape[2])).sum())
         return valid * Hkv * d * 2 * 2
     es = 1 if inp.k.dtype == torch.int8 else 2
+    if getattr(inp, "k_new", None) is not None:
+        # fused append: the new rows are read once and written once, and the
+        # attention reads the prefix including them
+        n = inp.k_new.shape[1]
+        return kv_bytes([L + n for L in inp.lengths_host], Hkv, d, 2) + 2 * kv_bytes([n] * B, Hkv, d, 2)
     b = kv_bytes(inp.lengths_host, Hkv, d, es)
     if es == 1:
         b += sum(inp.lengths_host) * Hkv * 4 * 2   # fp32 per-token scales
@@ -416,6 +428,21 @@ def extras(args, device, stream, peak, kernel):
             measure("gather_K%d_cap%d" % (K, cap), inp, 100)
             del inp
     torch.cuda.empty_cache()
+    # fused append: the MTP-verify and ragged workloads as one step that
+    # writes the window's rows (4 / 6 per sequence) and attends
+    for name, n in (("mtp_verify", 4), ("ragged", 6)):
+        inp = W.workload(name, seed=1, device=device)
+        g = torch.Generator(device=device)
+        g.manual_seed(7)
+        B, _, _, d = inp.q.shape
+        Hkv = inp.k.shape[1]
+        inp.k_new = W.randn_bf16((B, n, Hkv, d), g, device)
+        inp.v_new = W.randn_bf16((B, n, Hkv, d), g, device)
+        inp.lengths_host = [L - n for L in inp.lengths_host]
+        inp.kv_lengths = inp.kv_lengths - n
+        measure("append_" + name, inp, 200 if name == "mtp_verify" else 50)
+        del inp
+        torch.cuda.empty_cache()
     # paged caches: the ragged and int8 workloads with their pages scattered
     # over a pool (bytes: the same K/V rows as the flat caches)
     for name in ("paged_ps16", "paged_ps64", "paged_ps256", "paged_int8_ps64",

@@ -122,6 +122,10 @@ struct Call {
     int mode;         // fd::Mode
     int kv_int8;
     const fd_opts *opts;
+    // fused append (dense bf16 only): new rows [B, n_q, Hkv, d]; the lengths
+    // array to update at the end of the launch (or null)
+    const fd_tensor *k_new = nullptr, *v_new = nullptr;
+    int32_t *len_update = nullptr;
 };
 
 int run(const Call &c) {
@@ -181,6 +185,19 @@ int run(const Call &c) {
     if (c.mode != fd::kGather && !c.kv_lengths) return FD_ERR_ARG;
     if (c.mode == fd::kGather && (c.idx_len < 0 || (!c.idx && c.idx_len > 0))) return FD_ERR_ARG;
     if (c.causal != 0 && c.causal != 1) return FD_ERR_ARG;
+    const bool append = c.k_new != nullptr;
+    if (append) {
+        if (c.mode != fd::kDense || c.kv_int8) return FD_ERR_ARG;
+        if ((rc = check_tensor(c.k_new, 4)) || (rc = check_tensor(c.v_new, 4))) return rc;
+        if (c.k_new->dtype != FD_BF16 || c.v_new->dtype != FD_BF16) return FD_ERR_ARG;
+        const int64_t want[4] = {B, n_q, Hkv, d};
+        for (int i = 0; i < 4; ++i)
+            if (c.k_new->shape[i] != want[i] || c.v_new->shape[i] != want[i]) return FD_ERR_ARG;
+        if (c.k_new->stride[3] != 1 || c.v_new->stride[3] != 1) return FD_ERR_ARG;
+        if (!aligned16(c.k_new->data) || !aligned16(c.v_new->data)) return FD_ERR_ALIGN;
+        for (int i = 0; i < 3; ++i)
+            if (c.k_new->stride[i] % 8 || c.v_new->stride[i] % 8) return FD_ERR_ALIGN;
+    }
 
     fd_workspace *ws = o.ws;
     if (!ws) return FD_ERR_WORKSPACE;
@@ -219,6 +236,14 @@ int run(const Call &c) {
     p.counters = ws->counters;
     p.status = ws->status;
     p.partials = ws->partials;
+    if (append) {
+        p.n_new = (int32_t)n_q;
+        p.k_new = static_cast<const uint16_t *>(c.k_new->data);
+        p.v_new = static_cast<const uint16_t *>(c.v_new->data);
+        for (int i = 0; i < 4; ++i) { p.kns[i] = c.k_new->stride[i]; p.vns[i] = c.v_new->stride[i]; }
+        p.len_update = c.len_update;
+        p.grid = ws->status + 32;   // two launch counters in the status block
+    }
 
     // Kernel choice: the tensor-core kernel serves what fd::tc_supports
     // accepts (dense bf16 and head_dim-128 int8 caches, bf16 gather over a
@@ -279,6 +304,20 @@ int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache, const fd_tens
     if (scale == 0.f && q->ndim == 4 && q->shape[3] > 0) scale = 1.f / sqrtf((float)q->shape[3]);
     Call c{q, k_cache, v_cache, nullptr, nullptr, out, nullptr, idx, idx_len, nullptr, 0,
            q->ndim == 4 ? (int32_t)q->shape[1] : 0, 0, scale, fd::kGather, 0, opts};
+    return run(c);
+}
+
+int fd_decode_append(const fd_tensor *q, const fd_tensor *k_cache, const fd_tensor *v_cache,
+                     const fd_tensor *k_new, const fd_tensor *v_new, int32_t *kv_lengths,
+                     int32_t update_lengths, int32_t causal, float scale, const fd_tensor *out,
+                     const fd_opts *opts) {
+    if (!q || !k_new || !v_new) return FD_ERR_ARG;
+    if (update_lengths != 0 && update_lengths != 1) return FD_ERR_ARG;
+    Call c{q, k_cache, v_cache, nullptr, nullptr, out, kv_lengths, nullptr, 0, nullptr, 0,
+           q->ndim == 4 ? (int32_t)q->shape[1] : 0, causal, scale, fd::kDense, 0, opts};
+    c.k_new = k_new;
+    c.v_new = v_new;
+    c.len_update = update_lengths ? kv_lengths : nullptr;
     return run(c);
 }
 

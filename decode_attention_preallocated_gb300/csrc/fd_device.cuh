@@ -46,9 +46,42 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
 // ceil(L_b / tile) tiles; a gather launch has nseg = B*n_q*Hkv segments of
 // ceil(idx_len / tile) tiles each.
 __device__ __forceinline__ int64_t seq_len(const Params &p, int b) {
-    int64_t L = (int64_t)__ldg(p.kv_lengths + b);
-    if (L < 0 || L > p.cap) atomicOr(p.status, kDevBadLength);
-    return clamp_len(L, p.cap);
+    const int64_t raw = (int64_t)__ldg(p.kv_lengths + b);
+    if (raw < 0 || raw + p.n_new > p.cap) atomicOr(p.status, kDevBadLength);
+    return clamp_len(clamp_len(raw, p.cap) + p.n_new, p.cap);
+}
+
+// Fused append: position of sequence b's first appended row (its length
+// before the call, clamped to [0, cap]).
+__device__ __forceinline__ int64_t append_base(const Params &p, int b) {
+    return clamp_len((int64_t)__ldg(p.kv_lengths + b), p.cap);
+}
+
+// Fused append, end of the launch: once every block of the grid has passed
+// here (so no block reads kv_lengths any more), the last one writes the new
+// lengths (if asked) and resets the launch counters for the next launch.
+// Called by every thread of every block.
+static __device__ __noinline__ void append_exit(const Params &p) {
+    __shared__ int last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        last = atomicAdd(p.grid + 1, 1) == (int)gridDim.x - 1;
+        if (last) __threadfence();
+    }
+    __syncthreads();
+    if (!last) return;
+    if (p.len_update)
+        for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+            const int64_t raw = (int64_t)p.kv_lengths[b];
+            p.len_update[b] = (int32_t)clamp_len(clamp_len(raw, p.cap) + p.n_new, p.cap);
+        }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        p.grid[0] = 0;
+        p.grid[1] = 0;
+        __threadfence();
+    }
 }
 
 // Paged caches: which page of its sequence logical position pos falls on,

@@ -50,6 +50,18 @@ struct Params {
     int32_t page_size, max_pages;
     int32_t page_shift;    // log2(page_size) when it is a power of two, else -1
     int64_t num_pages;
+    // fused append (flat bf16 caches): n_new rows per (sequence, kv head),
+    // k_new / v_new [B, n_new, Hkv, d], are written at positions
+    // base_b .. base_b + n_new - 1 with base_b = kv_lengths[b] (clamped to
+    // [0, cap]) and attended as part of the prefix, whose length is then
+    // min(base_b + n_new, cap); len_update (non-null) receives that length
+    // when the launch ends.  n_new = 0 otherwise.
+    int32_t n_new;
+    const uint16_t *k_new; int64_t kns[4];
+    const uint16_t *v_new; int64_t vns[4];
+    int32_t *len_update;
+    int32_t *grid;         // [2] launch counters in the workspace (barrier,
+                           // exit), zero between launches
     void *out;             int64_t os[4];
     // workspace
     int32_t *counters;     // [nseg], zero between launches

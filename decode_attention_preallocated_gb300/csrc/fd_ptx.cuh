@@ -95,6 +95,12 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
 
 // Writes by this thread's generic proxy become visible to the async proxy
 // (TMA, tcgen05.mma) after this fence.
+// Orders this thread's generic-proxy global writes before later async-proxy
+// (TMA) accesses, and the reverse.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

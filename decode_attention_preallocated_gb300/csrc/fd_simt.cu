@@ -36,7 +36,7 @@ struct Layout {
                + 3 * (size_t)T * 8           // positions, K and V row offsets (int64,
                                              // 8-byte aligned here)
                + (size_t)rows * (T + 1) * 4  // P
-               + 3 * (size_t)T * 4           // k scale, v scale, valid
+               + 4 * (size_t)T * 4           // k scale, v scale, valid, appended
                + 3 * (size_t)rows * 4;       // m, l, alpha
     }
 };
@@ -54,8 +54,7 @@ __device__ __forceinline__ uint32_t i8pair_to_bf16x2(int lo, int hi) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads)
-simt_kernel(const __grid_constant__ Params p) {
+__device__ __forceinline__ void simt_body(const Params &p) {
     using Ly = Layout<D>;
     extern __shared__ __align__(16) unsigned char smem[];
     const int rows = p.rows;
@@ -70,7 +69,8 @@ simt_kernel(const __grid_constant__ Params p) {
     float *ksc = Ps + rows * (T + 1);
     float *vsc = ksc + T;
     int *tval = reinterpret_cast<int *>(vsc + T);
-    float *m_s = reinterpret_cast<float *>(tval + T);
+    int *tnew = tval + T;                      // fused append: the row comes from k_new / v_new
+    float *m_s = reinterpret_cast<float *>(tnew + T);
     float *l_s = m_s + rows;
     float *a_s = l_s + rows;
 
@@ -169,6 +169,19 @@ simt_kernel(const __grid_constant__ Params p) {
                 tval[tid] = ok;
                 tko[tid] = o0 * p.ks[0] + (int64_t)hk * p.ks[1] + o2 * p.ks[2];
                 tvo[tid] = o0 * p.vs[0] + (int64_t)hk * p.vs[1] + o2 * p.vs[2];
+                // Fused append: positions from the old length on are row
+                // pos - base of k_new / v_new (this block, which owns the
+                // tile, also writes them into the caches).
+                int isnew = 0;
+                if (ok && p.n_new > 0) {
+                    const int64_t base = append_base(p, b);
+                    if (pos >= base) {
+                        isnew = 1;
+                        tko[tid] = (int64_t)b * p.kns[0] + (pos - base) * p.kns[1] + (int64_t)hk * p.kns[2];
+                        tvo[tid] = (int64_t)b * p.vns[0] + (pos - base) * p.vns[1] + (int64_t)hk * p.vns[2];
+                    }
+                }
+                tnew[tid] = isnew;
                 float kscale = 1.f, vscale = 1.f;
                 if (ok && p.kv_int8) {
                     kscale = p.k_scale[o0 * p.kss[0] + (int64_t)hk * p.kss[1] + o2 * p.kss[2]];
@@ -185,7 +198,15 @@ simt_kernel(const __grid_constant__ Params p) {
                     const int which = e / (T * CPR);
                     const int jj = (e / CPR) % T, cc = e % CPR;
                     uint4 w = make_uint4(0, 0, 0, 0);
-                    if (tval[jj]) {
+                    if (tval[jj] && tnew[jj]) {
+                        const uint16_t *src = (which ? p.v_new + tvo[jj] : p.k_new + tko[jj]) + cc * 8;
+                        w = *reinterpret_cast<const uint4 *>(src);
+                        const int64_t *cs = which ? p.vs : p.ks;
+                        uint16_t *cache = const_cast<uint16_t *>(
+                            static_cast<const uint16_t *>(which ? p.v : p.k));
+                        *reinterpret_cast<uint4 *>(cache + (int64_t)b * cs[0] + (int64_t)hk * cs[1] +
+                                                   tpos[jj] * cs[2] + cc * 8) = w;
+                    } else if (tval[jj]) {
                         const char *src = which ? vbase + (tvo[jj] + cc * 8) * 2
                                                 : kbase + (tko[jj] + cc * 8) * 2;
                         w = ldg_stream(src);
@@ -387,6 +408,13 @@ simt_kernel(const __grid_constant__ Params p) {
         }
         t = piece_end;
     }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+simt_kernel(const __grid_constant__ Params p) {
+    simt_body<D>(p);
+    if (p.n_new > 0) append_exit(p);
 }
 
 template <int D>

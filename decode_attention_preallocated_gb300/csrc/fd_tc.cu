@@ -18,9 +18,9 @@ int launch_d(const TcArgs &args, int G, cudaStream_t st) {
     // capacity.
     const Params &p = args.p;
     if (D == 256 && p.nseg * 8 <= (int64_t)G) {
-        if (rows <= 16 && G <= resident_blocks<D, 16, false, 16, false, true, false>())
+        if (rows <= 16 && G <= resident_blocks<D, 16, false, 16, false, true, false, false>())
             return launch_dn<D, 16, false, 16, false, true>(args, G, st);
-        if (rows > 16 && rows <= 32 && G <= resident_blocks<D, 32, false, 32, false, true, false>())
+        if (rows > 16 && rows <= 32 && G <= resident_blocks<D, 32, false, 32, false, true, false, false>())
             return launch_dn<D, 32, false, 32, false, true>(args, G, st);
     }
     if (rows <= 16) return launch_dn<D, 16, false>(args, G, st);
@@ -53,13 +53,16 @@ bool tc_supports(const Params &p) {
     const bool mode = p.mode == kDense ||
                       (p.mode == kGather && !p.kv_int8 && gather_rows(p, &rs, &Y, g)) ||
                       tc_supports_paged(p);
-    return mode && shape && p.rows >= 1 && p.cap < (int64_t)1 << 31 && p.B < (1 << 30) &&
-           p.Hkv < (1 << 30) && q_aligned;
+    // fused append: flat bf16 caches (fd_tc_append.cu)
+    const bool append = p.n_new == 0 || (p.mode == kDense && !p.kv_int8);
+    return mode && shape && append && p.rows >= 1 && p.cap < (int64_t)1 << 31 &&
+           p.B < (1 << 30) && p.Hkv < (1 << 30) && q_aligned;
 }
 
 int launch_tc(const Params &p, int G, cudaStream_t st) {
     if (!tc_supports(p)) return -2;
     if (p.mode == kPaged) return launch_tc_paged(p, G, st);
+    if (p.n_new > 0) return launch_tc_append(p, G, st);
     TcArgs args;
     memset(&args, 0, sizeof args);
     args.p = p;

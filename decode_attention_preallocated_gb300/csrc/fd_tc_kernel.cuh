@@ -522,9 +522,61 @@ __device__ __noinline__ bool share_merge_segment(const Params &p, Bars *bs, Walk
     return true;
 }
 
-template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG>
+// Fused append: this block's share of the new rows, copied into the caches
+// (16-byte chunks spread over every thread of the grid).
+__device__ __noinline__ void append_rows(const Params &p) {
+    const int cpr = p.d / 8;
+    const int64_t per = (int64_t)p.B * p.Hkv * p.n_new * cpr;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < 2 * per; e += stride) {
+        const int which = e >= per;
+        int64_t r = which ? e - per : e;
+        const int cc = (int)(r % cpr);
+        r /= cpr;
+        const int i = (int)(r % p.n_new);
+        r /= p.n_new;
+        const int hk = (int)(r % p.Hkv);
+        const int b = (int)(r / p.Hkv);
+        const int64_t pos = append_base(p, b) + i;
+        if (pos >= p.cap) continue;
+        const int64_t *ns = which ? p.vns : p.kns;
+        const int64_t *cs = which ? p.vs : p.ks;
+        const uint16_t *src = (which ? p.v_new : p.k_new) + (int64_t)b * ns[0] + (int64_t)i * ns[1] +
+                              (int64_t)hk * ns[2] + cc * 8;
+        uint16_t *dst = const_cast<uint16_t *>(static_cast<const uint16_t *>(which ? p.v : p.k)) +
+                        (int64_t)b * cs[0] + (int64_t)hk * cs[1] + pos * cs[2] + cc * 8;
+        *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+    }
+}
+
+// Fused append: every block of the (cooperative, all blocks resident)
+// launch counts itself in once its share of the new rows is written ...
+__device__ __noinline__ void append_arrive(const Params &p) {
+    ptx::fence_proxy_async_global();
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) atomicAdd(p.grid, 1);
+}
+
+// ... and the producer waits for every block's count before its first cache
+// read, so no TMA load of a tile holding new positions starts before they
+// are in the caches (set-up overlaps the wait).  Bounded; giving up sets
+// FD_DEV_INTERNAL and the launch's output is not valid.
+__device__ __noinline__ void append_wait(const Params &p) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t n = 0; ld_acquire(p.grid) < (int)gridDim.x; ++n) {
+        __nanosleep(32);
+        if ((n & 63) == 63 && ptx::globaltimer_ns() - t0 > kWaitNs) {
+            atomicOr(p.status, kDevTimeout);
+            break;
+        }
+    }
+}
+
+template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant__ TcArgs a) {
     static_assert(!(GA && PG), "gather and paged loads are separate modes");
+    static_assert(!AP || (!I8 && !GA && !PG), "fused append: flat bf16 caches");
     using C = Cfg<D, N, I8, NV, GA>;
     constexpr int kSoftmaxThreads = C::SMT;
     const Params &p = a.p;
@@ -543,8 +595,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
     // The swizzled operand layouts need 1024-byte aligned buffers; the
     // dynamic shared window starts aligned, and a block that finds otherwise
     // reports it instead of computing.
+    // Fused append: the new rows go into the caches before any tile is read
+    // (the producer waits for every block's rows before its first load).
+    if (AP) {
+        append_rows(p);
+        append_arrive(p);
+    }
     if (smem_base & 1023u) {
         if (tid == 0) atomicOr(p.status, kDevTimeout);
+        if (AP) append_exit(p);
         return;
     }
 
@@ -652,6 +711,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         // nothing to stream: straight to the exit
     } else if (warp == kProducerWarp) {
         // ------------------------------------------------------ TMA producer
+        if (AP) {
+            if (lane == 0) append_wait(p);
+            __syncwarp();
+            ptx::fence_proxy_async_global();
+        }
         uint32_t issued = 0;
         bool ok = true;
         int piece = 0;
@@ -1475,6 +1539,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
     __syncthreads();
     ptx::tc_fence_after();
     if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    if (AP) append_exit(p);
 }
 
 // ------------------------------------------------------------- host side
@@ -1539,7 +1604,7 @@ inline bool make_gmap(CUtensorMap *m, const void *base, const Params &p, int64_t
 
 // Blocks of this instantiation that can be resident at once on the current
 // device (0 on error); sets the dynamic shared memory opt-in the first time.
-template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG>
+template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP>
 int resident_blocks() {
     using C = Cfg<D, N, I8, NV, GA>;
     static std::atomic<int> cached[64];
@@ -1548,9 +1613,9 @@ int resident_blocks() {
     int n = cached[dev].load(std::memory_order_acquire);
     if (n > 0) return n;
     int per_sm = 0, sms = 0;
-    if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV, GA, SH, PG>,
+    if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV, GA, SH, PG, AP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_kernel<D, N, I8, NV, GA, SH, PG>,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_kernel<D, N, I8, NV, GA, SH, PG, AP>,
                                                       kThreadsTC, C::SMEM) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
@@ -1559,15 +1624,19 @@ int resident_blocks() {
     return n;
 }
 
-template <int D, int N, bool I8, int NV = N, bool GA = false, bool SH = false, bool PG = false>
+template <int D, int N, bool I8, int NV = N, bool GA = false, bool SH = false, bool PG = false,
+          bool AP = false>
 int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
     using C = Cfg<D, N, I8, NV, GA>;
-    if (resident_blocks<D, N, I8, NV, GA, SH, PG>() <= 0) return -5;
-    if (!SH) {
-        tc_kernel<D, N, I8, NV, GA, SH, PG><<<G, kThreadsTC, C::SMEM, st>>>(args);
+    const int resident = resident_blocks<D, N, I8, NV, GA, SH, PG, AP>();
+    if (resident <= 0) return -5;
+    if (!SH && !AP) {
+        tc_kernel<D, N, I8, NV, GA, SH, PG, AP><<<G, kThreadsTC, C::SMEM, st>>>(args);
         return cudaGetLastError() == cudaSuccess ? 0 : -5;
     }
-    // shared merges: a cooperative launch (the caller checked the grid fits)
+    // shared merges or fused append: a cooperative launch (every block
+    // resident)
+    if (G > resident) return -2;
     TcArgs ca = args;
     ca.p.coop = 1;
     cudaLaunchConfig_t cfg = {};
@@ -1580,7 +1649,7 @@ int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_kernel<D, N, I8, NV, GA, SH, PG>, ca) == cudaSuccess ? 0 : -5;
+    return cudaLaunchKernelEx(&cfg, tc_kernel<D, N, I8, NV, GA, SH, PG, AP>, ca) == cudaSuccess ? 0 : -5;
 }
 
 }  // namespace

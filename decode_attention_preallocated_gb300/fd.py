@@ -6,9 +6,10 @@ stream.  There is no fallback: if libfd.so is missing or cannot be loaded,
 every call raises.
 
 Low-level names mirror the C ABI (``fd_decode``, ``fd_decode_int8``,
-``fd_decode_paged``, ``fd_decode_gather``, ``fd_workspace_create`` ...) and
-take ``FdTensor`` / ``FdOpts`` structures; ``decode``, ``decode_int8``,
-``decode_paged`` and ``decode_gather`` take
+``fd_decode_append``, ``fd_decode_paged``, ``fd_decode_gather``,
+``fd_workspace_create`` ...) and take ``FdTensor`` / ``FdOpts`` structures;
+``decode``, ``decode_int8``, ``decode_append``, ``decode_paged`` and
+``decode_gather`` take
 torch tensors, allocate ``out`` with torch when it is not given, and keep one
 workspace per (device, stream).
 """
@@ -71,6 +72,10 @@ _SIGNATURES = [
     ("fd_decode_gather", ctypes.c_int,
      [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_int32,
       _P(FdTensor), _P(FdOpts)]),
+    ("fd_decode_append", ctypes.c_int,
+     [_P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor),
+      ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _P(FdTensor),
+      _P(FdOpts)]),
     ("fd_decode_paged", ctypes.c_int,
      [_P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor),
       ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
@@ -359,6 +364,32 @@ def decode_int8(q, k_cache, v_cache, k_scale, v_scale, kv_lengths, n_q=None,
                                   kv_lengths.data_ptr(), int(n_q), int(bool(causal)),
                                   float(scale), ctypes.byref(to), ctypes.byref(o))
     _check(rc, "fd_decode_int8")
+    return out
+
+
+def decode_append(q, k_cache, v_cache, k_new, v_new, kv_lengths, causal=True, scale=None,
+                  update_lengths=True, out=None, out_dtype=torch.bfloat16, num_ctas=0,
+                  kernel=FD_KERNEL_AUTO, stream=None, workspace: Optional[Workspace] = None):
+    """One decode step with a fused append: writes k_new / v_new
+    [B, n_q, Hkv, d] (bf16) into k_cache / v_cache [B, Hkv, cap, d] at
+    positions kv_lengths[b] .. kv_lengths[b] + n_q - 1, attends q
+    [B, n_q, Hq, d] over the prefix including them (row i sees up to
+    kv_lengths[b] + i when causal) and, with update_lengths, advances
+    kv_lengths (int32 [B], on the device) by n_q when the launch ends."""
+    B, nq, Hq, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    Hkv = k_cache.shape[1]
+    rows = (Hq // max(Hkv, 1)) * nq
+    out, sh, ws = _prepare(q, k_cache, out, out_dtype, B * Hkv, rows, num_ctas,
+                           kernel, stream, workspace)
+    tq, tk, tv, tkn, tvn, to = map(as_fd_tensor, (q, k_cache, v_cache, k_new, v_new, out))
+    o = _opts(sh, ws, num_ctas, kernel)
+    with _on_device(q.device):
+        rc = lib().fd_decode_append(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                    ctypes.byref(tkn), ctypes.byref(tvn), kv_lengths.data_ptr(),
+                                    int(bool(update_lengths)), int(bool(causal)), float(scale),
+                                    ctypes.byref(to), ctypes.byref(o))
+    _check(rc, "fd_decode_append")
     return out
 
 

@@ -17,7 +17,8 @@
  *     drafts already written at L-n_q .. L-1) and row i sees 0 .. L-n_q+i
  *     (same issue, list item 2 and "Existing Solutions": a bottom-right
  *     aligned causal window, up to 6 rows).
- *     fd_decode_paged computes the same over a paged cache.
+ *     fd_decode_paged computes the same over a paged cache, and
+ *     fd_decode_append after writing the step's new rows into the cache.
  *   - fd_decode_gather: V = the cells listed for that (b, i) in idx
  *     ("attend the selected cells instead of masking the window",
  *     llama.cpp #28244, Conversation; "gather-based sparse attention for
@@ -163,6 +164,35 @@ int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache,
                      int32_t idx_len, const fd_tensor *out,
                      const fd_opts *opts);
 
+/*
+ * Dense prefix decode with a fused K/V append (bf16 caches): one launch
+ * writes the step's new rows into the caches and attends over the prefix
+ * including them, as flash_attn_with_kvcache does with k / v and
+ * cache_seqlens ("Qwen3.5 text generation attends over the full KV
+ * capacity", ComfyUI #16509: Existing Solutions).  For sequence b with
+ * base_b = kv_lengths[b] (clamped to [0, cap]):
+ *   - k_new[b, i, hk, :] and v_new[b, i, hk, :] are written to cache
+ *     positions base_b + i, i = 0 .. n_q - 1 (positions at or past cap are
+ *     not written, and FD_DEV_BAD_LENGTH is set);
+ *   - the result is fd_decode's with L_b = min(base_b + n_q, cap): the n_q
+ *     query rows are the new tokens, and with causal != 0 row i sees
+ *     positions 0 .. base_b + i;
+ *   - with update_lengths = 1, kv_lengths[b] becomes L_b when the launch
+ *     ends (0 leaves it unchanged).
+ *   k_new, v_new: [B, n_q, Hkv, d] bf16, device, 16-byte aligned base and
+ *   strides, inner stride 1 (the [B, n_q, Hkv, d] layout of q's new tokens).
+ *   k_cache, v_cache and kv_lengths are written by the call (caller-owned).
+ *   The tensor-core kernel runs it as a cooperative launch (every block
+ *   resident; an explicit opts->num_ctas above that returns
+ *   FD_ERR_UNSUPPORTED) and meets once at a grid-wide barrier after the
+ *   writes; its launch counters live in the workspace, so calls sharing a
+ *   workspace must not overlap.  Other arguments as fd_decode.
+ */
+int fd_decode_append(const fd_tensor *q, const fd_tensor *k_cache,
+                     const fd_tensor *v_cache, const fd_tensor *k_new,
+                     const fd_tensor *v_new, int32_t *kv_lengths,
+                     int32_t update_lengths, int32_t causal, float scale,
+                     const fd_tensor *out, const fd_opts *opts);
 /*
  * Dense prefix decode over a paged cache: the same visible set, causal
  * window and result as fd_decode / fd_decode_int8, but cache position j of

@@ -195,6 +195,40 @@ def dense(q, k, v, kv_lengths, n_q, causal, scale, k_scale=None,
     return out
 
 
+def append(q, k, v, k_new, v_new, kv_lengths, causal, scale):
+    """One decode step with an append, as flash_attn_with_kvcache defines it
+    (ComfyUI #16509, Existing Solutions): the new rows go into the cache at
+    each sequence's length, then ``dense`` attends over the longer prefix.
+
+    q [B, n, Hq, d] bf16 (the n new tokens); k, v [B, Hkv, cap, d] bf16;
+    k_new, v_new [B, n, Hkv, d] bf16; kv_lengths [B] host int32 (lengths
+    before the step).  With base_b = clamp(kv_lengths[b], 0, cap), row i of
+    sequence b is written at position base_b + i when that is below cap, and
+    the step's length is min(base_b + n, cap).  Returns (out float64
+    [B, n, Hq, d], k after, v after (uint16 bf16 bits, the inputs are not
+    modified), lengths after int32 [B]).
+    """
+    qa = _as_np(q)
+    ka = np.array(_as_np(k), copy=True)
+    va = np.array(_as_np(v), copy=True)
+    kn, vn = _as_np(k_new), _as_np(v_new)
+    B, n, Hq, d = qa.shape
+    _, Hkv, cap, _ = ka.shape
+    if kn.shape != (B, n, Hkv, d) or vn.shape != kn.shape:
+        raise ValueError("k_new / v_new must be [B, n_q, Hkv, d]")
+    lens = np.asarray(_as_np(kv_lengths), dtype=np.int64).reshape(B)
+    base = np.clip(lens, 0, cap)
+    for b in range(B):
+        for i in range(n):
+            pos = int(base[b]) + i
+            if pos < cap:
+                ka[b, :, pos, :] = kn[b, i]
+                va[b, :, pos, :] = vn[b, i]
+    after = np.minimum(base + n, cap).astype(np.int32)
+    out = dense(qa, ka, va, after, n, causal, scale)
+    return out, ka, va, after
+
+
 def paged(q, k_pages, v_pages, block_table, kv_lengths, n_q, causal, scale,
           k_scale=None, v_scale=None, _lib_override=None):
     """fp64 attention over a paged cache: the dense prefix definition with

@@ -165,6 +165,32 @@ def test_paged_validation(L):
     assert call_paged(q, k2, k2, o) == fd.FD_ERR_ALIGN
 
 
+def test_append_validation(L):
+    q, k, v, o = good(B=2, n_q=3)
+    kn = fake([2, 3, 2, 128])
+    op = fd.FdOpts()
+
+    def call(kn_, vn_, update=1, lens=0x200000, causal=1):
+        return L.fd_decode_append(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v),
+                                  ctypes.byref(kn_), ctypes.byref(vn_), lens, update, causal,
+                                  0.1, ctypes.byref(o), ctypes.byref(op))
+
+    q, k, v, o = good(B=2, n_q=3)
+    assert call(kn, kn) == fd.FD_ERR_WORKSPACE                  # valid up to the workspace
+    assert call(kn, kn, update=2) == fd.FD_ERR_ARG
+    assert call(kn, kn, lens=None) == fd.FD_ERR_ARG
+    assert call(fake([2, 2, 2, 128]), kn) == fd.FD_ERR_ARG       # n_new != n_q
+    assert call(kn, fake([2, 3, 1, 128])) == fd.FD_ERR_ARG       # Hkv
+    assert call(fake([2, 3, 2, 128], fd.FD_F32), kn) == fd.FD_ERR_ARG
+    assert call(fake([2, 3, 2, 128], ptr=0x100008), kn) == fd.FD_ERR_ALIGN
+    assert call(fake([2, 3, 2, 128], strides=[3 * 2 * 132, 2 * 132, 132, 1]), kn) == fd.FD_ERR_ALIGN
+    k8 = fake([2, 2, 64, 128], fd.FD_I8)
+    rc = L.fd_decode_append(ctypes.byref(q), ctypes.byref(k8), ctypes.byref(k8),
+                            ctypes.byref(kn), ctypes.byref(kn), 0x200000, 1, 1, 0.1,
+                            ctypes.byref(o), ctypes.byref(op))
+    assert rc == fd.FD_ERR_ARG                                   # bf16 caches only
+
+
 def test_workspace_size_formula(L):
     n = L.fd_workspace_bytes(10, 24, 256, 300)
     floats = (10 + 300) * 24 * 258
