@@ -65,6 +65,9 @@ def _bind(path):
     lib.fdo_gather.argtypes = [p, p, p, p, p, p, i32, p, p, p, p, i64,
                                i32, i32, i32, i32, i32, i64, f64, p]
     lib.fdo_gather.restype = i32
+    lib.fdo_gather_bias.argtypes = [p, p, p, p, p, p, i32, p, p, p, p, p, i64,
+                                    i32, i32, i32, i32, i32, i64, f64, p]
+    lib.fdo_gather_bias.restype = i32
     lib.fdo_set_threads.argtypes = [i32]
     lib.fdo_set_threads.restype = None
     lib.fdo_max_threads.argtypes = []
@@ -290,12 +293,16 @@ def paged(q, k_pages, v_pages, block_table, kv_lengths, n_q, causal, scale,
                   _lib_override=_lib_override)
 
 
-def gather(q, k, v, idx, scale, k_scale=None, v_scale=None,
+def gather(q, k, v, idx, scale, k_scale=None, v_scale=None, bias=None,
            _lib_override=None):
     """fp64 attention over the cache rows named by ``idx`` [B, n_q, K].
 
     One list per (sequence, query row), shared by every head of that row;
-    entries < 0 or >= cap are skipped.  Returns float64 [B, n_q, Hq, d].
+    entries < 0 or >= cap are skipped.  ``bias`` (optional, fp32 [B, n_q, K])
+    is added to the score of each list entry ("qwen4exp : gather-based sparse
+    attention for QSA decode", llama.cpp #28213, Overview: the mask entries
+    travel with the gathered cells); an entry whose bias is -inf is dropped.
+    Returns float64 [B, n_q, Hq, d].
     """
     lib = _lib_override or _load()
     qa = _as_np(q)
@@ -313,11 +320,22 @@ def gather(q, k, v, idx, scale, k_scale=None, v_scale=None,
     out = np.zeros((B, n_q, Hq, d), dtype=np.float64)
     qs, ks, vs = _strides(qa), _strides(ka), _strides(va)
     ss = _strides(ksa) if int8 else np.zeros(3, dtype=np.int64)
-    rc = lib.fdo_gather(_ptr(qa), _ptr(qs), _ptr(ka), _ptr(ks), _ptr(va),
-                        _ptr(vs), int8,
-                        _ptr(ksa) if int8 else None,
-                        _ptr(vsa) if int8 else None, _ptr(ss), _ptr(ia), K,
-                        B, n_q, Hq, Hkv, d, cap, float(scale), _ptr(out))
+    if bias is None:
+        rc = lib.fdo_gather(_ptr(qa), _ptr(qs), _ptr(ka), _ptr(ks), _ptr(va),
+                            _ptr(vs), int8,
+                            _ptr(ksa) if int8 else None,
+                            _ptr(vsa) if int8 else None, _ptr(ss), _ptr(ia), K,
+                            B, n_q, Hq, Hkv, d, cap, float(scale), _ptr(out))
+    else:
+        ba = np.ascontiguousarray(np.asarray(_as_np(bias), dtype=np.float32))
+        if ba.shape != ia.shape:
+            raise ValueError("bias must be [B, n_q, K] like idx")
+        rc = lib.fdo_gather_bias(_ptr(qa), _ptr(qs), _ptr(ka), _ptr(ks), _ptr(va),
+                                 _ptr(vs), int8,
+                                 _ptr(ksa) if int8 else None,
+                                 _ptr(vsa) if int8 else None, _ptr(ss), _ptr(ia),
+                                 _ptr(ba), K, B, n_q, Hq, Hkv, d, cap, float(scale),
+                                 _ptr(out))
     if rc != 0:
         raise RuntimeError("fdo_gather failed: %d" % rc)
     return out

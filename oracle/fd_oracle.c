@@ -27,8 +27,13 @@
  *     dense, non-causal : { j : 0 <= j < L }
  *     dense, causal     : { j : 0 <= j <= L - n_q + i }   (bottom-right)
  *     gather            : { idx[b,i,t] : 0 <= t < K, 0 <= idx[b,i,t] < cap }
+ *                         (with a per-cell bias: minus the cells whose bias
+ *                         bias[b,i,t] is -inf)
  *   with L = kv_lengths[b] clamped to [0, cap].
- *   s_j   = scale * sum_d q[b,i,h,d] * k[b,hk,j,d]
+ *   s_j   = scale * sum_d q[b,i,h,d] * k[b,hk,j,d]   (+ bias[b,i,t] for the
+ *           list entry t that names j: "qwen4exp : gather-based sparse
+ *           attention for QSA decode", llama.cpp #28213, Overview -- the
+ *           per-cell mask entries are gathered with the cells and added)
  *   out   = sum_{j in V} exp(s_j - max s) v[b,hk,j,:] / sum_{j in V} exp(s_j - max s)
  *   out   = 0 when V is empty.
  * k, v are the stored bf16 values, or int8 * fp32 scale for int8 caches
@@ -88,8 +93,8 @@ static double kv_at(const kv_src *src, int which, int64_t b, int64_t hk,
  * cache positions), weighted sum of the matching value rows. */
 static void attend_row(const kv_src *src, int64_t b, int64_t hk,
                        const double *qrow, int d, double scale,
-                       const int64_t *vis, int64_t n, double *score,
-                       double *orow)
+                       const int64_t *vis, const double *add, int64_t n,
+                       double *score, double *orow)
 {
     for (int dd = 0; dd < d; ++dd)
         orow[dd] = 0.0;
@@ -100,7 +105,7 @@ static void attend_row(const kv_src *src, int64_t b, int64_t hk,
         double dot = 0.0;
         for (int dd = 0; dd < d; ++dd)
             dot += qrow[dd] * kv_at(src, 0, b, hk, vis[t], dd);
-        score[t] = scale * dot;
+        score[t] = scale * dot + (add ? add[t] : 0.0);
         if (score[t] > mx)
             mx = score[t];
     }
@@ -116,10 +121,11 @@ static void attend_row(const kv_src *src, int64_t b, int64_t hk,
         orow[dd] /= den;
 }
 
-/* mode 0: dense prefix (causal or not); mode 1: index gather. */
+/* mode 0: dense prefix (causal or not); mode 1: index gather (bias: NULL,
+ * or one fp32 value per list entry added to its score, -inf dropping it). */
 static int run(int mode, const uint16_t *q, const int64_t *qs,
                const kv_src *src, const int32_t *kv_lengths,
-               const int32_t *idx, int64_t K, int B, int n_q, int Hq,
+               const int32_t *idx, const float *bias, int64_t K, int B, int n_q, int Hq,
                int Hkv, int d, int64_t cap, int causal, double scale,
                double *out)
 {
@@ -142,10 +148,11 @@ static int run(int mode, const uint16_t *q, const int64_t *qs,
         int64_t *vis = (int64_t *)malloc((size_t)(cnt > 0 ? cnt : 1) * sizeof *vis);
         double *score = (double *)malloc((size_t)(cnt > 0 ? cnt : 1) * sizeof *score);
         double *qrow = (double *)malloc((size_t)d * sizeof *qrow);
-        if (!vis || !score || !qrow) {
+        double *add = bias ? (double *)malloc((size_t)(cnt > 0 ? cnt : 1) * sizeof *add) : NULL;
+        if (!vis || !score || !qrow || (bias && !add)) {
 #pragma omp atomic write
             err = -2;
-            free(vis); free(score); free(qrow);
+            free(vis); free(score); free(qrow); free(add);
             continue;
         }
         for (int dd = 0; dd < d; ++dd)
@@ -162,12 +169,17 @@ static int run(int mode, const uint16_t *q, const int64_t *qs,
                 vis[n++] = j;
         } else {
             const int32_t *list = idx + (b * n_q + i) * K;
+            const float *brow = bias ? bias + (b * n_q + i) * K : NULL;
             for (int64_t t = 0; t < K; ++t)
-                if (list[t] >= 0 && (int64_t)list[t] < cap)
+                if (list[t] >= 0 && (int64_t)list[t] < cap &&
+                    !(brow && isinf(brow[t]) && brow[t] < 0)) {
+                    if (brow)
+                        add[n] = (double)brow[t];
                     vis[n++] = list[t];
+                }
         }
-        attend_row(src, b, hk, qrow, d, scale, vis, n, score, orow);
-        free(vis); free(score); free(qrow);
+        attend_row(src, b, hk, qrow, d, scale, vis, add, n, score, orow);
+        free(vis); free(score); free(qrow); free(add);
     }
     return err;
 }
@@ -182,7 +194,7 @@ int fdo_dense(const uint16_t *q, const int64_t *q_strides,
 {
     kv_src src = {k, v, kv_int8, k_strides, v_strides, k_scale, v_scale,
                   scale_strides};
-    return run(0, q, q_strides, &src, kv_lengths, NULL, 0, B, n_q, Hq, Hkv,
+    return run(0, q, q_strides, &src, kv_lengths, NULL, NULL, 0, B, n_q, Hq, Hkv,
                d, cap, causal, scale, out);
 }
 
@@ -196,8 +208,24 @@ int fdo_gather(const uint16_t *q, const int64_t *q_strides,
 {
     kv_src src = {k, v, kv_int8, k_strides, v_strides, k_scale, v_scale,
                   scale_strides};
-    return run(1, q, q_strides, &src, NULL, idx, K, B, n_q, Hq, Hkv, d, cap,
+    return run(1, q, q_strides, &src, NULL, idx, NULL, K, B, n_q, Hq, Hkv, d, cap,
                0, scale, out);
+}
+
+/* Index gather with one additive fp32 bias per list entry, bias [B, n_q, K]
+ * contiguous, aligned with idx. */
+int fdo_gather_bias(const uint16_t *q, const int64_t *q_strides,
+                    const void *k, const int64_t *k_strides,
+                    const void *v, const int64_t *v_strides, int kv_int8,
+                    const float *k_scale, const float *v_scale,
+                    const int64_t *scale_strides, const int32_t *idx,
+                    const float *bias, int64_t K, int B, int n_q, int Hq,
+                    int Hkv, int d, int64_t cap, double scale, double *out)
+{
+    kv_src src = {k, v, kv_int8, k_strides, v_strides, k_scale, v_scale,
+                  scale_strides};
+    return run(1, q, q_strides, &src, NULL, idx, bias, K, B, n_q, Hq, Hkv, d,
+               cap, 0, scale, out);
 }
 
 void fdo_set_threads(int n)

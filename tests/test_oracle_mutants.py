@@ -17,12 +17,15 @@ import oracle
 from oracle import bruteforce
 from decode_attention_preallocated_gb300 import workloads as W
 from golden_cases import fixture_names, load as load_fixture
-from test_oracle_pins import dense_mask, dq, gather_mask, sdpa_masked
+from test_oracle_pins import dense_mask, dq, gather_mask, sdpa_bias, sdpa_masked
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "fd_oracle.c")
 
 MUTANTS = {
-    "drop_scale": ("score[t] = scale * dot;", "score[t] = dot;"),
+    "drop_scale": ("score[t] = scale * dot +", "score[t] = dot +"),
+    "bias_ignored": ("add[n] = (double)brow[t];", "add[n] = 0.0;"),
+    "bias_negated": ("add[n] = (double)brow[t];", "add[n] = -(double)brow[t];"),
+    "bias_neg_inf_kept": ("!(brow && isinf(brow[t]) && brow[t] < 0)", "1"),
     "causal_off_by_one": ("L - n_q + i : L - 1", "L - n_q + i - 1 : L - 1"),
     "causal_wrong_direction": ("L - n_q + i : L - 1", "L - 1 - i : L - 1"),
     "gqa_modulo_mapping": ("const int64_t hk = h / g;", "const int64_t hk = h % Hkv;"),
@@ -50,6 +53,17 @@ def build_mutant(name, tmpdir):
     subprocess.run(["gcc", "-O1", "-fPIC", "-shared", "-fopenmp", "-std=c99",
                     "-o", path_so, path_c, "-lm"], check=True)
     return oracle.load_variant(path_so)
+
+
+def gather_bias_values(idx, seed):
+    """Seeded per-cell biases for a gather list: N(0, 2), a few -inf, and one
+    row that is -inf throughout."""
+    g = torch.Generator().manual_seed(seed)
+    bias = torch.randn(idx.shape, generator=g) * 2.0
+    bias[0, 0, 1] = -float("inf")
+    bias[-1, -1, 3] = -float("inf")
+    bias[0, -1, :] = -float("inf")
+    return bias
 
 
 def battery(lib):
@@ -82,6 +96,12 @@ def battery(lib):
                       gather_mask(inp.idx, 40), inp.scale)
     if not np.allclose(out, ref.numpy(), rtol=0, atol=1e-12):
         failed.append("sdpa_gather")
+    bias = gather_bias_values(inp.idx, 10)
+    out = lib.gather(inp.q, inp.k, inp.v, inp.idx, inp.scale, bias=bias)
+    ref = sdpa_bias(inp.q.double(), inp.k.double(), inp.v.double(), inp.idx, bias, 40,
+                    inp.scale)
+    if not np.allclose(out, ref.numpy(), rtol=0, atol=1e-12):
+        failed.append("sdpa_gather_bias")
     inp = W.dense_inputs(2, 2, 4, 2, 4, 9, [6, 9], 11, True)
     out = lib.dense(inp.q, inp.k, inp.v, inp.kv_lengths, 2, True, inp.scale)
     ref = bruteforce.attend(inp.q.double().tolist(), inp.k.double().tolist(),

@@ -45,6 +45,31 @@ def sdpa_masked(q, k, v, mask, scale):
     return out
 
 
+def sdpa_bias(q, k, v, idx, bias, cap, scale):
+    """torch SDPA in float64 with an additive float mask built from a gather
+    list and its per-cell biases (cells not listed, out of range or -inf are
+    -inf); rows with nothing visible -> 0.  idx must list distinct cells."""
+    B, n_q, K = idx.shape
+    m = torch.full((B, n_q, cap), -float("inf"), dtype=torch.float64)
+    for b in range(B):
+        for i in range(n_q):
+            for t, j in enumerate(idx[b, i].tolist()):
+                if 0 <= j < cap:
+                    m[b, i, j] = float(bias[b, i, t])
+    g = q.shape[2] // k.shape[1]
+    kk = k.repeat_interleave(g, dim=1)
+    vv = v.repeat_interleave(g, dim=1)
+    qq = q.permute(0, 2, 1, 3)
+    visible = torch.isfinite(m)
+    safe = torch.where(visible, m, torch.full_like(m, -1e300))
+    mm = safe[:, None, :, :].expand(B, q.shape[2], n_q, cap)
+    out = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=mm, scale=scale)
+    out = out.permute(0, 2, 1, 3).contiguous()
+    empty = ~visible.any(dim=-1)
+    out[empty[:, :, None, None].expand_as(out)] = 0.0
+    return out
+
+
 def dense_mask(lengths, n_q, cap, causal):
     """Visible-key mask built from the definition by hand."""
     B = len(lengths)
