@@ -204,7 +204,8 @@ def call_fn(inp, out, ws, kernel, num_ctas=0):
                                        workspace=ws, kernel=kernel, num_ctas=num_ctas)
     if inp.idx is not None:
         return lambda: fd.decode_gather(inp.q, inp.k, inp.v, inp.idx, scale=inp.scale, out=out,
-                                        workspace=ws, kernel=kernel, num_ctas=num_ctas)
+                                        workspace=ws, kernel=kernel, num_ctas=num_ctas,
+                                        bias=getattr(inp, "bias", None))
     if inp.k.dtype == torch.int8:
         return lambda: fd.decode_int8(inp.q, inp.k, inp.v, inp.k_scale, inp.v_scale,
                                       inp.kv_lengths, n_q=inp.n_q, causal=inp.causal,
@@ -421,6 +422,13 @@ def extras(args, device, stream, peak, kernel):
         inp = W.dense_inputs(1, 4, 16, 4, 256, cap, [3000], 1, True, device=device)
         measure("mtp_verify_cap%d" % cap, inp)
         del inp
+    # gather with a per-entry bias (N(0, 2), as a mask-derived list carries)
+    inp = W.workload("gather", seed=1, device=device)
+    g = torch.Generator(device=device)
+    g.manual_seed(3)
+    inp.bias = torch.randn(inp.idx.shape, generator=g, device=device) * 2.0
+    measure("gather_bias", inp)
+    del inp
     # gather: time follows the list length, not the capacity
     for K in (512, 2048, 8192):
         for cap in (8192, 32768, 131072):

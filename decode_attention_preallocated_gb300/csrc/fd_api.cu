@@ -126,6 +126,7 @@ struct Call {
     // array to update at the end of the launch (or null)
     const fd_tensor *k_new = nullptr, *v_new = nullptr;
     int32_t *len_update = nullptr;
+    const float *bias = nullptr;   // gather: per-entry score bias (or null)
 };
 
 int run(const Call &c) {
@@ -223,6 +224,7 @@ int run(const Call &c) {
     }
     p.kv_lengths = c.kv_lengths;
     p.idx = c.idx;
+    p.bias = c.mode == fd::kGather ? c.bias : nullptr;
     if (paged) {
         p.block_table = c.block_table;
         p.page_size = (int32_t)rows_per;
@@ -304,6 +306,19 @@ int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache, const fd_tens
     if (scale == 0.f && q->ndim == 4 && q->shape[3] > 0) scale = 1.f / sqrtf((float)q->shape[3]);
     Call c{q, k_cache, v_cache, nullptr, nullptr, out, nullptr, idx, idx_len, nullptr, 0,
            q->ndim == 4 ? (int32_t)q->shape[1] : 0, 0, scale, fd::kGather, 0, opts};
+    return run(c);
+}
+
+int fd_decode_gather_bias(const fd_tensor *q, const fd_tensor *k_cache,
+                          const fd_tensor *v_cache, const int32_t *idx, const float *bias,
+                          int32_t idx_len, const fd_tensor *out, const fd_opts *opts) {
+    if (!q || !opts) return FD_ERR_ARG;
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 3)) return FD_ERR_ALIGN;
+    float scale = opts->scale;
+    if (scale == 0.f && q->ndim == 4 && q->shape[3] > 0) scale = 1.f / sqrtf((float)q->shape[3]);
+    Call c{q, k_cache, v_cache, nullptr, nullptr, out, nullptr, idx, idx_len, nullptr, 0,
+           q->ndim == 4 ? (int32_t)q->shape[1] : 0, 0, scale, fd::kGather, 0, opts};
+    c.bias = bias;
     return run(c);
 }
 

@@ -43,6 +43,8 @@ struct Params {
     const float *v_scale;  int64_t vss[3];
     const int32_t *kv_lengths;
     const int32_t *idx;
+    const float *bias;     // gather: optional [B, n_q, idx_len] fp32 added to each
+                           // entry's score (-inf drops the entry)
     // paged caches: logical position j of sequence b lives at row j % page_size
     // of pool page block_table[b * max_pages + j / page_size]; the caches'
     // strides are then (page, kv head, row in page); cap = max_pages * page_size

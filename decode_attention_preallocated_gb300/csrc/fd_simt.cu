@@ -36,7 +36,7 @@ struct Layout {
                + 3 * (size_t)T * 8           // positions, K and V row offsets (int64,
                                              // 8-byte aligned here)
                + (size_t)rows * (T + 1) * 4  // P
-               + 4 * (size_t)T * 4           // k scale, v scale, valid, appended
+               + 5 * (size_t)T * 4           // k scale, v scale, valid, appended, bias
                + 3 * (size_t)rows * 4;       // m, l, alpha
     }
 };
@@ -70,7 +70,8 @@ __device__ __forceinline__ void simt_body(const Params &p) {
     float *vsc = ksc + T;
     int *tval = reinterpret_cast<int *>(vsc + T);
     int *tnew = tval + T;                      // fused append: the row comes from k_new / v_new
-    float *m_s = reinterpret_cast<float *>(tnew + T);
+    float *tbias = reinterpret_cast<float *>(tnew + T);   // gather: entry bias (log2 units)
+    float *m_s = tbias + T;
     float *l_s = m_s + rows;
     float *a_s = l_s + rows;
 
@@ -150,12 +151,15 @@ __device__ __forceinline__ void simt_body(const Params &p) {
             if (tid < T) {
                 int64_t pos = j0 + tid;
                 int ok = tid < ntok;
+                float bias = 0.f;
                 if (ok && list) {
                     const int64_t cell = list[pos];
                     if (cell >= p.cap) atomicOr(p.status, kDevBadIndex);
-                    ok = cell >= 0 && cell < p.cap;
+                    if (p.bias) bias = p.bias[((int64_t)b * p.n_q + m0.i) * p.idx_len + pos];
+                    ok = cell >= 0 && cell < p.cap && bias != neg_inf();
                     pos = cell;
                 }
+                tbias[tid] = bias * 1.4426950408889634f;
                 // Where the position's row lives: (sequence, kv head, position)
                 // of a flat cache, (page, kv head, row in page) of a paged one.
                 int64_t o0 = b, o2 = pos;
@@ -269,7 +273,7 @@ __device__ __forceinline__ void simt_body(const Params &p) {
                         const int i = r % p.n_q;
                         vis = vis && tpos[lane] <= len - p.n_q + i;
                     }
-                    const float sc = vis ? acc[k] * ksc[lane] * p.scale_log2 : neg_inf();
+                    const float sc = vis ? acc[k] * ksc[lane] * p.scale_log2 + tbias[lane] : neg_inf();
                     float tmax = sc;
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1)

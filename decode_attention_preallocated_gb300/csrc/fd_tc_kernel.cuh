@@ -1221,11 +1221,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             // gather: the list cell this lane's position holds, read one tile
             // ahead; a cell is visible if 0 <= cell < cap (cap or more is
             // flagged FD_DEV_BAD_INDEX, negative is padding).
+            // With a bias list, the entry's bias (log2 units) rides along;
+            // -inf drops the entry.
             const int32_t *ilist = GA ? p.idx + ((int64_t)w.b * p.n_q + w.i) * p.idx_len : nullptr;
+            const float *blist =
+                GA && p.bias ? p.bias + ((int64_t)w.b * p.n_q + w.i) * p.idx_len : nullptr;
             int cell_n = -1;
+            float bias_n = 0.f;
             auto load_cell = [&](int64_t jj) {
                 const int64_t pos = (tt0 + jj) * TT + wt;
                 cell_n = pos < p.idx_len ? __ldg(ilist + pos) : -1;
+                if (blist) bias_n = pos < p.idx_len ? __ldg(blist + pos) : 0.f;
             };
             if (GA) load_cell(0);
             for (int64_t j = 0; j < n_in && ok; ++j) {
@@ -1238,11 +1244,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 // L - n_q + i for the row's query index i.  Gather: a valid
                 // cell of the list.  Paged: a position on a page of the pool.
                 bool in_len = token >= y0 && token < L;
+                float bl = 0.f;
                 if (GA) {
                     const int cell = cell_n;
+                    const float cb = bias_n;
                     if (j + 1 < n_in) load_cell(j + 1);
                     if (cell >= p.cap) atomicOr(p.status, kDevBadIndex);
-                    in_len = in_len && cell >= 0 && cell < p.cap;
+                    in_len = in_len && cell >= 0 && cell < p.cap && cb != neg_inf();
+                    bl = cb * 1.4426950408889634f;
                 }
                 const int pg_next = pg_n;
                 if (PG) {
@@ -1265,7 +1274,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 #pragma unroll
                 for (int r = 0; r < NH; ++r) {
                     const bool vis = in_len && cb0 + r < rows && token <= lim[r];
-                    sv[r] = vis ? sv[r] * sl : neg_inf();
+                    if (GA)
+                        sv[r] = vis ? __fmaf_rn(sv[r], sl, bl) : neg_inf();
+                    else
+                        sv[r] = vis ? sv[r] * sl : neg_inf();
                 }
                 // Refresh the running maxima only when some score passes
                 // mrun + kRescaleSlack (always on a segment's first tile).

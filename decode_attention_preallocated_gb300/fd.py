@@ -72,6 +72,9 @@ _SIGNATURES = [
     ("fd_decode_gather", ctypes.c_int,
      [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_int32,
       _P(FdTensor), _P(FdOpts)]),
+    ("fd_decode_gather_bias", ctypes.c_int,
+     [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_void_p,
+      ctypes.c_int32, _P(FdTensor), _P(FdOpts)]),
     ("fd_decode_append", ctypes.c_int,
      [_P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor),
       ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _P(FdTensor),
@@ -429,9 +432,11 @@ def decode_paged(q, k_pages, v_pages, block_table, kv_lengths, n_q=None,
 
 def decode_gather(q, k_cache, v_cache, idx, scale=None, out=None,
                   out_dtype=torch.bfloat16, num_ctas=0, kernel=FD_KERNEL_AUTO,
-                  stream=None, workspace: Optional[Workspace] = None):
+                  stream=None, workspace: Optional[Workspace] = None, bias=None):
     """Attention of q [B, n_q, Hq, d] over the cache cells listed in
-    idx [B, n_q, K] (int32, contiguous, on the device; < 0 = padding)."""
+    idx [B, n_q, K] (int32, contiguous, on the device; < 0 = padding).
+    bias (optional): fp32 [B, n_q, K] contiguous, added to each entry's
+    score (-inf drops the entry)."""
     B, nq, Hq, d = q.shape
     Hkv = k_cache.shape[1]
     if not idx.is_contiguous() or idx.dtype != torch.int32 or idx.dim() != 3:
@@ -441,6 +446,17 @@ def decode_gather(q, k_cache, v_cache, idx, scale=None, out=None,
                            kernel, stream, workspace)
     tq, tk, tv, to = map(as_fd_tensor, (q, k_cache, v_cache, out))
     o = _opts(sh, ws, num_ctas, kernel, 0.0 if scale is None else scale)
+    if bias is not None:
+        if (not bias.is_contiguous() or bias.dtype != torch.float32
+                or tuple(bias.shape) != tuple(idx.shape)):
+            raise ValueError("bias must be a contiguous float32 tensor shaped like idx")
+        with _on_device(q.device):
+            rc = lib().fd_decode_gather_bias(ctypes.byref(tq), ctypes.byref(tk),
+                                             ctypes.byref(tv), idx.data_ptr(), bias.data_ptr(),
+                                             int(idx.shape[2]), ctypes.byref(to),
+                                             ctypes.byref(o))
+        _check(rc, "fd_decode_gather_bias")
+        return out
     with _on_device(q.device):
         rc = lib().fd_decode_gather(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
                                     idx.data_ptr(), int(idx.shape[2]), ctypes.byref(to),

@@ -165,6 +165,19 @@ int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache,
                      const fd_opts *opts);
 
 /*
+ * Index-gather decode with a per-entry score bias: as fd_decode_gather, and
+ * bias[b, i, t] (fp32, device, [B, n_q, idx_len] contiguous, aligned with
+ * idx) is added to the scaled score of list entry t ("qwen4exp :
+ * gather-based sparse attention for QSA decode", llama.cpp #28213, Overview:
+ * the mask entries are gathered with the cells).  An entry whose bias is
+ * -inf is dropped, exactly as if it were padding; every other bias must be
+ * finite.  bias = NULL is fd_decode_gather.
+ */
+int fd_decode_gather_bias(const fd_tensor *q, const fd_tensor *k_cache,
+                          const fd_tensor *v_cache, const int32_t *idx,
+                          const float *bias, int32_t idx_len,
+                          const fd_tensor *out, const fd_opts *opts);
+/*
  * Dense prefix decode with a fused K/V append (bf16 caches): one launch
  * writes the step's new rows into the caches and attends over the prefix
  * including them, as flash_attn_with_kvcache does with k / v and
