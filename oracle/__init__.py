@@ -198,6 +198,41 @@ def dense(q, k, v, kv_lengths, n_q, causal, scale, k_scale=None,
     return out
 
 
+def topk_blocks(scores, kv_lengths, block_size, top_k):
+    """Index lists from block scores: top-k over blocks, then only the
+    winners expanded to cells ("qwen4exp : gather-based sparse attention for
+    QSA decode", llama.cpp #28213, review discussion: take top-k over blocks
+    and expand only the winners).
+
+    scores: fp32 [B, n_q, n_blocks], block j covering cells
+    j*block_size .. (j+1)*block_size - 1; kv_lengths [B] (host).  For row
+    (b, i), with L = kv_lengths[b] clamped to [0, n_blocks*block_size], the
+    candidates are the blocks whose first cell is below L; the top_k highest
+    scores win, ties going to the lower block index.  The winners are listed
+    in increasing block order, each expanded to its block_size cells, cells
+    at or past L written as -1, and the list padded with -1 to
+    top_k*block_size entries.  Returns int32 [B, n_q, top_k*block_size].
+    """
+    sc = np.asarray(_as_np(scores), dtype=np.float32)
+    B, n_q, nb = sc.shape
+    lens = np.asarray(_as_np(kv_lengths), dtype=np.int64).reshape(B)
+    W = top_k * block_size
+    out = np.full((B, n_q, W), -1, dtype=np.int32)
+    for b in range(B):
+        L = int(min(max(lens[b], 0), nb * block_size))
+        nvalid = min(nb, -(-L // block_size))
+        cand = np.arange(nvalid)
+        for i in range(n_q):
+            s = sc[b, i, :nvalid].astype(np.float64)
+            # sort by score descending, then block index ascending
+            order = np.lexsort((cand, -s))
+            chosen = np.sort(order[:top_k])
+            cells = (chosen[:, None] * block_size + np.arange(block_size)[None, :]).ravel()
+            cells = np.where(cells < L, cells, -1)
+            out[b, i, :cells.size] = cells
+    return out
+
+
 def append(q, k, v, k_new, v_new, kv_lengths, causal, scale):
     """One decode step with an append, as flash_attn_with_kvcache defines it
     (ComfyUI #16509, Existing Solutions): the new rows go into the cache at
