@@ -393,6 +393,7 @@ def extras(args, device, stream, peak, kernel):
     capacity-independence check and the depth sweep (µs/call and GB/s from
     CUDA graph replay; us_python_loop: the same calls launched one by one
     from Python, which host overhead bounds for the small workloads)."""
+    from decode_attention_preallocated_gb300 import fd
     from decode_attention_preallocated_gb300 import workloads as W
     res = {}
 
@@ -459,7 +460,44 @@ def extras(args, device, stream, peak, kernel):
         measure(name, inp, 50)
         del inp
         torch.cuda.empty_cache()
+    # block top-k selection (gather lists from block scores), alone and
+    # followed by the gather it feeds
+    def measure_fn(tag, fn, nbytes, n=200):
+        for _ in range(5):
+            fn()
+        calls = min(n, GRAPH_CALLS)
+        g = capture(fn, calls, stream)
+        ms = time_graph(g, calls, max(1, n // calls), stream)
+        del g
+        res[tag] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
+                    "frac": round(nbytes / ms / 1e6 / peak, 4), "bytes": nbytes}
+
+    for tag, B, n_q, nb, bs, k in (("topk_131k_1row", 1, 1, 2048, 64, 32),
+                                   ("topk_32k_48rows", 8, 6, 512, 64, 32),
+                                   ("topk_2m_1row", 1, 1, 32768, 64, 32)):
+        g = torch.Generator(device=device)
+        g.manual_seed(5)
+        scores = torch.randn((B, n_q, nb), generator=g, device=device)
+        lens = torch.full((B,), nb * bs, dtype=torch.int32, device=device)
+        idx = torch.empty((B, n_q, k * bs), dtype=torch.int32, device=device)
+        measure_fn(tag, lambda: fd.topk_blocks(scores, lens, bs, k, out=idx),
+                   scores.numel() * 4 + idx.numel() * 4)
     inp = W.dense_inputs(1, 1, 32, 4, 128, 131072, [131072], 1, False, device=device)
+    g = torch.Generator(device=device)
+    g.manual_seed(6)
+    scores = torch.randn((1, 1, 2048), generator=g, device=device)
+    idx = torch.empty((1, 1, 2048), dtype=torch.int32, device=device)
+    out_g = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=device)
+    ws_g = workspace_for(inp, device)
+
+    def select_gather():
+        fd.topk_blocks(scores, inp.kv_lengths, 64, 32, out=idx)
+        fd.decode_gather(inp.q, inp.k, inp.v, idx, scale=inp.scale, out=out_g, workspace=ws_g,
+                         kernel=kernel)
+
+    measure_fn("select_gather_131k_32q4kv", select_gather,
+               2048 * 4 * 2 + 2048 * 4 * 128 * 2 * 2)
+    ws_g.close()
     measure("dense_scan_131k_32q4kv", inp, 50)
     del inp
     for L in (32768, 65536, 131072):

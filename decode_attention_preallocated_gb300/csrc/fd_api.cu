@@ -309,6 +309,24 @@ int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache, const fd_tens
     return run(c);
 }
 
+int fd_topk_blocks(const float *scores, int32_t B, int32_t n_q, int32_t n_blocks,
+                   const int32_t *kv_lengths, int32_t block_size, int32_t top_k, int32_t *idx,
+                   void *stream) {
+    if (!scores || !kv_lengths || !idx) return FD_ERR_ARG;
+    if (B < 1 || n_q < 1 || n_blocks < 1 || block_size < 1 || top_k < 1) return FD_ERR_ARG;
+    if ((int64_t)B * n_q > ((int64_t)1 << 31) - 1) return FD_ERR_ARG;
+    if (n_blocks > fd::kTopkMaxBlocks) return FD_ERR_UNSUPPORTED;
+    if ((int64_t)n_blocks * block_size >= ((int64_t)1 << 31) ||
+        (int64_t)top_k * block_size >= ((int64_t)1 << 28))
+        return FD_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(scores) & 3) || (reinterpret_cast<uintptr_t>(idx) & 3) ||
+        (reinterpret_cast<uintptr_t>(kv_lengths) & 3))
+        return FD_ERR_ALIGN;
+    const int rc = fd::launch_topk(scores, B, n_q, n_blocks, kv_lengths, block_size, top_k, idx,
+                                   static_cast<cudaStream_t>(stream));
+    return rc == 0 ? FD_OK : (rc == -2 ? FD_ERR_UNSUPPORTED : FD_ERR_CUDA);
+}
+
 int fd_decode_gather_bias(const fd_tensor *q, const fd_tensor *k_cache,
                           const fd_tensor *v_cache, const int32_t *idx, const float *bias,
                           int32_t idx_len, const fd_tensor *out, const fd_opts *opts) {

@@ -27,4 +27,12 @@ int launch_tc_paged(const Params &p, int num_ctas, cudaStream_t stream);
 // so num_ctas may not exceed the blocks resident at once (else -2).
 int launch_tc_append(const Params &p, int num_ctas, cudaStream_t stream);
 
+// Block top-k selection for the gather lists (fd_topk.cu): one thread block
+// per (sequence, query row); n_blocks <= kTopkMaxBlocks (their keys live in
+// shared memory).
+constexpr int kTopkMaxBlocks = 32768;
+int topk_max_blocks();
+int launch_topk(const float *scores, int B, int n_q, int n_blocks, const int32_t *kv_lengths,
+                int block_size, int top_k, int32_t *idx, cudaStream_t stream);
+
 }  // namespace fd

@@ -72,6 +72,9 @@ _SIGNATURES = [
     ("fd_decode_gather", ctypes.c_int,
      [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_int32,
       _P(FdTensor), _P(FdOpts)]),
+    ("fd_topk_blocks", ctypes.c_int,
+     [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+      ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
     ("fd_decode_gather_bias", ctypes.c_int,
      [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_void_p,
       ctypes.c_int32, _P(FdTensor), _P(FdOpts)]),
@@ -367,6 +370,26 @@ def decode_int8(q, k_cache, v_cache, k_scale, v_scale, kv_lengths, n_q=None,
                                   kv_lengths.data_ptr(), int(n_q), int(bool(causal)),
                                   float(scale), ctypes.byref(to), ctypes.byref(o))
     _check(rc, "fd_decode_int8")
+    return out
+
+
+def topk_blocks(scores, kv_lengths, block_size, top_k, out=None, stream=None):
+    """Gather lists from block scores: scores fp32 [B, n_q, n_blocks]
+    (contiguous, on the device), kv_lengths int32 [B].  Returns (or fills)
+    idx int32 [B, n_q, top_k*block_size]: the top_k blocks of each row in
+    increasing order, expanded to cells, -1 past the length or unused."""
+    if not scores.is_cuda or scores.dtype != torch.float32 or scores.dim() != 3 \
+            or not scores.is_contiguous():
+        raise ValueError("scores must be a contiguous CUDA float32 [B, n_q, n_blocks] tensor")
+    B, n_q, nb = scores.shape
+    W = int(top_k) * int(block_size)
+    if out is None:
+        out = torch.empty((B, n_q, W), dtype=torch.int32, device=scores.device)
+    sh = _stream_handle(stream, scores.device)
+    with _on_device(scores.device):
+        rc = lib().fd_topk_blocks(scores.data_ptr(), B, n_q, nb, kv_lengths.data_ptr(),
+                                  int(block_size), int(top_k), out.data_ptr(), sh)
+    _check(rc, "fd_topk_blocks")
     return out
 
 

@@ -165,6 +165,32 @@ int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache,
                      const fd_opts *opts);
 
 /*
+ * Gather lists from block scores (no counterpart call in the pages; the
+ * step they ask for next): for each (sequence b, query row i), top_k of the
+ * blocks are selected by score and only the winners are expanded to cells
+ * ("qwen4exp : gather-based sparse attention for QSA decode", llama.cpp
+ * #28213, review discussion: take top-k over blocks and expand only the
+ * winners, instead of selecting over every cell).
+ *   scores: device fp32 [B, n_q, n_blocks], contiguous; block j covers cells
+ *     j*block_size .. (j+1)*block_size - 1.  Scores must not be NaN.
+ *   kv_lengths: device int32 [B]; L_b clamped to [0, n_blocks*block_size].
+ *     The candidates of row (b, i) are the blocks whose first cell is below
+ *     L_b; the top_k highest scores win, ties going to the lower index
+ *     (-0 and +0 tie).
+ *   idx: device int32 [B, n_q, top_k*block_size], contiguous, written: the
+ *     winners in increasing block order, each as its block_size cells, cells
+ *     at or past L_b as -1, padded with -1 when fewer than top_k blocks are
+ *     candidates.  The result feeds fd_decode_gather (idx_len =
+ *     top_k*block_size).
+ *   n_blocks <= 32768 (FD_ERR_UNSUPPORTED beyond); n_blocks*block_size below
+ *   2^31.  Queued on `stream`; allocates nothing, reads nothing back,
+ *   graph-capturable.  Returns FD_OK or a negative FD_ERR_* code.
+ */
+int fd_topk_blocks(const float *scores, int32_t B, int32_t n_q,
+                   int32_t n_blocks, const int32_t *kv_lengths,
+                   int32_t block_size, int32_t top_k, int32_t *idx,
+                   void *stream);
+/*
  * Index-gather decode with a per-entry score bias: as fd_decode_gather, and
  * bias[b, i, t] (fp32, device, [B, n_q, idx_len] contiguous, aligned with
  * idx) is added to the scaled score of list entry t ("qwen4exp :

@@ -191,6 +191,19 @@ def test_append_validation(L):
     assert rc == fd.FD_ERR_ARG                                   # bf16 caches only
 
 
+def test_topk_validation(L):
+    # every check fails before anything is launched
+    assert L.fd_topk_blocks(None, 1, 1, 8, 0x200000, 4, 2, 0x300000, None) == fd.FD_ERR_ARG
+    assert L.fd_topk_blocks(0x100000, 1, 1, 8, None, 4, 2, 0x300000, None) == fd.FD_ERR_ARG
+    assert L.fd_topk_blocks(0x100000, 1, 1, 8, 0x200000, 4, 2, None, None) == fd.FD_ERR_ARG
+    assert L.fd_topk_blocks(0x100000, 0, 1, 8, 0x200000, 4, 2, 0x300000, None) == fd.FD_ERR_ARG
+    assert L.fd_topk_blocks(0x100000, 1, 1, 8, 0x200000, 0, 2, 0x300000, None) == fd.FD_ERR_ARG
+    assert L.fd_topk_blocks(0x100000, 1, 1, 8, 0x200000, 4, 0, 0x300000, None) == fd.FD_ERR_ARG
+    assert L.fd_topk_blocks(0x100000, 1, 1, 32769, 0x200000, 4, 2, 0x300000,
+                            None) == fd.FD_ERR_UNSUPPORTED
+    assert L.fd_topk_blocks(0x100002, 1, 1, 8, 0x200000, 4, 2, 0x300000, None) == fd.FD_ERR_ALIGN
+
+
 def test_workspace_size_formula(L):
     n = L.fd_workspace_bytes(10, 24, 256, 300)
     floats = (10 + 300) * 24 * 258
