@@ -49,6 +49,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The waiting part of mbar_wait, out of line: for kernels whose hot loops
+// crowd the instruction caches (a call costs registers around it, so only
+// kernels with registers to spare take it).
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity,
+                                            volatile int *abort, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
 // Wait until the phase with the given parity has completed.  Gives up after
 // `limit_ns` (or when *abort is set by another thread) and returns false, so
 // no wait in the kernel can spin forever.

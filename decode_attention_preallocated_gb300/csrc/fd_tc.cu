@@ -1,7 +1,8 @@
 // fd_tc.cu -- launches of the tensor-core decode kernel (fd_tc_kernel.cuh)
-// over flat caches ([B, Hkv, cap, d], bf16 or int8) and in index-gather mode,
-// and the kernel-choice queries of the C ABI layer.  Paged caches are
-// launched from fd_tc_paged.cu.
+// over flat bf16 caches ([B, Hkv, cap, d]) and in index-gather mode, and the
+// kernel-choice queries of the C ABI layer.  Flat int8 caches are launched
+// from fd_tc_int8.cu, paged caches from fd_tc_paged.cu, fused appends from
+// fd_tc_append.cu.
 #include "fd_tc_kernel.cuh"
 
 namespace fd {
@@ -63,6 +64,7 @@ int launch_tc(const Params &p, int G, cudaStream_t st) {
     if (!tc_supports(p)) return -2;
     if (p.mode == kPaged) return launch_tc_paged(p, G, st);
     if (p.n_new > 0) return launch_tc_append(p, G, st);
+    if (p.mode == kDense && p.kv_int8) return launch_tc_int8(p, G, st);
     TcArgs args;
     memset(&args, 0, sizeof args);
     args.p = p;
@@ -87,10 +89,6 @@ int launch_tc(const Params &p, int G, cudaStream_t st) {
     if (!make_map(&args.tk, p.k, p.ks, p) || !make_map(&args.tv, p.v, p.vs, p) ||
         !make_qmap(&args.tq, p))
         return -5;
-    if (p.kv_int8)
-        return p.rows <= 8    ? launch_dn<128, 16, true, 8>(args, G, st)
-               : p.rows <= 16 ? launch_dn<128, 16, true>(args, G, st)
-                              : launch_dn<128, 32, true>(args, G, st);
     if (p.d == 128) return launch_d<128>(args, G, st);
     return launch_d<256>(args, G, st);
 }

@@ -573,6 +573,18 @@ __device__ __noinline__ void append_wait(const Params &p) {
     }
 }
 
+// Bounded mbarrier wait; the int8 kernels (registers to spare, hot loops
+// that crowd the instruction caches) keep only the first test inline.
+template <bool OOL>
+__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                         uint64_t limit_ns) {
+    if (OOL) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        return ptx::mbar_wait_slow(bar, parity, abort, limit_ns);
+    }
+    return ptx::mbar_wait(bar, parity, abort, limit_ns);
+}
+
 template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant__ TcArgs a) {
     static_assert(!(GA && PG), "gather and paged loads are separate modes");
@@ -732,7 +744,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             // 128-byte swizzle the QK descriptors expect.
             if (lane == 0) {
                 if (piece > 0) {
-                    ok = ptx::mbar_wait(&bs->q_free, (piece - 1) & 1, abort_flag, kWaitNs);
+                    ok = bar_wait<(I8 && NV <= 8)>(&bs->q_free, (piece - 1) & 1, abort_flag, kWaitNs);
                     if (!ok) note_timeout(bs, p, 8, issued, piece);
                 }
                 if (ok) {
@@ -835,7 +847,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     if (!I8) {
                         const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
                         if (lane == 0) {
-                            ok = ptx::mbar_wait(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+                            ok = bar_wait<(I8 && NV <= 8)>(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
                             if (!ok) note_timeout(bs, p, 1, issued, 0);
                             else ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
                         }
@@ -860,7 +872,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         // each) into the raw ring
                         const uint32_t rs = issued % C::NRX, ph = (issued / C::NRX) & 1;
                         if (lane == 0) {
-                            ok = ptx::mbar_wait(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
+                            ok = bar_wait<(I8 && NV <= 8)>(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
                             if (!ok) note_timeout(bs, p, 1, issued, 0);
                             else ptx::mbar_arrive_expect_tx(&bs->raw_full[rs], C::RAW);
                         }
@@ -877,7 +889,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 } else if (lane == 0 && I8) {
                     // int8 codes -> raw ring (one box of TT positions x D codes)
                     const uint32_t rs = issued % C::NRX, ph = (issued / C::NRX) & 1;
-                    ok = ptx::mbar_wait(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
+                    ok = bar_wait<(I8 && NV <= 8)>(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
                     if (!ok) note_timeout(bs, p, 1, issued, 0);
                     if (ok) {
                         ptx::mbar_arrive_expect_tx(&bs->raw_full[rs], C::RAW);
@@ -887,7 +899,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     }
                 } else if (lane == 0) {
                     const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
-                    ok = ptx::mbar_wait(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+                    ok = bar_wait<(I8 && NV <= 8)>(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
                     if (!ok) note_timeout(bs, p, 1, issued, 0);
                     if (ok) {
                         ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
@@ -912,7 +924,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             const uint32_t n = issued < RING ? issued : RING;
             for (uint32_t k = 0; k < n; ++k) {
                 const uint32_t idx = issued - 1 - k;
-                ptx::mbar_wait(I8 ? &bs->raw_full[idx % RING] : &bs->slot_full[idx % RING],
+                bar_wait<(I8 && NV <= 8)>(I8 ? &bs->raw_full[idx % RING] : &bs->slot_full[idx % RING],
                                (idx / RING) & 1, abort_flag, kWaitNs);
             }
         }
@@ -926,11 +938,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         // S^T[pos, row] = sum_d K[pos, d] Q[row, d] for tile number tc.
         auto issue_qk = [&](uint32_t tc) -> bool {
             const uint32_t sb = tc & 1, u = tc >> 1, ki = k_fill(tc, pa), ks = ki % C::NS;
-            if (!ptx::mbar_wait(&bs->slot_full[ks], (ki / C::NS) & 1, abort_flag, kWaitNs)) {
+            if (!bar_wait<(I8 && NV <= 8)>(&bs->slot_full[ks], (ki / C::NS) & 1, abort_flag, kWaitNs)) {
                 note_timeout(bs, p, 3, tc, piece);
                 return false;
             }
-            if (!ptx::mbar_wait(&bs->s_free[sb], (u & 1) ^ 1, abort_flag, kWaitNs)) {
+            if (!bar_wait<(I8 && NV <= 8)>(&bs->s_free[sb], (u & 1) ^ 1, abort_flag, kWaitNs)) {
                 note_timeout(bs, p, 4, tc, piece);
                 return false;
             }
@@ -953,11 +965,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         auto issue_pv = [&](uint32_t tc, bool first) -> bool {
             const uint32_t vi = v_fill(tc, pb), vs = vi % C::NS;
             const uint32_t ps = tc % C::PST, pu = tc / C::PST;
-            if (!ptx::mbar_wait(&bs->slot_full[vs], (vi / C::NS) & 1, abort_flag, kWaitNs)) {
+            if (!bar_wait<(I8 && NV <= 8)>(&bs->slot_full[vs], (vi / C::NS) & 1, abort_flag, kWaitNs)) {
                 note_timeout(bs, p, 6, tc, piece);
                 return false;
             }
-            if (!ptx::mbar_wait(&bs->p_full[ps], pu & 1, abort_flag, kWaitNs)) {
+            if (!bar_wait<(I8 && NV <= 8)>(&bs->p_full[ps], pu & 1, abort_flag, kWaitNs)) {
                 note_timeout(bs, p, 7, tc, piece);
                 return false;
             }
@@ -1001,7 +1013,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             if (lane == 0) {
                 // Software pipeline: QK of tile j+1 is issued before PV of
                 // tile j, so the next scores are ready when softmax finishes.
-                ok = ptx::mbar_wait(&bs->q_full, piece & 1, abort_flag, kWaitNs);
+                ok = bar_wait<(I8 && NV <= 8)>(&bs->q_full, piece & 1, abort_flag, kWaitNs);
                 if (!ok) note_timeout(bs, p, 2, tile_ctr, piece);
                 ptx::tc_fence_after();
                 ok = ok && issue_qk(tile_ctr);
@@ -1013,7 +1025,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         if (j + 2 == n_in) ptx::mma_commit(&bs->q_free);
                     }
                     if (j == 0 && piece > 0) {
-                        ok = ptx::mbar_wait(&bs->o_free, (piece - 1) & 1, abort_flag, kWaitNs);
+                        ok = bar_wait<(I8 && NV <= 8)>(&bs->o_free, (piece - 1) & 1, abort_flag, kWaitNs);
                         if (!ok) note_timeout(bs, p, 5, tile_ctr, piece);
                     }
                     ok = ok && issue_pv(tile_ctr + j, j == 0);
@@ -1029,7 +1041,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         // Drain: all MMAs issued by this thread complete before TMEM is freed.
         if (lane == 0 && issued_any) {
             ptx::mma_commit(&bs->exit_mma);
-            ptx::mbar_wait(&bs->exit_mma, 0, abort_flag, kWaitNs);
+            bar_wait<(I8 && NV <= 8)>(&bs->exit_mma, 0, abort_flag, kWaitNs);
         }
     } else if (I8 && warp >= 4) {
         // ------------------------------------- int8 -> bf16 widening (warps 4-7)
@@ -1051,7 +1063,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             const int64_t n_fill = 2 * (piece_end - t);
             for (int64_t k = 0; k < n_fill && ok; ++k, ++f) {
                 const uint32_t rs = f % C::NRX, ss = f % C::NS;
-                ok = ptx::mbar_wait(&bs->raw_full[rs], (f / C::NRX) & 1, abort_flag, kWaitNs);
+                ok = bar_wait<(I8 && NV <= 8)>(&bs->raw_full[rs], (f / C::NRX) & 1, abort_flag, kWaitNs);
                 if (!ok) { note_timeout(bs, p, 17, f, piece); break; }
                 // Thread ct takes 16 codes (dims 16*q16 .. 16*q16+15) of
                 // positions r0 + RSTEP*k: one 16-byte load and two swizzled
@@ -1080,7 +1092,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 // in registers; then wait for a bf16 slot the MMAs released.
                 ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive(&bs->raw_empty[rs]);
-                ok = ptx::mbar_wait(&bs->slot_empty[ss], ((f / C::NS) & 1) ^ 1, abort_flag, kWaitNs);
+                ok = bar_wait<(I8 && NV <= 8)>(&bs->slot_empty[ss], ((f / C::NS) & 1) ^ 1, abort_flag, kWaitNs);
                 if (!ok) { note_timeout(bs, p, 18, f, piece); break; }
 #pragma unroll
                 for (int k = 0; k < NK; ++k) {
@@ -1122,7 +1134,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         // the parity test cannot alias.
         auto wait_pv = [&](uint32_t k) -> bool {
             for (; o_seen <= k; ++o_seen)
-                if (!ptx::mbar_wait(&bs->o_done, o_seen & 1, abort_flag, kWaitNs)) {
+                if (!bar_wait<(I8 && NV <= 8)>(&bs->o_done, o_seen & 1, abort_flag, kWaitNs)) {
                     note_timeout(bs, p, 11, tile_ctr, piece);
                     return false;
                 }
@@ -1131,14 +1143,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         // Barrier over this warpgroup's 128 threads, bounded.
         auto wg_sync = [&]() -> bool {
             ptx::mbar_arrive(&bs->wg_bar[wg]);
-            if (ptx::mbar_wait(&bs->wg_bar[wg], (wg_ctr++) & 1, abort_flag, kWaitNs)) return true;
+            if (bar_wait<(I8 && NV <= 8)>(&bs->wg_bar[wg], (wg_ctr++) & 1, abort_flag, kWaitNs)) return true;
             note_timeout(bs, p, 10, tile_ctr, piece);
             return false;
         };
         // Barrier over both warpgroups, bounded.
         auto sm_sync = [&]() -> bool {
             ptx::mbar_arrive(&bs->sm_bar);
-            if (ptx::mbar_wait(&bs->sm_bar, (sm_ctr++) & 1, abort_flag, kWaitNs)) return true;
+            if (bar_wait<(I8 && NV <= 8)>(&bs->sm_bar, (sm_ctr++) & 1, abort_flag, kWaitNs)) return true;
             note_timeout(bs, p, 14, tile_ctr, piece);
             return false;
         };
@@ -1261,7 +1273,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 const float ksc = ksc_n, vsc = vsc_n;
                 if (I8 && j + 1 < n_in) load_scales(j + 1, pg_next);
                 pg_c = pg_next;
-                ok = ptx::mbar_wait(&bs->s_full[sb], u & 1, abort_flag, kWaitNs);
+                ok = bar_wait<(I8 && NV <= 8)>(&bs->s_full[sb], u & 1, abort_flag, kWaitNs);
                 if (!ok) { note_timeout(bs, p, 9, tile_ctr, piece); break; }
                 ptx::tc_fence_after();
                 float sv[NH];
@@ -1343,7 +1355,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 }
                 // P^T for the PV product.
                 const uint32_t ps = tile_ctr % C::PST, pu = tile_ctr / C::PST;
-                ok = ptx::mbar_wait(&bs->p_free[ps], (pu & 1) ^ 1, abort_flag, kWaitNs);
+                ok = bar_wait<(I8 && NV <= 8)>(&bs->p_free[ps], (pu & 1) ^ 1, abort_flag, kWaitNs);
                 if (!ok) { note_timeout(bs, p, 13, tile_ctr, piece); break; }
                 // PV of the previous tile must have completed before P of this
                 // tile is published (see wait_pv).
