@@ -79,13 +79,18 @@ def kv_bytes(lengths, Hkv, d, esize):
     return sum(int(L) for L in lengths) * Hkv * d * esize * 2
 
 
+# The sources the headline kernel (the tensor-core kernel over flat caches)
+# is built from: its template, its launch unit and the headers they include.
+TC_KERNEL_SOURCES = ("fd_device.cuh", "fd_internal.h", "fd_launch.h", "fd_ptx.cuh", "fd_tc.cu",
+                     "fd_tc_kernel.cuh")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_attention_preallocated_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in TC_KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 

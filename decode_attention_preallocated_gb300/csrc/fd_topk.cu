@@ -101,15 +101,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
         for (int shift = 24; shift >= 0; shift -= 8) {
             for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0u;
             __syncthreads();
-            // (keys of a warp that share a digit are counted by one atomic:
-            // the leading digits of similar scores crowd a few bins)
-            for (int j0 = 0; j0 < nvalid; j0 += kTopkThreads) {
-                const int j = j0 + tid;
-                const uint32_t k = j < nvalid ? keys[j] : 0u;
-                const bool match = j < nvalid && (k & mask) == prefix;
-                const uint32_t digit = match ? (k >> shift) & 255u : 256u;
-                const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-                if (match && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+            for (int j = tid; j < nvalid; j += kTopkThreads) {
+                const uint32_t k = keys[j];
+                if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
             }
             __syncthreads();
             if (warp == 0) {
