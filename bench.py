@@ -172,10 +172,30 @@ class ClockSampler:
 
 
 # -------------------------------------------------------------- workloads
-def make_inputs(name, seed, device):
-    """A named workload, or "sweep:L,B,Hq,Hkv,d,n_q": B sequences all of
-    length L in a cache of capacity L + 1000 (causal when n_q > 1)."""
+def append_inputs(name, seed, device):
+    """A named workload as one fused append step: its window's rows (n_q per
+    sequence) are new, written at L - n_q and attended; the lengths passed are
+    L - n_q, and the timed calls leave them there."""
     from decode_attention_preallocated_gb300 import workloads as W
+    inp = W.workload(name, seed=seed, device=device)
+    g = torch.Generator(device=device)
+    g.manual_seed(7)
+    B, n, _, d = inp.q.shape
+    Hkv = inp.k.shape[1]
+    inp.k_new = W.randn_bf16((B, n, Hkv, d), g, device)
+    inp.v_new = W.randn_bf16((B, n, Hkv, d), g, device)
+    inp.lengths_host = [L - n for L in inp.lengths_host]
+    inp.kv_lengths = inp.kv_lengths - n
+    return inp
+
+
+def make_inputs(name, seed, device):
+    """A named workload, "append_<workload>" (that workload as one fused
+    append step), or "sweep:L,B,Hq,Hkv,d,n_q": B sequences all of length L
+    in a cache of capacity L + 1000 (causal when n_q > 1)."""
+    from decode_attention_preallocated_gb300 import workloads as W
+    if name.startswith("append_"):
+        return append_inputs(name[len("append_"):], seed, device)
     if name.startswith("sweep:"):
         L, B, Hq, Hkv, d, nq = (int(x) for x in name[6:].split(","))
         return W.dense_inputs(B, nq, Hq, Hkv, d, L + 1000, [L] * B, seed, nq > 1,
@@ -444,16 +464,8 @@ def extras(args, device, stream, peak, kernel):
     torch.cuda.empty_cache()
     # fused append: the MTP-verify and ragged workloads as one step that
     # writes the window's rows (4 / 6 per sequence) and attends
-    for name, n in (("mtp_verify", 4), ("ragged", 6)):
-        inp = W.workload(name, seed=1, device=device)
-        g = torch.Generator(device=device)
-        g.manual_seed(7)
-        B, _, _, d = inp.q.shape
-        Hkv = inp.k.shape[1]
-        inp.k_new = W.randn_bf16((B, n, Hkv, d), g, device)
-        inp.v_new = W.randn_bf16((B, n, Hkv, d), g, device)
-        inp.lengths_host = [L - n for L in inp.lengths_host]
-        inp.kv_lengths = inp.kv_lengths - n
+    for name in ("mtp_verify", "ragged"):
+        inp = append_inputs(name, 1, device)
         measure("append_" + name, inp, 200 if name == "mtp_verify" else 50)
         del inp
         torch.cuda.empty_cache()
@@ -585,8 +597,8 @@ def run_fd(args):
     # q, both caches, kv_lengths (and the scales, index lists or block table
     # the workload has) from pinned host memory, decodes, and reads the output
     # back
-    names = [n for n in ("q", "k", "v", "kv_lengths", "k_scale", "v_scale", "idx", "block_table")
-             if getattr(inp, n) is not None]
+    names = [n for n in ("q", "k", "v", "kv_lengths", "k_scale", "v_scale", "idx", "block_table",
+                         "k_new", "v_new") if getattr(inp, n, None) is not None]
     host = {} if args.no_e2e else {n: getattr(inp, n).cpu().pin_memory() for n in names}
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in host.values())
