@@ -573,8 +573,11 @@ __device__ __noinline__ void append_wait(const Params &p) {
     }
 }
 
-// Bounded mbarrier wait; the int8 kernels (registers to spare, hot loops
-// that crowd the instruction caches) keep only the first test inline.
+// Bounded mbarrier wait.  Kernels whose hot loops crowd the instruction
+// caches keep only the first test inline and call the waiting loop: the int8
+// kernels in the producer, MMA and widening roles (few live registers
+// there), and in the softmax too where it has registers to spare (up to 8
+// rows).
 template <bool OOL>
 __device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                          uint64_t limit_ns) {
@@ -744,7 +747,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             // 128-byte swizzle the QK descriptors expect.
             if (lane == 0) {
                 if (piece > 0) {
-                    ok = bar_wait<(I8 && NV <= 8)>(&bs->q_free, (piece - 1) & 1, abort_flag, kWaitNs);
+                    ok = bar_wait<I8>(&bs->q_free, (piece - 1) & 1, abort_flag, kWaitNs);
                     if (!ok) note_timeout(bs, p, 8, issued, piece);
                 }
                 if (ok) {
@@ -847,7 +850,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     if (!I8) {
                         const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
                         if (lane == 0) {
-                            ok = bar_wait<(I8 && NV <= 8)>(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+                            ok = bar_wait<I8>(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
                             if (!ok) note_timeout(bs, p, 1, issued, 0);
                             else ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
                         }
@@ -872,7 +875,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         // each) into the raw ring
                         const uint32_t rs = issued % C::NRX, ph = (issued / C::NRX) & 1;
                         if (lane == 0) {
-                            ok = bar_wait<(I8 && NV <= 8)>(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
+                            ok = bar_wait<I8>(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
                             if (!ok) note_timeout(bs, p, 1, issued, 0);
                             else ptx::mbar_arrive_expect_tx(&bs->raw_full[rs], C::RAW);
                         }
@@ -889,7 +892,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 } else if (lane == 0 && I8) {
                     // int8 codes -> raw ring (one box of TT positions x D codes)
                     const uint32_t rs = issued % C::NRX, ph = (issued / C::NRX) & 1;
-                    ok = bar_wait<(I8 && NV <= 8)>(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
+                    ok = bar_wait<I8>(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
                     if (!ok) note_timeout(bs, p, 1, issued, 0);
                     if (ok) {
                         ptx::mbar_arrive_expect_tx(&bs->raw_full[rs], C::RAW);
@@ -899,7 +902,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     }
                 } else if (lane == 0) {
                     const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
-                    ok = bar_wait<(I8 && NV <= 8)>(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+                    ok = bar_wait<I8>(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
                     if (!ok) note_timeout(bs, p, 1, issued, 0);
                     if (ok) {
                         ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
@@ -924,7 +927,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             const uint32_t n = issued < RING ? issued : RING;
             for (uint32_t k = 0; k < n; ++k) {
                 const uint32_t idx = issued - 1 - k;
-                bar_wait<(I8 && NV <= 8)>(I8 ? &bs->raw_full[idx % RING] : &bs->slot_full[idx % RING],
+                bar_wait<I8>(I8 ? &bs->raw_full[idx % RING] : &bs->slot_full[idx % RING],
                                (idx / RING) & 1, abort_flag, kWaitNs);
             }
         }
@@ -938,11 +941,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         // S^T[pos, row] = sum_d K[pos, d] Q[row, d] for tile number tc.
         auto issue_qk = [&](uint32_t tc) -> bool {
             const uint32_t sb = tc & 1, u = tc >> 1, ki = k_fill(tc, pa), ks = ki % C::NS;
-            if (!bar_wait<(I8 && NV <= 8)>(&bs->slot_full[ks], (ki / C::NS) & 1, abort_flag, kWaitNs)) {
+            if (!bar_wait<I8>(&bs->slot_full[ks], (ki / C::NS) & 1, abort_flag, kWaitNs)) {
                 note_timeout(bs, p, 3, tc, piece);
                 return false;
             }
-            if (!bar_wait<(I8 && NV <= 8)>(&bs->s_free[sb], (u & 1) ^ 1, abort_flag, kWaitNs)) {
+            if (!bar_wait<I8>(&bs->s_free[sb], (u & 1) ^ 1, abort_flag, kWaitNs)) {
                 note_timeout(bs, p, 4, tc, piece);
                 return false;
             }
@@ -965,11 +968,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         auto issue_pv = [&](uint32_t tc, bool first) -> bool {
             const uint32_t vi = v_fill(tc, pb), vs = vi % C::NS;
             const uint32_t ps = tc % C::PST, pu = tc / C::PST;
-            if (!bar_wait<(I8 && NV <= 8)>(&bs->slot_full[vs], (vi / C::NS) & 1, abort_flag, kWaitNs)) {
+            if (!bar_wait<I8>(&bs->slot_full[vs], (vi / C::NS) & 1, abort_flag, kWaitNs)) {
                 note_timeout(bs, p, 6, tc, piece);
                 return false;
             }
-            if (!bar_wait<(I8 && NV <= 8)>(&bs->p_full[ps], pu & 1, abort_flag, kWaitNs)) {
+            if (!bar_wait<I8>(&bs->p_full[ps], pu & 1, abort_flag, kWaitNs)) {
                 note_timeout(bs, p, 7, tc, piece);
                 return false;
             }
@@ -1013,7 +1016,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             if (lane == 0) {
                 // Software pipeline: QK of tile j+1 is issued before PV of
                 // tile j, so the next scores are ready when softmax finishes.
-                ok = bar_wait<(I8 && NV <= 8)>(&bs->q_full, piece & 1, abort_flag, kWaitNs);
+                ok = bar_wait<I8>(&bs->q_full, piece & 1, abort_flag, kWaitNs);
                 if (!ok) note_timeout(bs, p, 2, tile_ctr, piece);
                 ptx::tc_fence_after();
                 ok = ok && issue_qk(tile_ctr);
@@ -1025,7 +1028,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         if (j + 2 == n_in) ptx::mma_commit(&bs->q_free);
                     }
                     if (j == 0 && piece > 0) {
-                        ok = bar_wait<(I8 && NV <= 8)>(&bs->o_free, (piece - 1) & 1, abort_flag, kWaitNs);
+                        ok = bar_wait<I8>(&bs->o_free, (piece - 1) & 1, abort_flag, kWaitNs);
                         if (!ok) note_timeout(bs, p, 5, tile_ctr, piece);
                     }
                     ok = ok && issue_pv(tile_ctr + j, j == 0);
@@ -1041,7 +1044,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         // Drain: all MMAs issued by this thread complete before TMEM is freed.
         if (lane == 0 && issued_any) {
             ptx::mma_commit(&bs->exit_mma);
-            bar_wait<(I8 && NV <= 8)>(&bs->exit_mma, 0, abort_flag, kWaitNs);
+            bar_wait<I8>(&bs->exit_mma, 0, abort_flag, kWaitNs);
         }
     } else if (I8 && warp >= 4) {
         // ------------------------------------- int8 -> bf16 widening (warps 4-7)
@@ -1063,7 +1066,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             const int64_t n_fill = 2 * (piece_end - t);
             for (int64_t k = 0; k < n_fill && ok; ++k, ++f) {
                 const uint32_t rs = f % C::NRX, ss = f % C::NS;
-                ok = bar_wait<(I8 && NV <= 8)>(&bs->raw_full[rs], (f / C::NRX) & 1, abort_flag, kWaitNs);
+                ok = bar_wait<I8>(&bs->raw_full[rs], (f / C::NRX) & 1, abort_flag, kWaitNs);
                 if (!ok) { note_timeout(bs, p, 17, f, piece); break; }
                 // Thread ct takes 16 codes (dims 16*q16 .. 16*q16+15) of
                 // positions r0 + RSTEP*k: one 16-byte load and two swizzled
@@ -1092,7 +1095,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 // in registers; then wait for a bf16 slot the MMAs released.
                 ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive(&bs->raw_empty[rs]);
-                ok = bar_wait<(I8 && NV <= 8)>(&bs->slot_empty[ss], ((f / C::NS) & 1) ^ 1, abort_flag, kWaitNs);
+                ok = bar_wait<I8>(&bs->slot_empty[ss], ((f / C::NS) & 1) ^ 1, abort_flag, kWaitNs);
                 if (!ok) { note_timeout(bs, p, 18, f, piece); break; }
 #pragma unroll
                 for (int k = 0; k < NK; ++k) {
