@@ -87,16 +87,20 @@ extern "C" {
                                     call's output is not valid              */
 
 /* kernel selection (fd_opts.kernel); AUTO takes the tensor-core kernel for
- * the dense modes it serves when q's base pointer and strides are 16-byte
- * aligned (q is read through a TMA tensor map there), the CUDA-core kernel
+ * the calls it serves when q's base pointer and strides are 16-byte aligned
+ * (q is read through a TMA tensor map there), the CUDA-core kernel
  * otherwise */
 #define FD_KERNEL_AUTO 0
 #define FD_KERNEL_SIMT 1         /* CUDA-core kernel, every mode           */
-#define FD_KERNEL_TC 2           /* tensor-core (tcgen05) kernel: dense
-                                    bf16 caches (head_dim 128/256, up to 64
-                                    rows) and dense int8 caches (head_dim
-                                    128, up to 32 rows), 16-byte aligned q
-                                    (else FD_ERR_UNSUPPORTED)              */
+#define FD_KERNEL_TC 2           /* tensor-core (tcgen05) kernel: bf16
+                                    caches (head_dim 128/256, up to 64
+                                    rows) and int8 caches (head_dim 128, up
+                                    to 32 rows), flat or paged (pools whose
+                                    rows form one strided 2-D array), the
+                                    fused append over flat bf16 caches,
+                                    and gather over bf16 caches whose rows
+                                    form one strided 2-D array; 16-byte
+                                    aligned q (else FD_ERR_UNSUPPORTED)    */
 
 #define FD_MAX_ROWS 64           /* query rows per kv head per launch unit */
 
