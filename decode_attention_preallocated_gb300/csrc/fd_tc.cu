@@ -69,8 +69,8 @@ int launch_tc(const Params &p, int G, cudaStream_t st) {
     memset(&args, 0, sizeof args);
     args.p = p;
     if (p.mode == kGather) {
-        int64_t rs, Y, g[3];
-        gather_rows(p, &rs, &Y, g);
+        int64_t rs = 0, Y = 0, g[3] = {0, 0, 0};
+        if (!gather_rows(p, &rs, &Y, g)) return -2;
         args.gs0 = g[0];
         args.gs1 = g[1];
         args.gs2 = g[2];
