@@ -1,0 +1,60 @@
+"""Host logic of bench.py (no GPU): the algorithmic bytes it divides by for
+every kind of call, the append workloads it builds, and the traffic record
+it reports only for the current kernel sources."""
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from decode_attention_preallocated_gb300 import workloads as W  # noqa: E402
+
+
+def test_bytes_count_the_filled_prefix_only():
+    inp = W.dense_inputs(2, 1, 8, 2, 128, 1000, [300, 17], 1, False)
+    assert bench.algorithmic_bytes(inp) == (300 + 17) * 2 * 128 * 2 * 2
+    i8 = W.dense_inputs(2, 1, 8, 2, 128, 1000, [300, 17], 1, False, int8=True)
+    assert bench.algorithmic_bytes(i8) == (300 + 17) * 2 * (128 * 2 + 8)
+
+
+def test_paged_bytes_equal_the_flat_bytes():
+    flat = W.dense_inputs(3, 2, 8, 2, 128, 640, [640, 5, 333], 2, True)
+    paged = W.paged_inputs(3, 2, 8, 2, 128, 64, 10, [640, 5, 333], 2, True)
+    assert bench.algorithmic_bytes(paged) == bench.algorithmic_bytes(flat)
+
+
+def test_gather_bytes_count_listed_cells():
+    inp = W.gather_inputs(1, 2, 8, 2, 128, 500, 40, 8, seed=3)
+    inp.idx[0, 0, :5] = -1
+    valid = 2 * 40 - 5
+    assert bench.algorithmic_bytes(inp) == valid * 2 * 128 * 2 * 2
+
+
+def test_append_inputs_and_bytes():
+    base = W.workload("mtp_verify", seed=1)
+    inp = bench.append_inputs("mtp_verify", 1, "cpu")
+    n = base.q.shape[1]
+    assert inp.k_new.shape == (1, n, 4, 256) and inp.v_new.shape == inp.k_new.shape
+    assert inp.kv_lengths.tolist() == [L - n for L in base.kv_lengths.tolist()]
+    assert inp.lengths_host == [L - n for L in base.lengths_host]
+    # the prefix read including the new rows, plus the new rows read and written
+    want = bench.kv_bytes(base.lengths_host, 4, 256, 2) + 2 * bench.kv_bytes([n], 4, 256, 2)
+    assert bench.algorithmic_bytes(inp) == want
+    assert bench.make_inputs("append_mtp_verify", 1, "cpu").k_new.shape == inp.k_new.shape
+
+
+def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
+    # the committed record matches the current sources; a record taken on
+    # other sources is not reported
+    assert bench.recorded_traffic("ragged") is not None
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "traffic_ragged.txt").write_text(
+        "kernel_sources: 0000000000000000\ndram_bytes_per_launch: 123\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    src = tmp_path / "decode_attention_preallocated_gb300"
+    os.symlink(os.path.join(ROOT, "decode_attention_preallocated_gb300"), src)
+    assert bench.recorded_traffic("ragged") is None
