@@ -35,7 +35,7 @@ def _rank_main(rank, world, port, out):
 
 def test_max_over_ranks_and_aggregate_with_two_gloo_ranks():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
     for rank in range(world):
         ms_max, gbs = out[rank]
