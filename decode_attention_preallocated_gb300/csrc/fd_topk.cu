@@ -10,7 +10,8 @@
 // memory; a radix select (four 8-bit digits, most significant first, one
 // 256-bin shared histogram per digit) finds the k-th largest key and how many
 // of the keys equal to it are taken; an ordered compaction (block-wide
-// scans) lists the winners in increasing block order, taking equal keys by
+// scans: per 1024-key chunk for few keys, over per-thread runs of 32 for
+// many) lists the winners in increasing block order, taking equal keys by
 // lowest index; the expansion writes block*size + c, or -1 past the length.
 // Scores are read once from HBM; everything else stays on chip.
 #include <cuda_runtime.h>
@@ -25,6 +26,8 @@ namespace {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kKeysPerThread = kTopkMaxBlocks / kTopkThreads;   // the compaction's run
+constexpr int kChunkedMax = 8192;   // up to here the chunked compaction is faster
 
 // Larger float -> larger key; -0 and +0 share a key, so they tie (and the
 // lower index wins), as they compare equal.
@@ -141,22 +144,60 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
         need_eq = sh_rem;
     }
 
-    // Ordered compaction, in place (a winner's slot never lies after its own
-    // index): winners are keys above the k-th, then keys equal to it by
-    // lowest index.
-    int nsel = 0, neq = 0;
-    for (int c0 = 0; c0 < nvalid; c0 += kTopkThreads) {
-        const int j = c0 + tid;
-        const uint32_t k = j < nvalid ? keys[j] : 0u;
-        const bool gt = j < nvalid && (take_all || k > kth);
-        const bool eq = j < nvalid && !take_all && k == kth;
+    // Ordered compaction, in place: winners are keys above the k-th, then
+    // keys equal to it by lowest index, listed in increasing order.
+    int nsel = 0;
+    if (nvalid <= kChunkedMax) {
+        // few keys: 1024-key chunks, two block-wide scans each (equal keys,
+        // then winners); a winner's slot never lies after its own index
+        int neq = 0;
+        for (int c0 = 0; c0 < nvalid; c0 += kTopkThreads) {
+            const int j = c0 + tid;
+            const uint32_t k = j < nvalid ? keys[j] : 0u;
+            const bool gt = j < nvalid && (take_all || k > kth);
+            const bool eq = j < nvalid && !take_all && k == kth;
+            int teq, tsel;
+            const int eq_rank = neq + block_exclusive_scan(eq ? 1 : 0, &teq, wsum);
+            const bool sel = gt || (eq && eq_rank < need_eq);
+            const int pos = nsel + block_exclusive_scan(sel ? 1 : 0, &tsel, wsum);
+            if (sel) keys[pos] = (uint32_t)j;
+            nsel += tsel;
+            neq += teq;
+            __syncthreads();
+        }
+    } else {
+        // many keys: thread t owns the run t*KPT .. t*KPT+KPT-1 (held in
+        // registers), so two scans in all give every thread its place
+        uint32_t run[kKeysPerThread];
+        const int r0 = tid * kKeysPerThread;
+        int n_eq = 0, n_gt = 0;
+#pragma unroll
+        for (int q = 0; q < kKeysPerThread; ++q) {
+            const int j = r0 + q;
+            run[q] = j < nvalid ? keys[j] : 0u;
+            if (j < nvalid) {
+                if (take_all || run[q] > kth) ++n_gt;
+                else if (run[q] == kth) ++n_eq;
+            }
+        }
         int teq, tsel;
-        const int eq_rank = neq + block_exclusive_scan(eq ? 1 : 0, &teq, wsum);
-        const bool sel = gt || (eq && eq_rank < need_eq);
-        const int pos = nsel + block_exclusive_scan(sel ? 1 : 0, &tsel, wsum);
-        if (sel) keys[pos] = (uint32_t)j;
-        nsel += tsel;
-        neq += teq;
+        const int eq_before = block_exclusive_scan(n_eq, &teq, wsum);
+        int eq_take = need_eq - eq_before;
+        eq_take = eq_take < 0 ? 0 : (eq_take > n_eq ? n_eq : eq_take);
+        int pos = block_exclusive_scan(n_gt + eq_take, &tsel, wsum);   // (ends with a barrier)
+        nsel = tsel;
+#pragma unroll
+        for (int q = 0; q < kKeysPerThread; ++q) {
+            const int j = r0 + q;
+            if (j < nvalid) {
+                bool sel = take_all || run[q] > kth;
+                if (!sel && run[q] == kth && eq_take > 0) {
+                    sel = true;
+                    --eq_take;
+                }
+                if (sel) keys[pos++] = (uint32_t)j;
+            }
+        }
         __syncthreads();
     }
 
