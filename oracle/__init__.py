@@ -198,6 +198,42 @@ def dense(q, k, v, kv_lengths, n_q, causal, scale, k_scale=None,
     return out
 
 
+def masked(q, k, v, kv_lengths, mask, n_q, causal, scale):
+    """fp64 attention over the filled prefix with an additive mask
+    ("qwen4exp : gather-based sparse attention for QSA decode", llama.cpp
+    #28213: the selection as a mask over the window; the Metal FA-vec kernel
+    skips the chunks it hides).
+
+    The visible positions of row (b, i) are those of ``dense`` whose
+    mask[b, i, j] is not -inf; each one's score gains mask[b, i, j].  The
+    positions and mask values are handed to ``gather`` as the row's list and
+    per-entry bias.  mask: fp32 [B, n_q, cap].  Returns float64
+    [B, n_q, Hq, d].
+    """
+    qa = _as_np(q)
+    ma = np.asarray(_as_np(mask), dtype=np.float32)
+    B = qa.shape[0]
+    cap = _as_np(k).shape[2]
+    if ma.shape != (B, n_q, cap):
+        raise ValueError("mask must be [B, n_q, cap]")
+    lens = np.clip(np.asarray(_as_np(kv_lengths), dtype=np.int64).reshape(B), 0, cap)
+    rows = []
+    for b in range(B):
+        L = int(lens[b])
+        for i in range(n_q):
+            last = L - n_q + i if causal else L - 1
+            cells = np.arange(max(0, min(L, last + 1)))
+            cells = cells[ma[b, i, cells] != -np.inf]
+            rows.append(cells)
+    K = max(1, max(len(r) for r in rows))
+    idx = np.full((B * n_q, K), -1, dtype=np.int32)
+    bias = np.zeros((B * n_q, K), dtype=np.float32)
+    for r, cells in enumerate(rows):
+        idx[r, :len(cells)] = cells
+        bias[r, :len(cells)] = ma[r // n_q, r % n_q, cells]
+    return gather(qa, k, v, idx.reshape(B, n_q, K), scale, bias=bias.reshape(B, n_q, K))
+
+
 def topk_blocks(scores, kv_lengths, block_size, top_k):
     """Index lists from block scores: top-k over blocks, then only the
     winners expanded to cells ("qwen4exp : gather-based sparse attention for
