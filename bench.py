@@ -439,6 +439,16 @@ def extras(args, device, stream, peak, kernel):
                     "us_python_loop": round(ms_host * 1e3, 2)}
         ws.close()
 
+    def measure_fn(tag, fn, nbytes, n=200):
+        for _ in range(5):
+            fn()
+        calls = min(n, GRAPH_CALLS)
+        g = capture(fn, calls, stream)
+        ms = time_graph(g, calls, max(1, n // calls), stream)
+        del g
+        res[tag] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
+                    "frac": round(nbytes / ms / 1e6 / peak, 4), "bytes": nbytes}
+
     for name in ("dense_1k", "mtp_verify", "gather", "int8"):
         inp = W.workload(name, seed=1, device=device)
         measure(name, inp, 50 if name == "int8" else 200)
@@ -455,6 +465,18 @@ def extras(args, device, stream, peak, kernel):
     inp.bias = torch.randn(inp.idx.shape, generator=g, device=device) * 2.0
     measure("gather_bias", inp)
     del inp
+    # the same selection as a mask over the whole window (CUDA-core kernel,
+    # hidden 32-position chunks skipped)
+    inp = W.workload("gather", seed=1, device=device)
+    mask = torch.full((1, 1, inp.k.shape[2]), -float("inf"), device=device)
+    mask[0, 0, inp.idx[0, 0].long()] = 0.0
+    ws_m = workspace_for(inp, device)
+    out_m = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=device)
+    measure_fn("masked_gather_list_131k", lambda: fd.decode_masked(
+        inp.q, inp.k, inp.v, inp.kv_lengths, mask, n_q=1, causal=False, scale=inp.scale,
+        out=out_m, workspace=ws_m), algorithmic_bytes(inp), 50)
+    ws_m.close()
+    del inp, mask
     # gather: time follows the list length, not the capacity
     for K in (512, 2048, 8192):
         for cap in (8192, 32768, 131072):
@@ -479,16 +501,6 @@ def extras(args, device, stream, peak, kernel):
         torch.cuda.empty_cache()
     # block top-k selection (gather lists from block scores), alone and
     # followed by the gather it feeds
-    def measure_fn(tag, fn, nbytes, n=200):
-        for _ in range(5):
-            fn()
-        calls = min(n, GRAPH_CALLS)
-        g = capture(fn, calls, stream)
-        ms = time_graph(g, calls, max(1, n // calls), stream)
-        del g
-        res[tag] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
-                    "frac": round(nbytes / ms / 1e6 / peak, 4), "bytes": nbytes}
-
     for tag, B, n_q, nb, bs, k in (("topk_131k_1row", 1, 1, 2048, 64, 32),
                                    ("topk_32k_48rows", 8, 6, 512, 64, 32),
                                    ("topk_2m_1row", 1, 1, 32768, 64, 32)):

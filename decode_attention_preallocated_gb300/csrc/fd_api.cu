@@ -127,6 +127,7 @@ struct Call {
     const fd_tensor *k_new = nullptr, *v_new = nullptr;
     int32_t *len_update = nullptr;
     const float *bias = nullptr;   // gather: per-entry score bias (or null)
+    const fd_tensor *mask = nullptr;   // masked: [B, n_q, cap] fp32
 };
 
 int run(const Call &c) {
@@ -186,6 +187,14 @@ int run(const Call &c) {
     if (c.mode != fd::kGather && !c.kv_lengths) return FD_ERR_ARG;
     if (c.mode == fd::kGather && (c.idx_len < 0 || (!c.idx && c.idx_len > 0))) return FD_ERR_ARG;
     if (c.causal != 0 && c.causal != 1) return FD_ERR_ARG;
+    if (c.mode == fd::kMasked) {
+        if ((rc = check_tensor(c.mask, 3))) return rc;
+        if (c.mask->dtype != FD_F32 || c.kv_int8) return FD_ERR_ARG;
+        if (c.mask->shape[0] != B || c.mask->shape[1] != n_q || c.mask->shape[2] != cap ||
+            c.mask->stride[2] != 1)
+            return FD_ERR_ARG;
+        if (reinterpret_cast<uintptr_t>(c.mask->data) & 3) return FD_ERR_ALIGN;
+    }
     const bool append = c.k_new != nullptr;
     if (append) {
         if (c.mode != fd::kDense || c.kv_int8) return FD_ERR_ARG;
@@ -225,6 +234,11 @@ int run(const Call &c) {
     p.kv_lengths = c.kv_lengths;
     p.idx = c.idx;
     p.bias = c.mode == fd::kGather ? c.bias : nullptr;
+    if (c.mode == fd::kMasked) {
+        p.mask = static_cast<const float *>(c.mask->data);
+        p.ms[0] = c.mask->stride[0];
+        p.ms[1] = c.mask->stride[1];
+    }
     if (paged) {
         p.block_table = c.block_table;
         p.page_size = (int32_t)rows_per;
@@ -337,6 +351,16 @@ int fd_decode_gather_bias(const fd_tensor *q, const fd_tensor *k_cache,
     Call c{q, k_cache, v_cache, nullptr, nullptr, out, nullptr, idx, idx_len, nullptr, 0,
            q->ndim == 4 ? (int32_t)q->shape[1] : 0, 0, scale, fd::kGather, 0, opts};
     c.bias = bias;
+    return run(c);
+}
+
+int fd_decode_masked(const fd_tensor *q, const fd_tensor *k_cache, const fd_tensor *v_cache,
+                     const int32_t *kv_lengths, const fd_tensor *mask, int32_t n_q,
+                     int32_t causal, float scale, const fd_tensor *out, const fd_opts *opts) {
+    if (!mask) return FD_ERR_ARG;
+    Call c{q, k_cache, v_cache, nullptr, nullptr, out, kv_lengths, nullptr, 0, nullptr, 0,
+           n_q, causal, scale, fd::kMasked, 0, opts};
+    c.mask = mask;
     return run(c);
 }
 

@@ -15,7 +15,10 @@ namespace fd {
 // kPaged: the dense prefix mode over a paged cache (a pool of fixed-size
 // pages and a per-sequence block table); it shares the dense mode's segments,
 // tiles and masks and differs only in where a position's row lives.
-enum Mode : int32_t { kDense = 0, kGather = 1, kPaged = 2 };
+// kMasked: the dense prefix mode with an additive per-(query row, position)
+// mask; the CUDA-core kernel skips tiles in which the mask leaves nothing
+// visible.
+enum Mode : int32_t { kDense = 0, kGather = 1, kPaged = 2, kMasked = 3 };
 
 // Everything a kernel needs, passed by value as one __grid_constant__ block.
 struct Params {
@@ -45,6 +48,8 @@ struct Params {
     const int32_t *idx;
     const float *bias;     // gather: optional [B, n_q, idx_len] fp32 added to each
                            // entry's score (-inf drops the entry)
+    const float *mask;     // masked: [B, n_q, cap] fp32 added to the scores
+    int64_t ms[2];         //   (strides of B and n_q; positions contiguous)
     // paged caches: logical position j of sequence b lives at row j % page_size
     // of pool page block_table[b * max_pages + j / page_size]; the caches'
     // strides are then (page, kv head, row in page); cap = max_pages * page_size

@@ -1,5 +1,6 @@
 // fd_simt.cu -- CUDA-core decode kernel: every mode (dense prefix, causal
-// window, index gather, paged cache, int8 cache), head_dim 128 and 256.
+// window, index gather, paged cache, int8 cache, masked prefix with
+// chunk skipping), head_dim 128 and 256.
 //
 // One thread block walks a contiguous range of 32-position tiles chosen by
 // the balanced split partitioner (fd_internal.h).  Per tile it stages K and
@@ -37,6 +38,7 @@ struct Layout {
                                              // 8-byte aligned here)
                + (size_t)rows * (T + 1) * 4  // P
                + 5 * (size_t)T * 4           // k scale, v scale, valid, appended, bias
+               + 6 * (size_t)T * 4           // masked mode: mask of each query row
                + 3 * (size_t)rows * 4;       // m, l, alpha
     }
 };
@@ -71,7 +73,8 @@ __device__ __forceinline__ void simt_body(const Params &p) {
     int *tval = reinterpret_cast<int *>(vsc + T);
     int *tnew = tval + T;                      // fused append: the row comes from k_new / v_new
     float *tbias = reinterpret_cast<float *>(tnew + T);   // gather: entry bias (log2 units)
-    float *m_s = tbias + T;
+    float *tmask = tbias + T;   // masked: [n_q][T] mask (log2 units), -inf outside the window
+    float *m_s = tmask + 6 * T;
     float *l_s = m_s + rows;
     float *a_s = l_s + rows;
 
@@ -148,6 +151,7 @@ __device__ __forceinline__ void simt_body(const Params &p) {
             const int64_t j0 = tt * T;
             const int ntok = (int)min((int64_t)T, len - j0);
             __syncthreads();   // previous tile fully consumed
+            int live = 0;
             if (tid < T) {
                 int64_t pos = j0 + tid;
                 int ok = tid < ntok;
@@ -193,8 +197,20 @@ __device__ __forceinline__ void simt_body(const Params &p) {
                 }
                 ksc[tid] = kscale;
                 vsc[tid] = vscale;
+                // Masked mode: each query row's mask value at this position
+                // (-inf where it hides the position or the window does).
+                if (p.mode == kMasked) {
+                    for (int i = 0; i < p.n_q; ++i) {
+                        float mv = neg_inf();
+                        if (ok && (!p.causal || pos <= len - p.n_q + i))
+                            mv = p.mask[(int64_t)b * p.ms[0] + (int64_t)i * p.ms[1] + pos];
+                        tmask[i * T + tid] = mv == neg_inf() ? neg_inf() : mv * 1.4426950408889634f;
+                        live |= mv != neg_inf();
+                    }
+                }
             }
-            __syncthreads();
+            // A tile the mask hides entirely is skipped: no K / V read.
+            if (__syncthreads_or(live) == 0 && p.mode == kMasked) continue;
             // Stage the K and V rows (zeros for positions that are not visible).
             if (!p.kv_int8) {
                 constexpr int CPR = D / 8;   // 16-byte chunks per row
@@ -273,7 +289,13 @@ __device__ __forceinline__ void simt_body(const Params &p) {
                         const int i = r % p.n_q;
                         vis = vis && tpos[lane] <= len - p.n_q + i;
                     }
-                    const float sc = vis ? acc[k] * ksc[lane] * p.scale_log2 + tbias[lane] : neg_inf();
+                    float mb = 0.f;
+                    if (p.mode == kMasked) {
+                        mb = tmask[(r % p.n_q) * T + lane];
+                        vis = vis && mb != neg_inf();
+                    }
+                    const float sc = vis ? acc[k] * ksc[lane] * p.scale_log2 + tbias[lane] + mb
+                                         : neg_inf();
                     float tmax = sc;
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1)

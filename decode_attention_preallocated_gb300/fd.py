@@ -78,6 +78,9 @@ _SIGNATURES = [
     ("fd_decode_gather_bias", ctypes.c_int,
      [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_void_p,
       ctypes.c_int32, _P(FdTensor), _P(FdOpts)]),
+    ("fd_decode_masked", ctypes.c_int,
+     [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, _P(FdTensor), ctypes.c_int32,
+      ctypes.c_int32, ctypes.c_float, _P(FdTensor), _P(FdOpts)]),
     ("fd_decode_append", ctypes.c_int,
      [_P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor),
       ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _P(FdTensor),
@@ -390,6 +393,30 @@ def topk_blocks(scores, kv_lengths, block_size, top_k, out=None, stream=None):
         rc = lib().fd_topk_blocks(scores.data_ptr(), B, n_q, nb, kv_lengths.data_ptr(),
                                   int(block_size), int(top_k), out.data_ptr(), sh)
     _check(rc, "fd_topk_blocks")
+    return out
+
+
+def decode_masked(q, k_cache, v_cache, kv_lengths, mask, n_q=None, causal=False, scale=None,
+                  out=None, out_dtype=torch.bfloat16, num_ctas=0, kernel=FD_KERNEL_AUTO,
+                  stream=None, workspace: Optional[Workspace] = None):
+    """As ``decode`` with an additive fp32 mask [B, n_q, cap] (positions
+    contiguous; -inf hides a position); chunks the mask hides for every query
+    row are not read (CUDA-core kernel)."""
+    B, nq, Hq, d = q.shape
+    n_q = nq if n_q is None else n_q
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    Hkv = k_cache.shape[1]
+    rows = (Hq // max(Hkv, 1)) * nq
+    out, sh, ws = _prepare(q, k_cache, out, out_dtype, B * Hkv, rows, num_ctas,
+                           kernel, stream, workspace)
+    tq, tk, tv, tm, to = map(as_fd_tensor, (q, k_cache, v_cache, mask, out))
+    o = _opts(sh, ws, num_ctas, kernel)
+    with _on_device(q.device):
+        rc = lib().fd_decode_masked(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                    kv_lengths.data_ptr(), ctypes.byref(tm), int(n_q),
+                                    int(bool(causal)), float(scale), ctypes.byref(to),
+                                    ctypes.byref(o))
+    _check(rc, "fd_decode_masked")
     return out
 
 

@@ -208,6 +208,24 @@ int fd_decode_gather_bias(const fd_tensor *q, const fd_tensor *k_cache,
                           const float *bias, int32_t idx_len,
                           const fd_tensor *out, const fd_opts *opts);
 /*
+ * Dense prefix decode with an additive mask, skipping hidden chunks: as
+ * fd_decode, and mask[b, i, j] (fp32, device, [B, n_q, cap], positions
+ * contiguous) is added to the scaled score of query row i at position j;
+ * -inf hides the position.  A 32-position chunk that the mask and the window
+ * hide for every query row of a sequence is not read at all: the masked scan
+ * whose cost follows the visible chunks ("qwen4exp : gather-based sparse
+ * attention for QSA decode", llama.cpp #28213, Metal measurements: the
+ * FA-vec kernel skips fully masked 32-cell chunks).  Mask values must be
+ * finite or -inf.  Served by the CUDA-core kernel (FD_KERNEL_TC returns
+ * FD_ERR_UNSUPPORTED); the tensor-core path for the same computation is
+ * fd_decode_gather_bias over the visible cells.  Other arguments as
+ * fd_decode.
+ */
+int fd_decode_masked(const fd_tensor *q, const fd_tensor *k_cache,
+                     const fd_tensor *v_cache, const int32_t *kv_lengths,
+                     const fd_tensor *mask, int32_t n_q, int32_t causal,
+                     float scale, const fd_tensor *out, const fd_opts *opts);
+/*
  * Dense prefix decode with a fused K/V append (bf16 caches): one launch
  * writes the step's new rows into the caches and attends over the prefix
  * including them, as flash_attn_with_kvcache does with k / v and

@@ -1,0 +1,91 @@
+"""GPU parity of the masked prefix with chunk skipping (fd_decode_masked,
+CUDA-core kernel) against the fp64 oracle: masks that hide most 32-position
+chunks, seeded finite biases, causal windows, ragged and empty sequences,
+head_dim 128 and 256, split counts, everything hidden, and the mask built
+from the gather workload's list."""
+import pytest
+import torch
+
+import oracle
+from decode_attention_preallocated_gb300 import build as fdbuild
+from decode_attention_preallocated_gb300 import fd
+from decode_attention_preallocated_gb300 import workloads as W
+from parity_util import compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    fdbuild.build()
+    fd.lib()
+
+
+def chunk_mask(B, n_q, cap, seed, keep=0.15):
+    """N(0, 2) biases on a random ~keep share of 32-position chunks (and on
+    a few single cells elsewhere), -inf on the rest."""
+    g = torch.Generator().manual_seed(seed)
+    m = torch.full((B, n_q, cap), -float("inf"))
+    nch = (cap + 31) // 32
+    live = torch.rand(B, nch, generator=g) < keep
+    for b in range(B):
+        for c in torch.nonzero(live[b]).flatten().tolist():
+            m[b, :, c * 32:(c + 1) * 32] = torch.randn(n_q, min(32, cap - c * 32), generator=g) * 2
+    cells = torch.randint(0, cap, (B, 8), generator=g)
+    for b in range(B):
+        m[b, 0, cells[b]] = 0.5
+    return m
+
+
+def run(inp, mask, out_dtype, num_ctas=0, kernel=fd.FD_KERNEL_AUTO):
+    ws = fd.Workspace(inp.q.shape[0] * inp.k.shape[1], 64, 256, 2048)
+    out = fd.decode_masked(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), inp.kv_lengths.cuda(),
+                           mask.cuda(), n_q=inp.n_q, causal=inp.causal, scale=inp.scale,
+                           out_dtype=out_dtype, num_ctas=num_ctas, kernel=kernel, workspace=ws)
+    torch.cuda.synchronize()
+    assert not ws.diagnostics()[0] & fd.FD_DEV_INTERNAL
+    ws.close()
+    return out
+
+
+CASES = {
+    "d128_decode": (3, 1, 8, 2, 128, 3000, [3000, 1, 1777], False),
+    "d256_mtp": (2, 4, 16, 4, 256, 2500, [2500, 999], True),
+    "rows64": (2, 2, 32, 1, 128, 1200, [1200, 0], True),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_masked_matches_oracle(case, out_dtype):
+    B, n_q, Hq, Hkv, d, cap, lens, causal = CASES[case]
+    inp = W.dense_inputs(B, n_q, Hq, Hkv, d, cap, lens, 120, causal)
+    mask = chunk_mask(B, n_q, cap, 121)
+    ref = torch.from_numpy(oracle.masked(inp.q, inp.k, inp.v, inp.kv_lengths, mask, n_q,
+                                         causal, inp.scale))
+    compare(run(inp, mask, out_dtype), ref, out_dtype, case)
+
+
+@pytest.mark.parametrize("ctas", [1, 7, 300])
+def test_masked_split_counts_and_hidden_rows(ctas):
+    inp = W.dense_inputs(2, 3, 8, 2, 256, 2000, [2000, 1500], 122, True)
+    mask = chunk_mask(2, 3, 2000, 123, keep=0.3)
+    mask[1, 2, :] = -float("inf")                       # a row with nothing visible
+    ref = torch.from_numpy(oracle.masked(inp.q, inp.k, inp.v, inp.kv_lengths, mask, 3, True,
+                                         inp.scale))
+    got = run(inp, mask, torch.float32, num_ctas=ctas)
+    compare(got, ref, torch.float32, "masked splits")
+    assert torch.count_nonzero(got[1, 2].cpu()) == 0
+
+
+def test_masked_from_a_gather_list_and_tensor_core_refusal():
+    # the gather workload's selection as a mask over the whole window
+    inp = W.gather_inputs(1, 1, 32, 4, 128, 131072, 2048, 128, seed=1)
+    mask = torch.full((1, 1, 131072), -float("inf"))
+    mask[0, 0, inp.idx[0, 0].long()] = 0.0
+    dense = W.DecodeInputs(q=inp.q, k=inp.k, v=inp.v, kv_lengths=inp.kv_lengths, n_q=1,
+                           causal=False, scale=inp.scale)
+    ref = torch.from_numpy(oracle.gather(inp.q, inp.k, inp.v, inp.idx, inp.scale))
+    compare(run(dense, mask, torch.bfloat16), ref, torch.bfloat16, "masked = gather")
+    with pytest.raises(fd.FdError):
+        run(dense, mask, torch.float32, kernel=fd.FD_KERNEL_TC)
