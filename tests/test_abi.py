@@ -191,6 +191,26 @@ def test_append_validation(L):
     assert rc == fd.FD_ERR_ARG                                   # bf16 caches only
 
 
+def test_masked_validation(L):
+    q, k, v, o = good(B=2, n_q=3, cap=64)
+    m = fake([2, 3, 64], fd.FD_F32)
+    op = fd.FdOpts()
+
+    def call(mask, lens=0x200000, k_=k):
+        return L.fd_decode_masked(ctypes.byref(q), ctypes.byref(k_), ctypes.byref(k_), lens,
+                                  ctypes.byref(mask) if mask is not None else None, 3, 1, 0.1,
+                                  ctypes.byref(o), ctypes.byref(op))
+
+    assert call(m) == fd.FD_ERR_WORKSPACE                         # valid up to the workspace
+    assert call(None) == fd.FD_ERR_ARG
+    assert call(m, lens=None) == fd.FD_ERR_ARG
+    assert call(fake([2, 3, 63], fd.FD_F32)) == fd.FD_ERR_ARG      # not [B, n_q, cap]
+    assert call(fake([2, 3, 64], fd.FD_BF16)) == fd.FD_ERR_ARG     # not fp32
+    assert call(fake([2, 3, 64], fd.FD_F32, strides=[384, 128, 2])) == fd.FD_ERR_ARG
+    assert call(fake([2, 3, 64], fd.FD_F32, ptr=0x100002)) == fd.FD_ERR_ALIGN
+    assert call(m, k_=fake([2, 2, 64, 128], fd.FD_I8)) == fd.FD_ERR_ARG   # bf16 caches only
+
+
 def test_topk_validation(L):
     # every check fails before anything is launched
     assert L.fd_topk_blocks(None, 1, 1, 8, 0x200000, 4, 2, 0x300000, None) == fd.FD_ERR_ARG
