@@ -6,10 +6,11 @@ stream.  There is no fallback: if libfd.so is missing or cannot be loaded,
 every call raises.
 
 Low-level names mirror the C ABI (``fd_decode``, ``fd_decode_int8``,
-``fd_decode_append``, ``fd_decode_paged``, ``fd_decode_gather``,
+``fd_decode_append``, ``fd_decode_paged``, ``fd_decode_masked``,
+``fd_decode_gather``, ``fd_decode_gather_bias``, ``fd_topk_blocks``,
 ``fd_workspace_create`` ...) and take ``FdTensor`` / ``FdOpts`` structures;
-``decode``, ``decode_int8``, ``decode_append``, ``decode_paged`` and
-``decode_gather`` take
+``decode``, ``decode_int8``, ``decode_append``, ``decode_paged``,
+``decode_masked``, ``decode_gather`` and ``topk_blocks`` take
 torch tensors, allocate ``out`` with torch when it is not given, and keep one
 workspace per (device, stream).
 """
