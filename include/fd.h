@@ -17,12 +17,15 @@
  *     drafts already written at L-n_q .. L-1) and row i sees 0 .. L-n_q+i
  *     (same issue, list item 2 and "Existing Solutions": a bottom-right
  *     aligned causal window, up to 6 rows).
- *     fd_decode_paged computes the same over a paged cache, and
- *     fd_decode_append after writing the step's new rows into the cache.
+ *     fd_decode_paged computes the same over a paged cache,
+ *     fd_decode_append after writing the step's new rows into the cache, and
+ *     fd_decode_masked with an additive mask over the prefix.
  *   - fd_decode_gather: V = the cells listed for that (b, i) in idx
  *     ("attend the selected cells instead of masking the window",
  *     llama.cpp #28244, Conversation; "gather-based sparse attention for
- *     QSA decode", llama.cpp #28213: per-token lists for multi-row verify).
+ *     QSA decode", llama.cpp #28213: per-token lists for multi-row verify);
+ *     fd_decode_gather_bias adds a bias per list entry, and fd_topk_blocks
+ *     builds the lists from block scores.
  * The prefix is split across thread blocks and the last block to finish a
  * (sequence, kv head) combines the splits inside the same launch
  * (comfy-kitchen #239, "GQA decode"); the query heads of one GQA group share
