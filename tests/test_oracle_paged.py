@@ -142,3 +142,27 @@ def test_paged_recipe_shapes():
     t = inp.block_table.flatten().tolist()
     assert len(set(t)) == len(t) and min(t) >= 0 and max(t) < inp.k.shape[0]
     assert inp.shape["cap"] == 256
+
+
+def test_int8_token_major_pool_matches_head_major():
+    inp = W.paged_inputs(2, 3, 8, 2, 16, 7, 6, [40, 9], 91, True, int8=True)
+    ref = run_paged(inp, inp.k, inp.v, inp.block_table, inp.k_scale, inp.v_scale)
+    km = inp.k.transpose(1, 2).contiguous().transpose(1, 2)
+    vm = inp.v.transpose(1, 2).contiguous().transpose(1, 2)
+    ksm = inp.k_scale.transpose(1, 2).contiguous().transpose(1, 2)
+    vsm = inp.v_scale.transpose(1, 2).contiguous().transpose(1, 2)
+    got = run_paged(inp, km, vm, inp.block_table, ksm, vsm)
+    torch.testing.assert_close(got, ref, rtol=0, atol=0)
+
+
+def test_poisoned_recipe_touches_only_free_rows():
+    lens = [45, 3]
+    inp = W.paged_inputs(2, 1, 4, 2, 8, 8, 6, lens, 92, False, tail="nan")
+    P, Hkv, ps, d = inp.k.shape
+    used = torch.zeros(P, ps, dtype=torch.bool)
+    for b, L in enumerate(lens):
+        for j in range(L):
+            used[int(inp.block_table[b, j // ps]), j % ps] = True
+    nan_rows = torch.isnan(inp.k).all(dim=-1).all(dim=1)     # [P, ps]
+    assert torch.equal(nan_rows, ~used)
+    assert torch.isfinite(inp.k[used.unsqueeze(1).expand(P, Hkv, ps)]).all()
