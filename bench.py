@@ -306,6 +306,48 @@ def time_graph(g, calls, replays, stream):
     return a.elapsed_time(b) / (calls * replays)
 
 
+def time_stats(fn, stream, calls=10, replays=20):
+    """Per-call time (us) over `replays` individually timed replays of a
+    graph of `calls` back-to-back calls: mean, median, min and p90 of the
+    per-replay averages."""
+    g = capture(fn, calls, stream)
+    g.replay()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(replays + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for r in range(replays):
+            g.replay()
+            evs[r + 1].record(stream)
+    evs[-1].synchronize()
+    per = sorted(1e3 * evs[r].elapsed_time(evs[r + 1]) / calls for r in range(replays))
+    del g
+    p90 = per[min(len(per) - 1, int(math.ceil(0.9 * len(per))) - 1)]
+    return {"mean": sum(per) / len(per), "median": statistics.median(per), "min": per[0],
+            "p90": p90}
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
 def workspace_for(inp, device):
     from decode_attention_preallocated_gb300 import fd
     B, n_q, Hq, d = inp.q.shape
@@ -365,6 +407,109 @@ def cpu_view(inp):
         lengths_host=list(inp.lengths_host), name=inp.name)
 
 
+def oracle_call(inp_cpu, sl):
+    """The fp64 oracle on the sequences `sl` of a workload (CPU view)."""
+    import oracle
+    if inp_cpu.idx is not None:
+        return oracle.gather(inp_cpu.q[sl], inp_cpu.k[sl], inp_cpu.v[sl], inp_cpu.idx[sl],
+                             inp_cpu.scale)
+    return oracle.dense(inp_cpu.q[sl], inp_cpu.k[sl], inp_cpu.v[sl],
+                        inp_cpu.lengths_host[sl], inp_cpu.n_q, inp_cpu.causal, inp_cpu.scale,
+                        None if inp_cpu.k_scale is None else inp_cpu.k_scale[sl],
+                        None if inp_cpu.v_scale is None else inp_cpu.v_scale[sl])
+
+
+def oracle_us(inp_cpu, threads, budget_s=None):
+    """Microseconds per whole call of the fp64 oracle with `threads` threads.
+    Without a budget the whole batch runs as one call; with one, whole
+    sequences run one by one until the budget is spent and the time is
+    scaled by the batch's algorithmic bytes over the sample's.  Returns
+    (us, sample text)."""
+    import oracle
+    oracle.set_threads(threads)
+    B = inp_cpu.q.shape[0]
+    total = algorithmic_bytes(inp_cpu)
+    if budget_s is None:
+        t0 = time.perf_counter()
+        oracle_call(inp_cpu, slice(0, B))
+        return 1e6 * (time.perf_counter() - t0), "whole call"
+    t_used, done, seqs = 0.0, 0, 0
+    while seqs < B and (seqs == 0 or t_used < budget_s):
+        sl = slice(seqs, seqs + 1)
+        t0 = time.perf_counter()
+        oracle_call(inp_cpu, sl)
+        t_used += time.perf_counter() - t0
+        sub = type(inp_cpu)(q=inp_cpu.q[sl], k=inp_cpu.k[sl], v=inp_cpu.v[sl],
+                            kv_lengths=inp_cpu.kv_lengths[sl], n_q=inp_cpu.n_q,
+                            causal=inp_cpu.causal, scale=inp_cpu.scale,
+                            k_scale=None if inp_cpu.k_scale is None else inp_cpu.k_scale[sl],
+                            idx=None if inp_cpu.idx is None else inp_cpu.idx[sl],
+                            lengths_host=inp_cpu.lengths_host[sl])
+        done += algorithmic_bytes(sub)
+        seqs += 1
+    if seqs == B:
+        return 1e6 * t_used, "whole batch, sequence by sequence"
+    return 1e6 * t_used * total / done, "%d of %d sequences, scaled by bytes" % (seqs, B)
+
+
+# The five workloads BASELINE.json names, in its order, with their tags in
+# the bench line.
+BASELINE_CONFIGS = (("c1_dense_1k", "dense_1k"), ("c2_mtp_verify", "mtp_verify"),
+                    ("c3_ragged", "ragged"), ("c4_gather", "gather"), ("c5_int8", "int8"))
+
+
+def baseline_configs(device, stream, peak, kernel, with_cpu=True, cpu_budget=8.0):
+    """The five named workloads: GPU us per call (mean, median, min, p90 over
+    individually timed replays of a 10-call graph), KV GB/s and fraction of
+    the peak, and the fp64 oracle's us per call on the host cores with every
+    core and with one.  The int8 workload's oracle runs once per thread
+    count (one of its four sequences with one thread, scaled); the ragged
+    workload's one-thread run takes whole sequences for about cpu_budget
+    seconds."""
+    from decode_attention_preallocated_gb300 import workloads as W
+    cores = len(os.sched_getaffinity(0))
+    res = {}
+    for tag, name in BASELINE_CONFIGS:
+        inp = W.workload(name, seed=1, device=device)
+        ws = workspace_for(inp, device)
+        out = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=device)
+        fn = call_fn(inp, out, ws, kernel)
+        for _ in range(5):
+            fn()
+        st = time_stats(fn, stream, calls=10, replays=10 if name in ("ragged", "int8") else 20)
+        nb = algorithmic_bytes(inp)
+        e = {"us": round(st["mean"], 2), "med": round(st["median"], 2),
+             "min": round(st["min"], 2), "p90": round(st["p90"], 2),
+             "GBps": round(nb / st["mean"] / 1e3, 1),
+             "frac": round(nb / st["mean"] / 1e3 / peak, 4)}
+        ws.close()
+        if with_cpu:
+            ci = cpu_view(inp)
+            big = name in ("ragged", "int8")
+            us_n, _ = oracle_us(ci, cores)
+            us_1, how = oracle_us(ci, 1, (cpu_budget if name == "ragged" else 0.0) if big else None)
+            e["cpu_us"] = round(us_n, 1)
+            e["cpu1_us"] = round(us_1, 1)
+            if big:
+                e["cpu1_sample"] = how
+            del ci
+        res[tag] = e
+        del inp, out
+        torch.cuda.empty_cache()
+    for cap in (3000, 131072):
+        inp = W.dense_inputs(1, 4, 16, 4, 256, cap, [3000], 1, True, device=device)
+        ws = workspace_for(inp, device)
+        out = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=device)
+        fn = call_fn(inp, out, ws, kernel)
+        for _ in range(5):
+            fn()
+        res["c2_mtp_verify"]["cap%d_us" % cap] = round(time_stats(fn, stream)["mean"], 2)
+        ws.close()
+        del inp, out
+    res["cpu"] = {"cores": cores, "model": cpu_model()}
+    return res
+
+
 # --------------------------------------------------------------- the arms
 def run_reference(args):
     rank, world, local = rank_info()
@@ -414,10 +559,10 @@ def run_reference(args):
 
 
 def extras(args, device, stream, peak, kernel):
-    """Per-mode timings beside the headline: the other workloads, the
-    capacity-independence check and the depth sweep (µs/call and GB/s from
-    CUDA graph replay; us_python_loop: the same calls launched one by one
-    from Python, which host overhead bounds for the small workloads)."""
+    """Per-mode timings beside the headline: the next rows' workloads, the
+    gather's capacity sweep and the depth sweep (µs/call and GB/s from CUDA
+    graph replay; us_python_loop: the same calls launched one by one from
+    Python, which host overhead bounds for the small workloads)."""
     from decode_attention_preallocated_gb300 import fd
     from decode_attention_preallocated_gb300 import workloads as W
     res = {}
@@ -449,15 +594,7 @@ def extras(args, device, stream, peak, kernel):
         res[tag] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / ms / 1e6, 1),
                     "frac": round(nbytes / ms / 1e6 / peak, 4), "bytes": nbytes}
 
-    for name in ("dense_1k", "mtp_verify", "gather", "int8"):
-        inp = W.workload(name, seed=1, device=device)
-        measure(name, inp, 50 if name == "int8" else 200)
-        del inp
-        torch.cuda.empty_cache()
-    for cap in (3000, 131072):
-        inp = W.dense_inputs(1, 4, 16, 4, 256, cap, [3000], 1, True, device=device)
-        measure("mtp_verify_cap%d" % cap, inp)
-        del inp
+    # (the five named workloads are timed by baseline_configs)
     # gather with a per-entry bias (N(0, 2), as a mask-derived list carries)
     inp = W.workload("gather", seed=1, device=device)
     g = torch.Generator(device=device)
@@ -578,6 +715,9 @@ def run_fd(args):
     replays = -(-steps // gcalls)
     steps = replays * gcalls
     graph = capture(fn, gcalls, stream)
+    with torch.cuda.stream(stream):
+        graph.replay()          # untimed: the graph's first launch uploads it
+    torch.cuda.synchronize()
 
     def barrier():
         if world > 1:
@@ -639,7 +779,7 @@ def run_fd(args):
             cpu_inp = cpu_view(inp)
             gbs, cores, sample = oracle_sample(cpu_inp, budget_s=args.cpu_budget)
             cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                   "sample": sample}
+                   "sample": sample, "cpu_model": cpu_model()}
         result = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": steps, "warmup": warm, "ms_per_step": round(ms_max, 5),
@@ -665,6 +805,10 @@ def run_fd(args):
         }
         if not args.no_extras and world == 1:
             result["modes"] = extras(args, device, stream, peak, kernel)
+        if not args.no_configs and world == 1:
+            # last in the line, so that a tail of it keeps every named workload
+            result["configs"] = baseline_configs(device, stream, peak, kernel,
+                                                 not args.no_cpu_baseline, args.cpu_budget)
         print(json.dumps(result), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -687,6 +831,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload block (GPU stats and oracle timings)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()
     if args.impl == "reference":

@@ -22,9 +22,16 @@
 //     stale contents of an earlier call never matter; calls that overlap on
 //     the GPU (different streams, or different host threads without
 //     ordering) race on the array and must not be issued.
-//   * The first call on a device, with that device current, looks up the
-//     array's device address (cudaGetSymbolAddress) and caches it; make that
-//     first call before any stream capture.
+//   * Host code never sees the array's device address through its name, so
+//     every call that is not being captured looks the address up again
+//     (cudaGetSymbolAddress, with the caller's device current) and keeps it
+//     for that device; a call made while its stream is being captured uses
+//     the address kept by the last uncaptured call on the device.  The first
+//     call on a device (and the first after a device reset, or in another
+//     context) must therefore come before any stream capture.
+//   * The status word exists because the kernel writes it (a length outside
+//     [0, cap] is clamped and flagged, as in fd_decode); this entry point
+//     does not report it.
 #include <cuda_runtime.h>
 
 #include <math.h>
@@ -51,16 +58,22 @@ std::mutex g_scratch_mu;
 void *g_scratch_addr[64] = {};
 
 // Device address of g_fd_scratch on the current device (host code only ever
-// sees a stand-in for the array's name, never its device address).
-int scratch_on_current_device(void **out) {
+// sees a stand-in for the array's name, never its device address).  Looked
+// up on every call whose stream is not being captured, so a device reset or
+// another context made current is picked up; a captured call takes the
+// address the last uncaptured call on this device found.
+int scratch_on_current_device(cudaStream_t st, void **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FD_ERR_CUDA;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return FD_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    if (cs == cudaStreamCaptureStatusNone) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_fd_scratch) != cudaSuccess || !p) return FD_ERR_CUDA;
         g_scratch_addr[dev] = p;
     }
+    if (!g_scratch_addr[dev]) return FD_ERR_CUDA;   // first call inside a capture
     *out = g_scratch_addr[dev];
     return FD_OK;
 }
@@ -123,10 +136,10 @@ extern "C" int fd_decode_noalloc(const fd_tensor *q, const fd_tensor *k_cache,
         G = fit;
     }
 
-    void *scratch = nullptr;
-    int rc = scratch_on_current_device(&scratch);
-    if (rc != FD_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void *scratch = nullptr;
+    int rc = scratch_on_current_device(st, &scratch);
+    if (rc != FD_OK) return rc;
     // Counters and status must start at zero; the array keeps the last call's
     // contents, so clear them on this call's stream first.
     if (cudaMemsetAsync(scratch, 0, kPartialsOff, st) != cudaSuccess) return FD_ERR_CUDA;

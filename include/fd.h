@@ -296,18 +296,23 @@ int fd_decode_paged(const fd_tensor *q, const fd_tensor *k_pages,
  * `stream`, with the same arguments minus the workspace; num_ctas = 0 picks
  * the block count automatically.
  *
- * Its scratch (split partials, per-(sequence, kv head) completion counters,
- * status word) is a fixed 8 MiB array in device memory that every GPU which
- * loads libfd.so holds until the process exits.  Limits: at most 4096
+ * Its scratch (split partials, per-(sequence, kv head) completion counters
+ * and an internal status word, which this call does not report) is a fixed
+ * 8 MiB array in device memory that every GPU which loads libfd.so holds
+ * until the process exits.  Limits: at most 4096
  * (sequence, kv head) pairs, and the split partials must fit: the block count
  * is lowered to fit, and a problem that cannot fit even with one block per
  * (sequence, kv head), or an explicit num_ctas that does not fit, returns
  * FD_ERR_SCRATCH before anything is launched.  Each call clears the counters
  * and status word on `stream` first (cudaMemsetAsync, which allocates
  * nothing).  All calls share the one array: calls that overlap on the GPU
- * race and must not be issued.  The first call on a device (with that device
- * current) looks up the array's device address; make it before any stream
- * capture.  Returns FD_OK or a negative FD_ERR_* code.
+ * race and must not be issued.  Every call whose stream is not being
+ * captured looks up the array's device address (with the caller's device
+ * current); a captured call reuses the address the last uncaptured call on
+ * that device found.  So the first call on a device, and the first after a
+ * device reset or in another context, must come before any stream capture
+ * (a captured first call returns FD_ERR_CUDA).  Returns FD_OK or a negative
+ * FD_ERR_* code.
  */
 int fd_decode_noalloc(const fd_tensor *q, const fd_tensor *k_cache,
                       const fd_tensor *v_cache, const int32_t *kv_lengths,
@@ -321,6 +326,11 @@ int fd_decode_noalloc(const fd_tensor *q, const fd_tensor *k_cache,
  * Size for the largest segment count, row count, head_dim and num_ctas any
  * call will use.  fd_workspace_create allocates device memory (cudaMalloc)
  * and zeroes the counters on `stream`; it is the only allocating call.
+ * A workspace serves the calls of one stream at a time, in stream order: the
+ * scratch of the split combine belongs to one stream-ordered launch at a
+ * time, the rule comfy-kitchen #239 adopts for its GEMM workspace (commit
+ * list: the workspace is tied to each launch in stream order).  Two streams
+ * that may run decode calls at once need two workspaces.
  */
 size_t fd_workspace_bytes(int64_t max_segments, int32_t max_rows,
                           int32_t head_dim, int32_t max_ctas);

@@ -58,3 +58,19 @@ def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
     src = tmp_path / "decode_attention_preallocated_gb300"
     os.symlink(os.path.join(ROOT, "decode_attention_preallocated_gb300"), src)
     assert bench.recorded_traffic("ragged") is None
+
+
+def test_oracle_timing_whole_call_and_scaled_sample():
+    # whole call, and a one-sequence sample scaled by the batch's bytes
+    inp = W.dense_inputs(3, 2, 8, 2, 128, 300, [300, 100, 200], 4, True)
+    us, how = bench.oracle_us(inp, 1)
+    assert us > 0 and how == "whole call"
+    us1, how1 = bench.oracle_us(inp, 1, 0.0)
+    assert us1 > 0 and how1 == "1 of 3 sequences, scaled by bytes"
+    g = W.gather_inputs(1, 1, 8, 2, 128, 400, 64, 8, seed=2)
+    assert bench.oracle_us(g, 2)[0] > 0
+
+
+def test_baseline_config_tags_name_the_five_workloads():
+    assert [n for _, n in bench.BASELINE_CONFIGS] == list(W.WORKLOADS)
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
