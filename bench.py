@@ -230,7 +230,8 @@ def call_fn(inp, out, ws, kernel, num_ctas=0):
     if inp.idx is not None:
         return lambda: fd.decode_gather(inp.q, inp.k, inp.v, inp.idx, scale=inp.scale, out=out,
                                         workspace=ws, kernel=kernel, num_ctas=num_ctas,
-                                        bias=getattr(inp, "bias", None))
+                                        bias=getattr(inp, "bias", None), k_scale=inp.k_scale,
+                                        v_scale=inp.v_scale)
     if inp.k.dtype == torch.int8:
         return lambda: fd.decode_int8(inp.q, inp.k, inp.v, inp.k_scale, inp.v_scale,
                                       inp.kv_lengths, n_q=inp.n_q, causal=inp.causal,
@@ -246,6 +247,8 @@ def algorithmic_bytes(inp):
     Hkv = inp.k.shape[1]
     if inp.idx is not None:
         valid = int(((inp.idx >= 0) & (inp.idx < inp.k.shape[2])).sum())
+        if inp.k.dtype == torch.int8:   # codes plus the two fp32 scales of each cell
+            return valid * Hkv * (d * 2 + 8)
         return valid * Hkv * d * 2 * 2
     es = 1 if inp.k.dtype == torch.int8 else 2
     if getattr(inp, "k_new", None) is not None:
@@ -602,16 +605,32 @@ def extras(args, device, stream, peak, kernel):
     inp.bias = torch.randn(inp.idx.shape, generator=g, device=device) * 2.0
     measure("gather_bias", inp)
     del inp
-    # the same selection as a mask over the whole window (CUDA-core kernel,
-    # hidden 32-position chunks skipped)
+    # the gather workload over an int8 cache (per-cell fp32 scales)
+    inp = W.gather_inputs(1, 1, 32, 4, 128, 131072, 2048, 128, 1, device=device, int8=True)
+    measure("gather_int8", inp)
+    del inp
+    # the same selection as a mask over the whole window (hidden 32-position
+    # chunks not read), and masks that leave 5 % / 25 % of the chunks
+    # visible; bytes: the visible chunks' K / V rows
     inp = W.workload("gather", seed=1, device=device)
-    mask = torch.full((1, 1, inp.k.shape[2]), -float("inf"), device=device)
-    mask[0, 0, inp.idx[0, 0].long()] = 0.0
     ws_m = workspace_for(inp, device)
     out_m = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=device)
-    measure_fn("masked_gather_list_131k", lambda: fd.decode_masked(
-        inp.q, inp.k, inp.v, inp.kv_lengths, mask, n_q=1, causal=False, scale=inp.scale,
-        out=out_m, workspace=ws_m), algorithmic_bytes(inp), 50)
+    cap = inp.k.shape[2]
+    for tag, keep in (("masked_gather_list_131k", None), ("masked_5pct_131k", 0.05),
+                      ("masked_25pct_131k", 0.25)):
+        mask = torch.full((1, 1, cap), -float("inf"), device=device)
+        if keep is None:
+            mask[0, 0, inp.idx[0, 0].long()] = 0.0
+        else:
+            gm = torch.Generator(device=device)
+            gm.manual_seed(9)
+            live = torch.rand(cap // 32, generator=gm, device=device) < keep
+            mask.view(1, 1, -1, 32)[0, 0, live] = 0.0
+        chunks = int((mask.view(-1, 32) != -float("inf")).any(1).sum())
+        measure_fn(tag, lambda: fd.decode_masked(
+            inp.q, inp.k, inp.v, inp.kv_lengths, mask, n_q=1, causal=False, scale=inp.scale,
+            out=out_m, workspace=ws_m), chunks * 32 * inp.k.shape[1] * inp.q.shape[3] * 4, 50)
+        res[tag]["visible_chunks"] = chunks
     ws_m.close()
     del inp, mask
     # gather: time follows the list length, not the capacity

@@ -30,6 +30,7 @@ struct fd_workspace {
 namespace {
 
 constexpr int kVersion = 1;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s per internal wait
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -134,7 +135,8 @@ int run(const Call &c) {
     int rc;
     if (!c.opts) return FD_ERR_ARG;
     const fd_opts &o = *c.opts;
-    if (o.reserved[0] || o.reserved[1] || o.reserved[2]) return FD_ERR_ARG;
+    if (o.reserved[0] || o.reserved[1]) return FD_ERR_ARG;
+    if (o.wait_limit_us < 0 || o.wait_limit_us > 2000000) return FD_ERR_ARG;
     if (o.kernel != FD_KERNEL_AUTO && o.kernel != FD_KERNEL_SIMT && o.kernel != FD_KERNEL_TC)
         return FD_ERR_ARG;
     if (o.num_ctas < 0) return FD_ERR_ARG;
@@ -249,6 +251,7 @@ int run(const Call &c) {
             if (((int64_t)1 << sh) == rows_per) p.page_shift = sh;
     }
     p.out = c.out->data;
+    p.wait_ns = o.wait_limit_us > 0 ? (uint64_t)o.wait_limit_us * 1000u : kDefaultWaitNs;
     p.counters = ws->counters;
     p.status = ws->status;
     p.partials = ws->partials;
@@ -320,6 +323,17 @@ int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache, const fd_tens
     if (scale == 0.f && q->ndim == 4 && q->shape[3] > 0) scale = 1.f / sqrtf((float)q->shape[3]);
     Call c{q, k_cache, v_cache, nullptr, nullptr, out, nullptr, idx, idx_len, nullptr, 0,
            q->ndim == 4 ? (int32_t)q->shape[1] : 0, 0, scale, fd::kGather, 0, opts};
+    return run(c);
+}
+
+int fd_decode_gather_int8(const fd_tensor *q, const fd_tensor *k_cache, const fd_tensor *v_cache,
+                          const fd_tensor *k_scale, const fd_tensor *v_scale, const int32_t *idx,
+                          int32_t idx_len, const fd_tensor *out, const fd_opts *opts) {
+    if (!q || !opts) return FD_ERR_ARG;
+    float scale = opts->scale;
+    if (scale == 0.f && q->ndim == 4 && q->shape[3] > 0) scale = 1.f / sqrtf((float)q->shape[3]);
+    Call c{q, k_cache, v_cache, k_scale, v_scale, out, nullptr, idx, idx_len, nullptr, 0,
+           q->ndim == 4 ? (int32_t)q->shape[1] : 0, 0, scale, fd::kGather, 1, opts};
     return run(c);
 }
 
@@ -436,6 +450,26 @@ int fd_workspace_reset(fd_workspace *ws, void *stream) {
     const size_t n = reinterpret_cast<char *>(ws->partials) - static_cast<char *>(ws->base);
     return cudaMemsetAsync(ws->base, 0, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? FD_OK : FD_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+__global__ void fill_i32(int32_t *p, int64_t n, int32_t value) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        p[i] = value;
+}
+}  // namespace
+
+extern "C" {
+
+int fd_workspace_fill_counters(fd_workspace *ws, int32_t value, void *stream) {
+    if (!ws) return FD_ERR_ARG;
+    const int64_t n = ws->max_segments;
+    const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+    fill_i32<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(ws->counters, n, value);
+    return cudaGetLastError() == cudaSuccess ? FD_OK : FD_ERR_CUDA;
 }
 
 int fd_workspace_destroy(fd_workspace *ws) {

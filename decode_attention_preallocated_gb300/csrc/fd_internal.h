@@ -35,6 +35,8 @@ struct Params {
                            // each non-empty segment (0: plain tile split)
     int32_t coop;          // tensor-core kernel launched cooperatively (all
                            // blocks resident): split segments may share merges
+    uint64_t wait_ns;      // tensor-core kernel: bound on each internal wait (ns);
+                           // one that runs out sets FD_DEV_INTERNAL
     float scale_log2;      // scale * log2(e): scores are kept in the log2 domain
     int32_t idx_len;
     int64_t nseg;          // segments: B*Hkv (dense) or B*n_q*Hkv (gather)

@@ -23,8 +23,10 @@ int launch_tc(const Params &p, int num_ctas, cudaStream_t stream);
 // Paged caches (fd_tc_paged.cu); tc_supports covers them.
 bool tc_supports_paged(const Params &p);
 int launch_tc_paged(const Params &p, int num_ctas, cudaStream_t stream);
-// Flat int8 caches (fd_tc_int8.cu).
+// Flat int8 caches, dense prefix and gather (fd_tc_int8.cu).
 int launch_tc_int8(const Params &p, int num_ctas, cudaStream_t stream);
+// Masked prefix over flat bf16 caches (fd_tc_masked.cu).
+int launch_tc_masked(const Params &p, int num_ctas, cudaStream_t stream);
 // Fused append over flat bf16 caches (fd_tc_append.cu): a cooperative launch,
 // so num_ctas may not exceed the blocks resident at once (else -2).
 int launch_tc_append(const Params &p, int num_ctas, cudaStream_t stream);

@@ -151,6 +151,7 @@ extern "C" int fd_decode_noalloc(const fd_tensor *q, const fd_tensor *k_cache,
     p.mode = fd::kDense; p.causal = causal; p.kv_int8 = 0;
     p.out_f32 = out->dtype == FD_F32; p.tile = tile;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_ns = 2000000000ull;
     p.nseg = nseg;
     p.q = static_cast<const uint16_t *>(q->data);
     p.k = k_cache->data; p.v = v_cache->data;

@@ -80,6 +80,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     }
 }
 
+// Wait without an abort test, bounded by `limit_ns` only: for draining a
+// block's own copies and MMAs before it exits, which must complete even when
+// another role gave up.
+static __device__ __noinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // ----------------------------------------------------------------------- TMA
 // 4-D tiled tensor load into shared memory, completion signalled on `bar`.
 __device__ __forceinline__ void tma_load_4d(void *dst, const void *tmap, uint64_t *bar, int c0,

@@ -2,7 +2,7 @@
 // over flat bf16 caches ([B, Hkv, cap, d]) and in index-gather mode, and the
 // kernel-choice queries of the C ABI layer.  Flat int8 caches are launched
 // from fd_tc_int8.cu, paged caches from fd_tc_paged.cu, fused appends from
-// fd_tc_append.cu.
+// fd_tc_append.cu, the masked prefix from fd_tc_masked.cu.
 #include "fd_tc_kernel.cuh"
 
 namespace fd {
@@ -19,9 +19,9 @@ int launch_d(const TcArgs &args, int G, cudaStream_t st) {
     // capacity.
     const Params &p = args.p;
     if (D == 256 && p.nseg * 8 <= (int64_t)G) {
-        if (rows <= 16 && G <= resident_blocks<D, 16, false, 16, false, true, false, false>())
+        if (rows <= 16 && G <= resident_blocks<D, 16, false, 16, false, true, false, false, false>())
             return launch_dn<D, 16, false, 16, false, true>(args, G, st);
-        if (rows > 16 && rows <= 32 && G <= resident_blocks<D, 32, false, 32, false, true, false, false>())
+        if (rows > 16 && rows <= 32 && G <= resident_blocks<D, 32, false, 32, false, true, false, false, false>())
             return launch_dn<D, 32, false, 32, false, true>(args, G, st);
     }
     if (rows <= 16) return launch_dn<D, 16, false>(args, G, st);
@@ -45,14 +45,15 @@ bool tc_supports(const Params &p) {
     // Q goes through a tensor map: 16-byte aligned base and strides.
     const bool q_aligned = (reinterpret_cast<uintptr_t>(p.q) & 15) == 0 && p.qs[0] % 8 == 0 &&
                            p.qs[1] % 8 == 0 && p.qs[2] % 8 == 0;
-    // int8 caches: head_dim 128 and up to 32 rows (one softmax warpgroup).
-    const bool shape = p.kv_int8 ? (p.d == 128 && p.rows <= 32)
+    // int8 caches: head_dim 128 or 256 and up to 32 rows (one softmax
+    // warpgroup; the other four warps widen the codes).
+    const bool shape = p.kv_int8 ? ((p.d == 128 || p.d == 256) && p.rows <= 32)
                                  : ((p.d == 128 || p.d == 256) && p.rows <= 64);
     // gather: bf16 caches whose rows form one strided 2-D array; paged: pools
     // whose rows do (fd_tc_paged.cu)
     int64_t rs, Y, g[3];
-    const bool mode = p.mode == kDense ||
-                      (p.mode == kGather && !p.kv_int8 && gather_rows(p, &rs, &Y, g)) ||
+    const bool mode = p.mode == kDense || (p.mode == kMasked && !p.kv_int8) ||
+                      (p.mode == kGather && gather_rows(p, &rs, &Y, g)) ||
                       tc_supports_paged(p);
     // fused append: flat bf16 caches (fd_tc_append.cu)
     const bool append = p.n_new == 0 || (p.mode == kDense && !p.kv_int8);
@@ -64,7 +65,8 @@ int launch_tc(const Params &p, int G, cudaStream_t st) {
     if (!tc_supports(p)) return -2;
     if (p.mode == kPaged) return launch_tc_paged(p, G, st);
     if (p.n_new > 0) return launch_tc_append(p, G, st);
-    if (p.mode == kDense && p.kv_int8) return launch_tc_int8(p, G, st);
+    if (p.kv_int8) return launch_tc_int8(p, G, st);   // flat int8: dense or gather
+    if (p.mode == kMasked) return launch_tc_masked(p, G, st);
     TcArgs args;
     memset(&args, 0, sizeof args);
     args.p = p;

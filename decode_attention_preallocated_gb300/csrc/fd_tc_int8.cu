@@ -1,5 +1,6 @@
 // fd_tc_int8.cu -- launches of the tensor-core decode kernel over flat int8
-// caches (head_dim 128, up to 32 rows), in a translation unit of their own.
+// caches (head_dim 128 or 256, up to 32 rows), dense prefix and index gather,
+// in a translation unit of their own.
 #include "fd_tc_kernel.cuh"
 
 namespace fd {
@@ -8,13 +9,36 @@ int launch_tc_int8(const Params &p, int G, cudaStream_t st) {
     TcArgs args;
     memset(&args, 0, sizeof args);
     args.p = p;
+    const int rows = p.rows;
+    if (p.mode == kGather) {
+        // the listed cells' codes fetched row by row (tile::gather4) from the
+        // caches seen as 2-D arrays of rows
+        int64_t rs = 0, Y = 0, g[3] = {0, 0, 0};
+        if (!gather_rows(p, &rs, &Y, g)) return -2;
+        args.gs0 = g[0];
+        args.gs1 = g[1];
+        args.gs2 = g[2];
+        if (!make_gmap(&args.tk, p.k, p, rs, Y) || !make_gmap(&args.tv, p.v, p, rs, Y) ||
+            !make_qmap(&args.tq, p))
+            return -5;
+        if (p.d == 128)
+            return rows <= 8    ? launch_dn<128, 16, true, 8, true>(args, G, st)
+                   : rows <= 16 ? launch_dn<128, 16, true, 16, true>(args, G, st)
+                                : launch_dn<128, 32, true, 32, true>(args, G, st);
+        return rows <= 8    ? launch_dn<256, 16, true, 8, true>(args, G, st)
+               : rows <= 16 ? launch_dn<256, 16, true, 16, true>(args, G, st)
+                            : launch_dn<256, 32, true, 32, true>(args, G, st);
+    }
     if (!make_map(&args.tk, p.k, p.ks, p) || !make_map(&args.tv, p.v, p.vs, p) ||
         !make_qmap(&args.tq, p))
         return -5;
-    const int rows = p.rows;
-    return rows <= 8    ? launch_dn<128, 16, true, 8>(args, G, st)
-           : rows <= 16 ? launch_dn<128, 16, true>(args, G, st)
-                        : launch_dn<128, 32, true>(args, G, st);
+    if (p.d == 128)
+        return rows <= 8    ? launch_dn<128, 16, true, 8>(args, G, st)
+               : rows <= 16 ? launch_dn<128, 16, true>(args, G, st)
+                            : launch_dn<128, 32, true>(args, G, st);
+    return rows <= 8    ? launch_dn<256, 16, true, 8>(args, G, st)
+           : rows <= 16 ? launch_dn<256, 16, true>(args, G, st)
+                        : launch_dn<256, 32, true>(args, G, st);
 }
 
 }  // namespace fd

@@ -5,7 +5,7 @@
 //
 // Modes: the dense prefix (optionally causal) over flat or paged caches, and
 // index gather; bf16 caches at head_dim 128 / 256 with up to 64 packed query
-// rows, int8 caches at head_dim 128 with up to 32.
+// rows, int8 caches at head_dim 128 / 256 with up to 32.
 //
 // Work split: balanced consecutive ranges of work units over one block per
 // SM, where a segment is its tiles (128 positions) plus a few units for the
@@ -141,8 +141,11 @@ constexpr int kMaxGroups = 2;           // softmax warpgroups (bf16 caches)
 constexpr int kThreadsTC = 320;         // warps 0-7, producer, MMA issuer
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+// Bound on the waits that drain a block's own copies and MMAs before it
+// exits (they always end); the other waits take Params::wait_ns.
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr int kDevTimeout = 4;          // mirrors FD_DEV_INTERNAL
+constexpr uint32_t kBarsBytes = 512;    // barrier block; the reduction scratch follows
 // Scores (log2 units) may exceed a row's running maximum by this much before
 // the maximum is refreshed and O rescaled; P is then at most 2^8, which fp32
 // accumulators and the hi/lo bf16 split of P carry without loss.
@@ -193,14 +196,14 @@ struct Cfg {
     static constexpr uint32_t RED = GROUPS * RED_GROUP * 4;
     // Per-row element offsets into out for the current segment (int64), two
     // tables used by alternate pieces.
-    static constexpr uint32_t OFF_TBL = 512 + RED;
+    static constexpr uint32_t OFF_TBL = kBarsBytes + RED;
     static constexpr uint32_t TBL = 2 * N * 8;
     static constexpr uint32_t MISC = ((OFF_TBL + TBL) + 1023) / 1024 * 1024;
     static constexpr uint32_t BUDGET = 232448;   // max dynamic shared memory per block
     // int8 caches: a ring of NR raw tiles (TT positions x D codes, as TMA
     // lands them) in front of the bf16 slots the MMAs read.
     static constexpr uint32_t RAW = I8 ? TT * D : 0;
-    static constexpr int NR = I8 ? 6 : 0;
+    static constexpr int NR = I8 ? (D == 128 ? 6 : 2) : 0;
     static constexpr int NRX = I8 ? NR : 1;   // ring length for index arithmetic
     // Two P stages when that still leaves three K/V slots, else one.
     static constexpr int NS2 = (int)((BUDGET - MISC - QBYTES - 2 * PSTAGE - NR * RAW) / SLOT);
@@ -213,7 +216,8 @@ struct Cfg {
     static constexpr uint32_t OFF_P = OFF_Q + QBYTES;
     static constexpr uint32_t OFF_RAW = OFF_P + PST * PSTAGE;
     static constexpr uint32_t SMEM = OFF_RAW + NR * RAW;
-    static_assert(SMEM <= BUDGET, "shared memory budget");
+    // (the fused-append exit path declares a few bytes of static shared memory)
+    static_assert(SMEM + 64 <= BUDGET, "shared memory budget");
     static constexpr uint32_t COLS = 2 * N + DC * N;
     static constexpr uint32_t TMEM_COLS = COLS <= 32 ? 32 : COLS <= 64 ? 64 : COLS <= 128 ? 128 : 256;
     static constexpr int MERGE_UNROLL = (D == 256 && NV >= 32 && !I8) ? 1 : 2;
@@ -343,7 +347,7 @@ __device__ __forceinline__ bool next_piece(const Params &p, Walk &w) {
     return true;
 }
 
-struct Bars {   // at the start of shared memory; the reduction scratch follows at 512
+struct Bars {   // at the start of shared memory; the reduction scratch follows at kBarsBytes
     uint64_t slot_full[8], slot_empty[8];
     uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
     uint64_t q_full, q_free, o_done, o_free, exit_mma, sm_bar;
@@ -384,7 +388,7 @@ __device__ __forceinline__ int64_t tile_start(int64_t tt, int64_t L) {
     return y0 + TT > L ? L - TT : y0;
 }
 
-static_assert(sizeof(Bars) <= 512, "barrier block overlaps the reduction scratch");
+static_assert(sizeof(Bars) <= kBarsBytes, "barrier block overlaps the reduction scratch");
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -457,7 +461,7 @@ __device__ __noinline__ bool share_merge_segment(const Params &p, Bars *bs, Walk
     volatile int *abort_flag = &bs->abort_flag;
     auto sm_sync = [&]() -> bool {
         ptx::mbar_arrive(&bs->sm_bar);
-        if (ptx::mbar_wait(&bs->sm_bar, (sm_ctr++) & 1, abort_flag, kWaitNs)) return true;
+        if (ptx::mbar_wait(&bs->sm_bar, (sm_ctr++) & 1, abort_flag, p.wait_ns)) return true;
         note_timeout(bs, p, 14, 0, piece);
         return false;
     };
@@ -470,7 +474,7 @@ __device__ __noinline__ bool share_merge_segment(const Params &p, Bars *bs, Walk
         for (uint32_t n = 0; ld_acquire(p.counters + sg) < P; ++n) {
             __nanosleep(64);
             if ((n & 63) == 63 &&
-                (*abort_flag || ptx::globaltimer_ns() - t0 > kWaitNs)) {
+                (*abort_flag || ptx::globaltimer_ns() - t0 > p.wait_ns)) {
                 note_timeout(bs, p, 15, (uint32_t)k, piece);
                 break;
             }
@@ -566,7 +570,7 @@ __device__ __noinline__ void append_wait(const Params &p) {
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t n = 0; ld_acquire(p.grid) < (int)gridDim.x; ++n) {
         __nanosleep(32);
-        if ((n & 63) == 63 && ptx::globaltimer_ns() - t0 > kWaitNs) {
+        if ((n & 63) == 63 && ptx::globaltimer_ns() - t0 > p.wait_ns) {
             atomicOr(p.status, kDevTimeout);
             break;
         }
@@ -588,17 +592,18 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, volatil
     return ptx::mbar_wait(bar, parity, abort, limit_ns);
 }
 
-template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP>
+template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP, bool MK>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant__ TcArgs a) {
     static_assert(!(GA && PG), "gather and paged loads are separate modes");
     static_assert(!AP || (!I8 && !GA && !PG), "fused append: flat bf16 caches");
+    static_assert(!MK || (!I8 && !GA && !PG && !AP && !SH), "masked prefix: flat bf16 caches");
     using C = Cfg<D, N, I8, NV, GA>;
     constexpr int kSoftmaxThreads = C::SMT;
     const Params &p = a.p;
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t smem_base = ptx::smem_u32(smem);
     Bars *bs = reinterpret_cast<Bars *>(smem);
-    float *red = reinterpret_cast<float *>(smem + 512);   // per group [2][4][NH]
+    float *red = reinterpret_cast<float *>(smem + kBarsBytes);   // per group [2][4][NH]
     // Row tables: element offset of packed row r in out, one table per piece
     // parity (a group may start the next piece while a lagging warp of it
     // still stores the previous one).
@@ -690,6 +695,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             ptx::prefetch_tmap(&a.gv);
         }
     }
+    // Masked prefix: the K / V slots start as zeros (a hidden tile is never
+    // loaded and leaves the slot as it was, which must be finite).
+    if (MK && tid < kSoftmaxThreads) {
+        for (uint32_t e = tid; e < C::NS * C::SLOT / 16; e += kSoftmaxThreads)
+            *reinterpret_cast<uint4 *>(smem + C::OFF_SLOTS + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+        ptx::fence_proxy_async_smem();
+    }
     // P rows NV..N-1 are never written: zero them once.
     if (NV < N && tid < kSoftmaxThreads) {
         for (uint32_t e = tid; e < C::PST * C::PSTAGE / 16; e += kSoftmaxThreads)
@@ -747,7 +759,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             // 128-byte swizzle the QK descriptors expect.
             if (lane == 0) {
                 if (piece > 0) {
-                    ok = bar_wait<I8>(&bs->q_free, (piece - 1) & 1, abort_flag, kWaitNs);
+                    ok = bar_wait<I8>(&bs->q_free, (piece - 1) & 1, abort_flag, p.wait_ns);
                     if (!ok) note_timeout(bs, p, 8, issued, piece);
                 }
                 if (ok) {
@@ -813,6 +825,50 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             };
             if (GA) list_rows(tt0, yk);
             if (PG) next_rows(tt0);
+            // masked prefix: which 32-position chunks of a tile some query row
+            // sees (bit c = positions 32c .. 32c+31 of the tile as loaded):
+            // lane l reads the mask at positions 4l .. 4l+3 for every query
+            // index; a position counts if this tile owns it, it lies in the
+            // filled prefix (and the causal window) and its mask is not -inf.
+            // Hidden chunks are not copied (see the copy step below).
+            // The mask values of a tile are loaded one tile before they are
+            // evaluated, so the loads never stall the copies.
+            const float *mrow = MK ? p.mask + (int64_t)b * p.ms[0] : nullptr;
+            constexpr int kMaxQP = 6;
+            float mreg[MK ? 4 : 1][MK ? kMaxQP : 1];
+            auto mask_load = [&](int64_t tile) {
+                const int64_t y0 = tile * TT, ys0 = tile_start(tile, L);
+#pragma unroll
+                for (int r = 0; r < (MK ? 4 : 1); ++r) {
+                    const int64_t pos = ys0 + 4 * lane + r;
+                    const bool own = pos >= y0 && pos < L;
+#pragma unroll
+                    for (int i = 0; i < (MK ? kMaxQP : 1); ++i)
+                        mreg[r][i] = own && i < p.n_q ? __ldg(mrow + (int64_t)i * p.ms[1] + pos) : neg_inf();
+                }
+            };
+            auto mask_eval = [&](int64_t tile) -> uint32_t {
+                const int64_t ys0 = tile_start(tile, L);
+                bool v = false;
+#pragma unroll
+                for (int r = 0; r < (MK ? 4 : 1); ++r) {
+                    const int64_t pos = ys0 + 4 * lane + r;
+#pragma unroll
+                    for (int i = 0; i < (MK ? kMaxQP : 1); ++i)
+                        v = v || (mreg[r][i] != neg_inf() && (!p.causal || pos <= L - p.n_q + i));
+                }
+                const uint32_t bal = __ballot_sync(0xffffffffu, v);
+                uint32_t bits = 0;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) bits |= ((bal >> (8 * cc)) & 0xffu) ? 1u << cc : 0u;
+                return bits;
+            };
+            uint32_t mk_n = 0, mk_v0 = 0, mk_v1 = 0;
+            if (MK) {
+                mask_load(tt0);
+                mk_n = mask_eval(tt0);
+                if (n_in > 1) mask_load(tt0 + 1);
+            }
             for (int64_t step = 0; step < 2 * n_in && ok; ++step) {
                 int64_t j;
                 int kv;
@@ -850,7 +906,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     if (!I8) {
                         const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
                         if (lane == 0) {
-                            ok = bar_wait<I8>(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+                            ok = bar_wait<I8>(&bs->slot_empty[slot], ph ^ 1, abort_flag, p.wait_ns);
                             if (!ok) note_timeout(bs, p, 1, issued, 0);
                             else ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
                         }
@@ -875,34 +931,80 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         // each) into the raw ring
                         const uint32_t rs = issued % C::NRX, ph = (issued / C::NRX) & 1;
                         if (lane == 0) {
-                            ok = bar_wait<I8>(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
+                            ok = bar_wait<I8>(&bs->raw_empty[rs], ph ^ 1, abort_flag, p.wait_ns);
                             if (!ok) note_timeout(bs, p, 1, issued, 0);
                             else ptx::mbar_arrive_expect_tx(&bs->raw_full[rs], C::RAW);
                         }
                         ok = __shfl_sync(0xffffffffu, ok, 0);
+                        // (one 128-code box per 128 codes of the row: x = 64
+                        // pairs apart, TT * 128 bytes apart in the raw tile)
                         if (ok && tl) {
-                            if (lane < TT / a.prow)
-                                ptx::tma_load_4d(smem + C::OFF_RAW + rs * C::RAW + lane * a.prow * 128, map,
-                                                 &bs->raw_full[rs], 0, rrw, hk, rpg);
+                            if (lane < TT / a.prow) {
+#pragma unroll
+                                for (int cb = 0; cb < D / 128; ++cb)
+                                    ptx::tma_load_4d(smem + C::OFF_RAW + rs * C::RAW + cb * (TT * 128) +
+                                                         lane * a.prow * 128,
+                                                     map, &bs->raw_full[rs], cb * 64, rrw, hk, rpg);
+                            }
                         } else if (ok) {
-                            ptx::tma_gather4(smem + C::OFF_RAW + rs * C::RAW + 4 * lane * 128, map,
-                                             &bs->raw_full[rs], 0, y[0], y[1], y[2], y[3]);
+#pragma unroll
+                            for (int cb = 0; cb < D / 128; ++cb)
+                                ptx::tma_gather4(smem + C::OFF_RAW + rs * C::RAW + cb * (TT * 128) + 4 * lane * 128,
+                                                 map, &bs->raw_full[rs], cb * 64, y[0], y[1], y[2], y[3]);
                         }
+                    }
+                } else if (MK) {
+                    // K(j) takes the chunks found one tile ahead (kept for
+                    // V(j)); then the next tile's are read
+                    uint32_t bits;
+                    if (kv == 0) {
+                        bits = mk_n;
+                        if (j & 1) mk_v1 = bits; else mk_v0 = bits;
+                        if (j + 1 < n_in) mk_n = mask_eval(tt0 + j + 1);
+                        if (j + 2 < n_in) mask_load(tt0 + j + 2);
+                    } else {
+                        bits = (j & 1) ? mk_v1 : mk_v0;
+                    }
+                    const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
+                    // Only the chunks some row sees are loaded; a hidden chunk
+                    // keeps the slot's older, finite contents (zeros, or rows
+                    // of the filled prefix from an earlier tile), whose scores
+                    // are all masked, so their P is zero and the PV adds
+                    // nothing.  A tile with no visible chunk loads nothing.
+                    if (lane == 0) {
+                        ok = bar_wait<I8>(&bs->slot_empty[slot], ph ^ 1, abort_flag, p.wait_ns);
+                        if (!ok) note_timeout(bs, p, 1, issued, 0);
+                        else if (bits)
+                            ptx::mbar_arrive_expect_tx(&bs->slot_full[slot],
+                                                       (uint32_t)__popc(bits) * (C::KB * 32 * 128));
+                        else
+                            ptx::mbar_arrive(&bs->slot_full[slot]);
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    // lane 4*cb + cc: 32 rows (chunk cc) of the 64-column box cb
+                    if (ok && lane < 4 * C::KB && ((bits >> (lane & 3)) & 1u)) {
+                        const int cb = lane >> 2, cc = lane & 3;
+                        const int row = ys + 32 * cc;
+                        ptx::tma_load_4d(smem + C::OFF_SLOTS + slot * C::SLOT + cb * C::BOX + cc * (32 * 128),
+                                         kv ? (const void *)&a.tv : (const void *)&a.tk,
+                                         &bs->slot_full[slot], cb * 64, row, hk, b);
                     }
                 } else if (lane == 0 && I8) {
                     // int8 codes -> raw ring (one box of TT positions x D codes)
                     const uint32_t rs = issued % C::NRX, ph = (issued / C::NRX) & 1;
-                    ok = bar_wait<I8>(&bs->raw_empty[rs], ph ^ 1, abort_flag, kWaitNs);
+                    ok = bar_wait<I8>(&bs->raw_empty[rs], ph ^ 1, abort_flag, p.wait_ns);
                     if (!ok) note_timeout(bs, p, 1, issued, 0);
                     if (ok) {
                         ptx::mbar_arrive_expect_tx(&bs->raw_full[rs], C::RAW);
-                        ptx::tma_load_4d(smem + C::OFF_RAW + rs * C::RAW,
-                                         kv ? (const void *)&a.tv : (const void *)&a.tk,
-                                         &bs->raw_full[rs], 0, ys, hk, b);
+#pragma unroll
+                        for (int cb = 0; cb < D / 128; ++cb)
+                            ptx::tma_load_4d(smem + C::OFF_RAW + rs * C::RAW + cb * (TT * 128),
+                                             kv ? (const void *)&a.tv : (const void *)&a.tk,
+                                             &bs->raw_full[rs], cb * 64, ys, hk, b);
                     }
                 } else if (lane == 0) {
                     const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
-                    ok = bar_wait<I8>(&bs->slot_empty[slot], ph ^ 1, abort_flag, kWaitNs);
+                    ok = bar_wait<I8>(&bs->slot_empty[slot], ph ^ 1, abort_flag, p.wait_ns);
                     if (!ok) note_timeout(bs, p, 1, issued, 0);
                     if (ok) {
                         ptx::mbar_arrive_expect_tx(&bs->slot_full[slot], C::SLOT);
@@ -927,8 +1029,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             const uint32_t n = issued < RING ? issued : RING;
             for (uint32_t k = 0; k < n; ++k) {
                 const uint32_t idx = issued - 1 - k;
-                bar_wait<I8>(I8 ? &bs->raw_full[idx % RING] : &bs->slot_full[idx % RING],
-                               (idx / RING) & 1, abort_flag, kWaitNs);
+                ptx::mbar_wait_drain(I8 ? &bs->raw_full[idx % RING] : &bs->slot_full[idx % RING],
+                                     (idx / RING) & 1, kWaitNs);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -941,11 +1043,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         // S^T[pos, row] = sum_d K[pos, d] Q[row, d] for tile number tc.
         auto issue_qk = [&](uint32_t tc) -> bool {
             const uint32_t sb = tc & 1, u = tc >> 1, ki = k_fill(tc, pa), ks = ki % C::NS;
-            if (!bar_wait<I8>(&bs->slot_full[ks], (ki / C::NS) & 1, abort_flag, kWaitNs)) {
+            if (!bar_wait<I8>(&bs->slot_full[ks], (ki / C::NS) & 1, abort_flag, p.wait_ns)) {
                 note_timeout(bs, p, 3, tc, piece);
                 return false;
             }
-            if (!bar_wait<I8>(&bs->s_free[sb], (u & 1) ^ 1, abort_flag, kWaitNs)) {
+            if (!bar_wait<I8>(&bs->s_free[sb], (u & 1) ^ 1, abort_flag, p.wait_ns)) {
                 note_timeout(bs, p, 4, tc, piece);
                 return false;
             }
@@ -968,11 +1070,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         auto issue_pv = [&](uint32_t tc, bool first) -> bool {
             const uint32_t vi = v_fill(tc, pb), vs = vi % C::NS;
             const uint32_t ps = tc % C::PST, pu = tc / C::PST;
-            if (!bar_wait<I8>(&bs->slot_full[vs], (vi / C::NS) & 1, abort_flag, kWaitNs)) {
+            if (!bar_wait<I8>(&bs->slot_full[vs], (vi / C::NS) & 1, abort_flag, p.wait_ns)) {
                 note_timeout(bs, p, 6, tc, piece);
                 return false;
             }
-            if (!bar_wait<I8>(&bs->p_full[ps], pu & 1, abort_flag, kWaitNs)) {
+            if (!bar_wait<I8>(&bs->p_full[ps], pu & 1, abort_flag, p.wait_ns)) {
                 note_timeout(bs, p, 7, tc, piece);
                 return false;
             }
@@ -1016,7 +1118,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             if (lane == 0) {
                 // Software pipeline: QK of tile j+1 is issued before PV of
                 // tile j, so the next scores are ready when softmax finishes.
-                ok = bar_wait<I8>(&bs->q_full, piece & 1, abort_flag, kWaitNs);
+                ok = bar_wait<I8>(&bs->q_full, piece & 1, abort_flag, p.wait_ns);
                 if (!ok) note_timeout(bs, p, 2, tile_ctr, piece);
                 ptx::tc_fence_after();
                 ok = ok && issue_qk(tile_ctr);
@@ -1028,7 +1130,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         if (j + 2 == n_in) ptx::mma_commit(&bs->q_free);
                     }
                     if (j == 0 && piece > 0) {
-                        ok = bar_wait<I8>(&bs->o_free, (piece - 1) & 1, abort_flag, kWaitNs);
+                        ok = bar_wait<I8>(&bs->o_free, (piece - 1) & 1, abort_flag, p.wait_ns);
                         if (!ok) note_timeout(bs, p, 5, tile_ctr, piece);
                     }
                     ok = ok && issue_pv(tile_ctr + j, j == 0);
@@ -1044,7 +1146,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         // Drain: all MMAs issued by this thread complete before TMEM is freed.
         if (lane == 0 && issued_any) {
             ptx::mma_commit(&bs->exit_mma);
-            bar_wait<I8>(&bs->exit_mma, 0, abort_flag, kWaitNs);
+            ptx::mbar_wait_drain(&bs->exit_mma, 0, kWaitNs);
         }
     } else if (I8 && warp >= 4) {
         // ------------------------------------- int8 -> bf16 widening (warps 4-7)
@@ -1066,23 +1168,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             const int64_t n_fill = 2 * (piece_end - t);
             for (int64_t k = 0; k < n_fill && ok; ++k, ++f) {
                 const uint32_t rs = f % C::NRX, ss = f % C::NS;
-                ok = bar_wait<I8>(&bs->raw_full[rs], (f / C::NRX) & 1, abort_flag, kWaitNs);
+                ok = bar_wait<I8>(&bs->raw_full[rs], (f / C::NRX) & 1, abort_flag, p.wait_ns);
                 if (!ok) { note_timeout(bs, p, 17, f, piece); break; }
                 // Thread ct takes 16 codes (dims 16*q16 .. 16*q16+15) of
                 // positions r0 + RSTEP*k: one 16-byte load and two swizzled
                 // 16-byte stores each, all loads issued first.  Each group of
-                // 8 threads covers half of two rows, its low half of one and
-                // high half of the other, so its 8 loads and each of its two
-                // sets of 8 stores fall in 8 different bank groups.
-                constexpr int QPR = D / 16, RSTEP = 128 / QPR, NK = TT / RSTEP;
-                static_assert(!I8 || QPR == 8, "widening layout is for 128-code rows");
+                // 8 threads covers half of two rows (of one 128-code box of
+                // them), its low half of one and high half of the other, so
+                // its 8 loads and each of its two sets of 8 stores fall in 8
+                // different bank groups.
+                // Raw tile: RB boxes of [TT][128] codes, 128-byte swizzled
+                // (chunk c of row r at c ^ (r & 7)); head_dim 256 rows span
+                // two boxes, taken by alternate pairs of 8-thread groups.
+                constexpr int RB = D / 128, RSTEP = 16 / RB, NK = TT / RSTEP;
+                static_assert(!I8 || D == 128 || D == 256, "int8 tiles: head_dim 128 or 256");
                 const int quarter = ct >> 3, tq = ct & 7;
-                const int r0 = 2 * (quarter >> 1) + (tq >> 2);
-                const int q16 = (tq & 3) + 4 * ((tq >> 2) ^ (quarter & 1));
-                // (raw rows are 128 bytes with the 128-byte swizzle: chunk q16 of
-                // row r sits at q16 ^ (r & 7), and r & 7 == r0 & 7 here)
-                static_assert(!I8 || D == 128, "int8 tiles: one 128-byte row per position");
-                const unsigned char *raw = smem + C::OFF_RAW + rs * C::RAW + r0 * D + ((q16 ^ (r0 & 7)) << 4);
+                const int rbox = RB == 1 ? 0 : (quarter >> 1) & 1;
+                const int r0 = 2 * (quarter >> (RB == 1 ? 1 : 2)) + (tq >> 2);
+                const int c8 = (tq & 3) + 4 * ((tq >> 2) ^ (quarter & 1));
+                const int q16 = rbox * 8 + c8;    // 16-code group of the row
+                const unsigned char *raw = smem + C::OFF_RAW + rs * C::RAW + rbox * (TT * 128) +
+                                           r0 * 128 + ((c8 ^ (r0 & 7)) << 4);
                 unsigned char *dst = smem + C::OFF_SLOTS + ss * C::SLOT + (q16 >> 2) * C::BOX +
                                      r0 * 128;
                 // (r0 + RSTEP*k) & 7 == r0 & 7: the swizzled chunk offsets are per thread
@@ -1090,12 +1196,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 uint4 cw[NK];
 #pragma unroll
                 for (int k = 0; k < NK; ++k)
-                    cw[k] = *reinterpret_cast<const uint4 *>(raw + k * RSTEP * D);
+                    cw[k] = *reinterpret_cast<const uint4 *>(raw + k * RSTEP * 128);
                 // The raw slot is free for the next copy once the codes are
                 // in registers; then wait for a bf16 slot the MMAs released.
                 ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive(&bs->raw_empty[rs]);
-                ok = bar_wait<I8>(&bs->slot_empty[ss], ((f / C::NS) & 1) ^ 1, abort_flag, kWaitNs);
+                ok = bar_wait<I8>(&bs->slot_empty[ss], ((f / C::NS) & 1) ^ 1, abort_flag, p.wait_ns);
                 if (!ok) { note_timeout(bs, p, 18, f, piece); break; }
 #pragma unroll
                 for (int k = 0; k < NK; ++k) {
@@ -1137,7 +1243,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         // the parity test cannot alias.
         auto wait_pv = [&](uint32_t k) -> bool {
             for (; o_seen <= k; ++o_seen)
-                if (!bar_wait<(I8 && NV <= 8)>(&bs->o_done, o_seen & 1, abort_flag, kWaitNs)) {
+                if (!bar_wait<(I8 && NV <= 8)>(&bs->o_done, o_seen & 1, abort_flag, p.wait_ns)) {
                     note_timeout(bs, p, 11, tile_ctr, piece);
                     return false;
                 }
@@ -1146,14 +1252,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         // Barrier over this warpgroup's 128 threads, bounded.
         auto wg_sync = [&]() -> bool {
             ptx::mbar_arrive(&bs->wg_bar[wg]);
-            if (bar_wait<(I8 && NV <= 8)>(&bs->wg_bar[wg], (wg_ctr++) & 1, abort_flag, kWaitNs)) return true;
+            if (bar_wait<(I8 && NV <= 8)>(&bs->wg_bar[wg], (wg_ctr++) & 1, abort_flag, p.wait_ns)) return true;
             note_timeout(bs, p, 10, tile_ctr, piece);
             return false;
         };
         // Barrier over both warpgroups, bounded.
         auto sm_sync = [&]() -> bool {
             ptx::mbar_arrive(&bs->sm_bar);
-            if (bar_wait<(I8 && NV <= 8)>(&bs->sm_bar, (sm_ctr++) & 1, abort_flag, kWaitNs)) return true;
+            if (bar_wait<(I8 && NV <= 8)>(&bs->sm_bar, (sm_ctr++) & 1, abort_flag, p.wait_ns)) return true;
             note_timeout(bs, p, 14, tile_ctr, piece);
             return false;
         };
@@ -1216,8 +1322,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 if (n_in > 1) pg_n = page_at(1);
             }
             float ksc_n = 1.f, vsc_n = 1.f;
+            // (gather over int8 caches: the scales of the list's cells, the
+            // cell of a tile being read one tile before its scales)
+            int cell_nn = -1;
             auto load_scales = [&](int64_t jj, int pg) {
-                if (PG) {
+                if (GA) {
+                    if (pg >= 0 && pg < p.cap) {
+                        ksc_n = __ldg(ksrow + (int64_t)pg * p.kss[2]);
+                        vsc_n = __ldg(vsrow + (int64_t)pg * p.vss[2]);
+                    }
+                } else if (PG) {
                     const int64_t tok = (tt0 + jj) * TT + wt;
                     if (pg >= 0) {
                         const int64_t r = page_row(p, (int32_t)tok);
@@ -1232,7 +1346,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     }
                 }
             };
-            if (I8) load_scales(0, pg_c);
+            if (I8 && !GA) load_scales(0, pg_c);
             // gather: the list cell this lane's position holds, read one tile
             // ahead; a cell is visible if 0 <= cell < cap (cap or more is
             // flagged FD_DEV_BAD_INDEX, negative is padding).
@@ -1243,12 +1357,34 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 GA && p.bias ? p.bias + ((int64_t)w.b * p.n_q + w.i) * p.idx_len : nullptr;
             int cell_n = -1;
             float bias_n = 0.f;
+            auto list_cell = [&](int64_t jj) -> int {
+                const int64_t pos = (tt0 + jj) * TT + wt;
+                return pos < p.idx_len ? __ldg(ilist + pos) : -1;
+            };
             auto load_cell = [&](int64_t jj) {
                 const int64_t pos = (tt0 + jj) * TT + wt;
-                cell_n = pos < p.idx_len ? __ldg(ilist + pos) : -1;
+                cell_n = list_cell(jj);
                 if (blist) bias_n = pos < p.idx_len ? __ldg(blist + pos) : 0.f;
             };
             if (GA) load_cell(0);
+            if (GA && I8) {
+                if (n_in > 1) cell_nn = list_cell(1);
+                load_scales(0, cell_n);
+            }
+            // masked prefix: this position's mask value (log2 units, -inf
+            // hides it) for each query index, read one tile ahead
+            constexpr int kMaxQ = 6;
+            const float *mrow = MK ? p.mask + (int64_t)w.b * p.ms[0] : nullptr;
+            float mk_n[kMaxQ];
+            auto load_mask = [&](int64_t jj) {
+                const int64_t tok = tile_start(tt0 + jj, L) + wt;
+                const bool own = tok >= (tt0 + jj) * TT && tok < L;
+#pragma unroll
+                for (int i = 0; i < kMaxQ; ++i)
+                    mk_n[i] = own && i < p.n_q ? __ldg(mrow + (int64_t)i * p.ms[1] + tok) * 1.4426950408889634f
+                                               : neg_inf();
+            };
+            if (MK) load_mask(0);
             for (int64_t j = 0; j < n_in && ok; ++j) {
                 const int64_t y0 = (tt0 + j) * TT;
                 const int64_t token = (GA || PG) ? y0 + wt : tile_start(tt0 + j, L) + wt;
@@ -1263,7 +1399,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 if (GA) {
                     const int cell = cell_n;
                     const float cb = bias_n;
-                    if (j + 1 < n_in) load_cell(j + 1);
+                    if (I8) {
+                        cell_n = cell_nn;
+                        if (j + 2 < n_in) cell_nn = list_cell(j + 2);
+                    } else if (j + 1 < n_in) {
+                        load_cell(j + 1);
+                    }
                     if (cell >= p.cap) atomicOr(p.status, kDevBadIndex);
                     in_len = in_len && cell >= 0 && cell < p.cap && cb != neg_inf();
                     bl = cb * 1.4426950408889634f;
@@ -1273,10 +1414,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     in_len = in_len && pg_c >= 0;
                     if (j + 2 < n_in) pg_n = page_at(j + 2);
                 }
+                float mk[kMaxQ];
+                if (MK) {
+#pragma unroll
+                    for (int i = 0; i < kMaxQ; ++i) mk[i] = mk_n[i];
+                    if (j + 1 < n_in) load_mask(j + 1);
+                }
                 const float ksc = ksc_n, vsc = vsc_n;
-                if (I8 && j + 1 < n_in) load_scales(j + 1, pg_next);
+                if (I8 && j + 1 < n_in) load_scales(j + 1, GA ? cell_n : pg_next);
                 pg_c = pg_next;
-                ok = bar_wait<(I8 && NV <= 8)>(&bs->s_full[sb], u & 1, abort_flag, kWaitNs);
+                ok = bar_wait<(I8 && NV <= 8)>(&bs->s_full[sb], u & 1, abort_flag, p.wait_ns);
                 if (!ok) { note_timeout(bs, p, 9, tile_ctr, piece); break; }
                 ptx::tc_fence_after();
                 float sv[NH];
@@ -1286,13 +1433,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 ptx::mbar_arrive(&bs->s_free[sb]);
 
                 const float sl = I8 ? p.scale_log2 * ksc : p.scale_log2;
+                int mq = cb0 % p.n_q;   // masked prefix: query index of row r
 #pragma unroll
                 for (int r = 0; r < NH; ++r) {
-                    const bool vis = in_len && cb0 + r < rows && token <= lim[r];
-                    if (GA)
+                    bool vis = in_len && cb0 + r < rows && token <= lim[r];
+                    if (GA) {
                         sv[r] = vis ? __fmaf_rn(sv[r], sl, bl) : neg_inf();
-                    else
+                    } else if (MK) {
+                        float mb = mk[0];
+#pragma unroll
+                        for (int i = 1; i < kMaxQ; ++i) mb = mq == i ? mk[i] : mb;
+                        vis = vis && mb != neg_inf();
+                        sv[r] = vis ? __fmaf_rn(sv[r], sl, mb) : neg_inf();
+                        if (++mq == p.n_q) mq = 0;
+                    } else {
                         sv[r] = vis ? sv[r] * sl : neg_inf();
+                    }
                 }
                 // Refresh the running maxima only when some score passes
                 // mrun + kRescaleSlack (always on a segment's first tile).
@@ -1358,7 +1514,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 }
                 // P^T for the PV product.
                 const uint32_t ps = tile_ctr % C::PST, pu = tile_ctr / C::PST;
-                ok = bar_wait<(I8 && NV <= 8)>(&bs->p_free[ps], (pu & 1) ^ 1, abort_flag, kWaitNs);
+                ok = bar_wait<(I8 && NV <= 8)>(&bs->p_free[ps], (pu & 1) ^ 1, abort_flag, p.wait_ns);
                 if (!ok) { note_timeout(bs, p, 13, tile_ctr, piece); break; }
                 // PV of the previous tile must have completed before P of this
                 // tile is published (see wait_pv).
@@ -1572,16 +1728,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 // ------------------------------------------------------------- host side
 // [B, Hkv, cap, d] cache -> 4-D map (d, cap, Hkv, B); rows past the capacity
 // (or before 0) read as zeros.  bf16: box (64, 128, 1, 1) with the 128-byte
-// swizzle the MMA descriptors expect.  int8 (d = 128): the same 128-byte rows
-// (64 pairs of codes), also 128-byte swizzled (the widening threads read it).
-inline bool make_map(CUtensorMap *m, const void *base, const int64_t *st, const Params &p) {
+// swizzle the MMA descriptors expect.  int8: rows of d / 2 pairs of codes,
+// one box (64 pairs = 128 codes, 128 bytes) per 128 codes, also 128-byte
+// swizzled (the widening threads read it).
+inline bool make_map(CUtensorMap *m, const void *base, const int64_t *st, const Params &p,
+                     cuuint32_t box_rows = TT) {
     // (int8 codes are moved as pairs: 16-bit elements, d / 2 per row)
     const int es = p.kv_int8 ? 1 : 2;
     const cuuint64_t row_elems = p.kv_int8 ? (cuuint64_t)p.d / 2 : (cuuint64_t)p.d;
     cuuint64_t dims[4] = {row_elems, (cuuint64_t)p.cap, (cuuint64_t)p.Hkv, (cuuint64_t)p.B};
     cuuint64_t strides[3] = {(cuuint64_t)(st[2] * es), (cuuint64_t)(st[1] * es),
                              (cuuint64_t)(st[0] * es)};
-    cuuint32_t box[4] = {64u, (cuuint32_t)TT, 1, 1};
+    cuuint32_t box[4] = {64u, box_rows, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     return encode_cached(m, p.kv_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                          4, const_cast<void *>(base), dims, strides, box, estr,
@@ -1620,18 +1778,21 @@ inline bool gather_rows(const Params &p, int64_t *rs, int64_t *Y, int64_t g[3]) 
     return *Y < ((int64_t)1 << 31);
 }
 
+// (int8 caches: rows of d / 2 pairs of codes, one 128-code box per gather)
 inline bool make_gmap(CUtensorMap *m, const void *base, const Params &p, int64_t rs, int64_t Y) {
-    cuuint64_t dims[2] = {(cuuint64_t)p.d, (cuuint64_t)Y};
-    cuuint64_t strides[1] = {(cuuint64_t)rs * 2};
+    const int es = p.kv_int8 ? 1 : 2;
+    cuuint64_t dims[2] = {(cuuint64_t)(p.kv_int8 ? p.d / 2 : p.d), (cuuint64_t)Y};
+    cuuint64_t strides[1] = {(cuuint64_t)rs * es};
     cuuint32_t box[2] = {64, 1};
     cuuint32_t estr[2] = {1, 1};
-    return encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
-                         strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
+    return encode_cached(m, p.kv_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         2, const_cast<void *>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
 }
 
 // Blocks of this instantiation that can be resident at once on the current
 // device (0 on error); sets the dynamic shared memory opt-in the first time.
-template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP>
+template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP, bool MK>
 int resident_blocks() {
     using C = Cfg<D, N, I8, NV, GA>;
     static std::atomic<int> cached[64];
@@ -1640,9 +1801,9 @@ int resident_blocks() {
     int n = cached[dev].load(std::memory_order_acquire);
     if (n > 0) return n;
     int per_sm = 0, sms = 0;
-    if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV, GA, SH, PG, AP>,
+    if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_kernel<D, N, I8, NV, GA, SH, PG, AP>,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK>,
                                                       kThreadsTC, C::SMEM) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
@@ -1652,13 +1813,13 @@ int resident_blocks() {
 }
 
 template <int D, int N, bool I8, int NV = N, bool GA = false, bool SH = false, bool PG = false,
-          bool AP = false>
+          bool AP = false, bool MK = false>
 int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
     using C = Cfg<D, N, I8, NV, GA>;
-    const int resident = resident_blocks<D, N, I8, NV, GA, SH, PG, AP>();
+    const int resident = resident_blocks<D, N, I8, NV, GA, SH, PG, AP, MK>();
     if (resident <= 0) return -5;
     if (!SH && !AP) {
-        tc_kernel<D, N, I8, NV, GA, SH, PG, AP><<<G, kThreadsTC, C::SMEM, st>>>(args);
+        tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK><<<G, kThreadsTC, C::SMEM, st>>>(args);
         return cudaGetLastError() == cudaSuccess ? 0 : -5;
     }
     // shared merges or fused append: a cooperative launch (every block
@@ -1676,7 +1837,7 @@ int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_kernel<D, N, I8, NV, GA, SH, PG, AP>, ca) == cudaSuccess ? 0 : -5;
+    return cudaLaunchKernelEx(&cfg, tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK>, ca) == cudaSuccess ? 0 : -5;
 }
 
 }  // namespace

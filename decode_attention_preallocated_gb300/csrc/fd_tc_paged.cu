@@ -57,9 +57,9 @@ bool make_tiled_pmap(CUtensorMap *m, const void *base, const int64_t *st, const 
                          CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
 }
 
-// bf16 pools: rows of d elements, box (64, 1) per gather4 row; int8 pools
-// (d = 128): rows of 64 pairs of codes moved as 16-bit elements.  Both
-// 128-byte swizzled, as the tiled maps of flat caches.
+// bf16 pools: rows of d elements, box (64, 1) per gather4 row; int8 pools:
+// rows of d / 2 pairs of codes moved as 16-bit elements, one box per 128
+// codes.  Both 128-byte swizzled, as the tiled maps of flat caches.
 bool make_pmap(CUtensorMap *m, const void *base, const Params &p, int64_t rs, int64_t Y) {
     const int es = p.kv_int8 ? 1 : 2;
     const cuuint64_t row_elems = p.kv_int8 ? (cuuint64_t)p.d / 2 : (cuuint64_t)p.d;
@@ -101,10 +101,14 @@ int launch_tc_paged(const Params &p, int G, cudaStream_t st) {
         args.tv = args.gv;
     }
     const int rows = p.rows;
-    if (p.kv_int8)
+    if (p.kv_int8 && p.d == 128)
         return rows <= 8    ? launch_dn<128, 16, true, 8, false, false, true>(args, G, st)
                : rows <= 16 ? launch_dn<128, 16, true, 16, false, false, true>(args, G, st)
                             : launch_dn<128, 32, true, 32, false, false, true>(args, G, st);
+    if (p.kv_int8)
+        return rows <= 8    ? launch_dn<256, 16, true, 8, false, false, true>(args, G, st)
+               : rows <= 16 ? launch_dn<256, 16, true, 16, false, false, true>(args, G, st)
+                            : launch_dn<256, 32, true, 32, false, false, true>(args, G, st);
     if (p.d == 128)
         return rows <= 16   ? launch_dn<128, 16, false, 16, false, false, true>(args, G, st)
                : rows <= 32 ? launch_dn<128, 32, false, 32, false, false, true>(args, G, st)

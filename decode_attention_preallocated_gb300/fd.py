@@ -7,7 +7,8 @@ every call raises.
 
 Low-level names mirror the C ABI (``fd_decode``, ``fd_decode_int8``,
 ``fd_decode_append``, ``fd_decode_paged``, ``fd_decode_masked``,
-``fd_decode_gather``, ``fd_decode_gather_bias``, ``fd_topk_blocks``,
+``fd_decode_gather``, ``fd_decode_gather_int8``, ``fd_decode_gather_bias``,
+``fd_topk_blocks``,
 ``fd_workspace_create`` ...) and take ``FdTensor`` / ``FdOpts`` structures;
 ``decode``, ``decode_int8``, ``decode_append``, ``decode_paged``,
 ``decode_masked``, ``decode_gather`` and ``topk_blocks`` take
@@ -48,7 +49,8 @@ class FdTensor(ctypes.Structure):
 class FdOpts(ctypes.Structure):
     _fields_ = [("stream", ctypes.c_void_p), ("ws", ctypes.c_void_p),
                 ("num_ctas", ctypes.c_int32), ("kernel", ctypes.c_int32),
-                ("scale", ctypes.c_float), ("reserved", ctypes.c_int32 * 3)]
+                ("scale", ctypes.c_float), ("wait_limit_us", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 class FdError(RuntimeError):
@@ -73,6 +75,9 @@ _SIGNATURES = [
     ("fd_decode_gather", ctypes.c_int,
      [_P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p, ctypes.c_int32,
       _P(FdTensor), _P(FdOpts)]),
+    ("fd_decode_gather_int8", ctypes.c_int,
+     [_P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor), _P(FdTensor), ctypes.c_void_p,
+      ctypes.c_int32, _P(FdTensor), _P(FdOpts)]),
     ("fd_topk_blocks", ctypes.c_int,
      [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
       ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]),
@@ -99,6 +104,7 @@ _SIGNATURES = [
      [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
       ctypes.c_void_p, _P(ctypes.c_void_p)]),
     ("fd_workspace_reset", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    ("fd_workspace_fill_counters", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
     ("fd_workspace_destroy", ctypes.c_int, [ctypes.c_void_p]),
     ("fd_get_device_status", ctypes.c_int, [ctypes.c_void_p, _P(ctypes.c_int32)]),
     ("fd_get_device_diagnostics", ctypes.c_int, [ctypes.c_void_p, _P(ctypes.c_int32)]),
@@ -223,6 +229,13 @@ class Workspace:
         _check(lib().fd_workspace_reset(self.handle, _stream_handle(stream, self.device)),
                "fd_workspace_reset")
 
+    def fill_counters(self, value: int, stream=None):
+        """Test hook: every completion counter set to `value` (a negative one
+        stands for counters an aborted launch left behind)."""
+        _check(lib().fd_workspace_fill_counters(self.handle, int(value),
+                                                _stream_handle(stream, self.device)),
+               "fd_workspace_fill_counters")
+
     def device_status(self) -> int:
         st = ctypes.c_int32(0)
         with torch.cuda.device(self.device):
@@ -303,13 +316,14 @@ def seg_units(kernel, head_dim, kv_dtype=FD_BF16):
 
 
 # ---------------------------------------------------------- torch wrappers
-def _opts(stream_handle, ws, num_ctas, kernel, scale=0.0) -> FdOpts:
+def _opts(stream_handle, ws, num_ctas, kernel, scale=0.0, wait_limit_us=0) -> FdOpts:
     o = FdOpts()
     o.stream = stream_handle
     o.ws = ws.handle
     o.num_ctas = int(num_ctas)
     o.kernel = int(kernel)
     o.scale = float(scale)
+    o.wait_limit_us = int(wait_limit_us)
     return o
 
 
@@ -333,10 +347,11 @@ def _prepare(q, k, out, out_dtype, segments, rows, num_ctas, kernel, stream, ws)
 
 def decode(q, k_cache, v_cache, kv_lengths, n_q=None, causal=False, scale=None,
            out=None, out_dtype=torch.bfloat16, num_ctas=0, kernel=FD_KERNEL_AUTO,
-           stream=None, workspace: Optional[Workspace] = None):
+           stream=None, workspace: Optional[Workspace] = None, wait_limit_us=0):
     """Attention of q [B, n_q, Hq, d] over the first kv_lengths[b] positions of
     k_cache / v_cache [B, Hkv, cap, d] (bf16).  kv_lengths: int32 [B] on the
-    device.  Returns out [B, n_q, Hq, d]."""
+    device.  Returns out [B, n_q, Hq, d].  wait_limit_us bounds each internal
+    wait of the tensor-core kernel (0: 2 s)."""
     B, nq, Hq, d = q.shape
     n_q = nq if n_q is None else n_q
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -345,7 +360,7 @@ def decode(q, k_cache, v_cache, kv_lengths, n_q=None, causal=False, scale=None,
     out, sh, ws = _prepare(q, k_cache, out, out_dtype, B * Hkv, rows, num_ctas,
                            kernel, stream, workspace)
     tq, tk, tv, to = map(as_fd_tensor, (q, k_cache, v_cache, out))
-    o = _opts(sh, ws, num_ctas, kernel)
+    o = _opts(sh, ws, num_ctas, kernel, wait_limit_us=wait_limit_us)
     with _on_device(q.device):
         rc = lib().fd_decode(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
                              kv_lengths.data_ptr(), int(n_q), int(bool(causal)),
@@ -483,11 +498,13 @@ def decode_paged(q, k_pages, v_pages, block_table, kv_lengths, n_q=None,
 
 def decode_gather(q, k_cache, v_cache, idx, scale=None, out=None,
                   out_dtype=torch.bfloat16, num_ctas=0, kernel=FD_KERNEL_AUTO,
-                  stream=None, workspace: Optional[Workspace] = None, bias=None):
+                  stream=None, workspace: Optional[Workspace] = None, bias=None,
+                  k_scale=None, v_scale=None):
     """Attention of q [B, n_q, Hq, d] over the cache cells listed in
     idx [B, n_q, K] (int32, contiguous, on the device; < 0 = padding).
-    bias (optional): fp32 [B, n_q, K] contiguous, added to each entry's
-    score (-inf drops the entry)."""
+    bias (optional, bf16 caches): fp32 [B, n_q, K] contiguous, added to each
+    entry's score (-inf drops the entry).  int8 caches take fp32 k_scale /
+    v_scale [B, Hkv, cap] (fd_decode_gather_int8)."""
     B, nq, Hq, d = q.shape
     Hkv = k_cache.shape[1]
     if not idx.is_contiguous() or idx.dtype != torch.int32 or idx.dim() != 3:
@@ -497,6 +514,16 @@ def decode_gather(q, k_cache, v_cache, idx, scale=None, out=None,
                            kernel, stream, workspace)
     tq, tk, tv, to = map(as_fd_tensor, (q, k_cache, v_cache, out))
     o = _opts(sh, ws, num_ctas, kernel, 0.0 if scale is None else scale)
+    if k_cache.dtype == torch.int8:
+        if bias is not None or k_scale is None or v_scale is None:
+            raise ValueError("int8 caches take k_scale and v_scale, and no bias")
+        tks, tvs = as_fd_tensor(k_scale), as_fd_tensor(v_scale)
+        with _on_device(q.device):
+            rc = lib().fd_decode_gather_int8(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                             ctypes.byref(tks), ctypes.byref(tvs), idx.data_ptr(),
+                                             int(idx.shape[2]), ctypes.byref(to), ctypes.byref(o))
+        _check(rc, "fd_decode_gather_int8")
+        return out
     if bias is not None:
         if (not bias.is_contiguous() or bias.dtype != torch.float32
                 or tuple(bias.shape) != tuple(idx.shape)):

@@ -173,17 +173,28 @@ def dense_inputs(B, n_q, Hq, Hkv, d, cap, lengths, seed, causal,
 
 
 def gather_inputs(B, n_q, Hq, Hkv, d, cap, K, recent, seed, device="cpu",
-                  layout="bhtd", q_mult=1.0, name="") -> DecodeInputs:
+                  layout="bhtd", q_mult=1.0, name="", int8=False) -> DecodeInputs:
+    """Seeded gather inputs: one top-k-like list of K distinct cells per
+    (sequence, query row); int8=True quantises the caches per (token, kv
+    head) as dense_inputs does."""
     gen = _gen(seed, "cpu" if str(device) == "cpu" else device)
     q = randn_bf16((B, n_q, Hq, d), gen, device, q_mult)
-    k = make_cache(B, Hkv, cap, d, gen, device, layout)
-    v = make_cache(B, Hkv, cap, d, gen, device, layout)
+    ks = vs = None
+    if int8:
+        k, ks = quantize_per_token(make_cache(B, Hkv, cap, d, gen, device, layout, torch.float32))
+        v, vs = quantize_per_token(make_cache(B, Hkv, cap, d, gen, device, layout, torch.float32))
+        if layout == "bthd":
+            k = k.transpose(1, 2).contiguous().transpose(1, 2)
+            v = v.transpose(1, 2).contiguous().transpose(1, 2)
+    else:
+        k = make_cache(B, Hkv, cap, d, gen, device, layout)
+        v = make_cache(B, Hkv, cap, d, gen, device, layout)
     cpu_gen = _gen(seed + 7919, "cpu")
     idx = topk_like_indices(cap, K, recent, cpu_gen, B * n_q).view(B, n_q, K)
     return DecodeInputs(q=q, k=k, v=v,
                         kv_lengths=torch.full((B,), cap, dtype=torch.int32, device=device),
-                        n_q=n_q, causal=False, scale=1.0 / math.sqrt(d),
-                        idx=idx.to(device), lengths_host=[cap] * B, name=name)
+                        n_q=n_q, causal=False, scale=1.0 / math.sqrt(d), k_scale=ks,
+                        v_scale=vs, idx=idx.to(device), lengths_host=[cap] * B, name=name)
 
 
 def paged_inputs(B, n_q, Hq, Hkv, d, page_size, max_pages, lengths, seed, causal,

@@ -97,10 +97,11 @@ extern "C" {
 #define FD_KERNEL_SIMT 1         /* CUDA-core kernel, every mode           */
 #define FD_KERNEL_TC 2           /* tensor-core (tcgen05) kernel: bf16
                                     caches (head_dim 128/256, up to 64
-                                    rows) and int8 caches (head_dim 128, up
-                                    to 32 rows), flat or paged (pools whose
-                                    rows form one strided 2-D array), the
-                                    fused append over flat bf16 caches,
+                                    rows) and int8 caches (head_dim
+                                    128/256, up to 32 rows), flat or paged
+                                    (pools whose rows form one strided 2-D
+                                    array), the fused append and the
+                                    masked prefix over flat bf16 caches,
                                     and gather over bf16 caches whose rows
                                     form one strided 2-D array; 16-byte
                                     aligned q (else FD_ERR_UNSUPPORTED)    */
@@ -127,7 +128,13 @@ typedef struct fd_opts {
                                     the split count                          */
     int32_t kernel;              /* FD_KERNEL_*                              */
     float scale;                 /* fd_decode_gather only: 0 = 1/sqrt(d)     */
-    int32_t reserved[3];         /* must be zero                             */
+    int32_t wait_limit_us;       /* tensor-core kernel: bound on each of its
+                                    internal waits, in microseconds; 0 = the
+                                    default of 2 s.  A wait that runs out sets
+                                    FD_DEV_INTERNAL and the launch ends (its
+                                    output is then not valid).  Tests of that
+                                    path shorten it; 1 .. 2e6.              */
+    int32_t reserved[2];         /* must be zero                             */
 } fd_opts;
 
 /*
@@ -198,6 +205,20 @@ int fd_topk_blocks(const float *scores, int32_t B, int32_t n_q,
                    int32_t block_size, int32_t top_k, int32_t *idx,
                    void *stream);
 /*
+ * Index-gather decode over an int8 cache with per-position fp32 scales: as
+ * fd_decode_gather, with k = k_code * k_scale[b, hk, cell] and v likewise,
+ * k_scale / v_scale as in fd_decode_int8.  The gather measurements of
+ * "qwen4exp : gather-based sparse attention for QSA decode" (llama.cpp
+ * #28213, Additional information and review discussion) all run over a q8_0
+ * (8-bit) KV cache.  The tensor-core kernel serves head_dim 128 / 256 with up
+ * to 32 query rows per list (fetching each listed cell's codes with
+ * tile::gather4); the CUDA-core kernel serves the rest.
+ */
+int fd_decode_gather_int8(const fd_tensor *q, const fd_tensor *k_cache,
+                          const fd_tensor *v_cache, const fd_tensor *k_scale,
+                          const fd_tensor *v_scale, const int32_t *idx, int32_t idx_len,
+                          const fd_tensor *out, const fd_opts *opts);
+/*
  * Index-gather decode with a per-entry score bias: as fd_decode_gather, and
  * bias[b, i, t] (fp32, device, [B, n_q, idx_len] contiguous, aligned with
  * idx) is added to the scaled score of list entry t ("qwen4exp :
@@ -219,10 +240,12 @@ int fd_decode_gather_bias(const fd_tensor *q, const fd_tensor *k_cache,
  * whose cost follows the visible chunks ("qwen4exp : gather-based sparse
  * attention for QSA decode", llama.cpp #28213, Metal measurements: the
  * FA-vec kernel skips fully masked 32-cell chunks).  Mask values must be
- * finite or -inf.  Served by the CUDA-core kernel (FD_KERNEL_TC returns
- * FD_ERR_UNSUPPORTED); the tensor-core path for the same computation is
- * fd_decode_gather_bias over the visible cells.  Other arguments as
- * fd_decode.
+ * finite or -inf.  Both kernels serve it: the CUDA-core kernel skips a
+ * hidden chunk (its tiles are 32 positions); the tensor-core kernel, whose
+ * tiles are 128 positions, loads each tile as four 32-position chunks and
+ * copies only the chunks some query row sees.  Positions the mask hides
+ * must hold finite values (they lie in the filled prefix).  Other arguments
+ * as fd_decode.
  */
 int fd_decode_masked(const fd_tensor *q, const fd_tensor *k_cache,
                      const fd_tensor *v_cache, const int32_t *kv_lengths,
@@ -341,6 +364,14 @@ int fd_workspace_create(int64_t max_segments, int32_t max_rows,
  * only after a launch was aborted part-way; every completed launch leaves the
  * counters at zero). */
 int fd_workspace_reset(fd_workspace *ws, void *stream);
+/* Test hook for the failure path: sets every per-segment completion counter
+ * to `value` on `stream`.  A negative value stands for counters an aborted
+ * launch left behind: the next call whose blocks share the merge of a split
+ * segment (the tensor-core kernel's cooperative launches over few segments)
+ * then waits for pieces that never arrive, gives up after opts->wait_limit_us
+ * and sets FD_DEV_INTERNAL, recording the wait in fd_get_device_diagnostics;
+ * fd_workspace_reset restores the zeros.  Never needed in normal use. */
+int fd_workspace_fill_counters(fd_workspace *ws, int32_t value, void *stream);
 int fd_workspace_destroy(fd_workspace *ws);
 /* Synchronously reads the sticky status word (FD_DEV_* bits). */
 int fd_get_device_status(fd_workspace *ws, int32_t *status);

@@ -50,7 +50,7 @@ def run_gpu(inp, out_dtype=torch.bfloat16, num_ctas=0, kernel=fd.FD_KERNEL_AUTO,
     elif inp.idx is not None:
         out = fd.decode_gather(inp.q, inp.k, inp.v, inp.idx, scale=inp.scale,
                                out_dtype=out_dtype, num_ctas=num_ctas, kernel=kernel,
-                               workspace=workspace)
+                               workspace=workspace, k_scale=inp.k_scale, v_scale=inp.v_scale)
     elif inp.k.dtype == torch.int8:
         out = fd.decode_int8(inp.q, inp.k, inp.v, inp.k_scale, inp.v_scale,
                              inp.kv_lengths, n_q=inp.n_q, causal=inp.causal,
@@ -76,7 +76,8 @@ def run_oracle(inp):
                                              inp.kv_lengths.cpu(), inp.n_q, inp.causal,
                                              inp.scale, inp.k_scale, inp.v_scale))
     if inp.idx is not None:
-        return torch.from_numpy(oracle.gather(inp.q, inp.k, inp.v, inp.idx, inp.scale))
+        return torch.from_numpy(oracle.gather(inp.q, inp.k, inp.v, inp.idx, inp.scale,
+                                              inp.k_scale, inp.v_scale))
     lens = inp.kv_lengths.cpu()
     return torch.from_numpy(oracle.dense(inp.q, inp.k, inp.v, lens, inp.n_q, inp.causal,
                                          inp.scale, inp.k_scale, inp.v_scale))

@@ -83,6 +83,14 @@ def test_host_validation_codes(L):
     assert call_dense(q, k, v, o, causal=3) == fd.FD_ERR_ARG
     assert call_dense(q, k, v, o, kernel=7) == fd.FD_ERR_ARG
     assert call_dense(q, k, v, o, num_ctas=-1) == fd.FD_ERR_ARG
+    assert call_dense(q, k, v, o, wait_limit_us=-1) == fd.FD_ERR_ARG
+    assert call_dense(q, k, v, o, wait_limit_us=2000001) == fd.FD_ERR_ARG
+    assert call_dense(q, k, v, o, wait_limit_us=1000) == fd.FD_ERR_WORKSPACE
+    o2 = fd.FdOpts()
+    o2.reserved[1] = 1
+    assert fd.lib().fd_decode(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), 0x200000, 1, 0,
+                              0.1, ctypes.byref(o), ctypes.byref(o2)) == fd.FD_ERR_ARG
+    assert L.fd_workspace_fill_counters(None, -1, None) == fd.FD_ERR_ARG
     qq, kk, vv, oo = good(d=64)
     assert call_dense(qq, kk, vv, oo) == fd.FD_ERR_UNSUPPORTED
     qq, kk, vv, oo = good(n_q=7)

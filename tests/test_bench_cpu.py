@@ -47,16 +47,18 @@ def test_append_inputs_and_bytes():
 
 
 def test_traffic_record_follows_the_kernel_sources(tmp_path, monkeypatch):
-    # the committed record matches the current sources; a record taken on
-    # other sources is not reported
-    assert bench.recorded_traffic("ragged") is not None
+    # a record taken on the current kernel sources is reported; one taken on
+    # other sources is not
     prof = tmp_path / "profiles"
     prof.mkdir()
-    (prof / "traffic_ragged.txt").write_text(
-        "kernel_sources: 0000000000000000\ndram_bytes_per_launch: 123\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     src = tmp_path / "decode_attention_preallocated_gb300"
     os.symlink(os.path.join(ROOT, "decode_attention_preallocated_gb300"), src)
+    (prof / "traffic_ragged.txt").write_text(
+        "kernel_sources: %s\ndram_bytes_per_launch: 123\n" % bench.kernel_source_hash())
+    assert bench.recorded_traffic("ragged") == 123.0
+    (prof / "traffic_ragged.txt").write_text(
+        "kernel_sources: 0000000000000000\ndram_bytes_per_launch: 123\n")
     assert bench.recorded_traffic("ragged") is None
 
 
@@ -74,3 +76,9 @@ def test_oracle_timing_whole_call_and_scaled_sample():
 def test_baseline_config_tags_name_the_five_workloads():
     assert [n for _, n in bench.BASELINE_CONFIGS] == list(W.WORKLOADS)
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_int8_gather_bytes_count_codes_and_scales():
+    inp = W.gather_inputs(1, 2, 8, 2, 128, 500, 40, 8, seed=3, int8=True)
+    inp.idx[0, 1, :3] = -1
+    assert bench.algorithmic_bytes(inp) == (2 * 40 - 3) * 2 * (128 * 2 + 8)

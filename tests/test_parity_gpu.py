@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 KERNELS = [fd.FD_KERNEL_SIMT]
 DENSE_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]
-INT8_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]   # tensor cores: head_dim 128, <= 32 rows
+INT8_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]   # tensor cores: <= 32 rows
 GATHER_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]
 
 
@@ -43,8 +43,6 @@ def check(inp_cpu, out_dtype=torch.bfloat16, num_ctas=0, kernel=fd.FD_KERNEL_AUT
 @pytest.mark.parametrize("kernel", DENSE_KERNELS)
 def test_golden_fixture_on_gpu(name, d, kernel):
     fx = load_fixture(name, pad_d=d)
-    if kernel == fd.FD_KERNEL_TC and fx.get("int8") and d != 128:
-        pytest.skip("the tensor-core kernel serves head_dim-128 int8 caches")
     dev = lambda t: None if t is None else t.cuda()
     for out_dtype in (torch.float32, torch.bfloat16):
         if fx["mode"] == "gather":
@@ -245,6 +243,32 @@ def test_gather_tensor_core_splits_token_major(ctas, d):
         compare(got, run_oracle(inp), od, "gather tc token-major")
 
 
+@pytest.mark.parametrize("kernel", GATHER_KERNELS)
+@pytest.mark.parametrize("d,g,ctas", [(128, 8, 0), (128, 16, 7), (256, 4, 0), (256, 32, 300)])
+def test_gather_int8(kernel, d, g, ctas):
+    # int8 caches with per-cell scales: padding, an out-of-range cell, lists
+    # longer than a tile, 8 / 16 / 4 / 32 query heads per kv head
+    inp = W.gather_inputs(2, 2, 4 * g, 4, d, 3000, 300, 32, 41, int8=True)
+    inp.idx[0, 0, 5] = -1
+    inp.idx[1, 1, 9] = 3000
+    check(inp, torch.float32, kernel=kernel, num_ctas=ctas)
+    check(inp, torch.bfloat16, kernel=kernel, num_ctas=ctas)
+
+
+@pytest.mark.parametrize("kernel", GATHER_KERNELS)
+def test_gather_int8_workload_shape(kernel):
+    # the gather workload's shape (2048 of 131072 cells, 32 / 4 heads,
+    # head_dim 128) over an int8 cache, against the oracle
+    inp = W.gather_inputs(1, 1, 32, 4, 128, 131072, 2048, 128, 1, device="cuda", int8=True)
+    got = run_gpu(inp, torch.bfloat16, kernel=kernel)
+    torch.cuda.synchronize()
+    cpu = W.DecodeInputs(q=inp.q.cpu(), k=inp.k.cpu(), v=inp.v.cpu(),
+                         kv_lengths=inp.kv_lengths.cpu(), n_q=1, causal=False, scale=inp.scale,
+                         k_scale=inp.k_scale.cpu(), v_scale=inp.v_scale.cpu(),
+                         idx=inp.idx.cpu())
+    compare(got, run_oracle(cpu), torch.bfloat16, "int8 gather workload")
+
+
 # -------------------------------------------------------------------- int8
 @pytest.mark.parametrize("kernel", INT8_KERNELS)
 @pytest.mark.parametrize("causal,n_q", [(False, 1), (True, 4)])
@@ -257,8 +281,6 @@ def test_int8_small(kernel, causal, n_q):
 @pytest.mark.parametrize("kernel", INT8_KERNELS)
 @pytest.mark.parametrize("d", [128, 256])
 def test_int8_poisoned_tail_scales(kernel, d):
-    if kernel == fd.FD_KERNEL_TC and d != 128:
-        pytest.skip("tensor-core int8 path: head_dim 128")
     inp = W.dense_inputs(2, 1, 16, 4, d, 300, [150, 299], 25, False, int8=True, tail="nan")
     check(inp, torch.float32, kernel=kernel)
 
@@ -268,6 +290,17 @@ def test_int8_tensor_core_splits_and_32_rows(ctas):
     # 32 packed rows (8 heads per group x 4 causal rows), ragged lengths, the
     # segments cut into many split pieces
     inp = W.dense_inputs(3, 4, 32, 4, 128, 1500, [1500, 611, 129], 26, True, int8=True)
+    check(inp, torch.float32, kernel=fd.FD_KERNEL_TC, num_ctas=ctas)
+    check(inp, torch.bfloat16, kernel=fd.FD_KERNEL_TC, num_ctas=ctas)
+
+
+@pytest.mark.parametrize("ctas", [1, 5, 64, 0])
+@pytest.mark.parametrize("rows", [(8, 1, False), (4, 4, True), (8, 4, True)])
+def test_int8_tensor_core_head_dim_256(ctas, rows):
+    # head_dim 256 int8 caches on the tensor cores: 8 / 16 / 32 packed rows
+    # (group x window), ragged lengths with a partial last tile, split pieces
+    g, n_q, causal = rows
+    inp = W.dense_inputs(3, n_q, 4 * g, 4, 256, 1100, [1100, 389, 77], 31, causal, int8=True)
     check(inp, torch.float32, kernel=fd.FD_KERNEL_TC, num_ctas=ctas)
     check(inp, torch.bfloat16, kernel=fd.FD_KERNEL_TC, num_ctas=ctas)
 
@@ -347,6 +380,21 @@ def test_int8_workload_full_size_sampled(kernel):
                          scale=inp.scale, k_scale=inp.k_scale.cpu(),
                          v_scale=inp.v_scale.cpu())
     compare(got, run_oracle(cpu), torch.bfloat16, "int8 full")
+
+
+@pytest.mark.parametrize("kernel", INT8_KERNELS)
+def test_int8_head_dim_256_full_size(kernel):
+    # the int8 workload's shape at head_dim 256 (4 x 131072 tokens, 32 / 8
+    # heads, 2.1 GB of codes): every output row against the oracle
+    inp = W.dense_inputs(4, 1, 32, 8, 256, 131072, [131072] * 4, 2, False, device="cuda",
+                         int8=True)
+    got = run_gpu(inp, torch.bfloat16, kernel=kernel)
+    torch.cuda.synchronize()
+    cpu = W.DecodeInputs(q=inp.q.cpu(), k=inp.k.cpu(), v=inp.v.cpu(),
+                         kv_lengths=inp.kv_lengths.cpu(), n_q=1, causal=False,
+                         scale=inp.scale, k_scale=inp.k_scale.cpu(),
+                         v_scale=inp.v_scale.cpu())
+    compare(got, run_oracle(cpu), torch.bfloat16, "int8 d256 full")
 
 
 # -------------------------------------------------- kernel choice by layout

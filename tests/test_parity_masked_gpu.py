@@ -1,8 +1,8 @@
-"""GPU parity of the masked prefix with chunk skipping (fd_decode_masked,
-CUDA-core kernel) against the fp64 oracle: masks that hide most 32-position
+"""GPU parity of the masked prefix with chunk skipping (fd_decode_masked, on
+both kernels) against the fp64 oracle: masks that hide most 32-position
 chunks, seeded finite biases, causal windows, ragged and empty sequences,
-head_dim 128 and 256, split counts, everything hidden, and the mask built
-from the gather workload's list."""
+NaN past the lengths, head_dim 128 and 256, split counts, everything hidden,
+and the mask built from the gather workload's list."""
 import pytest
 import torch
 
@@ -48,37 +48,53 @@ def run(inp, mask, out_dtype, num_ctas=0, kernel=fd.FD_KERNEL_AUTO):
     return out
 
 
+KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]
+
 CASES = {
     "d128_decode": (3, 1, 8, 2, 128, 3000, [3000, 1, 1777], False),
     "d256_mtp": (2, 4, 16, 4, 256, 2500, [2500, 999], True),
+    "d256_ragged6": (3, 6, 16, 4, 256, 1400, [1400, 263, 1291], True),
+    "rows48": (2, 3, 64, 4, 128, 900, [900, 77], True),
     "rows64": (2, 2, 32, 1, 128, 1200, [1200, 0], True),
 }
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("case", sorted(CASES))
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
-def test_masked_matches_oracle(case, out_dtype):
+def test_masked_matches_oracle(case, out_dtype, kernel):
     B, n_q, Hq, Hkv, d, cap, lens, causal = CASES[case]
-    inp = W.dense_inputs(B, n_q, Hq, Hkv, d, cap, lens, 120, causal)
+    # NaN past each length: a read of the tail would reach the output
+    inp = W.dense_inputs(B, n_q, Hq, Hkv, d, cap, lens, 120, causal, tail="nan")
     mask = chunk_mask(B, n_q, cap, 121)
     ref = torch.from_numpy(oracle.masked(inp.q, inp.k, inp.v, inp.kv_lengths, mask, n_q,
                                          causal, inp.scale))
-    compare(run(inp, mask, out_dtype), ref, out_dtype, case)
+    compare(run(inp, mask, out_dtype, kernel=kernel), ref, out_dtype, case)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("ctas", [1, 7, 300])
-def test_masked_split_counts_and_hidden_rows(ctas):
+def test_masked_split_counts_and_hidden_rows(ctas, kernel):
     inp = W.dense_inputs(2, 3, 8, 2, 256, 2000, [2000, 1500], 122, True)
     mask = chunk_mask(2, 3, 2000, 123, keep=0.3)
     mask[1, 2, :] = -float("inf")                       # a row with nothing visible
     ref = torch.from_numpy(oracle.masked(inp.q, inp.k, inp.v, inp.kv_lengths, mask, 3, True,
                                          inp.scale))
-    got = run(inp, mask, torch.float32, num_ctas=ctas)
+    got = run(inp, mask, torch.float32, num_ctas=ctas, kernel=kernel)
     compare(got, ref, torch.float32, "masked splits")
     assert torch.count_nonzero(got[1, 2].cpu()) == 0
 
 
-def test_masked_from_a_gather_list_and_tensor_core_refusal():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_masked_everything_hidden_gives_zeros(kernel):
+    inp = W.dense_inputs(2, 2, 8, 2, 128, 700, [700, 300], 124, True)
+    mask = torch.full((2, 2, 700), -float("inf"))
+    got = run(inp, mask, torch.float32, kernel=kernel)
+    assert torch.count_nonzero(got.cpu()) == 0
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_masked_from_a_gather_list(kernel):
     # the gather workload's selection as a mask over the whole window
     inp = W.gather_inputs(1, 1, 32, 4, 128, 131072, 2048, 128, seed=1)
     mask = torch.full((1, 1, 131072), -float("inf"))
@@ -86,6 +102,5 @@ def test_masked_from_a_gather_list_and_tensor_core_refusal():
     dense = W.DecodeInputs(q=inp.q, k=inp.k, v=inp.v, kv_lengths=inp.kv_lengths, n_q=1,
                            causal=False, scale=inp.scale)
     ref = torch.from_numpy(oracle.gather(inp.q, inp.k, inp.v, inp.idx, inp.scale))
-    compare(run(dense, mask, torch.bfloat16), ref, torch.bfloat16, "masked = gather")
-    with pytest.raises(fd.FdError):
-        run(dense, mask, torch.float32, kernel=fd.FD_KERNEL_TC)
+    for od in (torch.bfloat16, torch.float32):
+        compare(run(dense, mask, od, kernel=kernel), ref, od, "masked = gather")

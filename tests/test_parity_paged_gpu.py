@@ -113,6 +113,16 @@ def test_paged_int8_tensor_core_splits(ctas):
     check(inp, torch.float32, kernel=fd.FD_KERNEL_TC, num_ctas=ctas)
 
 
+@pytest.mark.parametrize("ps", [16, 64, 100, 256])
+def test_paged_int8_head_dim_256_tensor_core(ps):
+    # head_dim 256 int8 pools: page runs of 16 / 64 / 256 positions, and a
+    # page size (100) whose tiles are gathered row by row
+    inp = W.paged_inputs(3, 4, 16, 4, 256, ps, 2000 // ps + 1, [1500, 611, 129], 40, True,
+                         int8=True, tail="nan")
+    check(inp, torch.float32, kernel=fd.FD_KERNEL_TC)
+    check(inp, torch.bfloat16, kernel=fd.FD_KERNEL_TC)
+
+
 def test_paged_layout_that_no_row_view_covers_falls_back():
     # pool rows padded to 136 elements and a page stride that is not a
     # multiple of the row stride: the tensor-core kernel declines, AUTO takes
