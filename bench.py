@@ -222,6 +222,10 @@ def call_fn(inp, out, ws, kernel, num_ctas=0):
                                         inp.kv_lengths, causal=inp.causal, scale=inp.scale,
                                         update_lengths=False, out=out, workspace=ws,
                                         kernel=kernel, num_ctas=num_ctas)
+    if getattr(inp, "mask", None) is not None:
+        return lambda: fd.decode_masked(inp.q, inp.k, inp.v, inp.kv_lengths, inp.mask,
+                                        n_q=inp.n_q, causal=inp.causal, scale=inp.scale, out=out,
+                                        workspace=ws, kernel=kernel, num_ctas=num_ctas)
     if inp.block_table is not None:
         return lambda: fd.decode_paged(inp.q, inp.k, inp.v, inp.block_table, inp.kv_lengths,
                                        n_q=inp.n_q, causal=inp.causal, scale=inp.scale,
@@ -251,6 +255,17 @@ def algorithmic_bytes(inp):
             return valid * Hkv * (d * 2 + 8)
         return valid * Hkv * d * 2 * 2
     es = 1 if inp.k.dtype == torch.int8 else 2
+    if getattr(inp, "mask", None) is not None:
+        # masked prefix: the K / V rows of the 32-position chunks some query
+        # row sees (the granularity at which the scan skips)
+        chunks = 0
+        for b_, L in enumerate(inp.lengths_host):
+            m = inp.mask[b_, :, :L]
+            pad = (-L) % 32
+            if pad:
+                m = torch.nn.functional.pad(m, (0, pad), value=-float("inf"))
+            chunks += int((m.reshape(m.shape[0], -1, 32) != -float("inf")).any(2).any(0).sum())
+        return chunks * 32 * Hkv * d * 2 * 2
     if getattr(inp, "k_new", None) is not None:
         # fused append: the new rows are read once and written once, and the
         # attention reads the prefix including them
@@ -373,23 +388,10 @@ def oracle_sample(inp_cpu, budget_s=10.0, max_calls=50):
     b = 0
     while t_used < budget_s and seqs < max_calls:
         sl = slice(b, b + 1)
-        L = [inp_cpu.lengths_host[b]]
         t0 = time.perf_counter()
-        if inp_cpu.idx is not None:
-            oracle.gather(inp_cpu.q[sl], inp_cpu.k[sl], inp_cpu.v[sl], inp_cpu.idx[sl],
-                          inp_cpu.scale)
-        else:
-            oracle.dense(inp_cpu.q[sl], inp_cpu.k[sl], inp_cpu.v[sl], L, inp_cpu.n_q,
-                         inp_cpu.causal, inp_cpu.scale,
-                         None if inp_cpu.k_scale is None else inp_cpu.k_scale[sl],
-                         None if inp_cpu.v_scale is None else inp_cpu.v_scale[sl])
+        oracle_call(inp_cpu, sl)
         t_used += time.perf_counter() - t0
-        sub = type(inp_cpu)(q=inp_cpu.q[sl], k=inp_cpu.k[sl], v=inp_cpu.v[sl],
-                            kv_lengths=inp_cpu.kv_lengths[sl], n_q=inp_cpu.n_q,
-                            causal=inp_cpu.causal, scale=inp_cpu.scale,
-                            k_scale=None if inp_cpu.k_scale is None else inp_cpu.k_scale[sl],
-                            idx=None if inp_cpu.idx is None else inp_cpu.idx[sl],
-                            lengths_host=L)
+        sub = sub_inputs(inp_cpu, sl)
         bytes_done += algorithmic_bytes(sub)
         seqs += 1
         b = (b + 1) % B
@@ -407,15 +409,31 @@ def cpu_view(inp):
         k_scale=None if inp.k_scale is None else inp.k_scale.cpu(),
         v_scale=None if inp.v_scale is None else inp.v_scale.cpu(),
         idx=None if inp.idx is None else inp.idx.cpu(),
-        lengths_host=list(inp.lengths_host), name=inp.name)
+        lengths_host=list(inp.lengths_host), name=inp.name,
+        mask=None if getattr(inp, "mask", None) is None else inp.mask.cpu())
+
+
+def sub_inputs(inp, sl):
+    """Sequences `sl` of a workload (CPU view)."""
+    cut = lambda t: None if t is None else t[sl]  # noqa: E731
+    return type(inp)(q=inp.q[sl], k=inp.k[sl], v=inp.v[sl], kv_lengths=inp.kv_lengths[sl],
+                     n_q=inp.n_q, causal=inp.causal, scale=inp.scale, k_scale=cut(inp.k_scale),
+                     v_scale=cut(inp.v_scale), idx=cut(inp.idx),
+                     lengths_host=inp.lengths_host[sl], mask=cut(getattr(inp, "mask", None)))
 
 
 def oracle_call(inp_cpu, sl):
     """The fp64 oracle on the sequences `sl` of a workload (CPU view)."""
     import oracle
+    if getattr(inp_cpu, "mask", None) is not None:
+        return oracle.masked(inp_cpu.q[sl], inp_cpu.k[sl], inp_cpu.v[sl],
+                             inp_cpu.lengths_host[sl], inp_cpu.mask[sl], inp_cpu.n_q,
+                             inp_cpu.causal, inp_cpu.scale)
     if inp_cpu.idx is not None:
         return oracle.gather(inp_cpu.q[sl], inp_cpu.k[sl], inp_cpu.v[sl], inp_cpu.idx[sl],
-                             inp_cpu.scale)
+                             inp_cpu.scale,
+                             None if inp_cpu.k_scale is None else inp_cpu.k_scale[sl],
+                             None if inp_cpu.v_scale is None else inp_cpu.v_scale[sl])
     return oracle.dense(inp_cpu.q[sl], inp_cpu.k[sl], inp_cpu.v[sl],
                         inp_cpu.lengths_host[sl], inp_cpu.n_q, inp_cpu.causal, inp_cpu.scale,
                         None if inp_cpu.k_scale is None else inp_cpu.k_scale[sl],
@@ -442,12 +460,7 @@ def oracle_us(inp_cpu, threads, budget_s=None):
         t0 = time.perf_counter()
         oracle_call(inp_cpu, sl)
         t_used += time.perf_counter() - t0
-        sub = type(inp_cpu)(q=inp_cpu.q[sl], k=inp_cpu.k[sl], v=inp_cpu.v[sl],
-                            kv_lengths=inp_cpu.kv_lengths[sl], n_q=inp_cpu.n_q,
-                            causal=inp_cpu.causal, scale=inp_cpu.scale,
-                            k_scale=None if inp_cpu.k_scale is None else inp_cpu.k_scale[sl],
-                            idx=None if inp_cpu.idx is None else inp_cpu.idx[sl],
-                            lengths_host=inp_cpu.lengths_host[sl])
+        sub = sub_inputs(inp_cpu, sl)
         done += algorithmic_bytes(sub)
         seqs += 1
     if seqs == B:

@@ -220,6 +220,7 @@ struct Cfg {
     static_assert(SMEM + 64 <= BUDGET, "shared memory budget");
     static constexpr uint32_t COLS = 2 * N + DC * N;
     static constexpr uint32_t TMEM_COLS = COLS <= 32 ? 32 : COLS <= 64 ? 64 : COLS <= 128 ? 128 : 256;
+    // pieces per iteration of the last arriver's single-pass merge (head_dim 256)
     static constexpr int MERGE_UNROLL = (D == 256 && NV >= 32 && !I8) ? 1 : 2;
     static constexpr uint32_t IDESC_QK = ptx::idesc_bf16(128, N, 0, 0);
     static constexpr uint32_t IDESC_PV = ptx::idesc_bf16(128, N, 1, 1);
@@ -1628,12 +1629,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 const int r1w = min(cb0 + NH, rows);       // this group merges rows cb0 .. r1w-1
                 if (!share_merge && bs->last_flag && r1w > cb0) {
                     __threadfence();
-                    // Merge the pieces' partials in one pass per row: running
-                    // maximum M, merged sum Ls and accumulator rescaled as each
-                    // piece arrives.  Thread -> 4 consecutive dims of rows
-                    // cb0 + rg + RG*k; row indices are clamped into range
-                    // (weight 0 beyond) so every load is unconditional and two
-                    // pieces' loads are in flight together.
+                    // Merge the pieces' partials.  head_dim 128 (launches
+                    // that often split a segment many ways): two passes per
+                    // row, the maximum M over the pieces, then the weighted
+                    // sums Ls and acc (weights 2^(m - M)), neither carrying a
+                    // dependence from one piece's loads to the next, so many
+                    // pieces' loads are in flight together.  head_dim 256:
+                    // one pass with a running maximum (the shared merge's
+                    // arithmetic, bit for bit; a smaller loop body, which
+                    // runs once from cold instruction caches).  Thread -> 4
+                    // consecutive dims of rows cb0 + rg + RG*k; row indices
+                    // are clamped into range (weight 0 beyond) so every load
+                    // is unconditional.
                     constexpr int TPR = D / 4, RG = 128 / TPR, RPT = NH / RG;
                     constexpr int CH = RPT < 8 ? RPT : 8;
                     const int dq = (wt % TPR) * 4, rg = wt / TPR;
@@ -1650,29 +1657,54 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                             M[k] = neg_inf();
                             Ls[k] = 0.f;
                         }
-                        // (one piece per iteration where the rows are many: the
-                        // merge runs once, from cold instruction caches, and a
-                        // smaller loop body measured faster there)
-#pragma unroll(C::MERGE_UNROLL)
-                        for (int c2 = c_first; c2 <= c_last; ++c2) {
-                            const float *sl = slot_ptr(p, s, c2);
+                        if (D == 128) {
+#pragma unroll 8
+                            for (int c2 = c_first; c2 <= c_last; ++c2) {
+                                const float *sl = slot_ptr(p, s, c2);
 #pragma unroll
-                            for (int k = 0; k < CH; ++k) {
-                                const float mv = __ldcg(sl + rows * D + rr[k]);
-                                const float lv = __ldcg(sl + rows * D + rows + rr[k]);
-                                const float4 v =
-                                    __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + dq));
-                                const float mn = fmaxf(M[k], mv);
-                                const float mu = mn == neg_inf() ? 0.f : mn;
-                                const float a = fast_exp2(M[k] - mu), w = fast_exp2(mv - mu);
-                                // (explicit roundings: the shared merge computes
-                                // the same values bit for bit)
-                                M[k] = mn;
-                                Ls[k] = __fmaf_rn(w, lv, Ls[k] * a);
-                                acc[k].x = __fmaf_rn(w, v.x, acc[k].x * a);
-                                acc[k].y = __fmaf_rn(w, v.y, acc[k].y * a);
-                                acc[k].z = __fmaf_rn(w, v.z, acc[k].z * a);
-                                acc[k].w = __fmaf_rn(w, v.w, acc[k].w * a);
+                                for (int k = 0; k < CH; ++k) M[k] = fmaxf(M[k], __ldcg(sl + rows * D + rr[k]));
+                            }
+#pragma unroll
+                            for (int k = 0; k < CH; ++k) M[k] = M[k] == neg_inf() ? 0.f : M[k];
+#pragma unroll 4
+                            for (int c2 = c_first; c2 <= c_last; ++c2) {
+                                const float *sl = slot_ptr(p, s, c2);
+#pragma unroll
+                                for (int k = 0; k < CH; ++k) {
+                                    const float mv = __ldcg(sl + rows * D + rr[k]);
+                                    const float lv = __ldcg(sl + rows * D + rows + rr[k]);
+                                    const float4 v =
+                                        __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + dq));
+                                    const float w = fast_exp2(mv - M[k]);
+                                    Ls[k] = __fmaf_rn(w, lv, Ls[k]);
+                                    acc[k].x = __fmaf_rn(w, v.x, acc[k].x);
+                                    acc[k].y = __fmaf_rn(w, v.y, acc[k].y);
+                                    acc[k].z = __fmaf_rn(w, v.z, acc[k].z);
+                                    acc[k].w = __fmaf_rn(w, v.w, acc[k].w);
+                                }
+                            }
+                        } else {
+#pragma unroll(C::MERGE_UNROLL)
+                            for (int c2 = c_first; c2 <= c_last; ++c2) {
+                                const float *sl = slot_ptr(p, s, c2);
+#pragma unroll
+                                for (int k = 0; k < CH; ++k) {
+                                    const float mv = __ldcg(sl + rows * D + rr[k]);
+                                    const float lv = __ldcg(sl + rows * D + rows + rr[k]);
+                                    const float4 v =
+                                        __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + dq));
+                                    const float mn = fmaxf(M[k], mv);
+                                    const float mu = mn == neg_inf() ? 0.f : mn;
+                                    const float a = fast_exp2(M[k] - mu), w = fast_exp2(mv - mu);
+                                    // (explicit roundings: the shared merge computes
+                                    // the same values bit for bit)
+                                    M[k] = mn;
+                                    Ls[k] = __fmaf_rn(w, lv, Ls[k] * a);
+                                    acc[k].x = __fmaf_rn(w, v.x, acc[k].x * a);
+                                    acc[k].y = __fmaf_rn(w, v.y, acc[k].y * a);
+                                    acc[k].z = __fmaf_rn(w, v.z, acc[k].z * a);
+                                    acc[k].w = __fmaf_rn(w, v.w, acc[k].w * a);
+                                }
                             }
                         }
 #pragma unroll

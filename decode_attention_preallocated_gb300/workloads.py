@@ -59,6 +59,8 @@ class DecodeInputs:
     # block_table[b, j // page_size]
     block_table: Optional[torch.Tensor] = None   # [B, max_pages] int32
     page_size: int = 0
+    # masked prefix: fp32 [B, n_q, cap] added to the scores (-inf hides)
+    mask: Optional[torch.Tensor] = None
 
     @property
     def shape(self):
@@ -278,6 +280,22 @@ def workload(name: str, seed: int = 1, device="cpu", tail="randn",
     if name == "int8":
         return dense_inputs(4, 1, 32, 8, 128, 131072, [131072] * 4, seed, False,
                             device, layout, tail, int8=True, name=name)
+    if name == "int8_d256":
+        # the int8 workload's shape at head_dim 256
+        return dense_inputs(4, 1, 32, 8, 256, 131072, [131072] * 4, seed, False, device,
+                            layout, tail, int8=True, name=name)
+    if name == "gather_int8":
+        # the gather workload over an int8 cache
+        return gather_inputs(1, 1, 32, 4, 128, 131072, 2048, 128, seed, device, layout,
+                             name=name, int8=True)
+    if name == "masked_list":
+        # the gather workload's selection as a mask over its whole prefix
+        inp = gather_inputs(1, 1, 32, 4, 128, 131072, 2048, 128, seed, device, layout,
+                            name=name)
+        inp.mask = torch.full((1, 1, 131072), -float("inf"), device=device)
+        inp.mask[0, 0, inp.idx[0, 0].long()] = 0.0
+        inp.idx = None
+        return inp
     if name.startswith("paged_ps"):
         # the ragged workload over a paged cache of page_size positions
         ps = int(name[len("paged_ps"):])

@@ -82,3 +82,29 @@ def test_int8_gather_bytes_count_codes_and_scales():
     inp = W.gather_inputs(1, 2, 8, 2, 128, 500, 40, 8, seed=3, int8=True)
     inp.idx[0, 1, :3] = -1
     assert bench.algorithmic_bytes(inp) == (2 * 40 - 3) * 2 * (128 * 2 + 8)
+
+
+def test_masked_bytes_count_visible_chunks():
+    inp = W.dense_inputs(2, 2, 8, 2, 128, 200, [200, 70], 5, False)
+    inp.mask = torch.full((2, 2, 200), -float("inf"))
+    inp.mask[0, 0, 3] = 0.0          # chunk 0 of sequence 0
+    inp.mask[0, 1, 40] = 1.0         # chunk 1 of sequence 0
+    inp.mask[0, 1, 41] = 1.0         # (same chunk)
+    inp.mask[1, 0, 65] = 0.0         # chunk 2 of sequence 1 (length 70)
+    inp.mask[1, 1, 100] = 0.0        # past the length: not counted
+    assert bench.algorithmic_bytes(inp) == 3 * 32 * 2 * 128 * 2 * 2
+
+
+def test_oracle_call_serves_every_named_kind():
+    # dense, int8, gather, int8 gather and masked inputs all reach the oracle
+    small = [W.dense_inputs(2, 2, 8, 2, 128, 100, [100, 40], 6, True),
+             W.dense_inputs(1, 1, 8, 2, 128, 100, [77], 6, False, int8=True),
+             W.gather_inputs(1, 1, 8, 2, 128, 300, 40, 8, seed=6),
+             W.gather_inputs(1, 1, 8, 2, 128, 300, 40, 8, seed=6, int8=True)]
+    m = W.dense_inputs(1, 1, 8, 2, 128, 100, [100], 6, False)
+    m.mask = torch.zeros((1, 1, 100))
+    m.mask[0, 0, 50:] = -float("inf")
+    small.append(m)
+    for inp in small:
+        out = bench.oracle_call(inp, slice(0, 1))
+        assert out.shape == (1,) + tuple(inp.q.shape[1:])
