@@ -623,14 +623,20 @@ def extras(args, device, stream, peak, kernel):
     measure("gather_int8", inp)
     del inp
     # the same selection as a mask over the whole window (hidden 32-position
-    # chunks not read), and masks that leave 5 % / 25 % of the chunks
-    # visible; bytes: the visible chunks' K / V rows
+    # chunks not read), and masks that leave 5 % / 25 % / all of the chunks
+    # visible; bytes: the visible chunks' K / V rows.  The tensor-core kernel
+    # lists the visible chunks first (the workspace has room); "_in_place"
+    # gives it a workspace sized for the call alone, so each tile of the
+    # prefix finds its chunks itself.
     inp = W.workload("gather", seed=1, device=device)
     ws_m = workspace_for(inp, device)
+    rows_m = inp.q.shape[2] // inp.k.shape[1]
+    G_m = fd.auto_num_ctas(fd.FD_KERNEL_TC, inp.q.shape[3], fd.FD_BF16, rows_m, 0)
+    ws_t = fd.Workspace(inp.k.shape[1], rows_m, inp.q.shape[3], G_m, device=device)
     out_m = torch.empty(inp.q.shape, dtype=torch.bfloat16, device=device)
     cap = inp.k.shape[2]
     for tag, keep in (("masked_gather_list_131k", None), ("masked_5pct_131k", 0.05),
-                      ("masked_25pct_131k", 0.25)):
+                      ("masked_25pct_131k", 0.25), ("masked_100pct_131k", 1.0)):
         mask = torch.full((1, 1, cap), -float("inf"), device=device)
         if keep is None:
             mask[0, 0, inp.idx[0, 0].long()] = 0.0
@@ -640,11 +646,18 @@ def extras(args, device, stream, peak, kernel):
             live = torch.rand(cap // 32, generator=gm, device=device) < keep
             mask.view(1, 1, -1, 32)[0, 0, live] = 0.0
         chunks = int((mask.view(-1, 32) != -float("inf")).any(1).sum())
+        nbytes = chunks * 32 * inp.k.shape[1] * inp.q.shape[3] * 4
         measure_fn(tag, lambda: fd.decode_masked(
             inp.q, inp.k, inp.v, inp.kv_lengths, mask, n_q=1, causal=False, scale=inp.scale,
-            out=out_m, workspace=ws_m), chunks * 32 * inp.k.shape[1] * inp.q.shape[3] * 4, 50)
+            out=out_m, workspace=ws_m, kernel=kernel), nbytes, 50)
         res[tag]["visible_chunks"] = chunks
+        if keep in (None, 0.05):
+            measure_fn(tag + "_in_place", lambda: fd.decode_masked(
+                inp.q, inp.k, inp.v, inp.kv_lengths, mask, n_q=1, causal=False,
+                scale=inp.scale, out=out_m, workspace=ws_t, kernel=kernel, num_ctas=G_m),
+                nbytes, 50)
     ws_m.close()
+    ws_t.close()
     del inp, mask
     # gather: time follows the list length, not the capacity
     for K in (512, 2048, 8192):

@@ -288,6 +288,15 @@ int run(const Call &c) {
         return FD_ERR_WORKSPACE;
     p.tile = tile;
     p.seg_units = seg_units;
+    // Masked prefix on the tensor-core kernel: where the workspace has room
+    // past the split partials, a pass lists the visible chunks first and the
+    // decode walks only those; otherwise each tile finds its chunks in place.
+    if (kernel == FD_KERNEL_TC && c.mode == fd::kMasked && B <= 65535) {
+        const size_t used = (size_t)(nseg + G) * (size_t)fd::slot_floats(rows, d);
+        const size_t need = (size_t)fd::tc_mask_list_ints(B, cap);   // 0: no list
+        if (need > 0 && used + need <= ws->partial_floats)
+            p.mlist = reinterpret_cast<const int32_t *>(ws->partials + used);
+    }
 
     cudaStream_t st = static_cast<cudaStream_t>(o.stream);
     rc = kernel == FD_KERNEL_TC ? fd::launch_tc(p, G, st) : fd::launch_simt(p, G, st);
@@ -495,6 +504,11 @@ int32_t fd_auto_num_ctas(int32_t kernel, int32_t head_dim, int32_t kv_dtype, int
                          int64_t max_units) {
     (void)head_dim; (void)kv_dtype; (void)rows;
     return auto_ctas(resolve(kernel, kv_dtype), max_units);
+}
+
+size_t fd_masked_list_bytes(int64_t B, int64_t cap) {
+    if (B < 1 || B > 65535 || cap < 1 || cap > ((int64_t)1 << 23)) return 0;
+    return (size_t)fd::tc_mask_list_ints(B, cap) * 4;
 }
 
 int32_t fd_tile_tokens(int32_t kernel, int32_t head_dim, int32_t kv_dtype) {

@@ -52,6 +52,14 @@ struct Params {
                            // entry's score (-inf drops the entry)
     const float *mask;     // masked: [B, n_q, cap] fp32 added to the scores
     int64_t ms[2];         //   (strides of B and n_q; positions contiguous)
+    // masked, tensor-core kernel: the visible 32-position chunks of each
+    // sequence in ascending order (row b starts at b * mls) and their count
+    // per sequence, written by the chunk-list pass before the decode launch;
+    // the decode then walks ceil(count / 4) tiles of four listed chunks.
+    // Null: each tile of the prefix finds its visible chunks in place.
+    const int32_t *mlist;
+    const int32_t *mcnt;
+    int64_t mls;
     // paged caches: logical position j of sequence b lives at row j % page_size
     // of pool page block_table[b * max_pages + j / page_size]; the caches'
     // strides are then (page, kv head, row in page); cap = max_pages * page_size

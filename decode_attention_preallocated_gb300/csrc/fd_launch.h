@@ -25,8 +25,13 @@ bool tc_supports_paged(const Params &p);
 int launch_tc_paged(const Params &p, int num_ctas, cudaStream_t stream);
 // Flat int8 caches, dense prefix and gather (fd_tc_int8.cu).
 int launch_tc_int8(const Params &p, int num_ctas, cudaStream_t stream);
-// Masked prefix over flat bf16 caches (fd_tc_masked.cu).
+// Masked prefix over flat bf16 caches: each tile finds its visible chunks in
+// place (fd_tc_masked.cu), or, with int32 scratch at p.mlist of
+// tc_mask_list_ints(B, cap) entries, a pass lists the visible chunks and the
+// decode walks only those (fd_tc_masked_list.cu).
 int launch_tc_masked(const Params &p, int num_ctas, cudaStream_t stream);
+int64_t tc_mask_list_ints(int64_t B, int64_t cap);
+int launch_tc_masked_list(const Params &p, int num_ctas, cudaStream_t stream);
 // Fused append over flat bf16 caches (fd_tc_append.cu): a cooperative launch,
 // so num_ctas may not exceed the blocks resident at once (else -2).
 int launch_tc_append(const Params &p, int num_ctas, cudaStream_t stream);

@@ -2,7 +2,8 @@
 // over flat bf16 caches ([B, Hkv, cap, d]) and in index-gather mode, and the
 // kernel-choice queries of the C ABI layer.  Flat int8 caches are launched
 // from fd_tc_int8.cu, paged caches from fd_tc_paged.cu, fused appends from
-// fd_tc_append.cu, the masked prefix from fd_tc_masked.cu.
+// fd_tc_append.cu, the masked prefix from fd_tc_masked.cu (chunks found in
+// place) and fd_tc_masked_list.cu (a chunk list first).
 #include "fd_tc_kernel.cuh"
 
 namespace fd {
@@ -66,7 +67,7 @@ int launch_tc(const Params &p, int G, cudaStream_t st) {
     if (p.mode == kPaged) return launch_tc_paged(p, G, st);
     if (p.n_new > 0) return launch_tc_append(p, G, st);
     if (p.kv_int8) return launch_tc_int8(p, G, st);   // flat int8: dense or gather
-    if (p.mode == kMasked) return launch_tc_masked(p, G, st);
+    if (p.mode == kMasked) return p.mlist ? launch_tc_masked_list(p, G, st) : launch_tc_masked(p, G, st);
     TcArgs args;
     memset(&args, 0, sizeof args);
     args.p = p;

@@ -159,7 +159,8 @@ struct TcArgs {   // CUtensorMap members carry their own alignment
     CUtensorMap tq;
     Params p;
     // gather: cache row (b, hk, pos) is row b*gs0 + hk*gs1 + pos*gs2 of tk / tv;
-    // paged: pool row (page, hk, r) is row page*gs0 + hk*gs1 + r*gs2 of gk / gv
+    // paged: pool row (page, hk, r) is row page*gs0 + hk*gs1 + r*gs2 of gk / gv;
+    // masked prefix: gk / gv load 128-row boxes, tk / tv 32-row chunks
     int64_t gs0, gs1, gs2;
     // paged: tk / tv are 4-D maps of the pool (d, page_size, Hkv, num_pages)
     // with box (64, prow, 1, 1); a tile wholly inside the length is TT / prow
@@ -243,13 +244,24 @@ struct Cfg {
 struct Walk {
     int64_t s;        // segment
     int64_t first;    // unit index of the segment's first tile
-    int64_t L;        // its sequence length (gather: the list length)
+    int64_t L;        // positions walked: the sequence length (gather: the list
+                      // length; masked with a chunk list: 32 per listed chunk)
     int32_t ntiles;   // its tile count
     int32_t b, hk;
     int32_t i;        // gather: query row of the list (dense: 0)
 };
 
 __device__ __forceinline__ int32_t tiles_of(int64_t L) { return (int32_t)((L + TT - 1) / TT); }
+
+// Positions a segment of sequence b walks: its length, or, for the masked
+// prefix with a chunk list, 32 per listed chunk (tile t of the segment then
+// holds list entries 4t .. 4t+3).  A count outside [0, ceil(cap / 32)] reads
+// as that bound.
+__device__ __forceinline__ int64_t walk_len(const Params &p, int b) {
+    if (!p.mcnt) return seq_len(p, b);
+    const int64_t n = (int64_t)__ldg(p.mcnt + b), nmax = (p.cap + 31) / 32;
+    return 32 * (n < 0 ? 0 : n > nmax ? nmax : n);
+}
 
 // Units of a segment of n tiles.
 __device__ __forceinline__ int64_t units_of(const Params &p, int64_t n) {
@@ -261,7 +273,7 @@ __device__ __forceinline__ int64_t total_units_tc(const Params &p) {
     if (p.mode == kGather) return p.nseg * units_of(p, tiles_of(p.idx_len));
     const int lane = threadIdx.x & 31;
     int64_t acc = 0;
-    for (int b = lane; b < p.B; b += 32) acc += units_of(p, tiles_of(seq_len(p, b)));
+    for (int b = lane; b < p.B; b += 32) acc += units_of(p, tiles_of(walk_len(p, b)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     return acc * p.Hkv;
@@ -286,7 +298,7 @@ __device__ __noinline__ bool first_piece_warp(const Params &p, int64_t t, Walk *
     int64_t base = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int b = b0 + lane;
-        const int64_t L = b < p.B ? seq_len(p, b) : 0;
+        const int64_t L = b < p.B ? walk_len(p, b) : 0;
         const int64_t n = tiles_of(L), u = units_of(p, n);
         const int64_t wt = (int64_t)p.Hkv * u;
         int64_t incl = wt;   // inclusive scan over the 32 lanes
@@ -340,7 +352,7 @@ __device__ __forceinline__ bool next_piece(const Params &p, Walk &w) {
         if (++w.hk == p.Hkv) {
             w.hk = 0;
             ++w.b;
-            w.L = seq_len(p, w.b);
+            w.L = walk_len(p, w.b);
             w.ntiles = tiles_of(w.L);
         }
     } while (w.ntiles == 0);
@@ -593,11 +605,15 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, volatil
     return ptx::mbar_wait(bar, parity, abort, limit_ns);
 }
 
-template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP, bool MK>
+template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP, int MK>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant__ TcArgs a) {
     static_assert(!(GA && PG), "gather and paged loads are separate modes");
     static_assert(!AP || (!I8 && !GA && !PG), "fused append: flat bf16 caches");
     static_assert(!MK || (!I8 && !GA && !PG && !AP && !SH), "masked prefix: flat bf16 caches");
+    // masked prefix: MK = 1 finds each tile's visible chunks in place, MK = 2
+    // walks the chunk list of the pass before the launch
+    static_assert(MK >= 0 && MK <= 2, "masked mode");
+    constexpr bool MP = MK == 1, ML = MK == 2;
     using C = Cfg<D, N, I8, NV, GA>;
     constexpr int kSoftmaxThreads = C::SMT;
     const Params &p = a.p;
@@ -630,7 +646,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 
     // Segments with nothing to attend still need their output rows zeroed.
     for (int64_t s = c; s < p.nseg; s += G)
-        if ((GA ? tiles_of(p.idx_len) : tiles_of(seq_len(p, (int)(s / p.Hkv)))) == 0)
+        if ((GA ? tiles_of(p.idx_len) : tiles_of(walk_len(p, (int)(s / p.Hkv)))) == 0)
             zero_segment(p, s);
     // The producer warp finds the block's tile range and first piece while
     // the others set up barriers and TMEM.
@@ -691,7 +707,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         ptx::prefetch_tmap(&a.tq);
         ptx::prefetch_tmap(&a.tk);
         ptx::prefetch_tmap(&a.tv);
-        if (PG) {
+        if (PG || MK) {
             ptx::prefetch_tmap(&a.gk);
             ptx::prefetch_tmap(&a.gv);
         }
@@ -834,17 +850,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             // Hidden chunks are not copied (see the copy step below).
             // The mask values of a tile are loaded one tile before they are
             // evaluated, so the loads never stall the copies.
-            const float *mrow = MK ? p.mask + (int64_t)b * p.ms[0] : nullptr;
+            const float *mrow = MP ? p.mask + (int64_t)b * p.ms[0] : nullptr;
             constexpr int kMaxQP = 6;
-            float mreg[MK ? 4 : 1][MK ? kMaxQP : 1];
+            float mreg[MP ? 4 : 1][MP ? kMaxQP : 1];
             auto mask_load = [&](int64_t tile) {
                 const int64_t y0 = tile * TT, ys0 = tile_start(tile, L);
 #pragma unroll
-                for (int r = 0; r < (MK ? 4 : 1); ++r) {
+                for (int r = 0; r < (MP ? 4 : 1); ++r) {
                     const int64_t pos = ys0 + 4 * lane + r;
                     const bool own = pos >= y0 && pos < L;
 #pragma unroll
-                    for (int i = 0; i < (MK ? kMaxQP : 1); ++i)
+                    for (int i = 0; i < (MP ? kMaxQP : 1); ++i)
                         mreg[r][i] = own && i < p.n_q ? __ldg(mrow + (int64_t)i * p.ms[1] + pos) : neg_inf();
                 }
             };
@@ -852,10 +868,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 const int64_t ys0 = tile_start(tile, L);
                 bool v = false;
 #pragma unroll
-                for (int r = 0; r < (MK ? 4 : 1); ++r) {
+                for (int r = 0; r < (MP ? 4 : 1); ++r) {
                     const int64_t pos = ys0 + 4 * lane + r;
 #pragma unroll
-                    for (int i = 0; i < (MK ? kMaxQP : 1); ++i)
+                    for (int i = 0; i < (MP ? kMaxQP : 1); ++i)
                         v = v || (mreg[r][i] != neg_inf() && (!p.causal || pos <= L - p.n_q + i));
                 }
                 const uint32_t bal = __ballot_sync(0xffffffffu, v);
@@ -865,10 +881,33 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 return bits;
             };
             uint32_t mk_n = 0, mk_v0 = 0, mk_v1 = 0;
-            if (MK) {
+            if (MP) {
                 mask_load(tt0);
                 mk_n = mask_eval(tt0);
                 if (n_in > 1) mask_load(tt0 + 1);
+            }
+            // masked prefix with a chunk list: tile t of the segment is list
+            // entries 4t .. 4t+3, chunk c being positions 32c .. 32c+31 of the
+            // sequence, loaded as rows min(32c, L - 32) .. + 31 (the last chunk
+            // of a length that is no multiple of 32 is right-aligned to end at
+            // the length, so nothing past the filled prefix is read).  Lane l
+            // holds entry 4 * tile + l for a window of eight tiles (ml_cur) and
+            // the next eight (ml_nxt); a copying lane (box cb, chunk cc at lane
+            // 4 * cb + cc) keeps its chunk of K(j) for V(j).  An entry outside
+            // the prefix's chunks is skipped.
+            const int64_t Lr = ML ? seq_len(p, b) : L;     // length of the filled prefix
+            const int32_t *mlrow = ML ? p.mlist + (int64_t)b * p.mls : nullptr;
+            const int64_t ml_n = L / 32;                    // listed chunks
+            const int64_t ml_nch = (Lr + 31) / 32;          // chunks of the prefix
+            auto ml_load = [&](int64_t tile) -> int {
+                const int64_t e = 4 * tile + lane;
+                const int c = e < ml_n ? __ldg(mlrow + e) : -1;
+                return c >= 0 && c < ml_nch ? c : -1;
+            };
+            int ml_cur = -1, ml_nxt = -1, ml_v0 = -1, ml_v1 = -1;
+            if (ML) {
+                ml_cur = ml_load(tt0);
+                if (n_in > 8) ml_nxt = ml_load(tt0 + 8);
             }
             for (int64_t step = 0; step < 2 * n_in && ok; ++step) {
                 int64_t j;
@@ -956,9 +995,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     }
                 } else if (MK) {
                     // K(j) takes the chunks found one tile ahead (kept for
-                    // V(j)); then the next tile's are read
+                    // V(j)); then the next tile's are read.  (chunk list: the
+                    // listed chunks of tile j, the window moving on every
+                    // eighth K fill)
                     uint32_t bits;
-                    if (kv == 0) {
+                    int mc = -1;
+                    if (ML) {
+                        if (kv == 0) {
+                            if (j > 0 && (j & 7) == 0) {
+                                ml_cur = ml_nxt;
+                                if (j + 8 < n_in) ml_nxt = ml_load(tt0 + j + 8);
+                            }
+                            mc = __shfl_sync(0xffffffffu, ml_cur, 4 * (int)(j & 7) + (lane & 3));
+                            if (j & 1) ml_v1 = mc; else ml_v0 = mc;
+                        } else {
+                            mc = (j & 1) ? ml_v1 : ml_v0;
+                        }
+                        bits = __ballot_sync(0xffffffffu, mc >= 0) & 0xfu;
+                    } else if (kv == 0) {
                         bits = mk_n;
                         if (j & 1) mk_v1 = bits; else mk_v0 = bits;
                         if (j + 1 < n_in) mk_n = mask_eval(tt0 + j + 1);
@@ -982,10 +1036,26 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                             ptx::mbar_arrive(&bs->slot_full[slot]);
                     }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
-                    // lane 4*cb + cc: 32 rows (chunk cc) of the 64-column box cb
-                    if (ok && lane < 4 * C::KB && ((bits >> (lane & 3)) & 1u)) {
+                    // Four chunks that are consecutive rows (every chunk of a
+                    // tile found in place, or four consecutive listed chunks
+                    // none of which is a right-aligned last one) are one
+                    // 128-row box per 64 columns (maps gk / gv); otherwise
+                    // lane 4*cb + cc copies 32 rows (chunk cc) of box cb.
+                    bool whole = bits == 0xfu;
+                    int row0 = ys;
+                    if (ML) {
+                        row0 = 32 * __shfl_sync(0xffffffffu, mc, 0);
+                        whole = __all_sync(0xffffffffu, mc == row0 / 32 + (lane & 3)) && row0 >= 0 &&
+                                (int64_t)row0 + TT <= Lr;
+                    }
+                    if (ok && whole) {
+                        if (lane < C::KB)
+                            ptx::tma_load_4d(smem + C::OFF_SLOTS + slot * C::SLOT + lane * C::BOX,
+                                             kv ? (const void *)&a.gv : (const void *)&a.gk,
+                                             &bs->slot_full[slot], lane * 64, row0, hk, b);
+                    } else if (ok && lane < 4 * C::KB && ((bits >> (lane & 3)) & 1u)) {
                         const int cb = lane >> 2, cc = lane & 3;
-                        const int row = ys + 32 * cc;
+                        const int row = ML ? (int)min((int64_t)32 * mc, Lr - 32) : ys + 32 * cc;
                         ptx::tma_load_4d(smem + C::OFF_SLOTS + slot * C::SLOT + cb * C::BOX + cc * (32 * 128),
                                          kv ? (const void *)&a.tv : (const void *)&a.tk,
                                          &bs->slot_full[slot], cb * 64, row, hk, b);
@@ -1272,6 +1342,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             const int64_t n_in = piece_end - t;
             const int64_t tt0 = t - w.first;
             const int64_t L = w.L;
+            const int64_t Lr = ML ? seq_len(p, w.b) : L;    // length of the filled prefix
             const int rows = p.rows;
 
             // Output offsets of this group's rows (one division sequence per
@@ -1290,7 +1361,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 int qi = cb0 % p.n_q;
 #pragma unroll
                 for (int r = 0; r < NH; ++r) {
-                    lim[r] = p.causal ? (int)(L - p.n_q + qi) : (int)(L - 1);
+                    lim[r] = p.causal ? (int)(Lr - p.n_q + qi) : (int)(Lr - 1);
                     if (++qi == p.n_q) qi = 0;
                 }
             }
@@ -1377,25 +1448,52 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             constexpr int kMaxQ = 6;
             const float *mrow = MK ? p.mask + (int64_t)w.b * p.ms[0] : nullptr;
             float mk_n[kMaxQ];
-            auto load_mask = [&](int64_t jj) {
-                const int64_t tok = tile_start(tt0 + jj, L) + wt;
-                const bool own = tok >= (tt0 + jj) * TT && tok < L;
+            // chunk list: warp wwarp holds positions 32 * wwarp .. + 31 of a
+            // tile, the chunk of list entry 4 * tile + wwarp, loaded as rows
+            // min(32c, Lr - 32) .. + 31, of which it owns those at or past 32c;
+            // the chunk of tile j + 1 is read during tile j - 1, its mask
+            // values during tile j
+            const int32_t *mlrow = ML ? p.mlist + (int64_t)w.b * p.mls : nullptr;
+            const int64_t ml_n = L / 32, ml_nch = (Lr + 31) / 32;
+            auto ml_chunk = [&](int64_t jj) -> int {
+                const int64_t e = 4 * (tt0 + jj) + wwarp;
+                const int c = e < ml_n ? __ldg(mlrow + e) : -1;
+                return c >= 0 && c < ml_nch ? c : -1;
+            };
+            auto ml_token = [&](int c) -> int64_t {
+                return c >= 0 ? min((int64_t)32 * c, Lr - 32) + lane : -1;
+            };
+            int mc_j = -1, mc_j1 = -1;    // chunks of tiles j and j + 1
+            if (ML) {
+                mc_j = ml_chunk(0);
+                if (n_in > 1) mc_j1 = ml_chunk(1);
+            }
+            auto load_mask = [&](int64_t jj, int c) {
+                int64_t tok;
+                bool own;
+                if (ML) {
+                    tok = ml_token(c);
+                    own = c >= 0 && tok >= (int64_t)32 * c;
+                } else {
+                    tok = tile_start(tt0 + jj, L) + wt;
+                    own = tok >= (tt0 + jj) * TT && tok < L;
+                }
 #pragma unroll
                 for (int i = 0; i < kMaxQ; ++i)
                     mk_n[i] = own && i < p.n_q ? __ldg(mrow + (int64_t)i * p.ms[1] + tok) * 1.4426950408889634f
                                                : neg_inf();
             };
-            if (MK) load_mask(0);
+            if (MK) load_mask(0, mc_j);
             for (int64_t j = 0; j < n_in && ok; ++j) {
                 const int64_t y0 = (tt0 + j) * TT;
-                const int64_t token = (GA || PG) ? y0 + wt : tile_start(tt0 + j, L) + wt;
+                const int64_t token = ML ? ml_token(mc_j) : (GA || PG) ? y0 + wt : tile_start(tt0 + j, L) + wt;
                 const uint32_t sb = tile_ctr & 1, u = tile_ctr >> 1;
                 // Visibility: a position this tile owns (the right-aligned last
                 // tile also holds positions the previous tile covered), inside
                 // the filled prefix and, for causal windows, at or before
                 // L - n_q + i for the row's query index i.  Gather: a valid
                 // cell of the list.  Paged: a position on a page of the pool.
-                bool in_len = token >= y0 && token < L;
+                bool in_len = ML ? mc_j >= 0 && token >= (int64_t)32 * mc_j : token >= y0 && token < L;
                 float bl = 0.f;
                 if (GA) {
                     const int cell = cell_n;
@@ -1419,7 +1517,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 if (MK) {
 #pragma unroll
                     for (int i = 0; i < kMaxQ; ++i) mk[i] = mk_n[i];
-                    if (j + 1 < n_in) load_mask(j + 1);
+                    if (j + 1 < n_in) load_mask(j + 1, mc_j1);
+                    if (ML) {
+                        mc_j = mc_j1;
+                        mc_j1 = j + 2 < n_in ? ml_chunk(j + 2) : -1;
+                    }
                 }
                 const float ksc = ksc_n, vsc = vsc_n;
                 if (I8 && j + 1 < n_in) load_scales(j + 1, GA ? cell_n : pg_next);
@@ -1824,7 +1926,7 @@ inline bool make_gmap(CUtensorMap *m, const void *base, const Params &p, int64_t
 
 // Blocks of this instantiation that can be resident at once on the current
 // device (0 on error); sets the dynamic shared memory opt-in the first time.
-template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP, bool MK>
+template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP, int MK>
 int resident_blocks() {
     using C = Cfg<D, N, I8, NV, GA>;
     static std::atomic<int> cached[64];
@@ -1845,7 +1947,7 @@ int resident_blocks() {
 }
 
 template <int D, int N, bool I8, int NV = N, bool GA = false, bool SH = false, bool PG = false,
-          bool AP = false, bool MK = false>
+          bool AP = false, int MK = 0>
 int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
     using C = Cfg<D, N, I8, NV, GA>;
     const int resident = resident_blocks<D, N, I8, NV, GA, SH, PG, AP, MK>();

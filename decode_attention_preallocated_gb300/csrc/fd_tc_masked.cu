@@ -15,7 +15,9 @@ int launch_tc_masked(const Params &p, int G, cudaStream_t st) {
     TcArgs args;
     memset(&args, 0, sizeof args);
     args.p = p;
+    // 32-row boxes (one chunk) and 128-row boxes (four consecutive chunks)
     if (!make_map(&args.tk, p.k, p.ks, p, 32) || !make_map(&args.tv, p.v, p.vs, p, 32) ||
+        !make_map(&args.gk, p.k, p.ks, p) || !make_map(&args.gv, p.v, p.vs, p) ||
         !make_qmap(&args.tq, p))
         return -5;
     const int rows = p.rows;

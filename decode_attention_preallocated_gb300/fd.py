@@ -111,6 +111,7 @@ _SIGNATURES = [
     ("fd_auto_num_ctas", ctypes.c_int32,
      [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64]),
     ("fd_tile_tokens", ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
+    ("fd_masked_list_bytes", ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     ("fd_plan", ctypes.c_int64,
      [_P(ctypes.c_int64), ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
       _P(ctypes.c_int32), _P(ctypes.c_int32)]),
@@ -296,6 +297,17 @@ def tile_tokens(kernel=FD_KERNEL_AUTO, head_dim=128, kv_dtype=FD_BF16) -> int:
     return int(lib().fd_tile_tokens(kernel, head_dim, kv_dtype))
 
 
+def masked_list_bytes(B, cap) -> int:
+    """Workspace bytes, past a masked call's split partials, that let the
+    tensor-core kernel list the visible chunks before it decodes."""
+    return int(lib().fd_masked_list_bytes(int(B), int(cap)))
+
+
+def slot_floats(rows, head_dim) -> int:
+    """Floats of one workspace slot of split partials (O, m and l of rows)."""
+    return rows * head_dim + ((2 * rows + 3) // 4) * 4
+
+
 def plan(seg_len, tile, num_ctas, seg_units=0):
     """Host mirror of the device partitioner: (total work units, first block
     of each segment, number of blocks sharing each segment).  Each non-empty
@@ -416,14 +428,18 @@ def decode_masked(q, k_cache, v_cache, kv_lengths, mask, n_q=None, causal=False,
                   out=None, out_dtype=torch.bfloat16, num_ctas=0, kernel=FD_KERNEL_AUTO,
                   stream=None, workspace: Optional[Workspace] = None):
     """As ``decode`` with an additive fp32 mask [B, n_q, cap] (positions
-    contiguous; -inf hides a position); chunks the mask hides for every query
-    row are not read (CUDA-core kernel)."""
+    contiguous; -inf hides a position); 32-position chunks the mask hides for
+    every query row are not read.  The default workspace leaves room for the
+    tensor-core kernel's chunk list (its time then follows the visible
+    chunks)."""
     B, nq, Hq, d = q.shape
     n_q = nq if n_q is None else n_q
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     Hkv = k_cache.shape[1]
     rows = (Hq // max(Hkv, 1)) * nq
-    out, sh, ws = _prepare(q, k_cache, out, out_dtype, B * Hkv, rows, num_ctas,
+    # room for the chunk list, counted in slots of the call's partials
+    extra = -(-masked_list_bytes(B, k_cache.shape[2]) // (4 * slot_floats(rows, d)))
+    out, sh, ws = _prepare(q, k_cache, out, out_dtype, B * Hkv + extra, rows, num_ctas,
                            kernel, stream, workspace)
     tq, tk, tv, tm, to = map(as_fd_tensor, (q, k_cache, v_cache, mask, out))
     o = _opts(sh, ws, num_ctas, kernel)

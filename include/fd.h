@@ -243,9 +243,16 @@ int fd_decode_gather_bias(const fd_tensor *q, const fd_tensor *k_cache,
  * finite or -inf.  Both kernels serve it: the CUDA-core kernel skips a
  * hidden chunk (its tiles are 32 positions); the tensor-core kernel, whose
  * tiles are 128 positions, loads each tile as four 32-position chunks and
- * copies only the chunks some query row sees.  Positions the mask hides
- * must hold finite values (they lie in the filled prefix).  Other arguments
- * as fd_decode.
+ * copies only the chunks some query row sees.  When the workspace holds
+ * fd_masked_list_bytes(B, cap) bytes past the call's split partials
+ * ((B*Hkv + num_ctas) slots of slot_floats(rows, d) floats, rows = (Hq/Hkv)
+ * * n_q, as fd_workspace_bytes counts them), a first pass on the stream lists
+ * each sequence's visible chunks in that room and the tensor-core launch
+ * walks only the listed chunks, four to a 128-position tile, so its time
+ * follows the visible chunks, not the length; with less room each tile of the
+ * prefix finds its visible chunks in place.  Positions the mask hides must
+ * hold finite values (they lie in the filled prefix).  Other arguments as
+ * fd_decode.
  */
 int fd_decode_masked(const fd_tensor *q, const fd_tensor *k_cache,
                      const fd_tensor *v_cache, const int32_t *kv_lengths,
@@ -390,6 +397,11 @@ int32_t fd_auto_num_ctas(int32_t kernel, int32_t head_dim, int32_t kv_dtype,
                          int32_t rows, int64_t max_units);
 /* Cache positions per K/V tile for a kernel / head_dim / cache dtype. */
 int32_t fd_tile_tokens(int32_t kernel, int32_t head_dim, int32_t kv_dtype);
+/* Workspace bytes the tensor-core kernel's chunk list of a masked call over
+ * B sequences of capacity cap takes past the call's split partials (the
+ * list, the counts and the listing pass's staging area); 0 for B or cap
+ * outside [1, 65535] or [1, 2^23], where no list is made. */
+size_t fd_masked_list_bytes(int64_t B, int64_t cap);
 
 /*
  * Host mirror of the device split partitioner, for inspection and tests.

@@ -240,6 +240,26 @@ def test_workspace_size_formula(L):
     assert L.fd_workspace_bytes(0, 1, 1, 1) == 0
 
 
+def test_masked_list_size(L):
+    # the list (ceil(cap / 32) entries per sequence, rounded up to 4), one
+    # count per sequence, and the listing pass's staging area (256 entries and
+    # one count per block of 256 chunks), all int32
+    def expect(B, cap):
+        nch = -(-cap // 32)
+        nblk = -(-nch // 256)
+        up4 = lambda x: -(-x // 4) * 4
+        return 4 * (B * up4(nch) + up4(B) + B * nblk * 256 + up4(B * nblk))
+
+    for B, cap in ((1, 131072), (8, 32768), (3, 20000), (1, 1), (5, 33), (65535, 4096),
+                   (2, 1 << 23)):
+        assert L.fd_masked_list_bytes(B, cap) == expect(B, cap), (B, cap)
+        assert fd.masked_list_bytes(B, cap) == expect(B, cap)
+    assert L.fd_masked_list_bytes(0, 64) == 0
+    assert L.fd_masked_list_bytes(65536, 64) == 0
+    assert L.fd_masked_list_bytes(1, 0) == 0
+    assert L.fd_masked_list_bytes(1, (1 << 23) + 1) == 0    # more than 1024 listing blocks
+
+
 @pytest.mark.parametrize("seed", range(40))
 def test_partition_covers_each_tile_once(L, seed):
     rnd = random.Random(seed)
