@@ -271,6 +271,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B and fp32 D.
 // a_mn / b_mn: operand stored MN-major (1) instead of K-major (0).
+// kind::f16 with fp16 A and B operands (format 0), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4)                        // D format: f32
+           | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16)
+           | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
     return (1u << 4)                        // D format: f32
            | (1u << 7)                      // A format: bf16

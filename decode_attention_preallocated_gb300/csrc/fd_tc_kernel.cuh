@@ -34,8 +34,10 @@
 //               hands a split partial to the in-launch combine (last block
 //               to arrive merges; comfy-kitchen #239, "GQA decode").
 //   int8 caches: warps 0-3 are the one softmax group and warps 4-7 widen the
-//               int8 tiles the producer loads into the bf16 slots the MMAs
-//               read; the per-position scales multiply scores and P.
+//               int8 tiles the producer loads into fp16 slots and convert
+//               each piece's Q to fp16, so the MMAs run on fp16 operands (P
+//               is written in fp16 too); the per-position scales multiply
+//               scores and P.
 // Flat caches: the last tile of a segment is loaded right-aligned (ending at
 // the length), so no row of the unused tail is ever read; positions the
 // previous tile already covered are masked.  Paged caches (PG) and index
@@ -174,7 +176,7 @@ template <int D, int N, bool I8, int NV, bool GA = false>
 struct Cfg {
     // bf16 caches: two softmax warpgroups split the rows (warps 0-7).  int8
     // caches: one softmax warpgroup (warps 0-3); warps 4-7 widen the int8
-    // tiles to bf16 for the MMAs.
+    // tiles to fp16 for the MMAs.
     static constexpr int GROUPS = I8 ? 1 : 2;
     static constexpr int SMT = 128 * GROUPS;     // softmax threads
     static constexpr int KB = D / 64;            // 128-byte boxes per cache row
@@ -223,8 +225,17 @@ struct Cfg {
     static constexpr uint32_t TMEM_COLS = COLS <= 32 ? 32 : COLS <= 64 ? 64 : COLS <= 128 ? 128 : 256;
     // pieces per iteration of the last arriver's single-pass merge (head_dim 256)
     static constexpr int MERGE_UNROLL = (D == 256 && NV >= 32 && !I8) ? 1 : 2;
-    static constexpr uint32_t IDESC_QK = ptx::idesc_bf16(128, N, 0, 0);
-    static constexpr uint32_t IDESC_PV = ptx::idesc_bf16(128, N, 1, 1);
+    // int8 caches: the MMAs take fp16 operands (codes widen to fp16 in two
+    // instructions per pair, Q is converted once per piece, P is written in
+    // fp16); bf16 caches: bf16 operands
+    static constexpr uint32_t IDESC_QK = I8 ? ptx::idesc_f16(128, N, 0, 0) : ptx::idesc_bf16(128, N, 0, 0);
+    static constexpr uint32_t IDESC_PV = I8 ? ptx::idesc_f16(128, N, 1, 1) : ptx::idesc_bf16(128, N, 1, 1);
+    // Scores (log2 units) may exceed a row's running maximum by this much
+    // before the maximum is refreshed, so P <= 2^SLACK: fp32 accumulators
+    // and the hi/lo split of P (bf16, or fp16 for int8 caches, where P also
+    // carries the position's v scale and must stay below the fp16 maximum)
+    // carry it without loss.
+    static constexpr float SLACK = I8 ? 4.f : kRescaleSlack;
     // P planes are MN-major (query rows contiguous per position) with 32-byte
     // swizzle: 16-row atoms of TT positions x 32 bytes.
     static constexpr uint32_t PATOM = TT * 32;
@@ -364,6 +375,7 @@ struct Bars {   // at the start of shared memory; the reduction scratch follows 
     uint64_t slot_full[8], slot_empty[8];
     uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
     uint64_t q_full, q_free, o_done, o_free, exit_mma, sm_bar;
+    uint64_t q_conv;          // int8 caches: Q converted to fp16 (the widening threads)
     uint64_t wg_bar[kMaxGroups];
     union {
         struct {
@@ -415,16 +427,32 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Two int8 codes (bytes k and k+1 of w) -> two bf16 holding the same integers,
-// exactly: byte ^ 0x80 = code + 128 in [0, 255] becomes the low mantissa
-// byte of the float 1.5 * 2^23 + code + 128, from which the constant is
-// subtracted exactly; integers of magnitude <= 128 are exact in bf16.
-__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t w, int k) {
-    const uint32_t u = w ^ 0x80808080u;
-    const float base = 12582912.f + 128.f;
-    const float f0 = __uint_as_float(__byte_perm(u, 0x4B400000u, 0x7650 | k)) - base;
-    const float f1 = __uint_as_float(__byte_perm(u, 0x4B400000u, 0x7650 | (k + 1))) - base;
-    return pack_bf16x2(f0, f1);
+// Two int8 codes (bytes k and k+1 of u = w ^ 0x80808080, i.e. code + 128)
+// -> two fp16 holding the same integers, exactly: each byte becomes the low
+// mantissa byte of the half 0x64XX = 1024 + byte, from which 1152 is
+// subtracted exactly (fp16 holds integers of magnitude <= 2048 exactly).
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t u, int k) {
+    const uint32_t h = __byte_perm(u, 0x64646464u, k == 0 ? 0x4140 : 0x4342);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    return r;
+}
+
+// Two floats -> two fp16 (round to nearest even, saturating at +-65504).
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ float f16lo(uint32_t w) {
+    float f;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.f32.f16 %0, l; }" : "=f"(f) : "r"(w));
+    return f;
+}
+__device__ __forceinline__ float f16hi(uint32_t w) {
+    float f;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.f32.f16 %0, h; }" : "=f"(f) : "r"(w));
+    return f;
 }
 
 __device__ __forceinline__ int ld_acquire(const int32_t *ptr) {
@@ -690,6 +718,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             ptx::mbar_init(&bs->p_free[i], 1);
         }
         ptx::mbar_init(&bs->q_full, 1);
+        ptx::mbar_init(&bs->q_conv, 128);
         ptx::mbar_init(&bs->q_free, 1);
         ptx::mbar_init(&bs->o_done, 1);
         ptx::mbar_init(&bs->o_free, kSoftmaxThreads);
@@ -1189,7 +1218,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             if (lane == 0) {
                 // Software pipeline: QK of tile j+1 is issued before PV of
                 // tile j, so the next scores are ready when softmax finishes.
-                ok = bar_wait<I8>(&bs->q_full, piece & 1, abort_flag, p.wait_ns);
+                // (int8 caches: once the widening threads have converted Q)
+                ok = bar_wait<I8>(I8 ? &bs->q_conv : &bs->q_full, piece & 1, abort_flag, p.wait_ns);
                 if (!ok) note_timeout(bs, p, 2, tile_ctr, piece);
                 ptx::tc_fence_after();
                 ok = ok && issue_qk(tile_ctr);
@@ -1220,14 +1250,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             ptx::mbar_wait_drain(&bs->exit_mma, 0, kWaitNs);
         }
     } else if (I8 && warp >= 4) {
-        // ------------------------------------- int8 -> bf16 widening (warps 4-7)
-        // Fill f of the raw ring becomes fill f of the bf16 slot ring, in the
-        // producer's order.  Codes widen exactly (|code| <= 127 has 8
-        // significant bits); the per-position scales are applied to the
-        // scores and to P by the softmax group, so nothing here rounds.
-        // Raw tile: row-major [TT][D] codes.  bf16 tile: KB boxes of
-        // [TT][64] with the 128-byte swizzle (16-byte chunk c of position r
-        // at c ^ (r & 7)), exactly what a TMA load of a bf16 cache produces.
+        // ------------------------------------- int8 -> fp16 widening (warps 4-7)
+        // Fill f of the raw ring becomes fill f of the fp16 slot ring, in the
+        // producer's order.  Codes widen exactly (fp16 holds every integer
+        // of magnitude <= 2048), two instructions per pair of codes; the
+        // per-position scales are applied to the scores and to P by the
+        // softmax group, so nothing here rounds.  Raw tile: row-major
+        // [TT][D] codes.  fp16 tile: KB boxes of [TT][64] with the 128-byte
+        // swizzle (16-byte chunk c of position r at c ^ (r & 7)), the layout
+        // of a TMA load of a 16-bit cache.
         const int ct = tid - 128;
         uint32_t f = 0;
         bool ok = true;
@@ -1237,6 +1268,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         while (ok) {
             const int64_t piece_end = min(t_end, w.first + w.ntiles);
             const int64_t n_fill = 2 * (piece_end - t);
+            // The piece's Q (bf16, as the producer loaded it) -> fp16 in place
+            // (exact for normal values up to 65504, saturating beyond); the
+            // MMA issuer waits for q_conv.  Padding rows are zeros either way.
+            ok = bar_wait<I8>(&bs->q_full, piece & 1, abort_flag, p.wait_ns);
+            if (!ok) { note_timeout(bs, p, 19, f, piece); break; }
+            for (uint32_t e = ct; e < C::QBYTES / 16; e += 128) {
+                uint4 *q4 = reinterpret_cast<uint4 *>(smem + C::OFF_Q) + e;
+                const uint4 v = *q4;
+                *q4 = make_uint4(pack_f16x2(bf16lo(v.x), bf16hi(v.x)), pack_f16x2(bf16lo(v.y), bf16hi(v.y)),
+                                 pack_f16x2(bf16lo(v.z), bf16hi(v.z)), pack_f16x2(bf16lo(v.w), bf16hi(v.w)));
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(&bs->q_conv);
             for (int64_t k = 0; k < n_fill && ok; ++k, ++f) {
                 const uint32_t rs = f % C::NRX, ss = f % C::NS;
                 ok = bar_wait<I8>(&bs->raw_full[rs], (f / C::NRX) & 1, abort_flag, p.wait_ns);
@@ -1277,12 +1321,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 #pragma unroll
                 for (int k = 0; k < NK; ++k) {
                     unsigned char *row = dst + k * RSTEP * 128;
+                    const uint32_t ux = cw[k].x ^ 0x80808080u, uy = cw[k].y ^ 0x80808080u;
+                    const uint32_t uz = cw[k].z ^ 0x80808080u, uw = cw[k].w ^ 0x80808080u;
                     *reinterpret_cast<uint4 *>(row + sw0) =
-                        make_uint4(i8x2_to_bf16x2(cw[k].x, 0), i8x2_to_bf16x2(cw[k].x, 2),
-                                   i8x2_to_bf16x2(cw[k].y, 0), i8x2_to_bf16x2(cw[k].y, 2));
+                        make_uint4(i8x2_to_f16x2(ux, 0), i8x2_to_f16x2(ux, 2),
+                                   i8x2_to_f16x2(uy, 0), i8x2_to_f16x2(uy, 2));
                     *reinterpret_cast<uint4 *>(row + sw1) =
-                        make_uint4(i8x2_to_bf16x2(cw[k].z, 0), i8x2_to_bf16x2(cw[k].z, 2),
-                                   i8x2_to_bf16x2(cw[k].w, 0), i8x2_to_bf16x2(cw[k].w, 2));
+                        make_uint4(i8x2_to_f16x2(uz, 0), i8x2_to_f16x2(uz, 2),
+                                   i8x2_to_f16x2(uw, 0), i8x2_to_f16x2(uw, 2));
                 }
                 ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive(&bs->slot_full[ss]);
@@ -1557,7 +1603,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 // mrun + kRescaleSlack (always on a segment's first tile).
                 bool need = false;
 #pragma unroll
-                for (int r = 0; r < NH; ++r) need = need || (sv[r] > mrun[r] + kRescaleSlack);
+                for (int r = 0; r < NH; ++r) need = need || (sv[r] > mrun[r] + C::SLACK);
                 need = __any_sync(0xffffffffu, need);
                 if (lane == 0) bs->vote[wg][tile_ctr & 1][wwarp] = need;
                 ok = wg_sync();
@@ -1582,7 +1628,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         // Only rows that passed their own threshold move,
                         // so a row's arithmetic never depends on another
                         // row's scores.
-                        const float mnew = tmax > mrun[r] + kRescaleSlack ? tmax : mrun[r];
+                        const float mnew = tmax > mrun[r] + C::SLACK ? tmax : mrun[r];
                         const float muse = mnew == neg_inf() ? 0.f : mnew;
                         alpha[r] = fast_exp2(mrun[r] - muse);
                         grow = grow || (alpha[r] < 1.f);
@@ -1629,7 +1675,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                     // P = hi + lo, both bf16: hi = rn(p), lo = rn(p - hi), so the
                     // PV product sees p to about 2^-17 relative, which fp32
                     // outputs need; bf16 outputs (2^-9 themselves) take P_hi
-                    // alone, which halves the PV MMAs.  Thread wt
+                    // alone, which halves the PV MMAs.  (int8 caches: both
+                    // fp16, about 2^-22 relative, p carrying the v scale.)  Thread wt
                     // writes its position's row: 8 query rows per 16-byte chunk,
                     // chunk c of a 16-row atom stored at c ^ bit 2 of wt.
                     unsigned char *prow = smem + C::OFF_P + ps * C::PSTAGE + wt * 32;
@@ -1641,9 +1688,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float p0 = sv[l8 * 8 + 2 * e], p1 = sv[l8 * 8 + 2 * e + 1];
-                            const uint32_t h = pack_bf16x2(p0, p1);
-                            hw[e] = h;
-                            lw[e] = pack_bf16x2(p0 - bf16lo(h), p1 - bf16hi(h));
+                            if (I8) {   // fp16 planes (int8 caches)
+                                const uint32_t h = pack_f16x2(p0, p1);
+                                hw[e] = h;
+                                lw[e] = pack_f16x2(p0 - f16lo(h), p1 - f16hi(h));
+                            } else {
+                                const uint32_t h = pack_bf16x2(p0, p1);
+                                hw[e] = h;
+                                lw[e] = pack_bf16x2(p0 - bf16lo(h), p1 - bf16hi(h));
+                            }
                         }
                         const uint32_t off = (a8 >> 1) * C::PATOM + (((a8 & 1) ^ sw) << 4);
                         *reinterpret_cast<uint4 *>(prow + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);

@@ -270,6 +270,12 @@ def workload(name: str, seed: int = 1, device="cpu", tail="randn",
     if name == "mtp_verify":
         return dense_inputs(1, 4, 16, 4, 256, 24007, [3000], seed, True, device,
                             layout, tail, name=name)
+    if name.startswith("mtp_verify_cap"):
+        # the MTP-verify workload in another capacity (the time and the bytes
+        # read must not depend on it)
+        cap = int(name[len("mtp_verify_cap"):])
+        return dense_inputs(1, 4, 16, 4, 256, cap, [3000], seed, True, device,
+                            layout, tail, name=name)
     if name == "ragged":
         lens = ragged_lengths(8, 1024, 32768, seed)
         return dense_inputs(8, 6, 16, 4, 256, 32768, lens, seed, True, device,

@@ -156,6 +156,14 @@ int fd_decode(const fd_tensor *q, const fd_tensor *k_cache,
  * (comfy-kitchen #239, commit list: bounded paged INT8 decode cache; the
  * cache here is not paged).  k_scale, v_scale: fp32 [B, Hkv, cap] with any
  * strides.  Other arguments as fd_decode.
+ * On the tensor-core kernel the products run on fp16 operands: the codes
+ * convert exactly, q is rounded to fp16 (exact for bf16 values of magnitude
+ * 2^-14 .. 65504; larger ones saturate at 65504), and each softmax weight
+ * (at most 16 before normalisation) times the position's v scale is held
+ * in fp16 with about 2^-22 relative error, saturating at 65504 (a v scale
+ * above 4094, i.e. dequantised |v| above about 5.2e5, can saturate).  The
+ * CUDA-core kernel has no such range limit.  The same holds for every
+ * int8 call (paged and gather).
  */
 int fd_decode_int8(const fd_tensor *q, const fd_tensor *k_cache,
                    const fd_tensor *v_cache, const fd_tensor *k_scale,
