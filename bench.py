@@ -297,7 +297,10 @@ GRAPH_CALLS = 50   # decode calls captured per CUDA graph
 def capture(fn, calls, stream):
     """A CUDA graph of `calls` back-to-back calls of fn on `stream` (the
     library allocates nothing and reads no device data on the host, so a
-    call captures as-is; a decode loop replays its step graph the same way)."""
+    call captures as-is; a decode loop replays its step graph the same way).
+    Calls still running on another stream finish first: a workspace serves
+    one stream at a time."""
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         fn()
     torch.cuda.synchronize()

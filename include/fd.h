@@ -368,7 +368,10 @@ int fd_decode_noalloc(const fd_tensor *q, const fd_tensor *k_cache,
  * scratch of the split combine belongs to one stream-ordered launch at a
  * time, the rule comfy-kitchen #239 adopts for its GEMM workspace (commit
  * list: the workspace is tied to each launch in stream order).  Two streams
- * that may run decode calls at once need two workspaces.
+ * that may run decode calls at once need two workspaces.  Calls that do
+ * overlap on one workspace can leave its counters inconsistent (results of
+ * later calls are then wrong: a merge is skipped, or a masked call keeps an
+ * older chunk list) until fd_workspace_reset.
  */
 size_t fd_workspace_bytes(int64_t max_segments, int32_t max_rows,
                           int32_t head_dim, int32_t max_ctas);
