@@ -305,6 +305,26 @@ def test_int8_tensor_core_head_dim_256(ctas, rows):
     check(inp, torch.bfloat16, kernel=fd.FD_KERNEL_TC, num_ctas=ctas)
 
 
+@pytest.mark.parametrize("d", [128, 256])
+def test_int8_tensor_core_large_value_scales(d):
+    # the tensor-core kernel multiplies in fp16: v scales up to 3000 (|v| up
+    # to 3.8e5, inside the documented 4094 bound) and q entries near 6e4 stay
+    # finite and match the oracle to fp16 / bf16 precision (relative check:
+    # the outputs are of order 1e5)
+    inp = W.dense_inputs(2, 1, 16, 4, d, 700, [700, 333], 33, False, int8=True)
+    inp.v_scale = inp.v_scale * 1.0e5           # dequantised |v| ~ 3e5 at 3 sigma
+    inp.q = inp.q.clone()
+    inp.q[0, 0, 0, 0] = 60000.0                 # one large q entry (its bf16 value, 59904, is exact in fp16)
+    ref = run_oracle(inp)
+    dev = to_dev(inp)
+    for od, tol in ((torch.float32, 1e-4), (torch.bfloat16, 4e-3)):
+        got = run_gpu(dev, od, 0, fd.FD_KERNEL_TC).double().cpu()
+        torch.cuda.synchronize()
+        assert torch.isfinite(got).all()
+        err = (got - ref.double()).abs().max() / ref.double().abs().max()
+        assert err < tol, (od, float(err))
+
+
 def test_int8_tensor_core_rejects_unserved_shapes():
     # more than 32 rows: the tensor-core kernel declines, AUTO takes the CUDA-core one
     inp = to_dev(W.dense_inputs(1, 2, 32, 1, 128, 200, [150], 27, True, int8=True))
