@@ -204,7 +204,7 @@ struct Cfg {
     static constexpr uint32_t MISC = ((OFF_TBL + TBL) + 1023) / 1024 * 1024;
     static constexpr uint32_t BUDGET = 232448;   // max dynamic shared memory per block
     // int8 caches: a ring of NR raw tiles (TT positions x D codes, as TMA
-    // lands them) in front of the bf16 slots the MMAs read.
+    // lands them) in front of the fp16 slots the MMAs read.
     static constexpr uint32_t RAW = I8 ? TT * D : 0;
     static constexpr int NR = I8 ? (D == 128 ? 6 : 2) : 0;
     static constexpr int NRX = I8 ? NR : 1;   // ring length for index arithmetic
@@ -567,6 +567,120 @@ __device__ __noinline__ bool share_merge_segment(const Params &p, Bars *bs, Walk
     return true;
 }
 
+// The last arriver's merge of split segment s (pieces in blocks c_first ..
+// c_last): rows cb0 .. r1w-1 (one softmax group's), thread wt of the group.
+template <int D, int NH, int MU>
+__device__ __forceinline__ void merge_split_rows(const Params &p, int64_t s, int c_first, int c_last,
+                                                 int cb0, int r1w, int wt, const int64_t *ooff) {
+    const int rows = p.rows;
+    // Merge the pieces' partials.  head_dim 128 (launches
+    // that often split a segment many ways): two passes per
+    // row, the maximum M over the pieces, then the weighted
+    // sums Ls and acc (weights 2^(m - M)), neither carrying a
+    // dependence from one piece's loads to the next, so many
+    // pieces' loads are in flight together.  head_dim 256:
+    // one pass with a running maximum (the shared merge's
+    // arithmetic, bit for bit; a smaller loop body, which
+    // runs once from cold instruction caches).  Thread -> 4
+    // consecutive dims of rows cb0 + rg + RG*k; row indices
+    // are clamped into range (weight 0 beyond) so every load
+    // is unconditional.
+    constexpr int TPR = D / 4, RG = 128 / TPR, RPT = NH / RG;
+    constexpr int CH = RPT < 8 ? RPT : 8;
+    const int dq = (wt % TPR) * 4, rg = wt / TPR;
+#pragma unroll 1
+    for (int k0 = 0; k0 < RPT && cb0 + rg + RG * k0 < r1w; k0 += CH) {
+        float4 acc[CH];
+        float M[CH], Ls[CH];
+        int rr[CH];
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const int r = cb0 + rg + RG * (k0 + k);
+            rr[k] = r < r1w ? r : r1w - 1;
+            acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            M[k] = neg_inf();
+            Ls[k] = 0.f;
+        }
+        if (D == 128) {
+#pragma unroll 8
+            for (int c2 = c_first; c2 <= c_last; ++c2) {
+                const float *sl = slot_ptr(p, s, c2);
+#pragma unroll
+                for (int k = 0; k < CH; ++k) M[k] = fmaxf(M[k], __ldcg(sl + rows * D + rr[k]));
+            }
+#pragma unroll
+            for (int k = 0; k < CH; ++k) M[k] = M[k] == neg_inf() ? 0.f : M[k];
+#pragma unroll 4
+            for (int c2 = c_first; c2 <= c_last; ++c2) {
+                const float *sl = slot_ptr(p, s, c2);
+#pragma unroll
+                for (int k = 0; k < CH; ++k) {
+                    const float mv = __ldcg(sl + rows * D + rr[k]);
+                    const float lv = __ldcg(sl + rows * D + rows + rr[k]);
+                    const float4 v =
+                        __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + dq));
+                    const float w = fast_exp2(mv - M[k]);
+                    Ls[k] = __fmaf_rn(w, lv, Ls[k]);
+                    acc[k].x = __fmaf_rn(w, v.x, acc[k].x);
+                    acc[k].y = __fmaf_rn(w, v.y, acc[k].y);
+                    acc[k].z = __fmaf_rn(w, v.z, acc[k].z);
+                    acc[k].w = __fmaf_rn(w, v.w, acc[k].w);
+                }
+            }
+        } else {
+#pragma unroll(MU)
+            for (int c2 = c_first; c2 <= c_last; ++c2) {
+                const float *sl = slot_ptr(p, s, c2);
+#pragma unroll
+                for (int k = 0; k < CH; ++k) {
+                    const float mv = __ldcg(sl + rows * D + rr[k]);
+                    const float lv = __ldcg(sl + rows * D + rows + rr[k]);
+                    const float4 v =
+                        __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + dq));
+                    const float mn = fmaxf(M[k], mv);
+                    const float mu = mn == neg_inf() ? 0.f : mn;
+                    const float a = fast_exp2(M[k] - mu), w = fast_exp2(mv - mu);
+                    // (explicit roundings: the shared merge computes
+                    // the same values bit for bit)
+                    M[k] = mn;
+                    Ls[k] = __fmaf_rn(w, lv, Ls[k] * a);
+                    acc[k].x = __fmaf_rn(w, v.x, acc[k].x * a);
+                    acc[k].y = __fmaf_rn(w, v.y, acc[k].y * a);
+                    acc[k].z = __fmaf_rn(w, v.z, acc[k].z * a);
+                    acc[k].w = __fmaf_rn(w, v.w, acc[k].w * a);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const int r = cb0 + rg + RG * (k0 + k);
+            if (r < r1w) {
+                const int64_t off = ooff[r] + dq;
+                const float inv = Ls[k] > 0.f ? 1.f / Ls[k] : 0.f;
+                const float o4[4] = {acc[k].x * inv, acc[k].y * inv, acc[k].z * inv,
+                                     acc[k].w * inv};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (p.out_f32)
+                        reinterpret_cast<float *>(p.out)[off + e] = o4[e];
+                    else
+                        reinterpret_cast<uint16_t *>(p.out)[off + e] = bf16_bits(o4[e]);
+                }
+            }
+        }
+    }
+}
+
+// The same, out of line: the flat int8 kernels with up to 8 rows (one
+// softmax group, widening warps beside it) run measurably faster with the
+// merge's registers and code outside the softmax loop (the int8 workload
+// 313.6 -> 296.5 us); every other instantiation is faster with it inline.
+template <int D, int NH, int MU>
+__device__ __noinline__ void merge_split_rows_ool(const Params &p, int64_t s, int c_first, int c_last,
+                                                  int cb0, int r1w, int wt, const int64_t *ooff) {
+    merge_split_rows<D, NH, MU>(p, s, c_first, c_last, cb0, r1w, wt, ooff);
+}
+
 // Fused append: this block's share of the new rows, copied into the caches
 // (16-byte chunks spread over every thread of the grid).
 __device__ __noinline__ void append_rows(const Params &p) {
@@ -701,7 +815,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         }
     }
     if (tid == 0) {
-        // bf16 slots are filled by TMA (one arrival plus bytes) or, for int8
+        // K/V slots are filled by TMA (one arrival plus bytes) or, for int8
         // caches, by the 128 widening threads.
         for (int i = 0; i < C::NS; ++i) {
             ptx::mbar_init(&bs->slot_full[i], I8 ? 128 : 1);
@@ -1313,7 +1427,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 for (int k = 0; k < NK; ++k)
                     cw[k] = *reinterpret_cast<const uint4 *>(raw + k * RSTEP * 128);
                 // The raw slot is free for the next copy once the codes are
-                // in registers; then wait for a bf16 slot the MMAs released.
+                // in registers; then wait for an fp16 slot the MMAs released.
                 ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive(&bs->raw_empty[rs]);
                 ok = bar_wait<I8>(&bs->slot_empty[ss], ((f / C::NS) & 1) ^ 1, abort_flag, p.wait_ns);
@@ -1784,102 +1898,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                 const int r1w = min(cb0 + NH, rows);       // this group merges rows cb0 .. r1w-1
                 if (!share_merge && bs->last_flag && r1w > cb0) {
                     __threadfence();
-                    // Merge the pieces' partials.  head_dim 128 (launches
-                    // that often split a segment many ways): two passes per
-                    // row, the maximum M over the pieces, then the weighted
-                    // sums Ls and acc (weights 2^(m - M)), neither carrying a
-                    // dependence from one piece's loads to the next, so many
-                    // pieces' loads are in flight together.  head_dim 256:
-                    // one pass with a running maximum (the shared merge's
-                    // arithmetic, bit for bit; a smaller loop body, which
-                    // runs once from cold instruction caches).  Thread -> 4
-                    // consecutive dims of rows cb0 + rg + RG*k; row indices
-                    // are clamped into range (weight 0 beyond) so every load
-                    // is unconditional.
-                    constexpr int TPR = D / 4, RG = 128 / TPR, RPT = NH / RG;
-                    constexpr int CH = RPT < 8 ? RPT : 8;
-                    const int dq = (wt % TPR) * 4, rg = wt / TPR;
-#pragma unroll 1
-                    for (int k0 = 0; k0 < RPT && cb0 + rg + RG * k0 < r1w; k0 += CH) {
-                        float4 acc[CH];
-                        float M[CH], Ls[CH];
-                        int rr[CH];
-#pragma unroll
-                        for (int k = 0; k < CH; ++k) {
-                            const int r = cb0 + rg + RG * (k0 + k);
-                            rr[k] = r < r1w ? r : r1w - 1;
-                            acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            M[k] = neg_inf();
-                            Ls[k] = 0.f;
-                        }
-                        if (D == 128) {
-#pragma unroll 8
-                            for (int c2 = c_first; c2 <= c_last; ++c2) {
-                                const float *sl = slot_ptr(p, s, c2);
-#pragma unroll
-                                for (int k = 0; k < CH; ++k) M[k] = fmaxf(M[k], __ldcg(sl + rows * D + rr[k]));
-                            }
-#pragma unroll
-                            for (int k = 0; k < CH; ++k) M[k] = M[k] == neg_inf() ? 0.f : M[k];
-#pragma unroll 4
-                            for (int c2 = c_first; c2 <= c_last; ++c2) {
-                                const float *sl = slot_ptr(p, s, c2);
-#pragma unroll
-                                for (int k = 0; k < CH; ++k) {
-                                    const float mv = __ldcg(sl + rows * D + rr[k]);
-                                    const float lv = __ldcg(sl + rows * D + rows + rr[k]);
-                                    const float4 v =
-                                        __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + dq));
-                                    const float w = fast_exp2(mv - M[k]);
-                                    Ls[k] = __fmaf_rn(w, lv, Ls[k]);
-                                    acc[k].x = __fmaf_rn(w, v.x, acc[k].x);
-                                    acc[k].y = __fmaf_rn(w, v.y, acc[k].y);
-                                    acc[k].z = __fmaf_rn(w, v.z, acc[k].z);
-                                    acc[k].w = __fmaf_rn(w, v.w, acc[k].w);
-                                }
-                            }
-                        } else {
-#pragma unroll(C::MERGE_UNROLL)
-                            for (int c2 = c_first; c2 <= c_last; ++c2) {
-                                const float *sl = slot_ptr(p, s, c2);
-#pragma unroll
-                                for (int k = 0; k < CH; ++k) {
-                                    const float mv = __ldcg(sl + rows * D + rr[k]);
-                                    const float lv = __ldcg(sl + rows * D + rows + rr[k]);
-                                    const float4 v =
-                                        __ldcg(reinterpret_cast<const float4 *>(sl + rr[k] * D + dq));
-                                    const float mn = fmaxf(M[k], mv);
-                                    const float mu = mn == neg_inf() ? 0.f : mn;
-                                    const float a = fast_exp2(M[k] - mu), w = fast_exp2(mv - mu);
-                                    // (explicit roundings: the shared merge computes
-                                    // the same values bit for bit)
-                                    M[k] = mn;
-                                    Ls[k] = __fmaf_rn(w, lv, Ls[k] * a);
-                                    acc[k].x = __fmaf_rn(w, v.x, acc[k].x * a);
-                                    acc[k].y = __fmaf_rn(w, v.y, acc[k].y * a);
-                                    acc[k].z = __fmaf_rn(w, v.z, acc[k].z * a);
-                                    acc[k].w = __fmaf_rn(w, v.w, acc[k].w * a);
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int k = 0; k < CH; ++k) {
-                            const int r = cb0 + rg + RG * (k0 + k);
-                            if (r < r1w) {
-                                const int64_t off = ooff[r] + dq;
-                                const float inv = Ls[k] > 0.f ? 1.f / Ls[k] : 0.f;
-                                const float o4[4] = {acc[k].x * inv, acc[k].y * inv, acc[k].z * inv,
-                                                     acc[k].w * inv};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    if (p.out_f32)
-                                        reinterpret_cast<float *>(p.out)[off + e] = o4[e];
-                                    else
-                                        reinterpret_cast<uint16_t *>(p.out)[off + e] = bf16_bits(o4[e]);
-                                }
-                            }
-                        }
-                    }
+                    if constexpr (I8 && NV <= 8 && !GA && !PG)
+                        merge_split_rows_ool<D, NH, C::MERGE_UNROLL>(p, s, c_first, c_last, cb0, r1w, wt, ooff);
+                    else
+                        merge_split_rows<D, NH, C::MERGE_UNROLL>(p, s, c_first, c_last, cb0, r1w, wt, ooff);
                 }
                 if (!share_merge && bs->last_flag && tid == 0) p.counters[s] = 0;
             }
