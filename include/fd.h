@@ -102,9 +102,10 @@ extern "C" {
                                     (pools whose rows form one strided 2-D
                                     array), the fused append and the
                                     masked prefix over flat bf16 caches,
-                                    and gather over bf16 caches whose rows
-                                    form one strided 2-D array; 16-byte
-                                    aligned q (else FD_ERR_UNSUPPORTED)    */
+                                    and gather over bf16 or int8 caches
+                                    whose rows form one strided 2-D array;
+                                    16-byte aligned q (else
+                                    FD_ERR_UNSUPPORTED)                    */
 
 #define FD_MAX_ROWS 64           /* query rows per kv head per launch unit */
 
