@@ -278,6 +278,21 @@ int run(const Call &c) {
         c.mode == fd::kGather ? nseg * (fd::ceil_div(c.idx_len, tile) + seg_units)
                               : nseg * (fd::ceil_div(cap, tile) + seg_units);
     int32_t G = o.num_ctas;
+    // bf16 gather on the tensor cores with an automatic grid: when every
+    // list fits one thread-block cluster of up to 16 blocks and all the
+    // clusters fit the device at once, one cluster per list merges its
+    // pieces through distributed shared memory (no global partials, fences
+    // or counters); the list length alone decides, never the capacity.
+    if (G == 0 && kernel == FD_KERNEL_TC && c.mode == fd::kGather && !c.kv_int8 && c.idx_len > 0) {
+        const int64_t ntiles = fd::ceil_div(c.idx_len, tile);
+        int dev = 0, sms = 0;
+        if (ntiles >= 2 && ntiles <= 16 && cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            nseg * ntiles <= (int64_t)sms) {
+            p.cl = (int32_t)ntiles;
+            G = (int32_t)(nseg * ntiles);
+        }
+    }
     if (G == 0) {
         G = auto_ctas(kernel, max_units);
         if (G <= 0) return FD_ERR_CUDA;

@@ -60,6 +60,10 @@ struct Params {
     const int32_t *mlist;
     const int32_t *mcnt;
     int64_t mls;
+    // gather, tensor-core kernel: when > 1, each list is one thread-block
+    // cluster of `cl` blocks (a share of its tiles each) whose partials merge
+    // through distributed shared memory; 0 otherwise
+    int32_t cl;
     // paged caches: logical position j of sequence b lives at row j % page_size
     // of pool page block_table[b * max_pages + j / page_size]; the caches'
     // strides are then (page, kv head, row in page); cap = max_pages * page_size

@@ -81,6 +81,20 @@ int launch_tc(const Params &p, int G, cudaStream_t st) {
             !make_qmap(&args.tq, p))
             return -5;
         const int rows = p.rows;
+        if (p.cl > 1) {
+            // one cluster of p.cl blocks per list, merging through
+            // distributed shared memory; -2 (the clusters do not all fit at
+            // once): the same grid splits as usual
+            const int rc =
+                p.d == 128 ? (rows <= 16   ? launch_dn<128, 16, false, 16, true, false, false, false, 0, true>(args, G, st)
+                              : rows <= 32 ? launch_dn<128, 32, false, 32, true, false, false, false, 0, true>(args, G, st)
+                                           : launch_dn<128, 64, false, 64, true, false, false, false, 0, true>(args, G, st))
+                           : (rows <= 16   ? launch_dn<256, 16, false, 16, true, false, false, false, 0, true>(args, G, st)
+                              : rows <= 32 ? launch_dn<256, 32, false, 32, true, false, false, false, 0, true>(args, G, st)
+                                           : launch_dn<256, 64, false, 64, true, false, false, false, 0, true>(args, G, st));
+            if (rc != -2) return rc;
+            args.p.cl = 0;
+        }
         if (p.d == 128)
             return rows <= 16   ? launch_dn<128, 16, false, 16, true>(args, G, st)
                    : rows <= 32 ? launch_dn<128, 32, false, 32, true>(args, G, st)

@@ -681,6 +681,56 @@ __device__ __noinline__ void merge_split_rows_ool(const Params &p, int64_t s, in
     merge_split_rows<D, NH, MU>(p, s, c_first, c_last, cb0, r1w, wt, ooff);
 }
 
+// Gather with cluster merges: this block's share of the merge of its
+// cluster's list.  The partial of block k (O[rows][D], m[rows], l[rows],
+// fp32) sits at shared address `part` of block k; thread tid of this block
+// (rank `rank`) merges float4 units rank * U / cl + tid, + 320, ... below
+// (rank + 1) * U / cl of the U = rows * D / 4, reading every block's partial
+// through distributed shared memory, and stores the normalised outputs.
+template <int D>
+__device__ __noinline__ void cluster_merge(const Params &p, uint32_t part, int tid) {
+    const int cs = p.cl, rank = (int)ptx::cluster_ctarank(), rows = p.rows;
+    const int64_t sg = ptx::cluster_id_x();
+    if (sg >= p.nseg) return;
+    const int64_t bi = sg / p.Hkv;
+    const int hk = (int)(sg % p.Hkv), b = (int)(bi / p.n_q), i = (int)(bi % p.n_q);
+    constexpr int UPR = D / 4;
+    const int U = rows * UPR;
+    const int u0 = (int)((int64_t)U * rank / cs), u1 = (int)((int64_t)U * (rank + 1) / cs);
+    for (int u = u0 + tid; u < u1; u += kThreadsTC) {
+        const int r = u / UPR, dq = (u % UPR) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float M = neg_inf(), Ls = 0.f;
+        for (int k = 0; k < cs; ++k) {
+            const uint32_t pk = ptx::map_cluster(part, (uint32_t)k);
+            const float mv = ptx::ld_cluster_f32(pk + (uint32_t)(rows * D + r) * 4);
+            if (mv == neg_inf()) continue;   // nothing seen (a block without tiles holds no O)
+            const float lv = ptx::ld_cluster_f32(pk + (uint32_t)(rows * D + rows + r) * 4);
+            const float4 v = ptx::ld_cluster_f32x4(pk + (uint32_t)(r * D + dq) * 4);
+            const float mn = fmaxf(M, mv);
+            const float mu = mn == neg_inf() ? 0.f : mn;
+            const float a = fast_exp2(M - mu), w = fast_exp2(mv - mu);
+            M = mn;
+            Ls = __fmaf_rn(w, lv, Ls * a);
+            acc.x = __fmaf_rn(w, v.x, acc.x * a);
+            acc.y = __fmaf_rn(w, v.y, acc.y * a);
+            acc.z = __fmaf_rn(w, v.z, acc.z * a);
+            acc.w = __fmaf_rn(w, v.w, acc.w * a);
+        }
+        const int64_t off = (int64_t)b * p.os[0] + (int64_t)i * p.os[1] +
+                            (int64_t)(hk * p.g + r) * p.os[2] + dq;
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        const float o4[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (p.out_f32)
+                reinterpret_cast<float *>(p.out)[off + e] = o4[e];
+            else
+                reinterpret_cast<uint16_t *>(p.out)[off + e] = bf16_bits(o4[e]);
+        }
+    }
+}
+
 // Fused append: this block's share of the new rows, copied into the caches
 // (16-byte chunks spread over every thread of the grid).
 __device__ __noinline__ void append_rows(const Params &p) {
@@ -747,7 +797,7 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, volatil
     return ptx::mbar_wait(bar, parity, abort, limit_ns);
 }
 
-template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP, int MK>
+template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP, int MK, bool CL>
 __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant__ TcArgs a) {
     static_assert(!(GA && PG), "gather and paged loads are separate modes");
     static_assert(!AP || (!I8 && !GA && !PG), "fused append: flat bf16 caches");
@@ -755,6 +805,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
     // masked prefix: MK = 1 finds each tile's visible chunks in place, MK = 2
     // walks the chunk list of the pass before the launch
     static_assert(MK >= 0 && MK <= 2, "masked mode");
+    static_assert(!CL || (GA && !I8 && !SH && !PG && !AP && !MK), "cluster merges: bf16 gather");
     constexpr bool MP = MK == 1, ML = MK == 2;
     using C = Cfg<D, N, I8, NV, GA>;
     constexpr int kSoftmaxThreads = C::SMT;
@@ -783,6 +834,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
     if (smem_base & 1023u) {
         if (tid == 0) atomicOr(p.status, kDevTimeout);
         if (AP) append_exit(p);
+        if (CL) {   // the cluster's blocks meet twice before they leave
+            ptx::cluster_sync();
+            ptx::cluster_sync();
+        }
         return;
     }
 
@@ -793,11 +848,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
     // The producer warp finds the block's tile range and first piece while
     // the others set up barriers and TMEM.
     if (warp == kProducerWarp) {
-        const int64_t tot = total_units_tc(p);
+        const int64_t tot = CL ? tiles_of(p.idx_len) : total_units_tc(p);
         Walk w{};
         int64_t tb = 0, te = 0;
         bool has = false;
-        if (tot > 0) {
+        if (CL) {
+            // cluster of p.cl blocks per list: block `rank` takes tiles
+            // [rank * n / cl, (rank + 1) * n / cl) of list `cluster id`
+            const int64_t sg = ptx::cluster_id_x(), rank = ptx::cluster_ctarank(), bi = sg / p.Hkv;
+            w.s = sg;
+            w.hk = (int)(sg % p.Hkv);
+            w.b = (int)(bi / p.n_q);
+            w.i = (int)(bi % p.n_q);
+            w.first = 0;
+            w.ntiles = (int32_t)tot;
+            w.L = p.idx_len;
+            tb = rank * tot / p.cl;
+            te = (rank + 1) * tot / p.cl;
+            has = sg < p.nseg && tb < te;
+        } else if (tot > 0) {
             const int32_t Gw = working_blocks(tot, G);
             if (c < Gw) {
                 const Split sp{tot, Gw};
@@ -1854,9 +1923,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
 
             // Blocks sharing the segment (owner() only where the piece is
             // cut at this block's range boundary).
-            const int c_first = w.first >= t_begin ? c : sp.owner(w.first);
-            const int c_last = w.first + w.ntiles <= t_end ? c : sp.owner(w.first + w.ntiles - 1);
-            if (c_first == c_last) {
+            const int c_first = CL ? c : w.first >= t_begin ? c : sp.owner(w.first);
+            const int c_last = CL ? c : w.first + w.ntiles <= t_end ? c : sp.owner(w.first + w.ntiles - 1);
+            if (CL) {
+                // the partial (O, m, l) stays in this block's K/V slots, idle
+                // after its only piece, for the cluster's merge at the end
+                float *part = reinterpret_cast<float *>(smem + C::OFF_SLOTS);
+#pragma unroll
+                for (int r = 0; r < NH; ++r) {
+                    if (cb0 + r < rows) {
+#pragma unroll
+                        for (int dc = 0; dc < C::DC; ++dc) part[(cb0 + r) * D + dc * 128 + wt] = o[dc][r];
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < NH; ++r) {
+                    if (r == wt && cb0 + r < rows) {
+                        part[rows * D + cb0 + r] = mrun[r];
+                        part[rows * D + rows + cb0 + r] = lsum[r];
+                    }
+                }
+            } else if (c_first == c_last) {
 #pragma unroll
                 for (int r = 0; r < NH; ++r) {
                     if (cb0 + r < rows) {
@@ -1930,6 +2017,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    if (CL) {
+        // A block with no tiles contributes nothing (m = -inf, l = 0).  Then
+        // every block's partial is in its shared memory; block `rank` merges
+        // its share of the list's rows x (D/4) float4 units from all of them
+        // (running maximum over the blocks in order, as the shared merge),
+        // and the cluster meets again before any block leaves.
+        float *part = reinterpret_cast<float *>(smem + C::OFF_SLOTS);
+        if (!has_work)
+            for (int r = tid; r < p.rows; r += kThreadsTC) {
+                part[p.rows * D + r] = neg_inf();
+                part[p.rows * D + p.rows + r] = 0.f;
+            }
+        ptx::cluster_sync();
+        cluster_merge<D>(p, smem_base + C::OFF_SLOTS, tid);
+        ptx::cluster_sync();
+    }
     if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
     if (AP) append_exit(p);
 }
@@ -2001,7 +2104,7 @@ inline bool make_gmap(CUtensorMap *m, const void *base, const Params &p, int64_t
 
 // Blocks of this instantiation that can be resident at once on the current
 // device (0 on error); sets the dynamic shared memory opt-in the first time.
-template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP, int MK>
+template <int D, int N, bool I8, int NV, bool GA, bool SH, bool PG, bool AP, int MK, bool CL = false>
 int resident_blocks() {
     using C = Cfg<D, N, I8, NV, GA>;
     static std::atomic<int> cached[64];
@@ -2010,9 +2113,9 @@ int resident_blocks() {
     int n = cached[dev].load(std::memory_order_acquire);
     if (n > 0) return n;
     int per_sm = 0, sms = 0;
-    if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK>,
+    if (cudaFuncSetAttribute(tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK, CL>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK>,
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK, CL>,
                                                       kThreadsTC, C::SMEM) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 0;
@@ -2022,13 +2125,42 @@ int resident_blocks() {
 }
 
 template <int D, int N, bool I8, int NV = N, bool GA = false, bool SH = false, bool PG = false,
-          bool AP = false, int MK = 0>
+          bool AP = false, int MK = 0, bool CL = false>
 int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
     using C = Cfg<D, N, I8, NV, GA>;
-    const int resident = resident_blocks<D, N, I8, NV, GA, SH, PG, AP, MK>();
+    const int resident = resident_blocks<D, N, I8, NV, GA, SH, PG, AP, MK, CL>();
     if (resident <= 0) return -5;
+    if (CL) {
+        // clusters of args.p.cl blocks, one per list (G = lists x cl); all
+        // of them resident at once, or -2 (the caller then splits as usual)
+        auto kern = tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK, CL>;
+        const int cs = args.p.cl;
+        if (cs < 2 || cs > 16 || G % cs) return -2;
+        if (cs > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                          cudaSuccess)
+            return -2;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)G);
+        cfg.blockDim = dim3(kThreadsTC);
+        cfg.dynamicSmemBytes = C::SMEM;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return -2;
+        }
+        if (clusters < G / cs) return -2;
+        return cudaLaunchKernelEx(&cfg, kern, args) == cudaSuccess ? 0 : -5;
+    }
     if (!SH && !AP) {
-        tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK><<<G, kThreadsTC, C::SMEM, st>>>(args);
+        tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK, CL><<<G, kThreadsTC, C::SMEM, st>>>(args);
         return cudaGetLastError() == cudaSuccess ? 0 : -5;
     }
     // shared merges or fused append: a cooperative launch (every block
@@ -2046,7 +2178,7 @@ int launch_dn(const TcArgs &args, int G, cudaStream_t st) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK>, ca) == cudaSuccess ? 0 : -5;
+    return cudaLaunchKernelEx(&cfg, tc_kernel<D, N, I8, NV, GA, SH, PG, AP, MK, CL>, ca) == cudaSuccess ? 0 : -5;
 }
 
 }  // namespace

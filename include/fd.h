@@ -181,6 +181,11 @@ int fd_decode_int8(const fd_tensor *q, const fd_tensor *k_cache,
  *   given: a cell listed twice counts twice (distinct cells reproduce the
  *   masked path exactly).  No length and no causal mask apply: the list is
  *   the visible set.  Scale: opts->scale, or 1/sqrt(d) when 0.
+ *   On the tensor-core kernel with opts->num_ctas = 0, lists of 2 to 16
+ *   tiles of 128 entries whose (sequence, query row, kv head) lists all fit
+ *   the device at once run as thread-block clusters, one per list, whose
+ *   blocks merge their partial results through distributed shared memory
+ *   instead of the workspace (the list length alone decides).
  */
 int fd_decode_gather(const fd_tensor *q, const fd_tensor *k_cache,
                      const fd_tensor *v_cache, const int32_t *idx,

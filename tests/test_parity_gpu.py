@@ -243,6 +243,25 @@ def test_gather_tensor_core_splits_token_major(ctas, d):
         compare(got, run_oracle(inp), od, "gather tc token-major")
 
 
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("g,idx_len", [(8, 2048), (4, 300), (16, 129), (32, 1000), (64, 640)])
+def test_gather_tensor_core_cluster_merges(d, g, idx_len):
+    # automatic grid: lists of 2-16 tiles whose clusters all fit the device
+    # merge through distributed shared memory (129 entries: a one-entry last
+    # tile; 64 rows: the widest instantiation); the same inputs on an
+    # explicit grid take the global merge.  Both against the oracle, with
+    # padding and an out-of-range cell in the lists.
+    B, n_q, Hkv = (1, 1, 4) if g >= 32 else (2, 2, 2)
+    inp = W.gather_inputs(B, n_q, g * Hkv, Hkv, d, 5000, idx_len, min(64, idx_len), 43)
+    inp.idx[0, 0, 3] = -1
+    inp.idx[-1, -1, idx_len // 2] = 5000
+    ref = run_oracle(inp)
+    for ctas in (0, 37):
+        for od in (torch.float32, torch.bfloat16):
+            check(inp, od, kernel=fd.FD_KERNEL_TC, num_ctas=ctas, ref=ref,
+                  what="gather d%d g%d len%d ctas%d" % (d, g, idx_len, ctas))
+
+
 @pytest.mark.parametrize("kernel", GATHER_KERNELS)
 @pytest.mark.parametrize("d,g,ctas", [(128, 8, 0), (128, 16, 7), (256, 4, 0), (256, 32, 300)])
 def test_gather_int8(kernel, d, g, ctas):
