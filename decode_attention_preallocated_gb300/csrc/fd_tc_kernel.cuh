@@ -206,7 +206,7 @@ struct Cfg {
     // int8 caches: a ring of NR raw tiles (TT positions x D codes, as TMA
     // lands them) in front of the fp16 slots the MMAs read.
     static constexpr uint32_t RAW = I8 ? TT * D : 0;
-    static constexpr int NR = I8 ? (D == 128 ? 6 : 2) : 0;
+    static constexpr int NR = I8 ? (D == 128 ? 3 : 2) : 0;
     static constexpr int NRX = I8 ? NR : 1;   // ring length for index arithmetic
     // Two P stages when that still leaves three K/V slots, else one.
     static constexpr int NS2 = (int)((BUDGET - MISC - QBYTES - 2 * PSTAGE - NR * RAW) / SLOT);
