@@ -495,10 +495,14 @@ __device__ __forceinline__ void note_timeout(Bars *bs, const Params &p, int site
 // merge units [share*U/P, (share+1)*U/P) of the rows x (D/4) float4 units from
 // the pieces' workspace slots (running maximum per row, pieces in order),
 // store them, and count the share done (the last one resets the counter).
+// A share of few units splits each unit's pieces over G threads (pieces
+// g, g + G, ...), so G times as many loads are in flight, and merges the G
+// partials through shared memory (scr: the block's free operand slots).
 // Kept out of line so that its registers do not weigh on the tile loop.
 template <int D, bool GA, int SMT>
-__device__ __noinline__ bool share_merge_segment(const Params &p, Bars *bs, Walk sw, int c0, int c1,
-                                                 int c, int tid, uint32_t &sm_ctr, int k, int piece) {
+__device__ __noinline__ bool share_merge_segment(const Params &p, Bars *bs, float *scr, Walk sw, int c0,
+                                                 int c1, int c, int tid, uint32_t &sm_ctr, int k,
+                                                 int piece) {
     volatile int *abort_flag = &bs->abort_flag;
     auto sm_sync = [&]() -> bool {
         ptx::mbar_arrive(&bs->sm_bar);
@@ -528,26 +532,37 @@ __device__ __noinline__ bool share_merge_segment(const Params &p, Bars *bs, Walk
     constexpr int UPR = D / 4;                    // float4 units per row
     const int64_t U = (int64_t)rows * UPR;
     const int64_t u0 = U * share / P, u1 = U * (share + 1) / P;
-    for (int64_t u = u0 + tid; u < u1; u += kSoftmaxThreads) {
+    const int nu = (int)(u1 - u0);
+    // One step of the running-maximum merge: fold partial (mv, lv, v) into
+    // (M, Ls, acc).  (Explicit roundings: the same arithmetic as the last
+    // arriver's single-pass merge.)
+    auto fold = [](float &M, float &Ls, float4 &acc, float mv, float lv, float4 v) {
+        const float mn = fmaxf(M, mv);
+        const float mu = mn == neg_inf() ? 0.f : mn;
+        const float a = fast_exp2(M - mu), wv = fast_exp2(mv - mu);
+        M = mn;
+        Ls = __fmaf_rn(wv, lv, Ls * a);
+        acc.x = __fmaf_rn(wv, v.x, acc.x * a);
+        acc.y = __fmaf_rn(wv, v.y, acc.y * a);
+        acc.z = __fmaf_rn(wv, v.z, acc.z * a);
+        acc.w = __fmaf_rn(wv, v.w, acc.w * a);
+    };
+    // Unit u's pieces c0 + g, c0 + g + G, ... in order.
+    auto merge_pieces = [&](int64_t u, int g, int G, float &M, float &Ls, float4 &acc) {
         const int r = (int)(u / UPR), dq = (int)(u % UPR) * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float M = neg_inf(), Ls = 0.f;
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        M = neg_inf();
+        Ls = 0.f;
 #pragma unroll 4
-        for (int c2 = c0; c2 <= c1; ++c2) {
+        for (int c2 = c0 + g; c2 <= c1; c2 += G) {
             const float *sl = slot_ptr(p, sg, c2);
             const float mv = __ldcg(sl + rows * D + r), lv = __ldcg(sl + rows * D + rows + r);
             const float4 v = __ldcg(reinterpret_cast<const float4 *>(sl + r * D + dq));
-            const float mn = fmaxf(M, mv);
-            const float mu = mn == neg_inf() ? 0.f : mn;
-            const float a = fast_exp2(M - mu), wv = fast_exp2(mv - mu);
-            // (the same roundings as the last arriver's merge, bit for bit)
-            M = mn;
-            Ls = __fmaf_rn(wv, lv, Ls * a);
-            acc.x = __fmaf_rn(wv, v.x, acc.x * a);
-            acc.y = __fmaf_rn(wv, v.y, acc.y * a);
-            acc.z = __fmaf_rn(wv, v.z, acc.z * a);
-            acc.w = __fmaf_rn(wv, v.w, acc.w * a);
+            fold(M, Ls, acc, mv, lv, v);
         }
+    };
+    auto store = [&](int64_t u, float Ls, float4 acc) {
+        const int r = (int)(u / UPR), dq = (int)(u % UPR) * 4;
         const int qi = GA ? sw.i : r % p.n_q, h = sw.hk * p.g + (GA ? r : r / p.n_q);
         const int64_t off = (int64_t)sw.b * p.os[0] + (int64_t)qi * p.os[1] +
                             (int64_t)h * p.os[2] + dq;
@@ -559,6 +574,36 @@ __device__ __noinline__ bool share_merge_segment(const Params &p, Bars *bs, Walk
                 reinterpret_cast<float *>(p.out)[off + e] = o4[e];
             else
                 reinterpret_cast<uint16_t *>(p.out)[off + e] = bf16_bits(o4[e]);
+        }
+    };
+    const int G = (nu > 0 && 2 * nu <= kSoftmaxThreads) ? min(P, kSoftmaxThreads / nu) : 1;
+    if (G >= 2) {
+        // thread tid = g * nu + i: group g of unit u0 + i
+        float4 *s4 = reinterpret_cast<float4 *>(scr);
+        float *sm = scr + 4 * kSoftmaxThreads, *sl = sm + kSoftmaxThreads;
+        if (tid < G * nu) {
+            const int g = tid / nu;
+            float M, Ls;
+            float4 acc;
+            merge_pieces(u0 + (tid - g * nu), g, G, M, Ls, acc);
+            s4[tid] = acc;
+            sm[tid] = M;
+            sl[tid] = Ls;
+        }
+        ok = sm_sync();
+        if (!ok) return false;
+        if (tid < nu) {
+            float M = neg_inf(), Ls = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int g = 0; g < G; ++g) fold(M, Ls, acc, sm[g * nu + tid], sl[g * nu + tid], s4[g * nu + tid]);
+            store(u0 + tid, Ls, acc);
+        }
+    } else {
+        for (int64_t u = u0 + tid; u < u1; u += kSoftmaxThreads) {
+            float M, Ls;
+            float4 acc;
+            merge_pieces(u, 0, 1, M, Ls, acc);
+            store(u, Ls, acc);
         }
     }
     ok = sm_sync();
@@ -580,7 +625,7 @@ __device__ __forceinline__ void merge_split_rows(const Params &p, int64_t s, int
     // dependence from one piece's loads to the next, so many
     // pieces' loads are in flight together.  head_dim 256:
     // one pass with a running maximum (the shared merge's
-    // arithmetic, bit for bit; a smaller loop body, which
+    // fold of one partial; a smaller loop body, which
     // runs once from cold instruction caches).  Thread -> 4
     // consecutive dims of rows cb0 + rg + RG*k; row indices
     // are clamped into range (weight 0 beyond) so every load
@@ -640,8 +685,8 @@ __device__ __forceinline__ void merge_split_rows(const Params &p, int64_t s, int
                     const float mn = fmaxf(M[k], mv);
                     const float mu = mn == neg_inf() ? 0.f : mn;
                     const float a = fast_exp2(M[k] - mu), w = fast_exp2(mv - mu);
-                    // (explicit roundings: the shared merge computes
-                    // the same values bit for bit)
+                    // (explicit roundings: the shared merge folds a
+                    // partial with the same operations)
                     M[k] = mn;
                     Ls[k] = __fmaf_rn(w, lv, Ls[k] * a);
                     acc[k].x = __fmaf_rn(w, v.x, acc[k].x * a);
@@ -2009,7 +2054,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             if (sw.first >= t_begin && sw.first + sw.ntiles <= t_end) continue;   // whole
             const int c0 = sw.first >= t_begin ? c : sp.owner(sw.first);
             const int c1 = sw.first + sw.ntiles <= t_end ? c : sp.owner(sw.first + sw.ntiles - 1);
-            ok = share_merge_segment<D, GA, kSoftmaxThreads>(p, bs, sw, c0, c1, c, tid, sm_ctr, k, piece);
+            ok = share_merge_segment<D, GA, kSoftmaxThreads>(
+                p, bs, reinterpret_cast<float *>(smem + C::OFF_SLOTS), sw, c0, c1, c, tid, sm_ctr, k, piece);
             if (!ok) { set_abort(bs, p); break; }
         }
     }
