@@ -90,6 +90,19 @@ def test_split_count_does_not_change_result(kernel, num_ctas):
 
 
 @pytest.mark.parametrize("kernel", DENSE_KERNELS)
+@pytest.mark.parametrize("num_ctas", [32, 48, 100, 152])
+@pytest.mark.parametrize("n_q", [1, 4, 6])
+def test_short_head_dim_256_launch_merges(kernel, num_ctas, n_q):
+    # one 3000-position sequence at head_dim 256 over 4 kv heads: a short
+    # launch, whose split segments the tensor-core kernel merges in shares;
+    # the grid sets the pieces per segment (about 8 to 30) and with the rows
+    # (4, 16 or 24) the threads that share one output unit's pieces (1 to
+    # about 30)
+    inp = W.dense_inputs(1, n_q, 16, 4, 256, 3000, [3000], 17, True)
+    check(inp, torch.float32, num_ctas=num_ctas, kernel=kernel)
+
+
+@pytest.mark.parametrize("kernel", DENSE_KERNELS)
 def test_capacity_beyond_length_is_never_read(kernel):
     # NaN in every cache row past the length, capacities from L to 4L
     L = 700
