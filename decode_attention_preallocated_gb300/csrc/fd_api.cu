@@ -271,12 +271,28 @@ int run(const Call &c) {
     const bool tc_ok = fd::tc_supports(p);
     int32_t kernel = o.kernel == FD_KERNEL_AUTO ? (tc_ok ? FD_KERNEL_TC : FD_KERNEL_SIMT) : o.kernel;
     if (kernel == FD_KERNEL_TC && !tc_ok) return FD_ERR_UNSUPPORTED;
+    // Flat dense int8 caches with more than 32 rows on the tensor cores: each
+    // kv head's query heads in `parts` parts of at most 32 rows, each part a
+    // segment of its own (the caches are read once per part).  Under
+    // FD_KERNEL_AUTO a workspace without room for the parts' segments takes
+    // the CUDA-core kernel, which serves the rows in one pass.
+    int32_t parts = 1;
+    if (kernel == FD_KERNEL_TC && c.kv_int8 && rows > 32) {
+        parts = fd::tc_int8_row_parts((int)n_q, (int)g);
+        if (parts < 2) return FD_ERR_UNSUPPORTED;
+        if (o.kernel == FD_KERNEL_AUTO && nseg * parts > ws->max_segments) {
+            kernel = FD_KERNEL_SIMT;
+            parts = 1;
+        }
+    }
+    const int64_t nseg_l = nseg * parts, rows_l = rows / parts;   // as launched
+    p.kvdiv = parts;
     const int tile = kernel_tile(kernel);
     const int32_t seg_units =
         kernel == FD_KERNEL_TC ? fd_seg_units(FD_KERNEL_TC, (int32_t)d, kvdt) : 0;
     const int64_t max_units =
         c.mode == fd::kGather ? nseg * (fd::ceil_div(c.idx_len, tile) + seg_units)
-                              : nseg * (fd::ceil_div(cap, tile) + seg_units);
+                              : nseg_l * (fd::ceil_div(cap, tile) + seg_units);
     int32_t G = o.num_ctas;
     // bf16 gather on the tensor cores with an automatic grid: when every
     // list fits one thread-block cluster of up to 16 blocks and all the
@@ -297,9 +313,9 @@ int run(const Call &c) {
         G = auto_ctas(kernel, max_units);
         if (G <= 0) return FD_ERR_CUDA;
     }
-    if (nseg > ws->max_segments || rows > ws->max_rows || d > ws->head_dim || G > ws->max_ctas)
+    if (nseg_l > ws->max_segments || rows > ws->max_rows || d > ws->head_dim || G > ws->max_ctas)
         return FD_ERR_WORKSPACE;
-    if ((size_t)(nseg + G) * (size_t)fd::slot_floats(rows, d) > ws->partial_floats)
+    if ((size_t)(nseg_l + G) * (size_t)fd::slot_floats(rows_l, d) > ws->partial_floats)
         return FD_ERR_WORKSPACE;
     p.tile = tile;
     p.seg_units = seg_units;

@@ -64,6 +64,12 @@ struct Params {
     // cluster of `cl` blocks (a share of its tiles each) whose partials merge
     // through distributed shared memory; 0 otherwise
     int32_t cl;
+    // flat int8 caches, tensor-core kernel, more than 32 rows: each kv head's
+    // query heads are served in `kvdiv` parts of g / kvdiv heads (at most 32
+    // rows each), as if there were Hkv * kvdiv kv heads: Hkv, g, rows and
+    // nseg then describe the parts, and kv head hk of a part reads the
+    // caches' kv head hk / kvdiv; 0 or 1 otherwise
+    int32_t kvdiv;
     // paged caches: logical position j of sequence b lives at row j % page_size
     // of pool page block_table[b * max_pages + j / page_size]; the caches'
     // strides are then (page, kv head, row in page); cap = max_pages * page_size

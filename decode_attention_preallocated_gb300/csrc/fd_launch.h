@@ -13,12 +13,17 @@ int launch_simt(const Params &p, int num_ctas, cudaStream_t stream);
 
 // Tensor-core kernel (fd_tc.cu, fd_tc_paged.cu): dense prefix (optionally
 // causal) over flat or paged caches and index gather; bf16 caches at head_dim
-// 128 / 256 with up to 64 packed rows, int8 at head_dim 128 with up to 32;
-// one block per SM.
+// 128 / 256 with up to 64 packed rows, int8 at head_dim 128 / 256 with up to
+// 32 (flat dense int8: more, in parts of a kv head's query heads, see
+// tc_int8_row_parts); one block per SM.
 int tc_tile_tokens();
 // Work units the split charges per segment start (Params::seg_units).
 int tc_seg_units(const Params &p);
 bool tc_supports(const Params &p);
+// Flat dense int8 caches with more than 32 rows (n_q x g): the fewest parts
+// k, k dividing g, such that n_q * g / k <= 32 (the launch then serves g / k
+// query heads per part and reads each kv head's caches k times); 0 if none.
+int tc_int8_row_parts(int n_q, int g);
 int launch_tc(const Params &p, int num_ctas, cudaStream_t stream);
 // Paged caches (fd_tc_paged.cu); tc_supports covers them.
 bool tc_supports_paged(const Params &p);

@@ -42,13 +42,22 @@ int tc_tile_tokens() { return TT; }
 // int8 tiles (codes and scales) stream about half the bytes of bf16 ones.
 int tc_seg_units(const Params &p) { return p.kv_int8 ? 14 : (p.d == 256 ? 6 : 9); }
 
+int tc_int8_row_parts(int n_q, int g) {
+    for (int k = 1; k <= g; ++k)
+        if (g % k == 0 && (int64_t)n_q * (g / k) <= 32) return k;
+    return 0;
+}
+
 bool tc_supports(const Params &p) {
     // Q goes through a tensor map: 16-byte aligned base and strides.
     const bool q_aligned = (reinterpret_cast<uintptr_t>(p.q) & 15) == 0 && p.qs[0] % 8 == 0 &&
                            p.qs[1] % 8 == 0 && p.qs[2] % 8 == 0;
     // int8 caches: head_dim 128 or 256 and up to 32 rows (one softmax
-    // warpgroup; the other four warps widen the codes).
-    const bool shape = p.kv_int8 ? ((p.d == 128 || p.d == 256) && p.rows <= 32)
+    // warpgroup; the other four warps widen the codes); flat dense launches
+    // with more rows run in parts of a kv head's query heads.
+    const bool int8_rows =
+        p.rows <= 32 || (p.mode == kDense && p.n_new == 0 && tc_int8_row_parts(p.n_q, p.g) > 0);
+    const bool shape = p.kv_int8 ? ((p.d == 128 || p.d == 256) && int8_rows)
                                  : ((p.d == 128 || p.d == 256) && p.rows <= 64);
     // gather: bf16 caches whose rows form one strided 2-D array; paged: pools
     // whose rows do (fd_tc_paged.cu)

@@ -1025,6 +1025,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
         while (ok) {
             const int64_t piece_end = min(t_end, w.first + w.ntiles);
             const int b = w.b, hk = w.hk;
+            // flat int8 caches served in parts of a kv head's query heads:
+            // the caches' kv head of part hk
+            const int hkc = (I8 && !GA && !PG) && p.kvdiv > 1 ? hk / p.kvdiv : hk;
             const int64_t L = w.L;
             // The segment's Q rows, once the previous piece's last QK has read
             // the buffer: one box per 64 columns covering query indices
@@ -1328,7 +1331,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
                         for (int cb = 0; cb < D / 128; ++cb)
                             ptx::tma_load_4d(smem + C::OFF_RAW + rs * C::RAW + cb * (TT * 128),
                                              kv ? (const void *)&a.tv : (const void *)&a.tk,
-                                             &bs->raw_full[rs], cb * 64, ys, hk, b);
+                                             &bs->raw_full[rs], cb * 64, ys, hkc, b);
                     }
                 } else if (lane == 0) {
                     const uint32_t slot = issued % C::NS, ph = (issued / C::NS) & 1;
@@ -1649,8 +1652,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) tc_kernel(const __grid_constant
             // not the row sums; nothing outside the filled prefix is read).
             // (paged: scales live beside their rows, page pg_n, row tok % page_size)
             const int64_t sb0 = PG ? 0 : (int64_t)w.b;
-            const float *ksrow = I8 ? p.k_scale + sb0 * p.kss[0] + (int64_t)w.hk * p.kss[1] : nullptr;
-            const float *vsrow = I8 ? p.v_scale + sb0 * p.vss[0] + (int64_t)w.hk * p.vss[1] : nullptr;
+            const int64_t hkc = (I8 && !GA && !PG) && p.kvdiv > 1 ? w.hk / p.kvdiv : w.hk;
+            const float *ksrow = I8 ? p.k_scale + sb0 * p.kss[0] + hkc * p.kss[1] : nullptr;
+            const float *vsrow = I8 ? p.v_scale + sb0 * p.vss[0] + hkc * p.vss[1] : nullptr;
             // paged: the pool page of this thread's position (-1 past the
             // length, or for a table entry outside the pool, which the
             // producer flags), read two tiles ahead so the scale reads of the

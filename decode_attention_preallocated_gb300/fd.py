@@ -391,7 +391,10 @@ def decode_int8(q, k_cache, v_cache, k_scale, v_scale, kv_lengths, n_q=None,
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     Hkv = k_cache.shape[1]
     rows = (Hq // max(Hkv, 1)) * nq
-    out, sh, ws = _prepare(q, k_cache, out, out_dtype, B * Hkv, rows, num_ctas,
+    # more than 32 rows: the tensor-core kernel serves each kv head's query
+    # heads in parts, a segment each (at most one per query head)
+    segments = B * Hq if rows > 32 else B * Hkv
+    out, sh, ws = _prepare(q, k_cache, out, out_dtype, segments, rows, num_ctas,
                            kernel, stream, workspace)
     tq, tk, tv, tks, tvs, to = map(as_fd_tensor, (q, k_cache, v_cache, k_scale, v_scale, out))
     o = _opts(sh, ws, num_ctas, kernel)

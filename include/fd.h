@@ -98,7 +98,9 @@ extern "C" {
 #define FD_KERNEL_TC 2           /* tensor-core (tcgen05) kernel: bf16
                                     caches (head_dim 128/256, up to 64
                                     rows) and int8 caches (head_dim
-                                    128/256, up to 32 rows), flat or paged
+                                    128/256, up to 32 rows; flat dense
+                                    int8 with more rows in parts, see
+                                    fd_decode_int8), flat or paged
                                     (pools whose rows form one strided 2-D
                                     array), the fused append and the
                                     masked prefix over flat bf16 caches,
@@ -165,6 +167,14 @@ int fd_decode(const fd_tensor *q, const fd_tensor *k_cache,
  * above 4094, i.e. dequantised |v| above about 5.2e5, can saturate).  The
  * CUDA-core kernel has no such range limit.  The same holds for every
  * int8 call (paged and gather).
+ * The tensor-core kernel takes up to 32 rows (n_q * g) at once.  With more,
+ * it serves each kv head's query heads in k parts of g / k heads, k the
+ * fewest dividing g that bring n_q * g / k to 32 or fewer, each part a
+ * segment of its own that reads the kv head's prefix again (k times the
+ * cache bytes); the workspace then needs B * Hkv * k segments (B * Hq always
+ * suffices).  Under FD_KERNEL_AUTO a workspace without that room, or a
+ * shape with no such k (g = 1), takes the CUDA-core kernel, which reads the
+ * prefix once; FD_KERNEL_TC returns FD_ERR_WORKSPACE or FD_ERR_UNSUPPORTED.
  */
 int fd_decode_int8(const fd_tensor *q, const fd_tensor *k_cache,
                    const fd_tensor *v_cache, const fd_tensor *k_scale,

@@ -357,12 +357,44 @@ def test_int8_tensor_core_large_value_scales(d):
         assert err < tol, (od, float(err))
 
 
+@pytest.mark.parametrize("ctas", [1, 7, 0])
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("shape", [(2, 32, 1), (4, 64, 4), (6, 32, 4), (5, 48, 4), (3, 21, 1), (6, 18, 2)])
+def test_int8_tensor_core_rows_in_parts(ctas, d, shape):
+    # more than 32 packed rows (n_q x g = 64, 64, 48, 60, 63, 54): the
+    # tensor-core kernel serves each kv head's query heads in 2 or 3 parts of
+    # at most 32 rows; causal windows, ragged lengths down to one position
+    n_q, Hq, Hkv = shape
+    inp = W.dense_inputs(3, n_q, Hq, Hkv, d, 700, [700, 257, 1], 34, True, int8=True)
+    check(inp, torch.float32, kernel=fd.FD_KERNEL_TC, num_ctas=ctas)
+    check(inp, torch.bfloat16, kernel=fd.FD_KERNEL_TC, num_ctas=ctas)
+
+
+def test_int8_rows_in_parts_need_workspace_segments():
+    # 64 rows in 2 parts need 2 segments per (sequence, kv head): a workspace
+    # with room for one per pair refuses the tensor-core kernel and sends
+    # FD_KERNEL_AUTO to the CUDA-core kernel, which serves the rows in one pass
+    inp = W.dense_inputs(2, 2, 32, 1, 128, 300, [300, 41], 35, True, int8=True)
+    dev = to_dev(inp)
+    ws = fd.Workspace(2, 64, 128, 1024)
+    with pytest.raises(fd.FdError):
+        run_gpu(dev, torch.float32, kernel=fd.FD_KERNEL_TC, workspace=ws)
+    torch.cuda.synchronize()
+    ws.reset()
+    got = run_gpu(dev, torch.float32, workspace=ws)
+    compare(got, run_oracle(inp), torch.float32, "int8 rows 64 auto, small workspace")
+    ws.close()
+
+
 def test_int8_tensor_core_rejects_unserved_shapes():
-    # more than 32 rows: the tensor-core kernel declines, AUTO takes the CUDA-core one
-    inp = to_dev(W.dense_inputs(1, 2, 32, 1, 128, 200, [150], 27, True, int8=True))
+    # gather over an int8 cache with more than 32 rows (48 query heads on one
+    # kv head): the tensor-core kernel declines and FD_KERNEL_AUTO takes the
+    # CUDA-core one
+    cpu = W.gather_inputs(1, 1, 48, 1, 128, 600, 200, 16, 27, int8=True)
+    inp = to_dev(cpu)
     with pytest.raises(fd.FdError):
         run_gpu(inp, torch.float32, kernel=fd.FD_KERNEL_TC)
-    compare(run_gpu(inp, torch.float32), run_oracle(inp), torch.float32, "int8 rows 64 auto")
+    compare(run_gpu(inp, torch.float32), run_oracle(cpu), torch.float32, "int8 gather rows 48 auto")
 
 
 # ------------------------------------------------------------- CUDA graphs
