@@ -376,7 +376,10 @@ def workspace_for(inp, device):
     g = Hq // Hkv
     if inp.idx is not None:
         return fd.Workspace(B * n_q * Hkv, g, 256, 4096, device=device)
-    return fd.Workspace(B * Hkv, g * n_q, 256, 4096, device=device)
+    # int8 caches with more than 32 rows run on the tensor cores in parts of
+    # the query heads, a segment each (at most one per query head)
+    parts = g if inp.k.dtype == torch.int8 and g * n_q > 32 else 1
+    return fd.Workspace(B * Hkv * parts, g * n_q, 256, 4096, device=device)
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -675,6 +678,18 @@ def extras(args, device, stream, peak, kernel):
         inp = append_inputs(name, 1, device)
         measure("append_" + name, inp, 200 if name == "mtp_verify" else 50)
         del inp
+        torch.cuda.empty_cache()
+    # int8 caches with 64 rows per kv head (4 causal rows x 16 heads), which
+    # the tensor-core kernel serves in two parts of 32 rows
+    for d in (128, 256):
+        tag = "int8_rows64_d%d" % d
+        try:
+            inp = W.dense_inputs(4, 4, 64, 4, d, 32768, [32768] * 4, 5, True, device=device,
+                                 int8=True)
+            measure(tag, inp, 50)
+        except Exception as e:   # an extra: recorded, never fatal to the line
+            res[tag] = {"error": repr(e)[:200]}
+        inp = None
         torch.cuda.empty_cache()
     # paged caches: the ragged and int8 workloads with their pages scattered
     # over a pool (bytes: the same K/V rows as the flat caches)
