@@ -17,7 +17,7 @@ pytestmark = pytest.mark.gpu
 
 KERNELS = [fd.FD_KERNEL_SIMT]
 DENSE_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]
-INT8_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]   # tensor cores: <= 32 rows
+INT8_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]   # tensor cores: <= 32 rows a launch
 GATHER_KERNELS = [fd.FD_KERNEL_SIMT, fd.FD_KERNEL_TC]
 
 
