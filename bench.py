@@ -474,8 +474,9 @@ def oracle_us(inp_cpu, threads, budget_s=None):
     return 1e6 * t_used * total / done, "%d of %d sequences, scaled by bytes" % (seqs, B)
 
 
-# The five workloads the benchmark spec names, in its order, with their tags in
-# the bench line.
+# The five reference workloads (1000-position dense, MTP verify, the ragged
+# batch, top-k gather, int8 at 131072 positions) with their tags in the bench
+# line.
 BASELINE_CONFIGS = (("c1_dense_1k", "dense_1k"), ("c2_mtp_verify", "mtp_verify"),
                     ("c3_ragged", "ragged"), ("c4_gather", "gather"), ("c5_int8", "int8"))
 
